@@ -1,0 +1,211 @@
+/*
+ * dllm.h -- C ABI of the GB300 sparse KV-cache refresh library (libdllm.so).
+ *
+ * One denoising step of a bidirectional (non-causal) diffusion-LLM layer with a
+ * sparse cache refresh, as stated by:
+ *   [SPA] "Singular proxies for adaptive caching in diffusion language models"
+ *         (SPA-Cache): "1. Update identification via singular proxy",
+ *         "2. Adaptive budget allocation", "3. Sparse execution";
+ *   [EC]  "EntropyCache": "How EntropyCache works", steps 1-3;
+ *   [TSPD] "Efficient diffusion LLMs via temporal-spatial parallel decoding and
+ *         confidence extrapolation": "Input features";
+ *   [POL] "Polestar: drift-aware cache correction and token commit for efficient
+ *         diffusion LLM inference": "1. Problem definition".
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Memory    All array pointers are DEVICE pointers owned by the caller, C-contiguous,
+ *           row-major with leading dimension equal to the logical width, and 16-byte
+ *           aligned.  The library never allocates device memory: scratch space is
+ *           the caller's workspace `ws` of `ws_bytes` bytes, sized by the matching
+ *           *_workspace_bytes() query (256-byte aligned).  Outputs never alias inputs
+ *           unless a parameter says so.
+ * Streams   `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *           stream).  Every compute call only enqueues work and returns; nothing
+ *           synchronises the host except dllm_check_status().
+ * dtype     DLLM_BF16: hidden states, weights, K/V caches and gains are bf16 and every
+ *           GEMM runs on the tcgen05 tensor cores with fp32 accumulation.
+ *           DLLM_F32: the same arrays are fp32 and every product runs on the CUDA
+ *           cores in fp32.  Proxies, drift, logits and all statistics are fp32 in
+ *           both cases.
+ * Errors    Every call returns DLLM_OK (0) or a negative code; the message of the
+ *           last failure on the calling thread is dllm_last_error().  Argument errors
+ *           are detected on the host before any launch.  Device-side conditions
+ *           (a bounded wait that ran out, a count larger than k_max) set bits of a
+ *           device status word read by dllm_check_status(); no kernel traps.
+ */
+#ifndef DLLM_H_
+#define DLLM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DLLM_OK 0
+#define DLLM_ERR_INVALID_ARG (-1) /* null pointer, bad size, misalignment, k > N ...  */
+#define DLLM_ERR_UNSUPPORTED (-2) /* shape/dtype combination without a kernel          */
+#define DLLM_ERR_WORKSPACE (-3)   /* ws_bytes smaller than the query returned          */
+#define DLLM_ERR_CUDA (-4)        /* a CUDA runtime call or launch failed              */
+#define DLLM_ERR_TIMEOUT (-5)     /* reported by dllm_check_status()                   */
+
+#define DLLM_F32 0
+#define DLLM_BF16 1
+
+/* Device status bits (dllm_check_status). */
+#define DLLM_STATUS_TIMEOUT 1u     /* a kernel's bounded mbarrier wait ran out          */
+#define DLLM_STATUS_COUNT_CLAMP 2u /* count[b] > k_max: extra rows were ignored         */
+
+/* Message of the last failed call on this thread ("" if none). */
+const char *dllm_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+int dllm_version(void);
+
+/* Reads (and with reset != 0 clears) the device status word of the current device.
+ * Synchronises the device.  Returns DLLM_ERR_TIMEOUT if the timeout bit is set,
+ * DLLM_OK otherwise; *status_out (optional) receives all bits. */
+int dllm_check_status(unsigned *status_out, int reset);
+
+/* ---------------------------------------------------------------------------
+ * [SPA] "1. Update identification via singular proxy"
+ *
+ * proxy_cur[t] = H[t] . P                 (t = b*N + i, P = Pt^T, [d x r])
+ * drift[t]     = 1 - <proxy_cur[t], proxy_cache[t]> / sqrt(|proxy_cur[t]|^2 |proxy_cache[t]|^2)
+ * with drift = 0 when both proxies are zero, 1 when exactly one is, and clamped to
+ * [0, 2].  Identical proxies give exactly 0.
+ *   H           [B, N, d]  dtype      layer input (residual stream before the norm)
+ *   Pt          [r, d]     dtype      proxy matrix, transposed: row j = column j of
+ *                                     U_r S_r of diag(gamma1) W_V^T (built once per layer)
+ *   proxy_cache [B, N, r]  fp32       proxies stored when each row was last refreshed
+ *   proxy_cur   [B, N, r]  fp32 out
+ *   drift       [B, N]     fp32 out
+ * Requirements: r % 32 == 0, r <= 1024; d % 64 == 0 for DLLM_BF16.
+ * No workspace.
+ * ------------------------------------------------------------------------- */
+int dllm_proxy_score(const void *H, const void *Pt, const float *proxy_cache, float *proxy_cur,
+                     float *drift, int B, int N, int d, int r, int dtype, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Selection.  [SPA] "1. ...": the rows with the lowest proxy similarity (largest
+ * drift) are recomputed, [SPA] "2. Adaptive budget allocation": at most k of them
+ * per layer; [EC] step 3: the current masked tokens and the k most recently decoded
+ * tokens are always recomputed (the forced set).
+ *
+ * For each sequence b:  F_b = entries of forced[b, 0..F) inside [0, N) (others are
+ * padding; duplicates count once);  eligible = rows not in F_b with drift > min_drift
+ * (NaN is never eligible);  the min(k, N - |F_b|) eligible rows with the largest
+ * drift are taken, equal drifts by lower row index;  idx[b, 0..count[b]) receives
+ * F_b union taken in ascending order and idx[b, count[b]..N) = -1.
+ *   drift  [B, N] fp32;  forced [B, F] int32 or NULL (then F is ignored);
+ *   idx    [B, N] int32 out;  count [B] int32 out.
+ * Requirements: N <= 16384, 0 <= k.  No workspace.
+ * ------------------------------------------------------------------------- */
+int dllm_select_topk(const float *drift, const int32_t *forced, int F, int k, float min_drift,
+                     int32_t *idx, int32_t *count, int B, int N, void *stream);
+
+/* Per-layer update ratio, [SPA] "2. Adaptive budget allocation" (a piecewise Gaussian
+ * over depth): rho(l) = base + (peak - base) exp(-(l - centre)^2 / (2 s^2)) with
+ * s = sigma_left below the centre and sigma_right from it on.  Host function. */
+double dllm_layer_rho(int l, double base, double peak, double centre, double sigma_left,
+                      double sigma_right);
+
+/* Drift budget of a layer: ceil(rho * N), at least 1 when rho > 0, at most N.  Host. */
+int dllm_layer_budget(double rho, int N);
+
+/* ---------------------------------------------------------------------------
+ * Layer weights.  nn.Linear layout in ([out, in]) is repacked once per layer:
+ *   w_qkv  [(n_q + 2 n_kv) hd, d]  rows Q | K | V; inside every head the rows are
+ *          ordered 0, hd/2, 1, hd/2+1, ... so that the two halves of each rotary pair
+ *          are neighbours (outputs are written back in the natural order);
+ *   w_o    [d, n_q hd];   w_gu [2F, d] with row 2j = gate j, row 2j+1 = up j;
+ *   w_down [d, F];        gamma1, gamma2 [d];  rope_inv_freq [hd/2] fp32.
+ * ------------------------------------------------------------------------- */
+typedef struct dllm_layer {
+    const void *w_qkv;
+    const void *w_o;
+    const void *w_gu;
+    const void *w_down;
+    const void *gamma1;
+    const void *gamma2;
+    const float *rope_inv_freq; /* [hd/2] fp32: rope_theta^(-2i/hd), built in double */
+    int d, n_q, n_kv, hd, F;
+    float eps;        /* RMSNorm epsilon                                     */
+    float rope_theta; /* rotary base                                          */
+    int use_rope;     /* 1: rotate Q and K (rotate-half pairs) at their rows  */
+    int dtype;        /* DLLM_BF16 or DLLM_F32                               */
+} dllm_layer;
+
+/* Bytes of packed weights for one layer (256-byte aligned sub-buffers). */
+size_t dllm_packed_layer_bytes(int d, int n_q, int n_kv, int hd, int F, int dtype);
+
+/* Repacks one layer's nn.Linear weights (device, dtype) into dst and fills *out with
+ * pointers into dst.  Sources may be freed once the stream has run the copy.
+ * Requirements: hd in {64, 128}; n_q % n_kv == 0; d, n_q hd, F multiples of 64 for
+ * DLLM_BF16 (of 2 for DLLM_F32). */
+int dllm_pack_layer(const void *w_q, const void *w_k, const void *w_v, const void *w_o,
+                    const void *w_g, const void *w_u, const void *w_d, const void *gamma1,
+                    const void *gamma2, int d, int n_q, int n_kv, int hd, int F, float eps,
+                    float rope_theta, int use_rope, int dtype, void *dst, size_t dst_bytes,
+                    dllm_layer *out, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * [SPA] "3. Sparse execution": recompute only the selected rows.
+ *
+ * For every sequence b and selected row i = idx[b, s], s < min(count[b], k_max):
+ *   xn = RMSNorm(H_in[b,i]) gamma1;  q, k, v = xn W_q^T, xn W_k^T, xn W_v^T;
+ *   rotary embedding of q and k at position i (rotate-half, base rope_theta);
+ *   K_cache[b,i] <- k, V_cache[b,i] <- v          (all selected rows first, so the
+ *                                                   queries see the partially updated cache)
+ *   a = softmax(q K_cache[b]^T / sqrt(hd)) V_cache[b] over all N rows (non-causal;
+ *       query head h reads KV head h / (n_q / n_kv));
+ *   h1 = H_in[b,i] + a W_o^T;  x2 = RMSNorm(h1) gamma2;
+ *   H_out_cache[b,i] <- h1 + (SiLU(x2 W_g^T) * (x2 W_u^T)) W_down^T;
+ *   proxy_cache[b,i] <- proxy_cur[b,i]              (when both pointers are non-NULL).
+ * Rows that are not selected are not written.
+ *   H_in        [B, N, d]        dtype
+ *   idx, count  as written by dllm_select_topk ([B, N] and [B] int32)
+ *   k_max       host upper bound on count[b]; larger counts are clamped and flagged
+ *   K_cache, V_cache [B, N, n_kv, hd] dtype (in/out); H_out_cache [B, N, d] dtype (in/out)
+ *   proxy_cache, proxy_cur [B, N, r] fp32 or NULL
+ * Requirements: k_max <= N; H_out_cache must not alias H_in.
+ * ------------------------------------------------------------------------- */
+size_t dllm_refresh_workspace_bytes(const dllm_layer *W, int B, int N, int k_max);
+
+int dllm_sparse_layer_refresh(const dllm_layer *W, const void *H_in, const int32_t *idx,
+                              const int32_t *count, int k_max, void *K_cache, void *V_cache,
+                              void *H_out_cache, float *proxy_cache, const float *proxy_cur, int r,
+                              int B, int N, void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Vocabulary step.  [TSPD] "Input features": top-1 confidence and predictive entropy
+ * per token; [EC] step 2: the maximum entropy E of the tokens decoded at this step,
+ * step 3: E > tau means a full forward at the next step; [POL] "1. Problem
+ * definition" / [TSPD]: static confidence-threshold commit.
+ *
+ * For every row (b, m) with valid[b, m] != 0, p = softmax(logits[b, m]):
+ *   conf = max p, entropy = -sum p ln p (nats), argmax = lowest id of the maximum.
+ * Per sequence: commit every valid row with conf >= conf_thresh; if none qualifies,
+ * commit the one valid row with the highest conf (lowest m on ties);
+ *   token[b, m] = argmax of committed rows, -1 otherwise;
+ *   max_entropy[b] = max entropy over committed rows (0 if none);
+ *   full_next[b] = max_entropy[b] > tau.
+ * conf and entropy of invalid rows are 0.
+ *   logits [B, M, V] fp32;  valid [B, M] uint8;  token [B, M] int32 out;
+ *   conf, entropy [B, M] fp32 out;  max_entropy [B] fp32 out;  full_next [B] int32 out.
+ * Requirements: M <= 1024, V >= 1.
+ * ------------------------------------------------------------------------- */
+size_t dllm_commit_workspace_bytes(int B, int M, int V);
+
+int dllm_commit_entropy(const float *logits, const uint8_t *valid, int B, int M, int V,
+                        float conf_thresh, float tau, int32_t *token, float *conf,
+                        float *entropy, float *max_entropy, int32_t *full_next, void *ws,
+                        size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DLLM_H_ */

@@ -1,0 +1,265 @@
+"""Thin torch binding of libdllm.so: the C entry points of include/dllm.h under the
+same names, taking torch tensors.  Only argument marshalling happens here (shape
+and dtype checks, pointers, the current CUDA stream, workspace tensors); every
+step of the refresh runs in the library's kernels.  Nothing falls back to another
+implementation: a missing library or a failed call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libdllm.so")
+
+DLLM_F32, DLLM_BF16 = 0, 1
+STATUS_TIMEOUT, STATUS_COUNT_CLAMP = 1, 2
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DllmError(RuntimeError):
+    pass
+
+
+class dllm_layer(C.Structure):
+    _fields_ = [("w_qkv", C.c_void_p), ("w_o", C.c_void_p), ("w_gu", C.c_void_p),
+                ("w_down", C.c_void_p), ("gamma1", C.c_void_p), ("gamma2", C.c_void_p),
+                ("rope_inv_freq", C.c_void_p),
+                ("d", C.c_int), ("n_q", C.c_int), ("n_kv", C.c_int), ("hd", C.c_int), ("F", C.c_int),
+                ("eps", C.c_float), ("rope_theta", C.c_float), ("use_rope", C.c_int),
+                ("dtype", C.c_int)]
+
+
+_SIGS = {
+    "dllm_last_error": (C.c_char_p, []),
+    "dllm_version": (C.c_int, []),
+    "dllm_check_status": (C.c_int, [C.POINTER(C.c_uint), C.c_int]),
+    "dllm_proxy_score": (C.c_int, [C.c_void_p] * 5 + [C.c_int] * 5 + [C.c_void_p]),
+    "dllm_select_topk": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_float,
+                                   C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p]),
+    "dllm_layer_rho": (C.c_double, [C.c_int] + [C.c_double] * 5),
+    "dllm_layer_budget": (C.c_int, [C.c_double, C.c_int]),
+    "dllm_packed_layer_bytes": (C.c_size_t, [C.c_int] * 6),
+    "dllm_pack_layer": (C.c_int, [C.c_void_p] * 9 + [C.c_int] * 5 + [C.c_float, C.c_float,
+                                                                      C.c_int, C.c_int, C.c_void_p,
+                                                                      C.c_size_t,
+                                                                      C.POINTER(dllm_layer),
+                                                                      C.c_void_p]),
+    "dllm_refresh_workspace_bytes": (C.c_size_t, [C.POINTER(dllm_layer), C.c_int, C.c_int, C.c_int]),
+    "dllm_sparse_layer_refresh": (C.c_int, [C.POINTER(dllm_layer), C.c_void_p, C.c_void_p,
+                                            C.c_void_p, C.c_int, C.c_void_p, C.c_void_p,
+                                            C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
+                                            C.c_int, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "dllm_commit_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
+    "dllm_commit_entropy": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
+                                      C.c_float, C.c_float] + [C.c_void_p] * 6 +
+                            [C.c_size_t, C.c_void_p]),
+}
+
+
+def exported_symbols():
+    """Names of every entry point the binding expects the library to export."""
+    return list(_SIGS)
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise DllmError(f"libdllm.so not built ({LIB_PATH}); run __graft_entry__.build()")
+            L = C.CDLL(LIB_PATH)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+        return _lib
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        msg = lib().dllm_last_error().decode(errors="replace")
+        raise DllmError(f"{what} failed ({rc}): {msg}")
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(device=None):
+    return C.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return DLLM_BF16
+    if t.dtype == torch.float32:
+        return DLLM_F32
+    raise DllmError(f"unsupported dtype {t.dtype}")
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise DllmError("tensors must be on a CUDA device")
+            if not t.is_contiguous():
+                raise DllmError("tensors must be contiguous")
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(nbytes: int, device, tag: str) -> torch.Tensor:
+    """Caller-side scratch buffer (the library itself never allocates)."""
+    key = (tag, device.index if device.index is not None else torch.cuda.current_device())
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+# --------------------------------------------------------------------------- status
+def check_status(reset: bool = True) -> int:
+    st = C.c_uint(0)
+    rc = lib().dllm_check_status(C.byref(st), 1 if reset else 0)
+    if rc == -5:
+        raise DllmError(f"device status 0x{st.value:x}: a kernel wait timed out")
+    _check(rc, "dllm_check_status")
+    return st.value
+
+
+# --------------------------------------------------------------------------- proxy
+def dllm_proxy_score(H, Pt, proxy_cache, proxy_cur=None, drift=None):
+    """H [B,N,d] (bf16|f32), Pt [r,d] same dtype, proxy_cache [B,N,r] f32 ->
+    (proxy_cur [B,N,r] f32, drift [B,N] f32)."""
+    B, N, d = H.shape
+    r = Pt.shape[0]
+    if Pt.shape != (r, d) or Pt.dtype != H.dtype:
+        raise DllmError("Pt must be [r, d] with H's dtype")
+    if proxy_cur is None:
+        proxy_cur = torch.empty((B, N, r), dtype=torch.float32, device=H.device)
+    if drift is None:
+        drift = torch.empty((B, N), dtype=torch.float32, device=H.device)
+    _cuda(H, Pt, proxy_cache, proxy_cur, drift)
+    _check(lib().dllm_proxy_score(_ptr(H), _ptr(Pt), _ptr(proxy_cache), _ptr(proxy_cur), _ptr(drift),
+                                  B, N, d, r, _dtype_code(H), _stream(H.device)), "dllm_proxy_score")
+    return proxy_cur, drift
+
+
+def build_proxy_matrix(w_v: torch.Tensor, gamma1: torch.Tensor, r: int) -> torch.Tensor:
+    """One-time set-up (not part of the per-step path): Pt = (U_r S_r)^T of
+    diag(gamma1) W_V^T via a double-precision SVD on the device, returned in w_v's dtype."""
+    A = gamma1.double()[:, None] * w_v.double().t()
+    U, S, _ = torch.linalg.svd(A, full_matrices=False)
+    return (U[:, :r] * S[:r]).t().contiguous().to(w_v.dtype)
+
+
+# --------------------------------------------------------------------------- selection
+def dllm_select_topk(drift, forced, k: int, min_drift: float = 1e-6, idx=None, count=None):
+    """drift [B,N] f32, forced [B,F] int32 (-1 padded) or None ->
+    (idx [B,N] int32 ascending, -1 padded;  count [B] int32)."""
+    B, N = drift.shape
+    F = 0 if forced is None else forced.shape[1]
+    if idx is None:
+        idx = torch.empty((B, N), dtype=torch.int32, device=drift.device)
+    if count is None:
+        count = torch.empty((B,), dtype=torch.int32, device=drift.device)
+    _cuda(drift, forced, idx, count)
+    _check(lib().dllm_select_topk(_ptr(drift), _ptr(forced), F, int(k), float(min_drift), _ptr(idx),
+                                  _ptr(count), B, N, _stream(drift.device)), "dllm_select_topk")
+    return idx, count
+
+
+def dllm_layer_rho(l: int, base=0.05, peak=0.30, centre=16.0, sigma_left=6.0, sigma_right=6.0):
+    return float(lib().dllm_layer_rho(int(l), base, peak, centre, sigma_left, sigma_right))
+
+
+def dllm_layer_budget(rho: float, N: int) -> int:
+    return int(lib().dllm_layer_budget(float(rho), int(N)))
+
+
+# --------------------------------------------------------------------------- layer
+class Layer:
+    """Packed weights of one layer on the device plus the dllm_layer descriptor."""
+
+    def __init__(self, packed: torch.Tensor, desc: dllm_layer):
+        self.packed = packed
+        self.desc = desc
+
+    @property
+    def dtype(self):
+        return torch.bfloat16 if self.desc.dtype == DLLM_BF16 else torch.float32
+
+
+def dllm_pack_layer(w: dict, n_q: int, n_kv: int, hd: int, eps: float = 1e-5,
+                    rope_theta: float = 10000.0, use_rope: bool = True) -> Layer:
+    """w: device tensors in nn.Linear layout (w_q, w_k, w_v, w_o, w_g, w_u, w_d, gamma1, gamma2)."""
+    keys = ("w_q", "w_k", "w_v", "w_o", "w_g", "w_u", "w_d", "gamma1", "gamma2")
+    ts = [w[k].contiguous() for k in keys]
+    _cuda(*ts)
+    dt = _dtype_code(ts[0])
+    if any(t.dtype != ts[0].dtype for t in ts):
+        raise DllmError("all weights must share one dtype")
+    d = ts[7].shape[0]
+    F = ts[4].shape[0]
+    nbytes = lib().dllm_packed_layer_bytes(d, n_q, n_kv, hd, F, dt)
+    packed = torch.empty(nbytes, dtype=torch.uint8, device=ts[0].device)
+    desc = dllm_layer()
+    _check(lib().dllm_pack_layer(*[_ptr(t) for t in ts], d, n_q, n_kv, hd, F, float(eps),
+                                 float(rope_theta), 1 if use_rope else 0, dt, _ptr(packed), nbytes,
+                                 C.byref(desc), _stream(ts[0].device)), "dllm_pack_layer")
+    return Layer(packed, desc)
+
+
+def dllm_refresh_workspace_bytes(layer: Layer, B: int, N: int, k_max: int) -> int:
+    return int(lib().dllm_refresh_workspace_bytes(C.byref(layer.desc), B, N, k_max))
+
+
+def dllm_sparse_layer_refresh(layer: Layer, H_in, idx, count, k_max: int, K_cache, V_cache,
+                              H_out_cache, proxy_cache=None, proxy_cur=None, ws=None):
+    """Refreshes the cache rows idx[b, :count[b]] in place (K_cache, V_cache,
+    H_out_cache, and proxy_cache when given)."""
+    B, N, d = H_in.shape
+    r = 0 if proxy_cache is None else proxy_cache.shape[-1]
+    _cuda(H_in, idx, count, K_cache, V_cache, H_out_cache, proxy_cache, proxy_cur)
+    need = dllm_refresh_workspace_bytes(layer, B, N, k_max)
+    if ws is None:
+        ws = _workspace(need, H_in.device, "refresh")
+    _check(lib().dllm_sparse_layer_refresh(C.byref(layer.desc), _ptr(H_in), _ptr(idx), _ptr(count),
+                                           int(k_max), _ptr(K_cache), _ptr(V_cache),
+                                           _ptr(H_out_cache), _ptr(proxy_cache), _ptr(proxy_cur), r,
+                                           B, N, _ptr(ws), ws.numel(), _stream(H_in.device)),
+           "dllm_sparse_layer_refresh")
+    return K_cache, V_cache, H_out_cache
+
+
+# --------------------------------------------------------------------------- vocab
+def dllm_commit_entropy(logits, valid, conf_thresh: float = 0.9, tau: float = 2.0, out=None, ws=None):
+    """logits [B,M,V] f32, valid [B,M] uint8 ->
+    (token [B,M] int32, conf [B,M], entropy [B,M], max_entropy [B], full_next [B] int32)."""
+    B, M, V = logits.shape
+    dev = logits.device
+    if out is None:
+        out = (torch.empty((B, M), dtype=torch.int32, device=dev),
+               torch.empty((B, M), dtype=torch.float32, device=dev),
+               torch.empty((B, M), dtype=torch.float32, device=dev),
+               torch.empty((B,), dtype=torch.float32, device=dev),
+               torch.empty((B,), dtype=torch.int32, device=dev))
+    tok, conf, ent, E, full = out
+    _cuda(logits, valid, *out)
+    need = int(lib().dllm_commit_workspace_bytes(B, M, V))
+    if ws is None:
+        ws = _workspace(need, dev, "commit")
+    _check(lib().dllm_commit_entropy(_ptr(logits), _ptr(valid), B, M, V, float(conf_thresh),
+                                     float(tau), _ptr(tok), _ptr(conf), _ptr(ent), _ptr(E),
+                                     _ptr(full), _ptr(ws), ws.numel(), _stream(dev)),
+           "dllm_commit_entropy")
+    return out

@@ -1,0 +1,409 @@
+// api.cu -- the extern "C" entry points of libdllm.so (declared in include/dllm.h):
+// argument checks, workspace carving and the launch sequence of each call.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "internal.h"
+
+#define DLLM_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace dllm {
+
+// Device status word (DLLM_STATUS_* bits); kernels receive its device address.
+__device__ unsigned g_status_word;
+
+namespace {
+
+thread_local std::string t_err;
+
+int fail(int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_err = buf;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+    return fail(DLLM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define CHECK_ARG(cond, ...)                                   \
+    do {                                                       \
+        if (!(cond)) return fail(DLLM_ERR_INVALID_ARG, __VA_ARGS__); \
+    } while (0)
+
+#define CHECK_CUDA(expr, what)                   \
+    do {                                         \
+        cudaError_t e_ = (expr);                 \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+    } while (0)
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t el_size(int dtype) { return dtype == DLLM_BF16 ? 2 : 4; }
+
+cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+constexpr int kMaxDev = 64;
+
+unsigned *status_ptr() {
+    static unsigned *ptrs[kMaxDev] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<unsigned *>(p);
+    }
+    return ptrs[dev];
+}
+
+struct PackLayout {
+    size_t qkv, o, gu, down, g1, g2, freq, total;
+};
+
+PackLayout pack_layout(int d, int n_q, int n_kv, int hd, int F, int dtype) {
+    const size_t el = el_size(dtype);
+    PackLayout L{};
+    size_t off = 0;
+    L.qkv = off;
+    off = align256(off + (size_t)(n_q + 2 * n_kv) * hd * d * el);
+    L.o = off;
+    off = align256(off + (size_t)d * n_q * hd * el);
+    L.gu = off;
+    off = align256(off + (size_t)2 * F * d * el);
+    L.down = off;
+    off = align256(off + (size_t)d * F * el);
+    L.g1 = off;
+    off = align256(off + (size_t)d * el);
+    L.g2 = off;
+    off = align256(off + (size_t)d * el);
+    L.freq = off;
+    off = align256(off + (size_t)(hd / 2) * 4);
+    L.total = off;
+    return L;
+}
+
+struct RefreshWs {
+    size_t xn, q, a, h1, xn2, u, total;
+};
+
+RefreshWs refresh_ws(const dllm_layer *W, int B, int k_max) {
+    const size_t M = (size_t)B * k_max, el = el_size(W->dtype);
+    const size_t dq = (size_t)W->n_q * W->hd;
+    RefreshWs r{};
+    size_t off = 0;
+    r.xn = off;
+    off = align256(off + M * W->d * el);
+    r.q = off;
+    off = align256(off + M * dq * el);
+    r.a = off;
+    off = align256(off + M * dq * el);
+    r.h1 = off;
+    off = align256(off + M * W->d * 4);
+    r.xn2 = off;
+    off = align256(off + M * W->d * el);
+    r.u = off;
+    off = align256(off + M * W->F * el);
+    r.total = off + 256;   // room to align the caller's base
+    return r;
+}
+
+int check_layer(const dllm_layer *W) {
+    CHECK_ARG(W, "layer is NULL");
+    CHECK_ARG(W->dtype == DLLM_BF16 || W->dtype == DLLM_F32, "dtype must be DLLM_BF16 or DLLM_F32");
+    CHECK_ARG(W->d > 0 && W->n_q > 0 && W->n_kv > 0 && W->F > 0, "layer sizes must be positive");
+    if (W->hd != 64 && W->hd != 128) return fail(DLLM_ERR_UNSUPPORTED, "hd must be 64 or 128 (got %d)", W->hd);
+    CHECK_ARG(W->n_q % W->n_kv == 0, "n_q must be a multiple of n_kv");
+    CHECK_ARG(W->w_qkv && W->w_o && W->w_gu && W->w_down && W->gamma1 && W->gamma2,
+              "layer weight pointer is NULL");
+    if (W->dtype == DLLM_BF16) {
+        if (W->d % 64 || W->F % 64 || (W->n_q * W->hd) % 64)
+            return fail(DLLM_ERR_UNSUPPORTED, "bf16 path needs d, F, n_q*hd multiples of 64");
+    } else {
+        if (W->d % 32 || W->F % 16)
+            return fail(DLLM_ERR_UNSUPPORTED, "f32 path needs d % 32 == 0 and F % 16 == 0");
+    }
+    return DLLM_OK;
+}
+
+}  // namespace
+
+int num_sms() {
+    static int cache[kMaxDev] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 148;
+    if (!cache[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n > 0 ? n : 148;
+    }
+    return cache[dev];
+}
+
+}  // namespace dllm
+
+using namespace dllm;
+
+DLLM_EXPORT const char *dllm_last_error(void) { return t_err.c_str(); }
+
+DLLM_EXPORT int dllm_version(void) { return 100; }
+
+DLLM_EXPORT int dllm_check_status(unsigned *status_out, int reset) {
+    CHECK_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+    unsigned v = 0;
+    CHECK_CUDA(cudaMemcpyFromSymbol(&v, g_status_word, sizeof v), "cudaMemcpyFromSymbol");
+    if (reset) {
+        const unsigned z = 0;
+        CHECK_CUDA(cudaMemcpyToSymbol(g_status_word, &z, sizeof z), "cudaMemcpyToSymbol");
+    }
+    if (status_out) *status_out = v;
+    if (v & DLLM_STATUS_TIMEOUT) return fail(DLLM_ERR_TIMEOUT, "a kernel wait timed out (status 0x%x)", v);
+    return DLLM_OK;
+}
+
+// ------------------------------------------------------------------ proxy score
+DLLM_EXPORT int dllm_proxy_score(const void *H, const void *Pt, const float *proxy_cache,
+                                 float *proxy_cur, float *drift, int B, int N, int d, int r,
+                                 int dtype, void *stream) {
+    CHECK_ARG(H && Pt && proxy_cache && proxy_cur && drift, "null pointer");
+    CHECK_ARG(B > 0 && N > 0 && d > 0 && r > 0, "sizes must be positive (B=%d N=%d d=%d r=%d)", B, N, d, r);
+    CHECK_ARG(r <= 1024, "r must be <= 1024");
+    CHECK_ARG(aligned16(H) && aligned16(Pt) && aligned16(proxy_cache) && aligned16(proxy_cur),
+              "arrays must be 16-byte aligned");
+    CHECK_ARG(dtype == DLLM_BF16 || dtype == DLLM_F32, "dtype must be DLLM_BF16 or DLLM_F32");
+    if (r % 32) return fail(DLLM_ERR_UNSUPPORTED, "r must be a multiple of 32 (got %d)", r);
+    cudaStream_t st = as_stream(stream);
+    const int rows = B * N;
+    EpiStoreF32 epi{proxy_cur, r, r};
+    cudaError_t e;
+    if (dtype == DLLM_BF16) {
+        if (d % 64) return fail(DLLM_ERR_UNSUPPORTED, "bf16 path needs d % 64 == 0 (got %d)", d);
+        e = gemm_tc(static_cast<const bf16 *>(Pt), r, d, static_cast<const bf16 *>(H), rows, epi, 0,
+                    status_ptr(), st);
+    } else {
+        e = gemm_simt(static_cast<const float *>(Pt), r, d, static_cast<const float *>(H), rows, epi, st);
+    }
+    CHECK_CUDA(e, "proxy projection launch");
+    CHECK_CUDA(cosine_drift(proxy_cur, proxy_cache, drift, rows, r, st), "cosine drift launch");
+    return DLLM_OK;
+}
+
+// ------------------------------------------------------------------ selection
+DLLM_EXPORT int dllm_select_topk(const float *drift, const int32_t *forced, int F, int k,
+                                 float min_drift, int32_t *idx, int32_t *count, int B, int N,
+                                 void *stream) {
+    CHECK_ARG(drift && idx && count, "null pointer");
+    CHECK_ARG(B > 0 && N > 0, "B and N must be positive");
+    CHECK_ARG(N <= 16384, "N must be <= 16384 (got %d)", N);
+    CHECK_ARG(k >= 0, "k must be >= 0");
+    if (!forced) F = 0;
+    CHECK_ARG(F >= 0, "F must be >= 0");
+    CHECK_CUDA(select_topk(drift, forced, F, k, min_drift, idx, count, B, N, as_stream(stream)),
+               "select launch");
+    return DLLM_OK;
+}
+
+DLLM_EXPORT double dllm_layer_rho(int l, double base, double peak, double centre, double sigma_left,
+                                  double sigma_right) {
+    const double s = (double)l < centre ? sigma_left : sigma_right;
+    const double z = ((double)l - centre) / s;
+    return base + (peak - base) * std::exp(-0.5 * z * z);
+}
+
+DLLM_EXPORT int dllm_layer_budget(double rho, int N) {
+    if (!(rho > 0.0) || N <= 0) return 0;
+    double k = std::ceil(rho * (double)N);
+    if (k < 1.0) k = 1.0;
+    if (k > (double)N) k = (double)N;
+    return (int)k;
+}
+
+// ------------------------------------------------------------------ weights
+DLLM_EXPORT size_t dllm_packed_layer_bytes(int d, int n_q, int n_kv, int hd, int F, int dtype) {
+    if (d <= 0 || n_q <= 0 || n_kv <= 0 || hd <= 0 || F <= 0) return 0;
+    return pack_layout(d, n_q, n_kv, hd, F, dtype).total;
+}
+
+DLLM_EXPORT int dllm_pack_layer(const void *w_q, const void *w_k, const void *w_v, const void *w_o,
+                                const void *w_g, const void *w_u, const void *w_d,
+                                const void *gamma1, const void *gamma2, int d, int n_q, int n_kv,
+                                int hd, int F, float eps, float rope_theta, int use_rope, int dtype,
+                                void *dst, size_t dst_bytes, dllm_layer *out, void *stream) {
+    CHECK_ARG(w_q && w_k && w_v && w_o && w_g && w_u && w_d && gamma1 && gamma2 && dst && out,
+              "null pointer");
+    CHECK_ARG(dtype == DLLM_BF16 || dtype == DLLM_F32, "dtype must be DLLM_BF16 or DLLM_F32");
+    CHECK_ARG(d > 0 && n_q > 0 && n_kv > 0 && F > 0, "sizes must be positive");
+    if (hd != 64 && hd != 128) return fail(DLLM_ERR_UNSUPPORTED, "hd must be 64 or 128 (got %d)", hd);
+    CHECK_ARG(n_q % n_kv == 0, "n_q must be a multiple of n_kv");
+    CHECK_ARG(rope_theta > 0.f, "rope_theta must be positive");
+    CHECK_ARG((reinterpret_cast<uintptr_t>(dst) & 255u) == 0, "dst must be 256-byte aligned");
+    const PackLayout L = pack_layout(d, n_q, n_kv, hd, F, dtype);
+    if (dst_bytes < L.total)
+        return fail(DLLM_ERR_WORKSPACE, "dst holds %zu bytes, %zu needed", dst_bytes, L.total);
+    cudaStream_t st = as_stream(stream);
+    uint8_t *base = static_cast<uint8_t *>(dst);
+    const size_t el = el_size(dtype);
+    const size_t dq = (size_t)n_q * hd, dkv = (size_t)n_kv * hd;
+    uint8_t *qkv = base + L.qkv;
+    if (dtype == DLLM_BF16) {
+        CHECK_CUDA(pack_rows_rope(static_cast<const bf16 *>(w_q), reinterpret_cast<bf16 *>(qkv), (int)dq, d, hd, st), "pack q");
+        CHECK_CUDA(pack_rows_rope(static_cast<const bf16 *>(w_k), reinterpret_cast<bf16 *>(qkv + dq * d * el), (int)dkv, d, hd, st), "pack k");
+        CHECK_CUDA(pack_rows_rope(static_cast<const bf16 *>(w_v), reinterpret_cast<bf16 *>(qkv + (dq + dkv) * d * el), (int)dkv, d, hd, st), "pack v");
+        CHECK_CUDA(pack_rows_interleave(static_cast<const bf16 *>(w_g), static_cast<const bf16 *>(w_u), reinterpret_cast<bf16 *>(base + L.gu), F, d, st), "pack gate/up");
+    } else {
+        CHECK_CUDA(pack_rows_rope(static_cast<const float *>(w_q), reinterpret_cast<float *>(qkv), (int)dq, d, hd, st), "pack q");
+        CHECK_CUDA(pack_rows_rope(static_cast<const float *>(w_k), reinterpret_cast<float *>(qkv + dq * d * el), (int)dkv, d, hd, st), "pack k");
+        CHECK_CUDA(pack_rows_rope(static_cast<const float *>(w_v), reinterpret_cast<float *>(qkv + (dq + dkv) * d * el), (int)dkv, d, hd, st), "pack v");
+        CHECK_CUDA(pack_rows_interleave(static_cast<const float *>(w_g), static_cast<const float *>(w_u), reinterpret_cast<float *>(base + L.gu), F, d, st), "pack gate/up");
+    }
+    CHECK_CUDA(cudaMemcpyAsync(base + L.o, w_o, (size_t)d * dq * el, cudaMemcpyDeviceToDevice, st), "copy w_o");
+    CHECK_CUDA(cudaMemcpyAsync(base + L.down, w_d, (size_t)d * F * el, cudaMemcpyDeviceToDevice, st), "copy w_down");
+    CHECK_CUDA(cudaMemcpyAsync(base + L.g1, gamma1, (size_t)d * el, cudaMemcpyDeviceToDevice, st), "copy gamma1");
+    CHECK_CUDA(cudaMemcpyAsync(base + L.g2, gamma2, (size_t)d * el, cudaMemcpyDeviceToDevice, st), "copy gamma2");
+    CHECK_CUDA(rope_inv_freq(reinterpret_cast<float *>(base + L.freq), hd, rope_theta, st), "rotary table");
+    out->w_qkv = base + L.qkv;
+    out->w_o = base + L.o;
+    out->w_gu = base + L.gu;
+    out->w_down = base + L.down;
+    out->gamma1 = base + L.g1;
+    out->gamma2 = base + L.g2;
+    out->rope_inv_freq = reinterpret_cast<const float *>(base + L.freq);
+    out->d = d;
+    out->n_q = n_q;
+    out->n_kv = n_kv;
+    out->hd = hd;
+    out->F = F;
+    out->eps = eps;
+    out->rope_theta = rope_theta;
+    out->use_rope = use_rope ? 1 : 0;
+    out->dtype = dtype;
+    return DLLM_OK;
+}
+
+// ------------------------------------------------------------------ sparse refresh
+DLLM_EXPORT size_t dllm_refresh_workspace_bytes(const dllm_layer *W, int B, int N, int k_max) {
+    (void)N;
+    if (!W || B <= 0 || k_max <= 0) return 0;
+    return refresh_ws(W, B, k_max).total;
+}
+
+namespace {
+
+template <class T>
+int refresh_impl(const dllm_layer *W, const T *H_in, SelRows sel, int B, T *K_cache, T *V_cache,
+                 T *H_out, float *proxy_cache, const float *proxy_cur, int r, uint8_t *ws,
+                 cudaStream_t st) {
+    const RefreshWs L = refresh_ws(W, B, sel.k_max);
+    const int M = B * sel.k_max;
+    const int d = W->d, dq = W->n_q * W->hd, dkv = W->n_kv * W->hd, F = W->F;
+    T *Xn = reinterpret_cast<T *>(ws + L.xn);
+    T *Qc = reinterpret_cast<T *>(ws + L.q);
+    T *Ac = reinterpret_cast<T *>(ws + L.a);
+    float *h1 = reinterpret_cast<float *>(ws + L.h1);
+    T *Xn2 = reinterpret_cast<T *>(ws + L.xn2);
+    T *U = reinterpret_cast<T *>(ws + L.u);
+    unsigned *status = status_ptr();
+    const T *wqkv = static_cast<const T *>(W->w_qkv);
+    const T *wo = static_cast<const T *>(W->w_o);
+    const T *wgu = static_cast<const T *>(W->w_gu);
+    const T *wdn = static_cast<const T *>(W->w_down);
+    const T *g1 = static_cast<const T *>(W->gamma1);
+    const T *g2 = static_cast<const T *>(W->gamma2);
+
+    // a3: gather + RMSNorm, proxy cache update
+    CHECK_CUDA(gather_rmsnorm<T>(H_in, sel, B, d, g1, W->eps, Xn, proxy_cache, proxy_cur, r, status, st),
+               "gather launch");
+    // a4: QKV projection, rotary embedding, K/V scattered into the cache
+    EpiQKV<T> eq{Qc, K_cache, V_cache, sel, W->rope_inv_freq, W->n_q, W->n_kv, W->hd, W->use_rope};
+    // a6: O projection + residual;  a7: FFN gate/up + SwiGLU;  a8: down + residual, scattered
+    EpiResidual<T> er{h1, H_in, sel, d};
+    EpiSwiGLU<T> es{U, F};
+    EpiDownScatter<T> ed{H_out, h1, sel, d};
+    if constexpr (sizeof(T) == 2) {
+        CHECK_CUDA(gemm_tc(wqkv, dq + 2 * dkv, d, Xn, M, eq, 0, status, st), "qkv gemm");
+        CHECK_CUDA(attention_simt<T>(Qc, K_cache, V_cache, Ac, sel, B, W->n_q, W->n_kv, W->hd, st), "attention");
+        CHECK_CUDA(gemm_tc(wo, d, dq, Ac, M, er, 0, status, st), "o gemm");
+        CHECK_CUDA(rmsnorm_rows<T>(h1, M, d, g2, W->eps, Xn2, st), "rmsnorm2");
+        CHECK_CUDA(gemm_tc(wgu, 2 * F, d, Xn2, M, es, 0, status, st), "gate/up gemm");
+        CHECK_CUDA(gemm_tc(wdn, d, F, U, M, ed, 0, status, st), "down gemm");
+    } else {
+        CHECK_CUDA(gemm_simt(wqkv, dq + 2 * dkv, d, Xn, M, eq, st), "qkv gemm");
+        CHECK_CUDA(attention_simt<T>(Qc, K_cache, V_cache, Ac, sel, B, W->n_q, W->n_kv, W->hd, st), "attention");
+        CHECK_CUDA(gemm_simt(wo, d, dq, Ac, M, er, st), "o gemm");
+        CHECK_CUDA(rmsnorm_rows<T>(h1, M, d, g2, W->eps, Xn2, st), "rmsnorm2");
+        CHECK_CUDA(gemm_simt(wgu, 2 * F, d, Xn2, M, es, st), "gate/up gemm");
+        CHECK_CUDA(gemm_simt(wdn, d, F, U, M, ed, st), "down gemm");
+    }
+    return DLLM_OK;
+}
+
+}  // namespace
+
+DLLM_EXPORT int dllm_sparse_layer_refresh(const dllm_layer *W, const void *H_in,
+                                          const int32_t *idx, const int32_t *count, int k_max,
+                                          void *K_cache, void *V_cache, void *H_out_cache,
+                                          float *proxy_cache, const float *proxy_cur, int r, int B,
+                                          int N, void *ws, size_t ws_bytes, void *stream) {
+    int rc = check_layer(W);
+    if (rc != DLLM_OK) return rc;
+    CHECK_ARG(H_in && idx && count && K_cache && V_cache && H_out_cache, "null pointer");
+    CHECK_ARG(B > 0 && N > 0, "B and N must be positive");
+    CHECK_ARG(k_max >= 0 && k_max <= N, "k_max must be in [0, N] (got %d, N=%d)", k_max, N);
+    CHECK_ARG(H_out_cache != H_in, "H_out_cache must not alias H_in");
+    CHECK_ARG(aligned16(H_in) && aligned16(K_cache) && aligned16(V_cache) && aligned16(H_out_cache),
+              "arrays must be 16-byte aligned");
+    CHECK_ARG(W->rope_inv_freq || !W->use_rope, "rope table missing (use dllm_pack_layer)");
+    if ((proxy_cache != nullptr) != (proxy_cur != nullptr))
+        return fail(DLLM_ERR_INVALID_ARG, "proxy_cache and proxy_cur must both be set or both NULL");
+    if (proxy_cache) CHECK_ARG(r > 0, "r must be positive when proxies are given");
+    if (k_max == 0) return DLLM_OK;
+    const size_t need = refresh_ws(W, B, k_max).total;
+    if (!ws || ws_bytes < need)
+        return fail(DLLM_ERR_WORKSPACE, "workspace holds %zu bytes, %zu needed", ws_bytes, need);
+    uint8_t *w8 = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255));
+    SelRows sel{idx, count, k_max, N};
+    cudaStream_t st = as_stream(stream);
+    if (W->dtype == DLLM_BF16)
+        return refresh_impl<bf16>(W, static_cast<const bf16 *>(H_in), sel, B, static_cast<bf16 *>(K_cache),
+                                  static_cast<bf16 *>(V_cache), static_cast<bf16 *>(H_out_cache),
+                                  proxy_cache, proxy_cur, r, w8, st);
+    return refresh_impl<float>(W, static_cast<const float *>(H_in), sel, B, static_cast<float *>(K_cache),
+                               static_cast<float *>(V_cache), static_cast<float *>(H_out_cache),
+                               proxy_cache, proxy_cur, r, w8, st);
+}
+
+// ------------------------------------------------------------------ vocabulary
+DLLM_EXPORT size_t dllm_commit_workspace_bytes(int B, int M, int V) {
+    if (B <= 0 || M < 0 || V <= 0) return 0;
+    return commit_ws_bytes(B, M, V) + 256;
+}
+
+DLLM_EXPORT int dllm_commit_entropy(const float *logits, const uint8_t *valid, int B, int M, int V,
+                                    float conf_thresh, float tau, int32_t *token, float *conf,
+                                    float *entropy, float *max_entropy, int32_t *full_next,
+                                    void *ws, size_t ws_bytes, void *stream) {
+    CHECK_ARG(max_entropy && full_next, "null pointer");
+    CHECK_ARG(B > 0 && M >= 0 && V > 0, "sizes must be positive");
+    CHECK_ARG(M <= 1024, "M must be <= 1024 (got %d)", M);
+    if (M > 0) CHECK_ARG(logits && valid && token && conf && entropy, "null pointer");
+    const size_t need = commit_ws_bytes(B, M, V) + 256;
+    if (!ws || ws_bytes < need)
+        return fail(DLLM_ERR_WORKSPACE, "workspace holds %zu bytes, %zu needed", ws_bytes, need);
+    void *w = reinterpret_cast<void *>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255));
+    CHECK_CUDA(commit_entropy(logits, valid, B, M, V, conf_thresh, tau, token, conf, entropy,
+                              max_entropy, full_next, w, as_stream(stream)),
+               "commit launch");
+    return DLLM_OK;
+}

@@ -1,0 +1,278 @@
+// gemm_tc.cu -- weight-stationary bf16 GEMM on the sm_103a tensor cores
+// (tcgen05.mma, fp32 accumulators in TMEM, operands staged by TMA).
+//
+// acc[f, m] = <W[f, :], X[m, :]>: the weight tile (128 rows of W) is the MMA's
+// A operand (M = 128) and a tile of BN token rows is its B operand (N = BN), so a
+// GEMM over few gathered tokens (the selected rows) wastes no MMA rows on padding.
+// Every CTA owns one (weight tile, token tile) pair and, when the tiles alone
+// cannot fill the GPU, a K slice of it: the CTAs of one K split form a
+// thread-block cluster and reduce their fp32 partial tiles through distributed
+// shared memory, then share the epilogue.  Weight bytes are read from HBM once.
+//
+// Roles (192 threads):  warp 0 lane 0  TMA producer (multi-stage ring)
+//                       warp 1         TMEM owner; lane 0 issues the MMAs
+//                       warps 2..5     TMEM -> shared partial tile -> epilogue
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace dllm {
+namespace {
+
+constexpr int BM = 128;                // weight rows per tile (MMA M)
+constexpr int BK = 64;                 // K per stage: one 128-byte swizzled row of bf16
+constexpr int kThreads = 192;
+constexpr int kWBytes = BM * BK * 2;   // 16 KB
+constexpr int kSmemLimit = 232448;     // 227 KB dynamic shared memory per CTA
+
+struct Shape {
+    int M_tok, N_out, K;
+    int BN, splits, stages;
+    int body_bytes;   // pipeline ring, reused for the fp32 partial tile [BN][128]
+};
+
+__host__ __device__ inline int stage_bytes(int BN) { return kWBytes + BN * BK * 2; }
+
+template <class Epi>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+              const Shape g, const Epi epi, unsigned *status) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;   // 1024-byte aligned: required by the 128-byte swizzle
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + g.body_bytes);
+    uint64_t *empty = full + g.stages;
+    uint64_t *done = empty + g.stages;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * g.BN;
+    const int n0 = blockIdx.y * BM;
+    const int split = g.splits > 1 ? (int)cluster_ctarank() : 0;
+    const int KB = g.K / BK;
+    const int kb0 = (int)((long long)split * KB / g.splits);
+    const int kb1 = (int)((long long)(split + 1) * KB / g.splits);
+    const int nkb = kb1 - kb0;
+    const uint32_t tmem_cols = g.BN <= 32 ? 32u : g.BN <= 64 ? 64u : g.BN <= 128 ? 128u : 256u;
+    const int sbytes = stage_bytes(g.BN);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < g.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmX);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {   // ---------------- TMA producer
+            int issued = 0;
+            for (int it = 0; it < nkb; ++it) {
+                const int s = it % g.stages;
+                const uint32_t ph = (uint32_t)(it / g.stages) & 1u;
+                if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status)) break;
+                uint8_t *sw = smem + s * sbytes;
+                mbar_arrive_expect_tx(&full[s], (uint32_t)sbytes);
+                tma_load_2d(sw, &tmW, &full[s], (kb0 + it) * BK, n0);
+                tma_load_2d(sw + kWBytes, &tmX, &full[s], (kb0 + it) * BK, m0);
+                ++issued;
+            }
+            if (*abort_flag) {   // every issued copy must land before the CTA can exit
+                for (int it = issued > g.stages ? issued - g.stages : 0; it < issued; ++it)
+                    mbar_drain(&full[it % g.stages], (uint32_t)(it / g.stages) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {   // ---------------- MMA issuer
+            const uint32_t idesc = idesc_bf16(BM, g.BN, 0);
+            for (int it = 0; it < nkb; ++it) {
+                const int s = it % g.stages;
+                const uint32_t ph = (uint32_t)(it / g.stages) & 1u;
+                if (!mbar_wait(&full[s], ph, abort_flag, status)) break;
+                tc_fence_after();
+                const uint32_t aw = smem_u32(smem + s * sbytes);
+                const uint32_t ax = aw + kWBytes;
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)   // K = 16 per MMA: +32 bytes inside the swizzle row
+                    mma_bf16(tmem, smem_desc_sw128(aw + k * 32, 16, 1024),
+                             smem_desc_sw128(ax + k * 32, 16, 1024), idesc, (it | k) != 0);
+                mma_commit(&empty[s]);   // frees the stage once these MMAs have read it
+            }
+            mma_commit(done);
+        }
+    } else {   // ---------------- epilogue warps: TMEM -> partial tile [BN][128] fp32
+        const int q = warp & 3;   // TMEM lane quarter this warp may access
+        mbar_wait(done, 0, abort_flag, status);
+        tc_fence_after();
+        float *part = reinterpret_cast<float *>(smem);
+        const int f = q * 32 + lane;
+        for (int c0 = 0; c0 < g.BN; c0 += 16) {
+            float v[16];
+            tmem_ld_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) part[(c0 + j) * BM + f] = v[j];
+        }
+    }
+    tc_fence_before();
+    if (g.splits > 1)
+        cluster_sync_all();
+    else
+        __syncthreads();
+
+    if (warp >= 2) {   // ---------------- K-split reduction + epilogue over this CTA's columns
+        const int q = warp & 3;
+        const int f = q * 32 + lane;
+        const int per = (g.BN + g.splits - 1) / g.splits;
+        const int c_begin = split * per;
+        const int c_end = min(g.BN, c_begin + per);
+        const float *part = reinterpret_cast<const float *>(smem);
+        const uint32_t part_s = smem_u32(smem);
+        if (n0 + q * 32 < g.N_out) {   // warp-uniform: N_out % 32 == 0
+            for (int c = c_begin; c < c_end; ++c) {
+                const int m = m0 + c;
+                if (m >= g.M_tok) break;
+                float acc;
+                if (g.splits == 1) {
+                    acc = part[c * BM + f];
+                } else {
+                    acc = 0.f;
+                    const uint32_t a = part_s + (uint32_t)(c * BM + f) * 4u;
+                    for (int r = 0; r < g.splits; ++r) acc += ld_dsmem_f32(mapa_shared(a, (uint32_t)r));
+                }
+                epi(n0 + f, m, acc);
+            }
+        }
+    }
+    if (g.splits > 1) cluster_sync_all();   // peers may still read this CTA's partial tile
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, tmem_cols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Row-major bf16 matrix [rows, cols], boxes of 64 columns x box_rows rows, 128-byte swizzle.
+bool make_tmap(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    auto enc = tmap_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Plan {
+    int BN, splits, stages, tok_tiles, w_tiles;
+    int body;
+    size_t smem;
+};
+
+int round16(int x) { return (x + 15) / 16 * 16; }
+
+Plan plan_gemm(int M_tok, int N_out, int K, int splits_req) {
+    const int sms = num_sms();
+    Plan p{};
+    p.w_tiles = (N_out + BM - 1) / BM;
+    const int KB = K / BK;
+    int BN = M_tok <= 256 ? round16(M_tok) : 256;
+    // smaller token tiles when even an 8-way K split would leave most SMs idle
+    while (BN > 64 && (long long)p.w_tiles * ((M_tok + BN - 1) / BN) * 8 < sms) BN = round16(BN / 2);
+    p.BN = BN;
+    p.tok_tiles = (M_tok + BN - 1) / BN;
+    const long long tiles = (long long)p.tok_tiles * p.w_tiles;
+    int s = splits_req > 0 ? splits_req : (int)(sms / tiles);
+    s = s < 1 ? 1 : (s > 8 ? 8 : s);
+    while (s > 1 && KB / s < 2) --s;
+    if (s > KB) s = KB;
+    p.splits = s < 1 ? 1 : s;
+    const int sb = stage_bytes(BN);
+    const int tail = 1024 + (2 * 8 + 1) * 8 + 64;
+    p.stages = (kSmemLimit - tail) / sb;
+    if (p.stages > 8) p.stages = 8;
+    const int part = BN * BM * 4;
+    p.body = p.stages * sb > part ? p.stages * sb : part;
+    p.smem = (size_t)1024 + p.body + (2 * p.stages + 1) * 8 + 64;
+    return p;
+}
+
+}  // namespace
+
+template <class Epi>
+cudaError_t gemm_tc(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, const Epi &epi,
+                    int splits, unsigned *status, cudaStream_t st) {
+    if (M_tok <= 0 || N_out <= 0) return cudaSuccess;
+    if (K % BK != 0 || N_out % 32 != 0) return cudaErrorInvalidValue;
+    const Plan p = plan_gemm(M_tok, N_out, K, splits);
+    if (p.stages < 2) return cudaErrorInvalidValue;
+    CUtensorMap tmW, tmX;
+    if (!make_tmap(&tmW, W, (uint64_t)N_out, (uint64_t)K, BM) ||
+        !make_tmap(&tmX, X, (uint64_t)M_tok, (uint64_t)K, (uint32_t)p.BN))
+        return cudaErrorInvalidValue;
+    Shape g{M_tok, N_out, K, p.BN, p.splits, p.stages, p.body};
+    auto kern = k_gemm_tc<Epi>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.tok_tiles, p.w_tiles, p.splits);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = p.splits;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.splits > 1 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, tmW, tmX, g, epi, status);
+}
+
+template cudaError_t gemm_tc<EpiStoreF32>(const bf16 *, int, int, const bf16 *, int,
+                                          const EpiStoreF32 &, int, unsigned *, cudaStream_t);
+template cudaError_t gemm_tc<EpiQKV<bf16>>(const bf16 *, int, int, const bf16 *, int,
+                                           const EpiQKV<bf16> &, int, unsigned *, cudaStream_t);
+template cudaError_t gemm_tc<EpiResidual<bf16>>(const bf16 *, int, int, const bf16 *, int,
+                                                const EpiResidual<bf16> &, int, unsigned *,
+                                                cudaStream_t);
+template cudaError_t gemm_tc<EpiSwiGLU<bf16>>(const bf16 *, int, int, const bf16 *, int,
+                                              const EpiSwiGLU<bf16> &, int, unsigned *,
+                                              cudaStream_t);
+template cudaError_t gemm_tc<EpiDownScatter<bf16>>(const bf16 *, int, int, const bf16 *, int,
+                                                   const EpiDownScatter<bf16> &, int, unsigned *,
+                                                   cudaStream_t);
+
+}  // namespace dllm

@@ -1,0 +1,69 @@
+// internal.h -- host-side interface between the C entry points (api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "epilogues.cuh"
+
+namespace dllm {
+
+int num_sms();   // SMs of the current device (cached per device)
+
+// ---------------------------------------------------------------- GEMMs
+// acc[f, m] = <W[f, :K], X[m, :K]>, W [N_out, K] and X [M_tok, K] row-major,
+// handed to `epi` (see epilogues.cuh).  N_out % 32 == 0.
+//
+// Tensor cores (bf16, tcgen05 + TMA): K % 64 == 0, rows 16-byte aligned.
+// `splits` = 0 picks the K split (cluster size) automatically.
+template <class Epi>
+cudaError_t gemm_tc(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, const Epi &epi,
+                    int splits, unsigned *status, cudaStream_t st);
+
+// CUDA cores (fp32 FMA): any K.
+template <class Epi>
+cudaError_t gemm_simt(const float *W, int N_out, int K, const float *X, int M_tok, const Epi &epi,
+                      cudaStream_t st);
+
+// ---------------------------------------------------------------- row kernels
+template <class T>
+cudaError_t gather_rmsnorm(const T *H, SelRows sel, int B, int d, const T *gamma, float eps, T *Xn,
+                           float *proxy_cache, const float *proxy_cur, int r, unsigned *status,
+                           cudaStream_t st);
+
+template <class T>
+cudaError_t rmsnorm_rows(const float *h1, int M, int d, const T *gamma, float eps, T *Xn2,
+                         cudaStream_t st);
+
+cudaError_t cosine_drift(const float *cur, const float *cached, float *drift, long rows, int r,
+                         cudaStream_t st);
+
+template <class T>
+cudaError_t pack_rows_rope(const T *src, T *dst, int rows, int cols, int hd, cudaStream_t st);
+
+template <class T>
+cudaError_t pack_rows_interleave(const T *a, const T *b, T *dst, int rows, int cols,
+                                 cudaStream_t st);
+
+cudaError_t rope_inv_freq(float *dst, int hd, float theta, cudaStream_t st);
+
+// ---------------------------------------------------------------- attention
+// A[m, h*hd:(h+1)*hd] = softmax(Q_h K_g^T / sqrt(hd)) V_g over all N rows of the
+// row's sequence, g = h / (n_q / n_kv); rows that are not live get zeros.
+template <class T>
+cudaError_t attention_simt(const T *Q, const T *Kc, const T *Vc, T *A, SelRows sel, int B,
+                           int n_q, int n_kv, int hd, cudaStream_t st);
+
+// ---------------------------------------------------------------- selection
+cudaError_t select_topk(const float *drift, const int32_t *forced, int F, int k, float min_drift,
+                        int32_t *idx, int32_t *count, int B, int N, cudaStream_t st);
+
+// ---------------------------------------------------------------- vocabulary
+size_t commit_ws_bytes(int B, int M, int V);
+cudaError_t commit_entropy(const float *logits, const uint8_t *valid, int B, int M, int V,
+                           float conf_thresh, float tau, int32_t *token, float *conf,
+                           float *entropy, float *max_entropy, int32_t *full_next, void *ws,
+                           cudaStream_t st);
+
+}  // namespace dllm

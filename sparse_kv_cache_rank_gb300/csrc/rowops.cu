@@ -1,0 +1,200 @@
+// rowops.cu -- per-row kernels of the refresh (SPA-Cache, "1. Update identification
+// via singular proxy" and "3. Sparse execution"): gather + RMSNorm of the selected
+// rows, RMSNorm of the attention residual, the cosine drift score, and the one-time
+// weight packing.  All of them are memory-bound row sweeps: one CTA (or warp) per
+// row, coalesced loads, shuffle reductions.
+#include "internal.h"
+
+namespace dllm {
+namespace {
+
+template <int NT>
+__device__ __forceinline__ float block_sum(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = 0.f;
+    if (threadIdx.x < 32) {
+        t = threadIdx.x < NT / 32 ? red[threadIdx.x] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (threadIdx.x == 0) red[32] = t;
+    }
+    __syncthreads();
+    return red[32];
+}
+
+// Xn[m] = RMSNorm(H[b, pos]) * gamma1 for the live selected rows, zeros otherwise;
+// proxy_cache[b, pos] <- proxy_cur[b, pos].
+template <class T>
+__global__ void __launch_bounds__(256) k_gather_rmsnorm(const T *__restrict__ H, SelRows sel, int d,
+                                                        const T *__restrict__ gamma, float eps,
+                                                        T *__restrict__ Xn, float *proxy_cache,
+                                                        const float *proxy_cur, int r,
+                                                        unsigned *status) {
+    __shared__ float red[33];
+    const int m = blockIdx.x;
+    int b, pos;
+    sel.locate(m, b, pos);
+    if (threadIdx.x == 0 && m % sel.k_max == 0 && sel.count[b] > sel.k_max)
+        raise_status(status, DLLM_STATUS_COUNT_CLAMP);
+    T *out = Xn + (size_t)m * d;
+    if (pos < 0) {
+        for (int e = threadIdx.x; e < d; e += 256) out[e] = from_f32<T>(0.f);
+        return;
+    }
+    const T *row = H + ((size_t)b * sel.N + pos) * d;
+    float ss = 0.f;
+    for (int e = threadIdx.x; e < d; e += 256) {
+        const float x = to_f32<T>(row[e]);
+        ss = fmaf(x, x, ss);
+    }
+    ss = block_sum<256>(ss, red);
+    const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+    for (int e = threadIdx.x; e < d; e += 256)
+        out[e] = from_f32<T>(to_f32<T>(row[e]) * inv * to_f32<T>(gamma[e]));
+    if (proxy_cache && proxy_cur) {
+        const size_t o = ((size_t)b * sel.N + pos) * r;
+        for (int e = threadIdx.x; e < r; e += 256) proxy_cache[o + e] = proxy_cur[o + e];
+    }
+}
+
+// Xn2[m] = RMSNorm(h1[m]) * gamma2 (h1 in fp32).
+template <class T>
+__global__ void __launch_bounds__(256) k_rmsnorm_rows(const float *__restrict__ h1, int d,
+                                                      const T *__restrict__ gamma, float eps,
+                                                      T *__restrict__ Xn2) {
+    __shared__ float red[33];
+    const float *row = h1 + (size_t)blockIdx.x * d;
+    float ss = 0.f;
+    for (int e = threadIdx.x; e < d; e += 256) ss = fmaf(row[e], row[e], ss);
+    ss = block_sum<256>(ss, red);
+    const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+    T *out = Xn2 + (size_t)blockIdx.x * d;
+    for (int e = threadIdx.x; e < d; e += 256) out[e] = from_f32<T>(row[e] * inv * to_f32<T>(gamma[e]));
+}
+
+// drift = 1 - cos(cur, cached), evaluated as |cur/|cur| - cached/|cached||^2 / 2, which
+// equals 1 - cos for unit vectors and keeps the small drifts of nearly unchanged rows
+// free of the cancellation in 1 - dot/norm.  Identical inputs give exactly 0; both
+// norms zero -> 0, one zero -> 1; clamped to [0, 2].  One warp per row.
+__global__ void __launch_bounds__(256) k_cosine_drift(const float *__restrict__ cur,
+                                                      const float *__restrict__ cached,
+                                                      float *__restrict__ drift, long rows, int r) {
+    const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const float *a = cur + row * r, *c = cached + row * r;
+    float na = 0.f, nc = 0.f;
+    for (int e = lane; e < r; e += 32) {
+        na = fmaf(a[e], a[e], na);
+        nc = fmaf(c[e], c[e], nc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        na += __shfl_xor_sync(0xffffffffu, na, o);
+        nc += __shfl_xor_sync(0xffffffffu, nc, o);
+    }
+    float out;
+    if (na == 0.f && nc == 0.f) {
+        out = 0.f;
+    } else if (na == 0.f || nc == 0.f) {
+        out = 1.f;
+    } else {
+        const float ia = 1.0f / sqrtf(na), ic = 1.0f / sqrtf(nc);
+        float s = 0.f;
+        for (int e = lane; e < r; e += 32) {
+            const float t = a[e] * ia - c[e] * ic;
+            s = fmaf(t, t, s);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        out = fminf(fmaxf(0.5f * s, 0.f), 2.f);
+    }
+    if (lane == 0) drift[row] = out;
+}
+
+// dst row (head h, p) = src row (head h, p even ? p/2 : p/2 + hd/2): rotary pairs adjacent.
+template <class T>
+__global__ void k_pack_rope(const T *__restrict__ src, T *__restrict__ dst, int cols, int hd) {
+    const int row = blockIdx.x;
+    const int h = row / hd, p = row - h * hd;
+    const int srow = h * hd + ((p & 1) ? (p >> 1) + hd / 2 : (p >> 1));
+    for (int e = threadIdx.x; e < cols; e += blockDim.x) dst[(size_t)row * cols + e] = src[(size_t)srow * cols + e];
+}
+
+// dst row 2j = a row j, dst row 2j+1 = b row j.
+template <class T>
+__global__ void k_pack_interleave(const T *__restrict__ a, const T *__restrict__ b,
+                                  T *__restrict__ dst, int cols) {
+    const int row = blockIdx.x;
+    const T *s = (row & 1) ? b : a;
+    const int j = row >> 1;
+    for (int e = threadIdx.x; e < cols; e += blockDim.x) dst[(size_t)row * cols + e] = s[(size_t)j * cols + e];
+}
+
+__global__ void k_rope_inv_freq(float *dst, int hd, float theta) {
+    const int i = threadIdx.x;
+    if (i < hd / 2) dst[i] = (float)pow((double)theta, -2.0 * (double)i / (double)hd);
+}
+
+}  // namespace
+
+template <class T>
+cudaError_t gather_rmsnorm(const T *H, SelRows sel, int B, int d, const T *gamma, float eps, T *Xn,
+                           float *proxy_cache, const float *proxy_cur, int r, unsigned *status,
+                           cudaStream_t st) {
+    const int M = B * sel.k_max;
+    if (M <= 0) return cudaSuccess;
+    k_gather_rmsnorm<T><<<M, 256, 0, st>>>(H, sel, d, gamma, eps, Xn, proxy_cache, proxy_cur, r, status);
+    return cudaGetLastError();
+}
+
+template <class T>
+cudaError_t rmsnorm_rows(const float *h1, int M, int d, const T *gamma, float eps, T *Xn2,
+                         cudaStream_t st) {
+    if (M <= 0) return cudaSuccess;
+    k_rmsnorm_rows<T><<<M, 256, 0, st>>>(h1, d, gamma, eps, Xn2);
+    return cudaGetLastError();
+}
+
+cudaError_t cosine_drift(const float *cur, const float *cached, float *drift, long rows, int r,
+                         cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    k_cosine_drift<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(cur, cached, drift, rows, r);
+    return cudaGetLastError();
+}
+
+template <class T>
+cudaError_t pack_rows_rope(const T *src, T *dst, int rows, int cols, int hd, cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    k_pack_rope<T><<<rows, 256, 0, st>>>(src, dst, cols, hd);
+    return cudaGetLastError();
+}
+
+template <class T>
+cudaError_t pack_rows_interleave(const T *a, const T *b, T *dst, int rows, int cols, cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    k_pack_interleave<T><<<2 * rows, 256, 0, st>>>(a, b, dst, cols);
+    return cudaGetLastError();
+}
+
+cudaError_t rope_inv_freq(float *dst, int hd, float theta, cudaStream_t st) {
+    k_rope_inv_freq<<<1, 128, 0, st>>>(dst, hd, theta);
+    return cudaGetLastError();
+}
+
+#define DLLM_ROWOPS(T)                                                                           \
+    template cudaError_t gather_rmsnorm<T>(const T *, SelRows, int, int, const T *, float, T *,  \
+                                           float *, const float *, int, unsigned *, cudaStream_t); \
+    template cudaError_t rmsnorm_rows<T>(const float *, int, int, const T *, float, T *,         \
+                                         cudaStream_t);                                          \
+    template cudaError_t pack_rows_rope<T>(const T *, T *, int, int, int, cudaStream_t);         \
+    template cudaError_t pack_rows_interleave<T>(const T *, const T *, T *, int, int, cudaStream_t);
+DLLM_ROWOPS(float)
+DLLM_ROWOPS(bf16)
+#undef DLLM_ROWOPS
+
+}  // namespace dllm

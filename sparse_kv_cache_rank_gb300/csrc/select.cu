@@ -1,0 +1,175 @@
+// select.cu -- per-sequence top-k of the drift scores (SPA-Cache, "1. Update
+// identification via singular proxy" and "2. Adaptive budget allocation") united
+// with the always-recomputed rows (EntropyCache, "How EntropyCache works", step 3).
+//
+// One CTA of 1024 threads per sequence, keys in shared memory.  The k-th largest
+// drift is found exactly by a 4-pass radix select on order-preserving 32-bit keys
+// (256-bin shared histograms); rows above it are taken, rows equal to it are taken
+// in index order until the budget is met (lower row index wins ties), and the union
+// with the forced rows is compacted in ascending order by a block-wide scan.
+#include "internal.h"
+
+namespace dllm {
+namespace {
+
+constexpr int kT = 1024;
+constexpr int kMaxN = 16384;
+
+// Exclusive block scan of one value per thread; returns the exclusive prefix and
+// writes the block total to *total.  All threads must call it.
+__device__ uint32_t block_scan(uint32_t v, uint32_t *wsum, uint32_t *total) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t w = wsum[lane];
+        uint32_t s = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        wsum[lane] = s - w;   // exclusive prefix of the warp totals
+        if (lane == 31) wsum[32] = s;
+    }
+    __syncthreads();
+    const uint32_t r = wsum[warp] + x - v;
+    *total = wsum[32];
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(kT) k_select_topk(const float *__restrict__ drift,
+                                                    const int32_t *__restrict__ forced, int F, int k,
+                                                    float min_drift, int32_t *__restrict__ idx,
+                                                    int32_t *__restrict__ count, int N) {
+    extern __shared__ uint32_t sm[];
+    uint32_t *key = sm;                                          // [N] 0 = not eligible
+    uint8_t *flag = reinterpret_cast<uint8_t *>(key + N);        // [N] 1 = forced
+    __shared__ uint32_t hist[256];
+    __shared__ uint32_t wsum[33];
+    __shared__ uint32_t sh_prefix, sh_rem;
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x;
+    const float *dr = drift + (size_t)b * N;
+
+    for (int i = tid; i < N; i += kT) flag[i] = 0;
+    __syncthreads();
+    if (forced)
+        for (int f = tid; f < F; f += kT) {
+            const int p = forced[(size_t)b * F + f];
+            if (p >= 0 && p < N) flag[p] = 1;
+        }
+    __syncthreads();
+
+    // contiguous chunk per thread keeps index order for the scans below
+    const int C = (N + kT - 1) / kT;
+    const int i0 = min(N, tid * C), i1 = min(N, i0 + C);
+    uint32_t nf = 0, ne = 0;
+    for (int i = i0; i < i1; ++i) {
+        uint32_t kk = 0;
+        const float x = dr[i];
+        if (flag[i]) {
+            ++nf;
+        } else if (x > min_drift) {   // false for NaN
+            const uint32_t u = __float_as_uint(x);
+            kk = (u & 0x80000000u) ? ~u : (u | 0x80000000u);   // order-preserving, > 0
+            ++ne;
+        }
+        key[i] = kk;
+    }
+    uint32_t tot_f, tot_e;
+    block_scan(nf, wsum, &tot_f);
+    block_scan(ne, wsum, &tot_e);
+    long long budget = (long long)N - tot_f;
+    if ((long long)k < budget) budget = k;
+    if (budget < 0) budget = 0;
+    const uint32_t take = (uint32_t)(budget < (long long)tot_e ? budget : (long long)tot_e);
+
+    // threshold T: take every key > T and the first `rem` keys == T (index order)
+    uint32_t T, rem;
+    if (take == 0) {
+        T = 0xFFFFFFFFu;
+        rem = 0;
+    } else if (take == tot_e) {
+        T = 0;
+        rem = 0;
+    } else {
+        uint32_t prefix = 0, mask = 0;
+        rem = take;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            for (int i = tid; i < 256; i += kT) hist[i] = 0;
+            __syncthreads();
+            for (int i = i0; i < i1; ++i) {
+                const uint32_t kk = key[i];
+                if (kk != 0 && (kk & mask) == prefix) atomicAdd(&hist[(kk >> shift) & 255u], 1u);
+            }
+            __syncthreads();
+            if (tid == 0) {
+                uint32_t cum = 0;
+                for (int dg = 255; dg >= 0; --dg) {
+                    const uint32_t h = hist[dg];
+                    if (cum + h >= rem) {
+                        sh_prefix = prefix | ((uint32_t)dg << shift);
+                        sh_rem = rem - cum;
+                        break;
+                    }
+                    cum += h;
+                }
+            }
+            __syncthreads();
+            prefix = sh_prefix;
+            rem = sh_rem;
+            mask |= 255u << shift;
+            __syncthreads();
+        }
+        T = prefix;
+    }
+
+    // rank of each key == T among equals, in index order
+    uint32_t neq = 0;
+    if (rem > 0)
+        for (int i = i0; i < i1; ++i) neq += (key[i] == T);
+    uint32_t tot_eq;
+    uint32_t eq_before = block_scan(neq, wsum, &tot_eq);
+    uint32_t nsel = 0;
+    for (int i = i0; i < i1; ++i) {
+        const uint32_t kk = key[i];
+        bool s = flag[i] != 0 || (kk != 0 && kk > T);
+        if (!s && rem > 0 && kk == T && kk != 0) {
+            s = eq_before < rem;
+            ++eq_before;
+        }
+        flag[i] = s ? 2 : 0;
+        nsel += s;
+    }
+    uint32_t total;
+    uint32_t out = block_scan(nsel, wsum, &total);
+    int32_t *row = idx + (size_t)b * N;
+    for (int i = i0; i < i1; ++i)
+        if (flag[i] == 2) row[out++] = i;
+    for (int i = (int)total + tid; i < N; i += kT) row[i] = -1;
+    if (tid == 0) count[b] = (int32_t)total;
+}
+
+}  // namespace
+
+cudaError_t select_topk(const float *drift, const int32_t *forced, int F, int k, float min_drift,
+                        int32_t *idx, int32_t *count, int B, int N, cudaStream_t st) {
+    if (B <= 0 || N <= 0) return cudaSuccess;
+    if (N > kMaxN) return cudaErrorInvalidValue;
+    const size_t smem = (size_t)N * 5;
+    cudaError_t e = cudaFuncSetAttribute(k_select_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    k_select_topk<<<B, kT, smem, st>>>(drift, forced, F, k, min_drift, idx, count, N);
+    return cudaGetLastError();
+}
+
+}  // namespace dllm

@@ -1,0 +1,198 @@
+// vocab.cu -- the vocabulary-side decision (EntropyCache, "How EntropyCache works",
+// steps 2-3; TSPD "Input features"; Polestar "1. Problem definition").
+//
+// Pass 1 streams each logit row once (one CTA per row slice) and keeps, per thread,
+// the running state of the row's softmax in a single sweep:
+//   m = max logit, a = its lowest index, s = sum e^(l - m), t = sum (l - m) e^(l - m),
+// so that p_max = 1/s and entropy = -sum p ln p = ln s - t/s.  States merge exactly
+// under a change of reference maximum m -> M:  s' = s e^(m-M), t' = e^(m-M)(t + (m-M) s).
+// Pass 2 (one CTA per sequence) merges the slices of each row and applies the commit
+// rule and the full-refresh decision.
+#include <cfloat>
+
+#include "internal.h"
+
+namespace dllm {
+namespace {
+
+struct RowState {
+    float m, s, t;
+    int a;
+};
+
+__device__ __forceinline__ RowState merge(RowState x, RowState y) {
+    if (y.s == 0.f) return x;
+    if (x.s == 0.f) return y;
+    RowState r;
+    if (y.m > x.m || (y.m == x.m && y.a < x.a)) {
+        RowState tmp = x;
+        x = y;
+        y = tmp;
+    }
+    // x holds the larger maximum (lower index on equal maxima)
+    const float c = expf(y.m - x.m);
+    r.m = x.m;
+    r.a = x.a;
+    r.s = x.s + y.s * c;
+    r.t = x.t + c * (y.t + (y.m - x.m) * y.s);
+    return r;
+}
+
+constexpr int kT1 = 256;
+
+__global__ void __launch_bounds__(kT1) k_row_stats(const float *__restrict__ logits,
+                                                   const uint8_t *__restrict__ valid, int V,
+                                                   int slices, RowState *__restrict__ part) {
+    const int row = blockIdx.y, sl = blockIdx.x;
+    if (!valid[row]) return;
+    const int chunk = (V + slices - 1) / slices;
+    const int v0 = sl * chunk, v1 = min(V, v0 + chunk);
+    const float *l = logits + (size_t)row * V;
+    RowState st{-INFINITY, 0.f, 0.f, INT_MAX};
+    for (int v = v0 + threadIdx.x; v < v1; v += kT1) {
+        const float x = l[v];
+        if (st.s == 0.f) {
+            st = RowState{x, 1.f, 0.f, v};
+        } else if (x > st.m) {
+            const float c = expf(st.m - x);
+            st.t = c * (st.t + (st.m - x) * st.s);
+            st.s = st.s * c + 1.f;
+            st.m = x;
+            st.a = v;
+        } else {
+            const float e = expf(x - st.m);
+            st.s += e;
+            st.t = fmaf(x - st.m, e, st.t);
+        }
+    }
+    // warp then block merge
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        RowState y;
+        y.m = __shfl_xor_sync(0xffffffffu, st.m, o);
+        y.s = __shfl_xor_sync(0xffffffffu, st.s, o);
+        y.t = __shfl_xor_sync(0xffffffffu, st.t, o);
+        y.a = __shfl_xor_sync(0xffffffffu, st.a, o);
+        st = merge(st, y);
+    }
+    __shared__ RowState ws[kT1 / 32];
+    if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = st;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        RowState r = ws[0];
+        for (int w = 1; w < kT1 / 32; ++w) r = merge(r, ws[w]);
+        part[(size_t)row * slices + sl] = r;
+    }
+}
+
+// One CTA per sequence, thread m = row m of the block of candidates.
+__global__ void __launch_bounds__(1024) k_commit(const RowState *__restrict__ part, int slices,
+                                                 const uint8_t *__restrict__ valid, int M,
+                                                 float conf_thresh, float tau, int32_t *token,
+                                                 float *conf, float *entropy, float *max_entropy,
+                                                 int32_t *full_next) {
+    const int b = blockIdx.x, m = threadIdx.x;
+    __shared__ float s_conf[32];
+    __shared__ int s_row[32];
+    __shared__ unsigned s_emax;
+    if (m == 0) s_emax = 0u;
+    const bool live = m < M && valid[(size_t)b * M + m];
+    float p = 0.f, H = 0.f;
+    int am = -1;
+    if (live) {
+        const RowState *ps = part + ((size_t)b * M + m) * slices;
+        RowState r = ps[0];
+        for (int i = 1; i < slices; ++i) r = merge(r, ps[i]);
+        p = 1.0f / r.s;
+        H = fmaxf(logf(r.s) - r.t / r.s, 0.f);
+        am = r.a;
+    }
+    if (m < M) {
+        conf[(size_t)b * M + m] = p;
+        entropy[(size_t)b * M + m] = H;
+    }
+    const bool pass = live && p >= conf_thresh;
+    const int any = __syncthreads_or(pass);
+    // highest confidence among live rows, lowest row on ties (used when none passes)
+    float bc = live ? p : -1.f;
+    int br = live ? m : INT_MAX;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float oc = __shfl_xor_sync(0xffffffffu, bc, o);
+        const int orow = __shfl_xor_sync(0xffffffffu, br, o);
+        if (oc > bc || (oc == bc && orow < br)) {
+            bc = oc;
+            br = orow;
+        }
+    }
+    if ((m & 31) == 0) {
+        s_conf[m >> 5] = bc;
+        s_row[m >> 5] = br;
+    }
+    __syncthreads();
+    if (m < 32) {
+        const int nw = (blockDim.x + 31) / 32;
+        bc = m < nw ? s_conf[m] : -1.f;
+        br = m < nw ? s_row[m] : INT_MAX;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float oc = __shfl_xor_sync(0xffffffffu, bc, o);
+            const int orow = __shfl_xor_sync(0xffffffffu, br, o);
+            if (oc > bc || (oc == bc && orow < br)) {
+                bc = oc;
+                br = orow;
+            }
+        }
+        if (m == 0) s_row[0] = bc >= 0.f ? br : -1;
+    }
+    __syncthreads();
+    const bool commit = any ? pass : (live && m == s_row[0]);
+    if (m < M) token[(size_t)b * M + m] = commit ? am : -1;
+    if (commit) atomicMax(&s_emax, __float_as_uint(H));   // H >= 0: bit order = value order
+    __syncthreads();
+    if (m == 0) {
+        const float E = __uint_as_float(s_emax);
+        max_entropy[b] = E;
+        full_next[b] = E > tau ? 1 : 0;
+    }
+}
+
+int slices_for(int rows, int V) {
+    const int sms = num_sms();
+    int s = (2 * sms + rows - 1) / (rows > 0 ? rows : 1);
+    const int cap = (V + 2047) / 2048;
+    if (s > cap) s = cap;
+    return s < 1 ? 1 : s;
+}
+
+}  // namespace
+
+size_t commit_ws_bytes(int B, int M, int V) {
+    const int rows = B * M;
+    return (size_t)rows * slices_for(rows, V) * sizeof(RowState);
+}
+
+cudaError_t commit_entropy(const float *logits, const uint8_t *valid, int B, int M, int V,
+                           float conf_thresh, float tau, int32_t *token, float *conf,
+                           float *entropy, float *max_entropy, int32_t *full_next, void *ws,
+                           cudaStream_t st) {
+    if (B <= 0) return cudaSuccess;
+    const int rows = B * M;
+    RowState *part = reinterpret_cast<RowState *>(ws);
+    if (rows > 0) {
+        const int slices = slices_for(rows, V);
+        k_row_stats<<<dim3(slices, rows), kT1, 0, st>>>(logits, valid, V, slices, part);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        const int threads = ((M + 31) / 32) * 32;
+        k_commit<<<B, threads, 0, st>>>(part, slices, valid, M, conf_thresh, tau, token, conf, entropy,
+                                        max_entropy, full_next);
+    } else {
+        const int threads = 32;
+        k_commit<<<B, threads, 0, st>>>(part, 1, valid, 0, conf_thresh, tau, token, conf, entropy,
+                                        max_entropy, full_next);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace dllm

@@ -1,0 +1,233 @@
+"""GPU-vs-oracle parity through the C ABI (via the thin torch binding).
+
+Sets and tokens: bit-exact when both sides decide on the same fp32 values (the GPU's
+drift / confidence fed to the oracle's rule), and within the 1e-5 near-tie band
+against the oracle's own scores.  fp32 reductions: 1e-4 relative.  Layer outputs:
+bf16 max-relative error <= 2e-2 with cosine >= 0.999; fp32 <= 1e-4.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+from sparse_kv_cache_rank_gb300 import synth
+from cases import (assert_close_layer, assert_drift_close, check_selection_band, forced_rows,
+                   layer_case, normwise_rel, to_dev, to_np, torch_dtype, FP32_REDUCTION_RTOL)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from sparse_kv_cache_rank_gb300 import binding
+    binding.lib()
+    binding.check_status(reset=True)
+    return binding
+
+
+# shapes: several tiles and ragged tails on every axis the kernels tile
+SMALL_BF16 = synth.LayerShape("small-bf16-gqa", B=2, N=200, d=256, n_q=4, n_kv=2, hd=64, F=320,
+                              r=64, rho=0.25, dtype="bf16", prompt=100, k_recent=4)
+MID_BF16 = synth.LayerShape("mid-bf16-hd128", B=1, N=333, d=512, n_q=4, n_kv=4, hd=128, F=704,
+                            r=128, rho=0.3, dtype="bf16", prompt=200)
+TINY_BF16 = dataclasses.replace(synth.TINY, name="tiny-bf16", dtype="bf16")
+
+
+# --------------------------------------------------------------------------- proxy
+@pytest.mark.parametrize("shape", [synth.TINY, TINY_BF16, SMALL_BF16, MID_BF16], ids=lambda s: s.name)
+def test_proxy_score_parity(B, orc, shape):
+    c = layer_case(orc, shape, 10)
+    dt = torch_dtype(shape)
+    cur, drift = B.dllm_proxy_score(to_dev(c.H_cur, dt), to_dev(c.P.T.copy(), dt), to_dev(c.pc0))
+    torch.cuda.synchronize()
+    cur_o, drift_o = orc.proxy_score(c.H_cur, c.P, c.pc0)
+    assert normwise_rel(to_np(cur), cur_o) < FP32_REDUCTION_RTOL
+    assert_drift_close(to_np(drift), drift_o)
+
+
+def test_proxy_identical_inputs_zero_drift(B, orc):
+    c = layer_case(orc, SMALL_BF16, 11)
+    H = to_dev(c.H_prev, torch.bfloat16)
+    Pt = to_dev(c.P.T.copy(), torch.bfloat16)
+    cur, _ = B.dllm_proxy_score(H, Pt, torch.ones((2, 200, 64), device="cuda"))
+    _, drift = B.dllm_proxy_score(H, Pt, cur.clone())
+    assert (drift == 0).all().item()
+
+
+@pytest.mark.parametrize("N", [1024, 4096])
+def test_proxy_llada_width(B, orc, N):
+    """LLaDA-8B width (d = 4096, r = 128) over N rows; oracle on every row."""
+    g = synth.rng(12)
+    d, r = 4096, 128
+    H0 = synth.round_bf16(g.standard_normal((1, N, d), dtype=np.float32))
+    H1 = synth.round_bf16(H0 + g.standard_normal((1, N, d), dtype=np.float32) * np.float32(0.05))
+    P = synth.round_bf16((g.standard_normal((d, r)) * 0.02).astype(np.float32))
+    pc, _ = orc.proxy_score(H0, P, np.ones((1, N, r), np.float32))
+    cur, drift = B.dllm_proxy_score(to_dev(H1, torch.bfloat16), to_dev(P.T.copy(), torch.bfloat16),
+                                    to_dev(pc))
+    cur_o, drift_o = orc.proxy_score(H1, P, pc)
+    assert normwise_rel(to_np(cur), cur_o) < FP32_REDUCTION_RTOL
+    assert_drift_close(to_np(drift), drift_o)
+
+
+# --------------------------------------------------------------------------- selection
+@pytest.mark.parametrize("Bq,N,k,F,ties", [(1, 1, 1, 0, False), (3, 37, 5, 3, True),
+                                            (2, 1024, 164, 0, False), (1, 1024, 164, 40, True),
+                                            (4, 5000, 800, 17, True), (1, 16384, 2000, 64, False),
+                                            (2, 300, 0, 8, False), (2, 300, 400, 8, False)])
+def test_select_bit_exact(B, orc, Bq, N, k, F, ties):
+    g = synth.rng(1000 + N + k)
+    if ties:
+        drift = g.choice(np.array([0, 1e-7, 1e-3, 2e-3, 0.1, 0.1, 0.5], np.float32), size=(Bq, N))
+    else:
+        drift = (g.random((Bq, N)) ** 3).astype(np.float32)
+    forced = g.integers(-3, N + 3, size=(Bq, F)).astype(np.int32) if F else None
+    idx, cnt = B.dllm_select_topk(to_dev(drift), to_dev(forced) if F else None, k)
+    idx_o, cnt_o = orc.select_topk(drift, forced, k)
+    np.testing.assert_array_equal(to_np(cnt), cnt_o)
+    np.testing.assert_array_equal(to_np(idx), idx_o)
+
+
+def test_select_degenerate(B, orc):
+    z = np.zeros((2, 64), np.float32)
+    idx, cnt = B.dllm_select_topk(to_dev(z), None, 10)
+    assert (to_np(cnt) == 0).all() and (to_np(idx) == -1).all()
+    nan = np.full((1, 64), np.nan, np.float32)
+    nan[0, 9] = 0.3
+    idx, cnt = B.dllm_select_topk(to_dev(nan), None, 10)
+    assert to_np(cnt)[0] == 1 and to_np(idx)[0, 0] == 9
+
+
+# --------------------------------------------------------------------------- refresh
+def _step(B, orc, c, k, forced, out_mask=None, full=False):
+    """One step on the GPU and on the oracle; returns everything to compare."""
+    sh = c.shape
+    dt = torch_dtype(sh)
+    Bn, N = sh.B, sh.N
+    H = to_dev(c.H_cur, dt)
+    pc = to_dev(c.pc0)
+    cur, drift = B.dllm_proxy_score(H, to_dev(c.P.T.copy(), dt), pc)
+    fo = to_dev(forced) if forced is not None else None
+    idx, cnt = B.dllm_select_topk(drift, fo, k)
+    k_max = min(N, k + (0 if forced is None else forced.shape[1]))
+    layer = B.dllm_pack_layer({n: to_dev(v, dt) for n, v in c.w.items()}, sh.n_q, sh.n_kv, sh.hd,
+                              eps=sh.eps, rope_theta=sh.rope_theta)
+    K = to_dev(c.K0, dt)
+    V = to_dev(c.V0, dt)
+    O = to_dev(c.O0, dt)
+    B.dllm_sparse_layer_refresh(layer, H, idx, cnt, k_max, K, V, O, pc, cur)
+    torch.cuda.synchronize()
+    assert B.check_status() == 0
+    g = dict(cur=to_np(cur), drift=to_np(drift), idx=to_np(idx), cnt=to_np(cnt), K=to_np(K),
+             V=to_np(V), O=to_np(O), pc=to_np(pc))
+    # oracle: proxy and drift on its own; the selection is taken on the GPU's drift
+    # (same fp32 values -> same decision) and must match bit for bit
+    cur_o, drift_o = orc.proxy_score(c.H_cur, c.P, c.pc0)
+    idx_o, cnt_o = orc.select_topk(g["drift"], forced, k)
+    L = orc.Layer(c.w, sh.n_q, sh.n_kv, sh.hd, eps=sh.eps, rope_theta=sh.rope_theta)
+    Ko, Vo, Oo, pco = c.K0.copy(), c.V0.copy(), c.O0.copy(), c.pc0.copy()
+    orc.layer_refresh(L, c.H_cur, idx_o, cnt_o, Ko, Vo, Oo, pco, g["cur"], out_mask=out_mask)
+    o = dict(cur=cur_o, drift=drift_o, idx=idx_o, cnt=cnt_o, K=Ko, V=Vo, O=Oo, pc=pco)
+    return g, o
+
+
+def _compare_step(c, g, o, forced, k, out_mask=None):
+    sh = c.shape
+    np.testing.assert_array_equal(g["cnt"], o["cnt"])
+    np.testing.assert_array_equal(g["idx"], o["idx"])
+    assert_drift_close(g["drift"], o["drift"])
+    check_selection_band(g["idx"], g["cnt"], o["drift"], forced, k)
+    for b in range(sh.B):
+        I = g["idx"][b, :g["cnt"][b]]
+        rest = np.setdiff1d(np.arange(sh.N), I)
+        # untouched rows keep their exact bits
+        for name, ref in (("K", c.K0), ("V", c.V0), ("O", c.O0), ("pc", c.pc0)):
+            np.testing.assert_array_equal(g[name][b, rest], ref[b, rest], err_msg=name)
+        np.testing.assert_array_equal(g["pc"][b, I], g["cur"][b, I])
+        assert_close_layer(g["K"][b, I], o["K"][b, I], sh.dtype, f"K b={b}")
+        assert_close_layer(g["V"][b, I], o["V"][b, I], sh.dtype, f"V b={b}")
+        rows = I if out_mask is None else I[out_mask[b, I] != 0]
+        assert_close_layer(g["O"][b, rows], o["O"][b, rows], sh.dtype, f"H_out b={b}")
+        # the update itself (output minus input), not only the residual stream
+        assert_close_layer(g["O"][b, rows] - c.H_cur[b, rows], o["O"][b, rows] - c.H_cur[b, rows],
+                           sh.dtype, f"H_out - H_in b={b}")
+
+
+@pytest.mark.parametrize("shape", [synth.TINY, TINY_BF16, SMALL_BF16, MID_BF16], ids=lambda s: s.name)
+def test_refresh_step_parity(B, orc, shape):
+    c = layer_case(orc, shape, 20)
+    forced = forced_rows(shape, 21) if shape.k_recent else None
+    k = orc.budget(shape.rho, shape.N)
+    g, o = _step(B, orc, c, k, forced)
+    _compare_step(c, g, o, forced, k)
+
+
+@pytest.mark.parametrize("shape", [synth.TINY, SMALL_BF16], ids=lambda s: s.name)
+def test_full_selection_is_full_recompute(B, orc, shape):
+    """Selecting every row from stale caches equals the oracle's dense forward on H_t."""
+    c = layer_case(orc, shape, 30)
+    g, _ = _step(B, orc, c, shape.N, None)
+    assert (g["cnt"] == shape.N).all()
+    L = orc.Layer(c.w, shape.n_q, shape.n_kv, shape.hd, eps=shape.eps, rope_theta=shape.rope_theta)
+    Kf, Vf, Of = orc.layer_full(L, c.H_cur)
+    assert_close_layer(g["K"], Kf, shape.dtype, "K")
+    assert_close_layer(g["V"], Vf, shape.dtype, "V")
+    assert_close_layer(g["O"], Of, shape.dtype, "H_out")
+
+
+def test_refresh_llada_layer_sampled(B, orc):
+    """LLaDA-8B-shaped layer at full size (N=1024, d=4096, 32x128, F=12288, 16%):
+    K/V of every selected row, layer outputs of 12 sampled selected rows."""
+    sh = synth.LLADA_LAYER
+    c = layer_case(orc, sh, 40, consistent=False, svd_proxy=False)
+    k = orc.budget(sh.rho, sh.N)
+    assert k == 164
+    # the oracle needs the selection before it can sample: take it from a GPU proxy pass
+    H = to_dev(c.H_cur, torch.bfloat16)
+    _, drift = B.dllm_proxy_score(H, to_dev(c.P.T.copy(), torch.bfloat16), to_dev(c.pc0))
+    idx, cnt = B.dllm_select_topk(drift, None, k)
+    I = to_np(idx)[0, :to_np(cnt)[0]]
+    mask = np.zeros((1, sh.N), np.uint8)
+    mask[0, I[synth.rng(41).permutation(len(I))[:12]]] = 1
+    g, o = _step(B, orc, c, k, None, out_mask=mask)
+    _compare_step(c, g, o, None, k, out_mask=mask)
+    # every strongly perturbed row is in the selection
+    assert set(c.hot[0].tolist()) <= set(g["idx"][0, :g["cnt"][0]].tolist())
+
+
+# --------------------------------------------------------------------------- vocabulary
+@pytest.mark.parametrize("Bq,M,V,scale", [(1, 24, 4096, 1.0), (1, 24, 4096, 10.0),
+                                          (2, 32, 126464, 0.43), (8, 32, 152064, 0.43),
+                                          (3, 5, 7, 1.0), (1, 1000, 64, 4.0)])
+def test_commit_entropy_parity(B, orc, Bq, M, V, scale):
+    logits = synth.commit_logits(Bq, M, V, 50 + M, std=3.0 * scale)
+    valid = np.ones((Bq, M), np.uint8)
+    valid[-1, ::3] = 0
+    tok, conf, ent, E, full = B.dllm_commit_entropy(to_dev(logits), to_dev(valid))
+    torch.cuda.synchronize()
+    am_o, pm_o, H_o = orc.vocab_stats(logits)
+    v = valid.astype(bool)
+    conf, ent = to_np(conf), to_np(ent)
+    np.testing.assert_allclose(conf[v], pm_o[v], rtol=FP32_REDUCTION_RTOL, atol=1e-9)
+    np.testing.assert_allclose(ent[v], H_o[v], rtol=FP32_REDUCTION_RTOL, atol=1e-6)
+    assert (conf[~v] == 0).all() and (ent[~v] == 0).all()
+    # the rule on the GPU's own fp32 statistics must give the same tokens bit for bit
+    t_o, E_o, f_o = orc.commit_rule(am_o, conf, ent, valid)
+    np.testing.assert_array_equal(to_np(tok), t_o)
+    np.testing.assert_array_equal(to_np(E), E_o)
+    np.testing.assert_array_equal(to_np(full), f_o)
+    # and against the oracle's own statistics, away from the threshold
+    t_r, _, _ = orc.commit_rule(am_o, pm_o, H_o, valid)
+    near = np.abs(pm_o - 0.9) < 1e-5
+    same = (to_np(tok) == t_r) | near
+    assert same.all()
+
+
+def test_commit_no_valid_rows(B):
+    logits = torch.zeros((2, 4, 16), device="cuda")
+    valid = torch.zeros((2, 4), dtype=torch.uint8, device="cuda")
+    tok, conf, ent, E, full = B.dllm_commit_entropy(logits, valid)
+    assert (tok == -1).all().item() and (E == 0).all().item() and (full == 0).all().item()
