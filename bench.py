@@ -1,0 +1,432 @@
+#!/usr/bin/env python3
+"""Throughput of the sparse KV-cache refresh step on GB300.
+
+One step (the "layer" workload, LLaDA-8B-shaped layer: B=1, N=1024, d=4096,
+32 MHA heads x 128, SwiGLU 12288, proxy rank 128, update ratio 16% -> k=164):
+    dllm_proxy_score   singular proxy + cosine drift of every row
+    dllm_select_topk   top-k drifted rows
+    dllm_sparse_layer_refresh   gather/RMSNorm, QKV + rotary + KV scatter, attention
+                       over the full cache, O + residual, RMSNorm, SwiGLU, down + scatter
+on resident inputs; consecutive steps alternate between two drifted inputs so that
+every step selects k rows (a refreshed row's cached proxy is the one it was refreshed
+with).  The weights (436 MB) exceed the 129 MB L2, so no L2 flush is needed.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+Under torchrun every rank runs an independent replica (weak scaling, no collective on
+the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse-refresh denoise steps/s & tokens/s (LLaDA-8B shape); % of roofline"
+UNIT = "steps/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="approximate budget of the CPU-oracle sample")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), float(j.get("bf16_tflops_sustained", j["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# --------------------------------------------------------------------------- clocks
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- work model
+def layer_kernel_work(sh, M):
+    """Algorithmic bytes and FLOPs of each kernel of one layer step with M refreshed rows
+    (weights and caches counted once, bf16 = 2 bytes, fp32 = 4)."""
+    B, N, d, r, F = sh.B, sh.N, sh.d, sh.r, sh.F
+    dq, dkv = sh.d_q, sh.d_kv
+    return {
+        "proxy_gemm": (2 * B * N * d + 2 * r * d + 4 * B * N * r, 2 * B * N * d * r),
+        "cosine": (8 * B * N * r + 4 * B * N, 0),
+        "select": (4 * B * N + 4 * B * N + 4 * B, 0),
+        "gather": (2 * M * d * 2 + 8 * M * r, 0),
+        "qkv": (2 * (dq + 2 * dkv) * d + 2 * M * d + 2 * M * (dq + 2 * dkv), 2 * M * d * (dq + 2 * dkv)),
+        "attention": (2 * M * dq * 2 + 2 * B * N * 2 * dkv, 4 * M * N * dq),
+        "oproj": (2 * d * dq + 2 * M * dq + 2 * M * d + 4 * M * d, 2 * M * dq * d),
+        "rmsnorm2": (4 * M * d + 2 * M * d, 0),
+        "gateup": (2 * 2 * F * d + 2 * M * d + 2 * M * F, 2 * M * d * 2 * F),
+        "down": (2 * d * F + 2 * M * F + 4 * M * d + 2 * M * d, 2 * M * F * d),
+    }
+
+
+# --------------------------------------------------------------------------- native arm
+class LayerWorkload:
+    def __init__(self, sh, seed, dev):
+        import torch
+        from sparse_kv_cache_rank_gb300 import binding as B
+        self.B_ = B
+        self.sh = sh
+        self.dev = dev
+        bf = torch.bfloat16
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed)
+
+        def randn(*shape, std=1.0):
+            return torch.randn(shape, generator=gen, device=dev, dtype=torch.float32) * std
+
+        d, dq, dkv, F = sh.d, sh.d_q, sh.d_kv, sh.F
+        w = {"w_q": randn(dq, d, std=0.02).to(bf), "w_k": randn(dkv, d, std=0.02).to(bf),
+             "w_v": randn(dkv, d, std=0.02).to(bf), "w_o": randn(d, dq, std=0.02).to(bf),
+             "w_g": randn(F, d, std=0.02).to(bf), "w_u": randn(F, d, std=0.02).to(bf),
+             "w_d": randn(d, F, std=0.02).to(bf),
+             "gamma1": torch.ones(d, device=dev, dtype=bf), "gamma2": torch.ones(d, device=dev, dtype=bf)}
+        self.w = w
+        self.layer = B.dllm_pack_layer(w, sh.n_q, sh.n_kv, sh.hd, eps=sh.eps, rope_theta=sh.rope_theta)
+        self.Pt = B.build_proxy_matrix(w["w_v"], w["gamma1"], sh.r)
+        Bn, N = sh.B, sh.N
+        H_prev = randn(Bn, N, d)
+        n_hot = int(round(0.1 * N))
+
+        def drifted(base):
+            h = base + randn(Bn, N, d, std=0.05)
+            for b in range(Bn):
+                rows = torch.randperm(N, generator=gen, device=dev)[:n_hot]
+                h[b, rows] += randn(n_hot, d, std=0.5)
+            return h.to(bf).contiguous()
+
+        self.H = [drifted(H_prev), None]
+        self.H[1] = drifted(self.H[0].float())
+        H_prev = H_prev.to(bf).contiguous()
+        # caches: a full refresh (every row selected) on the previous step's input
+        self.K = torch.empty((Bn, N, sh.n_kv, sh.hd), device=dev, dtype=bf)
+        self.V = torch.empty_like(self.K)
+        self.O = torch.empty((Bn, N, d), device=dev, dtype=bf)
+        idx_all = torch.arange(N, device=dev, dtype=torch.int32).repeat(Bn, 1).contiguous()
+        cnt_all = torch.full((Bn,), N, device=dev, dtype=torch.int32)
+        B.dllm_sparse_layer_refresh(self.layer, H_prev, idx_all, cnt_all, N, self.K, self.V, self.O)
+        self.pc = torch.empty((Bn, N, sh.r), device=dev, dtype=torch.float32)
+        ones = torch.ones_like(self.pc)
+        B.dllm_proxy_score(H_prev, self.Pt, ones, proxy_cur=self.pc, drift=torch.empty((Bn, N), device=dev))
+        self.cur = torch.empty_like(self.pc)
+        self.drift = torch.empty((Bn, N), device=dev, dtype=torch.float32)
+        self.idx = torch.empty((Bn, N), device=dev, dtype=torch.int32)
+        self.cnt = torch.empty((Bn,), device=dev, dtype=torch.int32)
+        self.k = B.dllm_layer_budget(sh.rho, N)
+        need = B.dllm_refresh_workspace_bytes(self.layer, Bn, N, self.k)
+        self.ws = torch.empty(need, device=dev, dtype=torch.uint8)
+        self.H_prev = H_prev
+        self.s = 0
+        torch.cuda.synchronize(dev)
+
+    def step(self, H=None):
+        B = self.B_
+        if H is None:
+            H = self.H[self.s & 1]
+        self.s += 1
+        B.dllm_proxy_score(H, self.Pt, self.pc, proxy_cur=self.cur, drift=self.drift)
+        B.dllm_select_topk(self.drift, None, self.k, idx=self.idx, count=self.cnt)
+        B.dllm_sparse_layer_refresh(self.layer, H, self.idx, self.cnt, self.k, self.K, self.V, self.O,
+                                    self.pc, self.cur, ws=self.ws)
+
+
+def native(args):
+    import torch
+    import torch.distributed as dist
+    from sparse_kv_cache_rank_gb300 import binding as B
+    from sparse_kv_cache_rank_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    sh = synth.LLADA_LAYER
+    wl = LayerWorkload(sh, 1234 + rank, dev)
+    for _ in range(max(args.warmup, 3)):
+        wl.step()
+    torch.cuda.synchronize(dev)
+    B.check_status()
+    M = int(wl.cnt.sum().item())
+
+    # per-kernel breakdown (outside the timed region)
+    work = layer_kernel_work(sh, M)
+    per_kernel = {}
+    for name in work:
+        B.dllm_timer_start(name, 8)
+        for _ in range(4):
+            wl.step()
+        ms, n = B.dllm_timer_stop()
+        per_kernel[name] = ms / max(n, 1)
+    dominant = max(per_kernel, key=per_kernel.get)
+
+    # timed region
+    clocks = Clocks(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = B.dllm_launch_count()
+    B.dllm_timer_start(dominant, args.steps)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        wl.step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    dom_ms, dom_n = B.dllm_timer_stop()
+    launches = B.dllm_launch_count() - launches0
+    barrier()
+    clk = clocks.stop()
+    elapsed = e0.elapsed_time(e1) / 1e3
+    B.check_status()
+
+    # end to end through the same calls with host buffers: H2D of the step's input,
+    # D2H of the selection (the step's result) inside the timed region
+    Hh = [wl.H[0].cpu().pin_memory(), wl.H[1].cpu().pin_memory()]
+    Hd = torch.empty_like(wl.H[0])
+    idx_h = torch.empty(wl.idx.shape, dtype=torch.int32).pin_memory()
+    cnt_h = torch.empty(wl.cnt.shape, dtype=torch.int32).pin_memory()
+    for s in range(2):
+        Hd.copy_(Hh[s & 1], non_blocking=True)
+        wl.step(Hd)
+    torch.cuda.synchronize(dev)
+    barrier()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record()
+    for s in range(args.steps):
+        Hd.copy_(Hh[s & 1], non_blocking=True)
+        wl.step(Hd)
+        idx_h.copy_(wl.idx, non_blocking=True)
+        cnt_h.copy_(wl.cnt, non_blocking=True)
+    f1.record()
+    torch.cuda.synchronize(dev)
+    e2e_elapsed = f0.elapsed_time(f1) / 1e3
+    barrier()
+
+    t = torch.tensor([elapsed, e2e_elapsed], device=dev, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    elapsed, e2e_elapsed = float(t[0]), float(t[1])
+
+    bw, tc, tc_sus, src = peaks()
+    dom_bytes, dom_flops = work[dominant]
+    dom_s = dom_ms / 1e3 / max(dom_n, 1)
+    if dom_flops / (tc * 1e12) > dom_bytes / (bw * 1e9):
+        roof = {"bound": "tensor", "achieved": dom_flops / dom_s / 1e12, "peak": tc_sus, "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": dom_bytes / dom_s / 1e9, "peak": bw, "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = dominant
+    roof["peak_source"] = src
+    step_roof_s = sum(max(b / (bw * 1e9), f / (tc * 1e12)) for b, f in work.values())
+    steps_per_s = world * args.steps / elapsed
+    result = {
+        "metric": METRIC, "value": steps_per_s, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded random-init weights N(0,0.02), drift model: 10% rows +N(0,0.5), all +N(0,0.05))",
+        "config": {"workload": f"llada8b-layer B={sh.B} N={sh.N} d={sh.d} heads={sh.n_q}x{sh.hd} F={sh.F} "
+                               f"r={sh.r} rho={sh.rho} k={wl.k}",
+                   "l2": "inputs larger than L2 (436 MB of weights per step)",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": steps_per_s * sh.B * sh.N,
+        "refreshed_rows_per_s": steps_per_s * M,
+        "rows_per_step": M,
+        "roofline": roof,
+        "step_roofline_frac": step_roof_s / (elapsed / args.steps),
+        "kernel_ms": {k: round(v, 5) for k, v in per_kernel.items()},
+        "e2e": {"value": world * args.steps / e2e_elapsed, "unit": UNIT,
+                "h2d_bytes_per_step": int(wl.H[0].numel() * 2),
+                "d2h_bytes_per_step": int(wl.idx.numel() * 4 + wl.cnt.numel() * 4)},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+# --------------------------------------------------------------------------- oracle legs
+def _oracle_sample_inputs(wl):
+    """Host copies of one resident step's inputs (identical values to the GPU leg)."""
+    import torch
+    f = lambda t: t.float().cpu().numpy()
+    sh = wl.sh
+    w = {k: f(v) for k, v in wl.w.items()}
+    return dict(w=w, P=np.ascontiguousarray(f(wl.Pt).T), H=f(wl.H[0]), pc=f(wl.pc),
+                K=f(wl.K).reshape(sh.B, sh.N, sh.d_kv), V=f(wl.V).reshape(sh.B, sh.N, sh.d_kv),
+                O=f(wl.O))
+
+
+def _oracle_step_sample(orc, sh, inp, frac):
+    """A fraction `frac` of one layer step on the oracle: proxy + drift of frac*N rows,
+    selection over the whole sequence, refresh of frac*k rows (both linear in rows)."""
+    n_rows = max(1, int(round(frac * sh.N)))
+    cur, drift = orc.proxy_score(inp["H"][:, :n_rows], inp["P"], inp["pc"][:, :n_rows])
+    k = orc.budget(sh.rho, sh.N)
+    d_full = np.zeros((sh.B, sh.N), np.float32)
+    d_full[:, :n_rows] = drift
+    idx, cnt = orc.select_topk(d_full, None, k)
+    n_sel = max(1, int(round(frac * k)))
+    idx_s = np.full_like(idx, -1)
+    idx_s[:, :n_sel] = np.arange(n_sel, dtype=np.int32)[None] * max(1, sh.N // n_sel)
+    cnt_s = np.full(sh.B, n_sel, np.int32)
+    L = orc.Layer(inp["w"], sh.n_q, sh.n_kv, sh.hd, eps=sh.eps, rope_theta=sh.rope_theta)
+    K, V, O = inp["K"].copy(), inp["V"].copy(), inp["O"].copy()
+    orc.layer_refresh(L, inp["H"], idx_s, cnt_s, K, V, O)
+
+
+def cpu_baseline(wl, seconds):
+    import oracle as orc
+    orc.build()
+    cores = os.cpu_count() or 1
+    orc.set_threads(cores)
+    inp = _oracle_sample_inputs(wl)
+    frac = 1.0 / 8
+    t0 = time.perf_counter()
+    _oracle_step_sample(orc, wl.sh, inp, frac)
+    t1 = time.perf_counter() - t0
+    reps = max(1, min(8, int(seconds / max(t1, 1e-3))))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        _oracle_step_sample(orc, wl.sh, inp, frac)
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": frac / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{reps} x 1/8 of a layer step (proxy of N/8 rows, refresh of k/8 rows), "
+                      f"scaled by 8; {dt:.2f} s per sample"}
+
+
+def reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle as orc
+    from sparse_kv_cache_rank_gb300 import synth
+    orc.build()
+    cores = os.cpu_count() or 1
+    orc.set_threads(cores)
+    sh = synth.LLADA_LAYER
+    # same shapes and value distributions as the native arm, drawn on the host
+    g = synth.rng(1234)
+    bf = synth.round_bf16
+    w = synth.layer_weights(sh, 1234)
+    H = bf(g.standard_normal((sh.B, sh.N, sh.d), dtype=np.float32))
+    P = bf((g.standard_normal((sh.d, sh.r)) * 0.02).astype(np.float32))
+    sc = np.float32(0.02 * np.sqrt(sh.d))
+    inp = dict(w=w, P=P, H=H, pc=g.standard_normal((sh.B, sh.N, sh.r), dtype=np.float32),
+               K=bf(g.standard_normal((sh.B, sh.N, sh.d_kv), dtype=np.float32) * sc),
+               V=bf(g.standard_normal((sh.B, sh.N, sh.d_kv), dtype=np.float32) * sc),
+               O=bf(g.standard_normal((sh.B, sh.N, sh.d), dtype=np.float32)))
+    frac = 1.0 / 8
+    for _ in range(args.warmup):
+        _oracle_step_sample(orc, sh, inp, frac)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step_sample(orc, sh, inp, frac)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    v = frac / dt
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / v, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, same shapes and distributions as the native arm)",
+        "config": {"workload": f"llada8b-layer B={sh.B} N={sh.N} d={sh.d} heads={sh.n_q}x{sh.hd} "
+                               f"F={sh.F} r={sh.r} rho={sh.rho} k={orc.budget(sh.rho, sh.N)}"},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "each step = 1/8 of a layer step (proxy of N/8 rows, refresh of "
+                                   "k/8 rows) on the CPU oracle, scaled by 8"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        reference(args)
+    else:
+        native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -204,6 +204,29 @@ int dllm_commit_entropy(const float *logits, const uint8_t *valid, int B, int M,
                         float *entropy, float *max_entropy, int32_t *full_next, void *ws,
                         size_t ws_bytes, void *stream);
 
+/* ---------------------------------------------------------------------------
+ * Measurement support.  While a timer is armed, every launch of the chosen kernel
+ * (any stream) is bracketed by a pair of CUDA events, up to max_launches launches;
+ * dllm_timer_stop() synchronises the device, returns the summed event time and the
+ * number of timed launches, and disarms.  dllm_launch_count() is the number of
+ * kernels this library has launched in the process so far.
+ * ------------------------------------------------------------------------- */
+#define DLLM_KERNEL_PROXY_GEMM 1
+#define DLLM_KERNEL_COSINE 2
+#define DLLM_KERNEL_SELECT 3
+#define DLLM_KERNEL_GATHER 4
+#define DLLM_KERNEL_QKV 5
+#define DLLM_KERNEL_ATTENTION 6
+#define DLLM_KERNEL_OPROJ 7
+#define DLLM_KERNEL_RMSNORM2 8
+#define DLLM_KERNEL_GATEUP 9
+#define DLLM_KERNEL_DOWN 10
+#define DLLM_KERNEL_VOCAB 11
+
+int dllm_timer_start(int kernel_id, int max_launches);
+int dllm_timer_stop(double *total_ms, int *launches);
+unsigned long long dllm_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

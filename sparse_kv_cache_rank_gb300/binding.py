@@ -55,6 +55,9 @@ _SIGS = {
                                             C.c_void_p, C.c_int, C.c_void_p, C.c_void_p,
                                             C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
                                             C.c_int, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "dllm_timer_start": (C.c_int, [C.c_int, C.c_int]),
+    "dllm_timer_stop": (C.c_int, [C.POINTER(C.c_double), C.POINTER(C.c_int)]),
+    "dllm_launch_count": (C.c_ulonglong, []),
     "dllm_commit_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
     "dllm_commit_entropy": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                       C.c_float, C.c_float] + [C.c_void_p] * 6 +
@@ -134,6 +137,26 @@ def check_status(reset: bool = True) -> int:
         raise DllmError(f"device status 0x{st.value:x}: a kernel wait timed out")
     _check(rc, "dllm_check_status")
     return st.value
+
+
+# --------------------------------------------------------------------------- measurement
+KERNELS = {"proxy_gemm": 1, "cosine": 2, "select": 3, "gather": 4, "qkv": 5, "attention": 6,
+           "oproj": 7, "rmsnorm2": 8, "gateup": 9, "down": 10, "vocab": 11}
+
+
+def dllm_timer_start(kernel: str, max_launches: int) -> None:
+    _check(lib().dllm_timer_start(KERNELS[kernel], int(max_launches)), "dllm_timer_start")
+
+
+def dllm_timer_stop():
+    """-> (total milliseconds over the timed launches, number of timed launches)."""
+    ms, n = C.c_double(0), C.c_int(0)
+    _check(lib().dllm_timer_stop(C.byref(ms), C.byref(n)), "dllm_timer_stop")
+    return ms.value, n.value
+
+
+def dllm_launch_count() -> int:
+    return int(lib().dllm_launch_count())
 
 
 # --------------------------------------------------------------------------- proxy

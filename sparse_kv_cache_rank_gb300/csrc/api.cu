@@ -1,11 +1,13 @@
 // api.cu -- the extern "C" entry points of libdllm.so (declared in include/dllm.h):
 // argument checks, workspace carving and the launch sequence of each call.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "internal.h"
 
@@ -68,6 +70,37 @@ unsigned *status_ptr() {
     }
     return ptrs[dev];
 }
+
+
+// ---------------------------------------------------------------- measurement support
+std::atomic<unsigned long long> g_launches{0};
+
+struct KernelTimer {
+    std::mutex mu;
+    int armed = 0;
+    int cap = 0, n = 0;
+    std::vector<cudaEvent_t> ev;
+} g_timer;
+
+// Counts the launches of one library call site and, when the timer is armed for
+// this kernel, brackets them with a pair of events on the launch stream.
+struct Launch {
+    cudaEvent_t stop = nullptr;
+    cudaStream_t st;
+    Launch(int kernel_id, cudaStream_t s, int nlaunch = 1) : st(s) {
+        g_launches.fetch_add((unsigned long long)nlaunch, std::memory_order_relaxed);
+        if (g_timer.armed != kernel_id) return;
+        std::lock_guard<std::mutex> lock(g_timer.mu);
+        if (g_timer.armed != kernel_id || g_timer.n >= g_timer.cap) return;
+        cudaEvent_t start = g_timer.ev[2 * g_timer.n];
+        stop = g_timer.ev[2 * g_timer.n + 1];
+        ++g_timer.n;
+        cudaEventRecord(start, st);
+    }
+    ~Launch() {
+        if (stop) cudaEventRecord(stop, st);
+    }
+};
 
 struct PackLayout {
     size_t qkv, o, gu, down, g1, g2, freq, total;
@@ -190,13 +223,18 @@ DLLM_EXPORT int dllm_proxy_score(const void *H, const void *Pt, const float *pro
     cudaError_t e;
     if (dtype == DLLM_BF16) {
         if (d % 64) return fail(DLLM_ERR_UNSUPPORTED, "bf16 path needs d % 64 == 0 (got %d)", d);
+        Launch t(DLLM_KERNEL_PROXY_GEMM, st);
         e = gemm_tc(static_cast<const bf16 *>(Pt), r, d, static_cast<const bf16 *>(H), rows, epi, 0,
                     status_ptr(), st);
     } else {
+        Launch t(DLLM_KERNEL_PROXY_GEMM, st);
         e = gemm_simt(static_cast<const float *>(Pt), r, d, static_cast<const float *>(H), rows, epi, st);
     }
     CHECK_CUDA(e, "proxy projection launch");
-    CHECK_CUDA(cosine_drift(proxy_cur, proxy_cache, drift, rows, r, st), "cosine drift launch");
+    {
+        Launch t(DLLM_KERNEL_COSINE, st);
+        CHECK_CUDA(cosine_drift(proxy_cur, proxy_cache, drift, rows, r, st), "cosine drift launch");
+    }
     return DLLM_OK;
 }
 
@@ -210,6 +248,7 @@ DLLM_EXPORT int dllm_select_topk(const float *drift, const int32_t *forced, int 
     CHECK_ARG(k >= 0, "k must be >= 0");
     if (!forced) F = 0;
     CHECK_ARG(F >= 0, "F must be >= 0");
+    Launch t(DLLM_KERNEL_SELECT, as_stream(stream));
     CHECK_CUDA(select_topk(drift, forced, F, k, min_drift, idx, count, B, N, as_stream(stream)),
                "select launch");
     return DLLM_OK;
@@ -323,8 +362,11 @@ int refresh_impl(const dllm_layer *W, const T *H_in, SelRows sel, int B, T *K_ca
     const T *g2 = static_cast<const T *>(W->gamma2);
 
     // a3: gather + RMSNorm, proxy cache update
-    CHECK_CUDA(gather_rmsnorm<T>(H_in, sel, B, d, g1, W->eps, Xn, proxy_cache, proxy_cur, r, status, st),
-               "gather launch");
+    {
+        Launch t(DLLM_KERNEL_GATHER, st);
+        CHECK_CUDA(gather_rmsnorm<T>(H_in, sel, B, d, g1, W->eps, Xn, proxy_cache, proxy_cur, r, status, st),
+                   "gather launch");
+    }
     // a4: QKV projection, rotary embedding, K/V scattered into the cache
     EpiQKV<T> eq{Qc, K_cache, V_cache, sel, W->rope_inv_freq, W->n_q, W->n_kv, W->hd, W->use_rope};
     // a6: O projection + residual;  a7: FFN gate/up + SwiGLU;  a8: down + residual, scattered
@@ -332,19 +374,19 @@ int refresh_impl(const dllm_layer *W, const T *H_in, SelRows sel, int B, T *K_ca
     EpiSwiGLU<T> es{U, F};
     EpiDownScatter<T> ed{H_out, h1, sel, d};
     if constexpr (sizeof(T) == 2) {
-        CHECK_CUDA(gemm_tc(wqkv, dq + 2 * dkv, d, Xn, M, eq, 0, status, st), "qkv gemm");
-        CHECK_CUDA(attention_simt<T>(Qc, K_cache, V_cache, Ac, sel, B, W->n_q, W->n_kv, W->hd, st), "attention");
-        CHECK_CUDA(gemm_tc(wo, d, dq, Ac, M, er, 0, status, st), "o gemm");
-        CHECK_CUDA(rmsnorm_rows<T>(h1, M, d, g2, W->eps, Xn2, st), "rmsnorm2");
-        CHECK_CUDA(gemm_tc(wgu, 2 * F, d, Xn2, M, es, 0, status, st), "gate/up gemm");
-        CHECK_CUDA(gemm_tc(wdn, d, F, U, M, ed, 0, status, st), "down gemm");
+        { Launch t(DLLM_KERNEL_QKV, st); CHECK_CUDA(gemm_tc(wqkv, dq + 2 * dkv, d, Xn, M, eq, 0, status, st), "qkv gemm"); }
+        { Launch t(DLLM_KERNEL_ATTENTION, st); CHECK_CUDA(attention_simt<T>(Qc, K_cache, V_cache, Ac, sel, B, W->n_q, W->n_kv, W->hd, st), "attention"); }
+        { Launch t(DLLM_KERNEL_OPROJ, st); CHECK_CUDA(gemm_tc(wo, d, dq, Ac, M, er, 0, status, st), "o gemm"); }
+        { Launch t(DLLM_KERNEL_RMSNORM2, st); CHECK_CUDA(rmsnorm_rows<T>(h1, M, d, g2, W->eps, Xn2, st), "rmsnorm2"); }
+        { Launch t(DLLM_KERNEL_GATEUP, st); CHECK_CUDA(gemm_tc(wgu, 2 * F, d, Xn2, M, es, 0, status, st), "gate/up gemm"); }
+        { Launch t(DLLM_KERNEL_DOWN, st); CHECK_CUDA(gemm_tc(wdn, d, F, U, M, ed, 0, status, st), "down gemm"); }
     } else {
-        CHECK_CUDA(gemm_simt(wqkv, dq + 2 * dkv, d, Xn, M, eq, st), "qkv gemm");
-        CHECK_CUDA(attention_simt<T>(Qc, K_cache, V_cache, Ac, sel, B, W->n_q, W->n_kv, W->hd, st), "attention");
-        CHECK_CUDA(gemm_simt(wo, d, dq, Ac, M, er, st), "o gemm");
-        CHECK_CUDA(rmsnorm_rows<T>(h1, M, d, g2, W->eps, Xn2, st), "rmsnorm2");
-        CHECK_CUDA(gemm_simt(wgu, 2 * F, d, Xn2, M, es, st), "gate/up gemm");
-        CHECK_CUDA(gemm_simt(wdn, d, F, U, M, ed, st), "down gemm");
+        { Launch t(DLLM_KERNEL_QKV, st); CHECK_CUDA(gemm_simt(wqkv, dq + 2 * dkv, d, Xn, M, eq, st), "qkv gemm"); }
+        { Launch t(DLLM_KERNEL_ATTENTION, st); CHECK_CUDA(attention_simt<T>(Qc, K_cache, V_cache, Ac, sel, B, W->n_q, W->n_kv, W->hd, st), "attention"); }
+        { Launch t(DLLM_KERNEL_OPROJ, st); CHECK_CUDA(gemm_simt(wo, d, dq, Ac, M, er, st), "o gemm"); }
+        { Launch t(DLLM_KERNEL_RMSNORM2, st); CHECK_CUDA(rmsnorm_rows<T>(h1, M, d, g2, W->eps, Xn2, st), "rmsnorm2"); }
+        { Launch t(DLLM_KERNEL_GATEUP, st); CHECK_CUDA(gemm_simt(wgu, 2 * F, d, Xn2, M, es, st), "gate/up gemm"); }
+        { Launch t(DLLM_KERNEL_DOWN, st); CHECK_CUDA(gemm_simt(wdn, d, F, U, M, ed, st), "down gemm"); }
     }
     return DLLM_OK;
 }
@@ -402,8 +444,45 @@ DLLM_EXPORT int dllm_commit_entropy(const float *logits, const uint8_t *valid, i
     if (!ws || ws_bytes < need)
         return fail(DLLM_ERR_WORKSPACE, "workspace holds %zu bytes, %zu needed", ws_bytes, need);
     void *w = reinterpret_cast<void *>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255));
+    Launch t(DLLM_KERNEL_VOCAB, as_stream(stream), 2);
     CHECK_CUDA(commit_entropy(logits, valid, B, M, V, conf_thresh, tau, token, conf, entropy,
                               max_entropy, full_next, w, as_stream(stream)),
                "commit launch");
     return DLLM_OK;
 }
+
+// ------------------------------------------------------------------ measurement support
+DLLM_EXPORT int dllm_timer_start(int kernel_id, int max_launches) {
+    CHECK_ARG(kernel_id >= DLLM_KERNEL_PROXY_GEMM && kernel_id <= DLLM_KERNEL_VOCAB, "unknown kernel id %d", kernel_id);
+    CHECK_ARG(max_launches > 0 && max_launches <= 1 << 16, "max_launches must be in [1, 65536]");
+    std::lock_guard<std::mutex> lock(g_timer.mu);
+    CHECK_ARG(g_timer.armed == 0, "a timer is already armed");
+    for (cudaEvent_t e : g_timer.ev) cudaEventDestroy(e);
+    g_timer.ev.assign(2 * (size_t)max_launches, nullptr);
+    for (auto &e : g_timer.ev) CHECK_CUDA(cudaEventCreate(&e), "cudaEventCreate");
+    g_timer.cap = max_launches;
+    g_timer.n = 0;
+    g_timer.armed = kernel_id;
+    return DLLM_OK;
+}
+
+DLLM_EXPORT int dllm_timer_stop(double *total_ms, int *launches) {
+    std::lock_guard<std::mutex> lock(g_timer.mu);
+    CHECK_ARG(g_timer.armed != 0, "no timer armed");
+    g_timer.armed = 0;
+    CHECK_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+    double tot = 0.0;
+    for (int i = 0; i < g_timer.n; ++i) {
+        float ms = 0.f;
+        CHECK_CUDA(cudaEventElapsedTime(&ms, g_timer.ev[2 * i], g_timer.ev[2 * i + 1]), "cudaEventElapsedTime");
+        tot += ms;
+    }
+    if (total_ms) *total_ms = tot;
+    if (launches) *launches = g_timer.n;
+    for (cudaEvent_t e : g_timer.ev) cudaEventDestroy(e);
+    g_timer.ev.clear();
+    g_timer.n = g_timer.cap = 0;
+    return DLLM_OK;
+}
+
+DLLM_EXPORT unsigned long long dllm_launch_count(void) { return g_launches.load(); }

@@ -106,7 +106,8 @@ __global__ void __launch_bounds__(256) k_cosine_drift(const float *__restrict__ 
         const float ia = 1.0f / sqrtf(na), ic = 1.0f / sqrtf(nc);
         float s = 0.f;
         for (int e = lane; e < r; e += 32) {
-            const float t = a[e] * ia - c[e] * ic;
+            // separately rounded products (no FMA contraction): equal inputs give t == 0
+            const float t = __fsub_rn(__fmul_rn(a[e], ia), __fmul_rn(c[e], ic));
             s = fmaf(t, t, s);
         }
 #pragma unroll
