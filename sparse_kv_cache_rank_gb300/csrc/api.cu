@@ -129,10 +129,10 @@ PackLayout pack_layout(int d, int n_q, int n_kv, int hd, int F, int dtype) {
 }
 
 struct RefreshWs {
-    size_t xn, q, a, h1, xn2, u, total;
+    size_t xn, q, a, h1, xn2, u, attn, total;
 };
 
-RefreshWs refresh_ws(const dllm_layer *W, int B, int k_max) {
+RefreshWs refresh_ws(const dllm_layer *W, int B, int N, int k_max) {
     const size_t M = (size_t)B * k_max, el = el_size(W->dtype);
     const size_t dq = (size_t)W->n_q * W->hd;
     RefreshWs r{};
@@ -149,6 +149,8 @@ RefreshWs refresh_ws(const dllm_layer *W, int B, int k_max) {
     off = align256(off + M * W->d * el);
     r.u = off;
     off = align256(off + M * W->F * el);
+    r.attn = off;
+    if (W->dtype == DLLM_BF16) off = align256(off + attention_tc_ws_bytes(B, k_max, W->n_q, W->hd, N));
     r.total = off + 256;   // room to align the caller's base
     return r;
 }
@@ -333,9 +335,8 @@ DLLM_EXPORT int dllm_pack_layer(const void *w_q, const void *w_k, const void *w_
 
 // ------------------------------------------------------------------ sparse refresh
 DLLM_EXPORT size_t dllm_refresh_workspace_bytes(const dllm_layer *W, int B, int N, int k_max) {
-    (void)N;
-    if (!W || B <= 0 || k_max <= 0) return 0;
-    return refresh_ws(W, B, k_max).total;
+    if (!W || B <= 0 || N <= 0 || k_max <= 0) return 0;
+    return refresh_ws(W, B, N, k_max).total;
 }
 
 namespace {
@@ -344,7 +345,7 @@ template <class T>
 int refresh_impl(const dllm_layer *W, const T *H_in, SelRows sel, int B, T *K_cache, T *V_cache,
                  T *H_out, float *proxy_cache, const float *proxy_cur, int r, uint8_t *ws,
                  cudaStream_t st) {
-    const RefreshWs L = refresh_ws(W, B, sel.k_max);
+    const RefreshWs L = refresh_ws(W, B, sel.N, sel.k_max);
     const int M = B * sel.k_max;
     const int d = W->d, dq = W->n_q * W->hd, dkv = W->n_kv * W->hd, F = W->F;
     T *Xn = reinterpret_cast<T *>(ws + L.xn);
@@ -375,7 +376,14 @@ int refresh_impl(const dllm_layer *W, const T *H_in, SelRows sel, int B, T *K_ca
     EpiDownScatter<T> ed{H_out, h1, sel, d};
     if constexpr (sizeof(T) == 2) {
         { Launch t(DLLM_KERNEL_QKV, st); CHECK_CUDA(gemm_tc(wqkv, dq + 2 * dkv, d, Xn, M, eq, 0, status, st), "qkv gemm"); }
-        { Launch t(DLLM_KERNEL_ATTENTION, st); CHECK_CUDA(attention_simt<T>(Qc, K_cache, V_cache, Ac, sel, B, W->n_q, W->n_kv, W->hd, st), "attention"); }
+        {
+            const int na = attention_tc_splits(B, sel.k_max, W->n_q, sel.N) > 1 ? 2 : 1;
+            Launch t(DLLM_KERNEL_ATTENTION, st, na);
+            CHECK_CUDA(attention_tc(reinterpret_cast<const bf16 *>(Qc), reinterpret_cast<const bf16 *>(K_cache),
+                                    reinterpret_cast<const bf16 *>(V_cache), reinterpret_cast<bf16 *>(Ac), sel, B,
+                                    W->n_q, W->n_kv, W->hd, reinterpret_cast<float *>(ws + L.attn), status, st),
+                       "attention");
+        }
         { Launch t(DLLM_KERNEL_OPROJ, st); CHECK_CUDA(gemm_tc(wo, d, dq, Ac, M, er, 0, status, st), "o gemm"); }
         { Launch t(DLLM_KERNEL_RMSNORM2, st); CHECK_CUDA(rmsnorm_rows<T>(h1, M, d, g2, W->eps, Xn2, st), "rmsnorm2"); }
         { Launch t(DLLM_KERNEL_GATEUP, st); CHECK_CUDA(gemm_tc(wgu, 2 * F, d, Xn2, M, es, 0, status, st), "gate/up gemm"); }
@@ -411,7 +419,7 @@ DLLM_EXPORT int dllm_sparse_layer_refresh(const dllm_layer *W, const void *H_in,
         return fail(DLLM_ERR_INVALID_ARG, "proxy_cache and proxy_cur must both be set or both NULL");
     if (proxy_cache) CHECK_ARG(r > 0, "r must be positive when proxies are given");
     if (k_max == 0) return DLLM_OK;
-    const size_t need = refresh_ws(W, B, k_max).total;
+    const size_t need = refresh_ws(W, B, N, k_max).total;
     if (!ws || ws_bytes < need)
         return fail(DLLM_ERR_WORKSPACE, "workspace holds %zu bytes, %zu needed", ws_bytes, need);
     uint8_t *w8 = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255));

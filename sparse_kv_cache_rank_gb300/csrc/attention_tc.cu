@@ -1,0 +1,401 @@
+// attention_tc.cu -- non-causal attention of the selected queries over the whole
+// partially refreshed cache on the sm_103a tensor cores (SPA-Cache, "3. Sparse
+// execution": the sparse queries attend to the partially updated KV cache).
+//
+// One CTA = 128 selected rows of one sequence (MMA M) x one query head x one
+// slice of the key range.  Per 128-key tile:
+//   S  = Q K^T          tcgen05.mma, Q and K K-major (head dim contiguous), fp32 in TMEM
+//   P  = exp2(S*c - m)  softmax warps, one thread per query row, bf16 into shared
+//                       memory in the 128-byte-swizzled K-major layout
+//   PV = P V            tcgen05.mma, V read MN-major (head dim contiguous), fp32 in TMEM
+//   O  = O * corr + PV  in registers (streaming softmax)
+// K and V tiles are double-buffered by TMA; S is double-buffered in TMEM so the
+// next tile's Q K^T runs while the softmax of the current one is computed.
+// Rows of the key range beyond N are masked.  With several key slices, each CTA
+// writes (O, m, l) to the workspace and a combine kernel merges them.
+//
+// Roles (192 threads): warp 0 TMA, warp 1 TMEM owner + MMA issuer, warps 2..5 softmax.
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+
+namespace dllm {
+
+bool make_tmap(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+
+namespace {
+
+constexpr int AQ = 128;          // query rows per CTA
+constexpr int AKV = 128;         // keys per tile
+constexpr int kThreads = 192;
+constexpr int kChunk = 128 * 128;   // one 64-column (128-byte) box of 128 rows: 16 KB
+
+struct AttnArgs {
+    const int32_t *count;
+    int N, k_max, n_q, n_kv, B;
+    int kv_tiles, splits;
+    float scale_log2;                 // log2(e) / sqrt(hd)
+    bf16 *A;                          // [B*k_max, n_q*hd] (splits == 1)
+    float *part_o;                    // [splits][B*k_max][n_q*hd]   (splits > 1)
+    float *part_ml;                   // [splits][B*k_max][n_q][2]
+};
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_attention_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const AttnArgs a, unsigned *status) {
+    constexpr int NCH = HD / 64;               // 64-column boxes per row of Q / K / V
+    constexpr int QB = NCH * kChunk;           // bytes of the Q tile
+    constexpr int KB = NCH * kChunk;           // bytes of one K (or V) tile
+    constexpr int PB = 2 * kChunk;             // P tile: 128 rows x 128 keys bf16
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    uint8_t *smem = smem_raw + pad;
+    uint8_t *sQ = smem;
+    uint8_t *sK = sQ + QB;                     // [2][KB]
+    uint8_t *sV = sK + 2 * KB;                 // [2][KB]
+    uint8_t *sP = sV + 2 * KB;                 // [PB]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sP + PB);
+    uint64_t *q_full = bars + 0;
+    uint64_t *k_full = bars + 1;               // [2]
+    uint64_t *v_full = bars + 3;               // [2]
+    uint64_t *kv_empty = bars + 5;             // [2]
+    uint64_t *s_full = bars + 7;               // [2]
+    uint64_t *s_free = bars + 9;               // [2]
+    uint64_t *p_full = bars + 11;
+    uint64_t *pv_full = bars + 12;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q0 = blockIdx.x * AQ;
+    const int h = blockIdx.y;
+    const int b = blockIdx.z / a.splits;
+    const int split = blockIdx.z - b * a.splits;
+    const int g = h / (a.n_q / a.n_kv);
+    int live = a.count[b];
+    live = live < a.k_max ? live : a.k_max;
+    live -= q0;                                 // live query rows of this tile
+    const int t0 = (int)((long long)split * a.kv_tiles / a.splits);
+    const int t1 = (int)((long long)(split + 1) * a.kv_tiles / a.splits);
+    const int nt = t1 - t0;
+    const int dq = a.n_q * HD;
+    const size_t row0 = (size_t)b * a.k_max + q0;   // flattened row of query 0
+    if (live <= 0 || nt <= 0) {                  // nothing to compute: outputs of dead rows
+        if (warp >= 2 && a.splits == 1) {
+            const int r = (warp & 3) * 32 + lane;
+            if (q0 + r < a.k_max && r < AQ) {
+                bf16 *dst = a.A + (row0 + r) * dq + (size_t)h * HD;
+                for (int e = 0; e < HD; ++e) dst[e] = __float2bfloat16_rn(0.f);
+            }
+        } else if (warp >= 2) {
+            const int r = (warp & 3) * 32 + lane;
+            if (q0 + r < a.k_max) {
+                const size_t pm = ((size_t)split * a.B * a.k_max + row0 + r);
+                a.part_ml[(pm * a.n_q + h) * 2 + 0] = -INFINITY;
+                a.part_ml[(pm * a.n_q + h) * 2 + 1] = 0.f;
+                float *po = a.part_o + pm * dq + (size_t)h * HD;
+                for (int e = 0; e < HD; ++e) po[e] = 0.f;
+            }
+        }
+        return;
+    }
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&kv_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], 128);
+        }
+        mbar_init(p_full, 128);
+        mbar_init(pv_full, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS[2] = {tmem, tmem + 128};
+    const uint32_t tPV = tmem + 256;
+
+    if (warp == 0) {
+        if (lane == 0) {   // ---------------- TMA producer
+            mbar_arrive_expect_tx(q_full, QB);
+            for (int c = 0; c < NCH; ++c)
+                tma_load_2d(sQ + c * kChunk, &tmQ, q_full, h * HD + c * 64, (int)row0);
+            int issued = 0;
+            for (int it = 0; it < nt; ++it) {
+                const int s = it & 1;
+                const uint32_t ph = (uint32_t)(it >> 1) & 1u;
+                if (!mbar_wait(&kv_empty[s], ph ^ 1u, abort_flag, status)) break;
+                const int j0 = (t0 + it) * AKV;
+                const int y = b * a.N + j0;
+                mbar_arrive_expect_tx(&k_full[s], KB);
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_2d(sK + s * KB + c * kChunk, &tmK, &k_full[s], g * HD + c * 64, y);
+                mbar_arrive_expect_tx(&v_full[s], KB);
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_2d(sV + s * KB + c * kChunk, &tmV, &v_full[s], g * HD + c * 64, y);
+                ++issued;
+            }
+            if (*abort_flag) {
+                mbar_drain(q_full, 0);
+                for (int it = issued > 2 ? issued - 2 : 0; it < issued; ++it) {
+                    mbar_drain(&k_full[it & 1], (uint32_t)(it >> 1) & 1u);
+                    mbar_drain(&v_full[it & 1], (uint32_t)(it >> 1) & 1u);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {   // ---------------- MMA issuer
+            const uint32_t id_s = idesc_bf16(128, AKV, 0);
+            const uint32_t id_pv = idesc_bf16(128, HD, 1);
+            const uint32_t aq = smem_u32(sQ), ak = smem_u32(sK), av = smem_u32(sV), ap = smem_u32(sP);
+            bool ok = mbar_wait(q_full, 0, abort_flag, status);
+            auto issue_s = [&](int it) -> bool {
+                const int s = it & 1;
+                const uint32_t ph = (uint32_t)(it >> 1) & 1u;
+                if (!mbar_wait(&s_free[s], ph ^ 1u, abort_flag, status)) return false;
+                if (!mbar_wait(&k_full[s], ph, abort_flag, status)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t off = (uint32_t)((kk >> 2) * kChunk + (kk & 3) * 32);
+                    mma_bf16(tS[s], smem_desc_sw128(aq + off, 16, 1024),
+                             smem_desc_sw128(ak + s * KB + off, 16, 1024), id_s, kk > 0);
+                }
+                mma_commit(&s_full[s]);
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int it = 0; ok && it < nt; ++it) {
+                if (it + 1 < nt && !issue_s(it + 1)) break;
+                const int s = it & 1;
+                const uint32_t ph = (uint32_t)(it >> 1) & 1u;
+                if (!mbar_wait(p_full, (uint32_t)it & 1u, abort_flag, status)) break;
+                if (!mbar_wait(&v_full[s], ph, abort_flag, status)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < AKV / 16; ++kk) {
+                    // P: K-major, keys 16kk.. (+32 B inside the swizzled row, 16 KB per 64 keys)
+                    const uint32_t offp = (uint32_t)((kk >> 2) * kChunk + (kk & 3) * 32);
+                    // V: MN-major, keys 16kk.. start 16 rows (2 KB) further; LBO = next 64 dims
+                    const uint32_t offv = (uint32_t)(kk * 16 * 128);
+                    mma_bf16(tPV, smem_desc_sw128(ap + offp, 16, 1024),
+                             smem_desc_sw128(av + s * KB + offv, kChunk, 1024), id_pv, kk > 0);
+                }
+                mma_commit(pv_full);
+                mma_commit(&kv_empty[s]);
+            }
+        }
+    } else {   // ---------------- softmax warps: thread = query row
+        const int q = warp & 3;
+        const int r = q * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+        float o[HD];
+#pragma unroll
+        for (int e = 0; e < HD; ++e) o[e] = 0.f;
+        float m_run = -INFINITY, l_run = 0.f;
+        uint8_t *prow = sP + (r >> 3) * 1024 + (r & 7) * 128;
+        for (int it = 0; it < nt; ++it) {
+            const int s = it & 1;
+            const uint32_t ph = (uint32_t)(it >> 1) & 1u;
+            if (!mbar_wait(&s_full[s], ph, abort_flag, status)) break;
+            tc_fence_after();
+            const int j0 = (t0 + it) * AKV;
+            const int nvalid = a.N - j0;             // keys of this tile inside [0, N)
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c0 = 0; c0 < AKV; c0 += 16) {
+                float v[16];
+                tmem_ld_x16(tS[s] + lane_addr + (uint32_t)c0, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (c0 + j < nvalid) mt = fmaxf(mt, v[j]);
+            }
+            const float m_new = fmaxf(m_run, mt * a.scale_log2);
+            const float corr = exp2f(m_run - m_new);
+            float lsum = 0.f;
+#pragma unroll
+            for (int c0 = 0; c0 < AKV; c0 += 16) {
+                float v[16];
+                tmem_ld_x16(tS[s] + lane_addr + (uint32_t)c0, v);
+                tmem_ld_wait();
+                uint32_t pk[8];
+#pragma unroll
+                for (int j = 0; j < 16; j += 2) {
+                    const float p0 = (c0 + j < nvalid) ? exp2f(v[j] * a.scale_log2 - m_new) : 0.f;
+                    const float p1 = (c0 + j + 1 < nvalid) ? exp2f(v[j + 1] * a.scale_log2 - m_new) : 0.f;
+                    const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
+                    lsum += __low2float(pp) + __high2float(pp);
+                    pk[j >> 1] = *reinterpret_cast<const uint32_t *>(&pp);
+                }
+                // 16 keys = two 16-byte units of this row in the swizzled K-major layout
+                const int chunk = c0 >> 6;
+                const int unit = (c0 & 63) >> 3;
+#pragma unroll
+                for (int hlf = 0; hlf < 2; ++hlf) {
+                    const int u = (unit + hlf) ^ (r & 7);
+                    uint4 val = make_uint4(pk[4 * hlf], pk[4 * hlf + 1], pk[4 * hlf + 2], pk[4 * hlf + 3]);
+                    *reinterpret_cast<uint4 *>(prow + chunk * kChunk + u * 16) = val;
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&s_free[s]);
+            fence_proxy_async_smem();
+            mbar_arrive(p_full);
+            l_run = l_run * corr + lsum;
+            m_run = m_new;
+            if (!mbar_wait(pv_full, (uint32_t)it & 1u, abort_flag, status)) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < HD; c0 += 16) {
+                float v[16];
+                tmem_ld_x16(tPV + lane_addr + (uint32_t)c0, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) o[c0 + j] = fmaf(o[c0 + j], corr, v[j]);
+            }
+        }
+        if (q0 + r < a.k_max) {
+            const size_t row = row0 + r;
+            if (a.splits == 1) {
+                const float inv = (r < live && l_run > 0.f) ? 1.0f / l_run : 0.f;
+                bf16 *dst = a.A + row * dq + (size_t)h * HD;
+#pragma unroll
+                for (int e = 0; e < HD; e += 2)
+                    *reinterpret_cast<__nv_bfloat162 *>(dst + e) = __floats2bfloat162_rn(o[e] * inv, o[e + 1] * inv);
+            } else {
+                const size_t pm = (size_t)split * a.B * a.k_max + row;
+                a.part_ml[(pm * a.n_q + h) * 2 + 0] = r < live ? m_run : -INFINITY;
+                a.part_ml[(pm * a.n_q + h) * 2 + 1] = r < live ? l_run : 0.f;
+                float *po = a.part_o + pm * dq + (size_t)h * HD;
+#pragma unroll
+                for (int e = 0; e < HD; e += 4)
+                    *reinterpret_cast<float4 *>(po + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// A[row, h] = sum_s O_s e^(m_s - M) / sum_s l_s e^(m_s - M) over the key slices.
+template <int HD>
+__global__ void __launch_bounds__(HD) k_attention_combine(const float *__restrict__ part_o,
+                                                          const float *__restrict__ part_ml,
+                                                          int splits, int rows, int n_q,
+                                                          bf16 *__restrict__ A) {
+    const int row = blockIdx.x, h = blockIdx.y, e = threadIdx.x;
+    const int dq = n_q * HD;
+    float M = -INFINITY;
+    for (int s = 0; s < splits; ++s)
+        M = fmaxf(M, part_ml[(((size_t)s * rows + row) * n_q + h) * 2]);
+    float num = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+        for (int s = 0; s < splits; ++s) {
+            const size_t pm = (size_t)s * rows + row;
+            const float ms = part_ml[(pm * n_q + h) * 2];
+            if (ms == -INFINITY) continue;
+            const float w = exp2f(ms - M);
+            den = fmaf(part_ml[(pm * n_q + h) * 2 + 1], w, den);
+            num = fmaf(part_o[pm * dq + (size_t)h * HD + e], w, num);
+        }
+    }
+    A[(size_t)row * dq + (size_t)h * HD + e] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
+}
+
+template <int HD>
+size_t attn_smem() {
+    return 1024 + (size_t)(HD / 64) * kChunk * 5 + 2 * kChunk + 14 * 8 + 64;
+}
+
+}  // namespace
+
+int attention_tc_splits(int B, int k_max, int n_q, int N) {
+    const int qt = (k_max + AQ - 1) / AQ;
+    const long long base = (long long)qt * n_q * B;
+    const int kv_tiles = (N + AKV - 1) / AKV;
+    int s = (int)((num_sms() + base - 1) / base);
+    if (s > kv_tiles) s = kv_tiles;
+    if (s > 16) s = 16;
+    return s < 1 ? 1 : s;
+}
+
+size_t attention_tc_ws_bytes(int B, int k_max, int n_q, int hd, int N) {
+    const int s = attention_tc_splits(B, k_max, n_q, N);
+    if (s <= 1) return 0;
+    const size_t rows = (size_t)B * k_max;
+    return (size_t)s * rows * n_q * hd * 4 + (size_t)s * rows * n_q * 2 * 4 + 512;
+}
+
+cudaError_t attention_tc(const bf16 *Q, const bf16 *Kc, const bf16 *Vc, bf16 *A, SelRows sel, int B,
+                         int n_q, int n_kv, int hd, float *ws, unsigned *status, cudaStream_t st) {
+    const int M = B * sel.k_max;
+    if (M <= 0) return cudaSuccess;
+    if (hd != 64 && hd != 128) return cudaErrorInvalidValue;
+    CUtensorMap tq, tk, tv;
+    const int dq = n_q * hd, dkv = n_kv * hd;
+    if (!make_tmap(&tq, Q, (uint64_t)M, (uint64_t)dq, AQ) ||
+        !make_tmap(&tk, Kc, (uint64_t)B * sel.N, (uint64_t)dkv, AKV) ||
+        !make_tmap(&tv, Vc, (uint64_t)B * sel.N, (uint64_t)dkv, AKV))
+        return cudaErrorInvalidValue;
+    AttnArgs a{};
+    a.count = sel.count;
+    a.N = sel.N;
+    a.k_max = sel.k_max;
+    a.n_q = n_q;
+    a.n_kv = n_kv;
+    a.B = B;
+    a.kv_tiles = (sel.N + AKV - 1) / AKV;
+    a.splits = attention_tc_splits(B, sel.k_max, n_q, sel.N);
+    a.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
+    a.A = A;
+    if (a.splits > 1) {
+        a.part_o = ws;
+        a.part_ml = ws + (size_t)a.splits * M * dq;
+    }
+    dim3 grid((sel.k_max + AQ - 1) / AQ, n_q, B * a.splits);
+    cudaError_t e;
+    if (hd == 128) {
+        const size_t sm = attn_smem<128>();
+        e = cudaFuncSetAttribute(k_attention_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        if (e != cudaSuccess) return e;
+        k_attention_tc<128><<<grid, kThreads, sm, st>>>(tq, tk, tv, a, status);
+    } else {
+        const size_t sm = attn_smem<64>();
+        e = cudaFuncSetAttribute(k_attention_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+        if (e != cudaSuccess) return e;
+        k_attention_tc<64><<<grid, kThreads, sm, st>>>(tq, tk, tv, a, status);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess || a.splits == 1) return e;
+    dim3 g2(M, n_q);
+    if (hd == 128)
+        k_attention_combine<128><<<g2, 128, 0, st>>>(a.part_o, a.part_ml, a.splits, M, n_q, A);
+    else
+        k_attention_combine<64><<<g2, 64, 0, st>>>(a.part_o, a.part_ml, a.splits, M, n_q, A);
+    return cudaGetLastError();
+}
+
+}  // namespace dllm

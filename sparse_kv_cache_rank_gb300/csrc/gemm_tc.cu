@@ -182,6 +182,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
     return fn;
 }
 
+}  // namespace
+
 // Row-major bf16 matrix [rows, cols], boxes of 64 columns x box_rows rows, 128-byte swizzle.
 bool make_tmap(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
     auto enc = tmap_encoder();
@@ -194,6 +196,8 @@ bool make_tmap(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols, 
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 struct Plan {
     int BN, splits, stages, tok_tiles, w_tiles;

@@ -55,6 +55,13 @@ template <class T>
 cudaError_t attention_simt(const T *Q, const T *Kc, const T *Vc, T *A, SelRows sel, int B,
                            int n_q, int n_kv, int hd, cudaStream_t st);
 
+// Tensor cores (bf16, hd in {64, 128}); `ws` holds the split-KV partials
+// (attention_tc_ws_bytes, may be 0 when a single key slice is used).
+int attention_tc_splits(int B, int k_max, int n_q, int N);
+size_t attention_tc_ws_bytes(int B, int k_max, int n_q, int hd, int N);
+cudaError_t attention_tc(const bf16 *Q, const bf16 *Kc, const bf16 *Vc, bf16 *A, SelRows sel, int B,
+                         int n_q, int n_kv, int hd, float *ws, unsigned *status, cudaStream_t st);
+
 // ---------------------------------------------------------------- selection
 cudaError_t select_topk(const float *drift, const int32_t *forced, int F, int k, float min_drift,
                         int32_t *idx, int32_t *count, int B, int N, cudaStream_t st);

@@ -59,6 +59,25 @@ def assert_close_layer(x, ref, dtype: str, what: str):
     return rel, cs
 
 
+def assert_update_close(out, ref_out, h_in, dtype: str, what: str):
+    """The layer's update (output minus input).  A bf16 output carries the rounding
+    of the whole residual sum, so the update is compared against the reference output
+    rounded the same way, and the max error may include one bf16 ulp of |output|."""
+    from sparse_kv_cache_rank_gb300 import synth
+    ref = synth.round_bf16(ref_out) if dtype == "bf16" else ref_out
+    du = np.asarray(out, np.float64) - h_in
+    dr = np.asarray(ref, np.float64) - h_in
+    cs = cosine(du, dr)
+    err = np.abs(du - dr).max()
+    if dtype == "bf16":
+        ulp = 2.0 ** (np.floor(np.log2(np.abs(ref).max())) - 7)
+        bound = BF16_MAX_REL * np.abs(dr).max() + ulp
+        assert cs >= BF16_MIN_COS and err <= bound, f"{what}: err {err:.3e} > {bound:.3e} or cos {cs:.6f}"
+    else:
+        bound = F32_MAX_REL * np.abs(dr).max()
+        assert cs >= F32_MIN_COS and err <= bound, f"{what}: err {err:.3e} > {bound:.3e} or cos {cs:.8f}"
+
+
 def assert_drift_close(gpu, ref):
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)

@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 from sparse_kv_cache_rank_gb300 import synth
-from cases import (assert_close_layer, assert_drift_close, check_selection_band, forced_rows,
+from cases import (assert_close_layer, assert_drift_close, assert_update_close, check_selection_band, forced_rows,
                    layer_case, normwise_rel, to_dev, to_np, torch_dtype, FP32_REDUCTION_RTOL)
 
 torch = pytest.importorskip("torch")
@@ -152,8 +152,8 @@ def _compare_step(c, g, o, forced, k, out_mask=None):
         rows = I if out_mask is None else I[out_mask[b, I] != 0]
         assert_close_layer(g["O"][b, rows], o["O"][b, rows], sh.dtype, f"H_out b={b}")
         # the update itself (output minus input), not only the residual stream
-        assert_close_layer(g["O"][b, rows] - c.H_cur[b, rows], o["O"][b, rows] - c.H_cur[b, rows],
-                           sh.dtype, f"H_out - H_in b={b}")
+        assert_update_close(g["O"][b, rows], o["O"][b, rows], c.H_cur[b, rows], sh.dtype,
+                            f"H_out - H_in b={b}")
 
 
 @pytest.mark.parametrize("shape", [synth.TINY, TINY_BF16, SMALL_BF16, MID_BF16], ids=lambda s: s.name)
