@@ -205,6 +205,18 @@ int dllm_commit_entropy(const float *logits, const uint8_t *valid, int B, int M,
                         size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * Plain product on the tensor cores, the engine under every bf16 projection above
+ * (and the LM head of the vocabulary step: logits = RMSNorm(h) W_lm^T):
+ *   out[m, f] = sum_k X[m, k] W[f, k]          (fp32 accumulation and output)
+ *   X [M, K] bf16, W [N_out, K] bf16 (nn.Linear layout), out [M, N_out] fp32.
+ * splits: number of CTAs that share one output tile along K (a thread-block cluster
+ * reducing through distributed shared memory); 0 = chosen from the shape, 1..8.
+ * Requirements: K % 64 == 0, N_out % 32 == 0, 16-byte aligned rows.  No workspace.
+ * ------------------------------------------------------------------------- */
+int dllm_gemm_bf16(const void *X, const void *W, float *out, int M, int N_out, int K, int splits,
+                   void *stream);
+
+/* ---------------------------------------------------------------------------
  * Measurement support.  While a timer is armed, every launch of the chosen kernel
  * (any stream) is bracketed by a pair of CUDA events, up to max_launches launches;
  * dllm_timer_stop() synchronises the device, returns the summed event time and the
@@ -222,6 +234,7 @@ int dllm_commit_entropy(const float *logits, const uint8_t *valid, int B, int M,
 #define DLLM_KERNEL_GATEUP 9
 #define DLLM_KERNEL_DOWN 10
 #define DLLM_KERNEL_VOCAB 11
+#define DLLM_KERNEL_GEMM 12
 
 int dllm_timer_start(int kernel_id, int max_launches);
 int dllm_timer_stop(double *total_ms, int *launches);

@@ -58,6 +58,8 @@ _SIGS = {
     "dllm_timer_start": (C.c_int, [C.c_int, C.c_int]),
     "dllm_timer_stop": (C.c_int, [C.POINTER(C.c_double), C.POINTER(C.c_int)]),
     "dllm_launch_count": (C.c_ulonglong, []),
+    "dllm_gemm_bf16": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
+                                 C.c_int, C.c_void_p]),
     "dllm_commit_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
     "dllm_commit_entropy": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                       C.c_float, C.c_float] + [C.c_void_p] * 6 +
@@ -141,7 +143,7 @@ def check_status(reset: bool = True) -> int:
 
 # --------------------------------------------------------------------------- measurement
 KERNELS = {"proxy_gemm": 1, "cosine": 2, "select": 3, "gather": 4, "qkv": 5, "attention": 6,
-           "oproj": 7, "rmsnorm2": 8, "gateup": 9, "down": 10, "vocab": 11}
+           "oproj": 7, "rmsnorm2": 8, "gateup": 9, "down": 10, "vocab": 11, "gemm": 12}
 
 
 def dllm_timer_start(kernel: str, max_launches: int) -> None:
@@ -262,6 +264,21 @@ def dllm_sparse_layer_refresh(layer: Layer, H_in, idx, count, k_max: int, K_cach
                                            B, N, _ptr(ws), ws.numel(), _stream(H_in.device)),
            "dllm_sparse_layer_refresh")
     return K_cache, V_cache, H_out_cache
+
+
+# --------------------------------------------------------------------------- plain GEMM
+def dllm_gemm_bf16(X, W, out=None, splits: int = 0):
+    """X [M, K] bf16, W [N_out, K] bf16 -> out [M, N_out] fp32 = X W^T (tensor cores)."""
+    M, K = X.shape
+    N_out = W.shape[0]
+    if W.shape != (N_out, K) or X.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise DllmError("X [M,K] and W [N_out,K] must be bf16")
+    if out is None:
+        out = torch.empty((M, N_out), dtype=torch.float32, device=X.device)
+    _cuda(X, W, out)
+    _check(lib().dllm_gemm_bf16(_ptr(X), _ptr(W), _ptr(out), M, N_out, K, int(splits),
+                                _stream(X.device)), "dllm_gemm_bf16")
+    return out
 
 
 # --------------------------------------------------------------------------- vocab

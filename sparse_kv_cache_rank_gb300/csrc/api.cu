@@ -129,7 +129,7 @@ PackLayout pack_layout(int d, int n_q, int n_kv, int hd, int F, int dtype) {
 }
 
 struct RefreshWs {
-    size_t xn, q, a, h1, xn2, u, attn, total;
+    size_t xn, q, a, h1, xn2, u, rope, attn, total;
 };
 
 RefreshWs refresh_ws(const dllm_layer *W, int B, int N, int k_max) {
@@ -149,6 +149,8 @@ RefreshWs refresh_ws(const dllm_layer *W, int B, int N, int k_max) {
     off = align256(off + M * W->d * el);
     r.u = off;
     off = align256(off + M * W->F * el);
+    r.rope = off;
+    off = align256(off + M * (size_t)(W->hd / 2) * sizeof(float2));
     r.attn = off;
     if (W->dtype == DLLM_BF16) off = align256(off + attention_tc_ws_bytes(B, k_max, W->n_q, W->hd, N));
     r.total = off + 256;   // room to align the caller's base
@@ -221,7 +223,7 @@ DLLM_EXPORT int dllm_proxy_score(const void *H, const void *Pt, const float *pro
     if (r % 32) return fail(DLLM_ERR_UNSUPPORTED, "r must be a multiple of 32 (got %d)", r);
     cudaStream_t st = as_stream(stream);
     const int rows = B * N;
-    EpiStoreF32 epi{proxy_cur, r, r};
+    EpiStoreF32 epi{SelRows{}, proxy_cur, r, r};
     cudaError_t e;
     if (dtype == DLLM_BF16) {
         if (d % 64) return fail(DLLM_ERR_UNSUPPORTED, "bf16 path needs d % 64 == 0 (got %d)", d);
@@ -352,6 +354,7 @@ int refresh_impl(const dllm_layer *W, const T *H_in, SelRows sel, int B, T *K_ca
     T *Qc = reinterpret_cast<T *>(ws + L.q);
     T *Ac = reinterpret_cast<T *>(ws + L.a);
     float *h1 = reinterpret_cast<float *>(ws + L.h1);
+    float2 *rope_cs = W->use_rope ? reinterpret_cast<float2 *>(ws + L.rope) : nullptr;
     T *Xn2 = reinterpret_cast<T *>(ws + L.xn2);
     T *U = reinterpret_cast<T *>(ws + L.u);
     unsigned *status = status_ptr();
@@ -365,15 +368,16 @@ int refresh_impl(const dllm_layer *W, const T *H_in, SelRows sel, int B, T *K_ca
     // a3: gather + RMSNorm, proxy cache update
     {
         Launch t(DLLM_KERNEL_GATHER, st);
-        CHECK_CUDA(gather_rmsnorm<T>(H_in, sel, B, d, g1, W->eps, Xn, proxy_cache, proxy_cur, r, status, st),
+        CHECK_CUDA(gather_rmsnorm<T>(H_in, sel, B, d, g1, W->eps, Xn, proxy_cache, proxy_cur, r,
+                                     W->rope_inv_freq, W->hd / 2, rope_cs, status, st),
                    "gather launch");
     }
     // a4: QKV projection, rotary embedding, K/V scattered into the cache
-    EpiQKV<T> eq{Qc, K_cache, V_cache, sel, W->rope_inv_freq, W->n_q, W->n_kv, W->hd, W->use_rope};
+    EpiQKV<T> eq{sel, Qc, K_cache, V_cache, rope_cs, W->n_q, W->n_kv, W->hd, W->use_rope};
     // a6: O projection + residual;  a7: FFN gate/up + SwiGLU;  a8: down + residual, scattered
-    EpiResidual<T> er{h1, H_in, sel, d};
-    EpiSwiGLU<T> es{U, F};
-    EpiDownScatter<T> ed{H_out, h1, sel, d};
+    EpiResidual<T> er{sel, h1, H_in, d};
+    EpiSwiGLU<T> es{SelRows{}, U, F};
+    EpiDownScatter<T> ed{sel, H_out, h1, d};
     if constexpr (sizeof(T) == 2) {
         { Launch t(DLLM_KERNEL_QKV, st); CHECK_CUDA(gemm_tc(wqkv, dq + 2 * dkv, d, Xn, M, eq, 0, status, st), "qkv gemm"); }
         {
@@ -434,6 +438,23 @@ DLLM_EXPORT int dllm_sparse_layer_refresh(const dllm_layer *W, const void *H_in,
                                proxy_cache, proxy_cur, r, w8, st);
 }
 
+// ------------------------------------------------------------------ plain GEMM
+DLLM_EXPORT int dllm_gemm_bf16(const void *X, const void *W, float *out, int M, int N_out, int K,
+                               int splits, void *stream) {
+    CHECK_ARG(X && W && out, "null pointer");
+    CHECK_ARG(M > 0 && N_out > 0 && K > 0, "sizes must be positive");
+    CHECK_ARG(splits >= 0 && splits <= 8, "splits must be in [0, 8]");
+    CHECK_ARG(aligned16(X) && aligned16(W) && aligned16(out), "arrays must be 16-byte aligned");
+    if (K % 64 || N_out % 32) return fail(DLLM_ERR_UNSUPPORTED, "needs K %% 64 == 0 and N_out %% 32 == 0");
+    cudaStream_t st = as_stream(stream);
+    Launch t(DLLM_KERNEL_GEMM, st);
+    EpiStoreF32 epi{SelRows{}, out, N_out, N_out};
+    CHECK_CUDA(gemm_tc(static_cast<const bf16 *>(W), N_out, K, static_cast<const bf16 *>(X), M, epi,
+                       splits, status_ptr(), st),
+               "gemm launch");
+    return DLLM_OK;
+}
+
 // ------------------------------------------------------------------ vocabulary
 DLLM_EXPORT size_t dllm_commit_workspace_bytes(int B, int M, int V) {
     if (B <= 0 || M < 0 || V <= 0) return 0;
@@ -461,7 +482,7 @@ DLLM_EXPORT int dllm_commit_entropy(const float *logits, const uint8_t *valid, i
 
 // ------------------------------------------------------------------ measurement support
 DLLM_EXPORT int dllm_timer_start(int kernel_id, int max_launches) {
-    CHECK_ARG(kernel_id >= DLLM_KERNEL_PROXY_GEMM && kernel_id <= DLLM_KERNEL_VOCAB, "unknown kernel id %d", kernel_id);
+    CHECK_ARG(kernel_id >= DLLM_KERNEL_PROXY_GEMM && kernel_id <= DLLM_KERNEL_GEMM, "unknown kernel id %d", kernel_id);
     CHECK_ARG(max_launches > 0 && max_launches <= 1 << 16, "max_launches must be in [1, 65536]");
     std::lock_guard<std::mutex> lock(g_timer.mu);
     CHECK_ARG(g_timer.armed == 0, "a timer is already armed");

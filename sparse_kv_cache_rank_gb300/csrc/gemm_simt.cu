@@ -52,9 +52,13 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const float *__restrict__ W, 
     for (int j = 0; j < 8; ++j) {
         const int m = m0 + warp * 8 + j;
         if (m >= M_tok) break;
+        int b = 0, pos = -1;
+        if (Epi::kSel) epi.sel.locate(m, b, pos);
 #pragma unroll
-        for (int g = 0; g < 2; ++g)
-            if (f0 + g * 32 < N_out) epi(f0 + g * 32 + lane, m, acc[g][j]);
+        for (int g = 0; g < 2; ++g) {
+            const int f = f0 + g * 32 + lane;
+            if (f0 + g * 32 < N_out) epi(f, m, b, pos, acc[g][j], epi.pre(f, m, b, pos));
+        }
     }
 }
 

@@ -26,6 +26,8 @@ constexpr int BK = 64;                 // K per stage: one 128-byte swizzled row
 constexpr int kThreads = 192;
 constexpr int kWBytes = BM * BK * 2;   // 16 KB
 constexpr int kSmemLimit = 232448;     // 227 KB dynamic shared memory per CTA
+constexpr int kTailBytes = 256;        // barriers, TMEM slot, abort flag
+constexpr int kColBytes = 2 * 256 * 4; // per-column (sequence, position)
 
 struct Shape {
     int M_tok, N_out, K;
@@ -47,6 +49,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *done = empty + g.stages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int *col_b = reinterpret_cast<int *>(smem + g.body_bytes + kTailBytes);   // [BN]
+    int *col_pos = col_b + 256;                                                // [BN]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * g.BN;
@@ -117,6 +121,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {   // ---------------- epilogue warps: TMEM -> partial tile [BN][128] fp32
         const int q = warp & 3;   // TMEM lane quarter this warp may access
+        // while the main loop runs: resolve every token column's (sequence, position)
+        for (int c = threadIdx.x - 64; c < g.BN; c += kThreads - 64) {
+            int b = 0, pos = -1;
+            if (Epi::kSel && m0 + c < g.M_tok) epi.sel.locate(m0 + c, b, pos);
+            col_b[c] = b;
+            col_pos[c] = pos;
+        }
         mbar_wait(done, 0, abort_flag, status);
         tc_fence_after();
         float *part = reinterpret_cast<float *>(smem);
@@ -140,22 +151,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int f = q * 32 + lane;
         const int per = (g.BN + g.splits - 1) / g.splits;
         const int c_begin = split * per;
-        const int c_end = min(g.BN, c_begin + per);
+        const int c_end = min(min(g.BN, c_begin + per), g.M_tok - m0);
         const float *part = reinterpret_cast<const float *>(smem);
-        const uint32_t part_s = smem_u32(smem);
+        const uint32_t part_s = smem_u32(smem) + (uint32_t)f * 4u;
         if (n0 + q * 32 < g.N_out) {   // warp-uniform: N_out % 32 == 0
-            for (int c = c_begin; c < c_end; ++c) {
-                const int m = m0 + c;
-                if (m >= g.M_tok) break;
-                float acc;
+            // 8 columns per batch: every shared / remote / global load of the batch is
+            // issued before the first one is consumed
+            for (int c = c_begin; c < c_end; c += 8) {
+                float acc[8], pre[8];
                 if (g.splits == 1) {
-                    acc = part[c * BM + f];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[j] = part[min(c + j, c_end - 1) * BM + f];
                 } else {
-                    acc = 0.f;
-                    const uint32_t a = part_s + (uint32_t)(c * BM + f) * 4u;
-                    for (int r = 0; r < g.splits; ++r) acc += ld_dsmem_f32(mapa_shared(a, (uint32_t)r));
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+                    for (int r = 0; r < g.splits; ++r) {
+                        const uint32_t base = mapa_shared(part_s, (uint32_t)r);
+                        float v[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            v[j] = ld_dsmem_f32(base + (uint32_t)(min(c + j, c_end - 1) * BM) * 4u);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) acc[j] += v[j];
+                    }
                 }
-                epi(n0 + f, m, acc);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int cc = min(c + j, c_end - 1);
+                    pre[j] = epi.pre(n0 + f, m0 + cc, col_b[cc], col_pos[cc]);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (c + j < c_end) epi(n0 + f, m0 + c + j, col_b[c + j], col_pos[c + j], acc[j], pre[j]);
             }
         }
     }
@@ -224,12 +251,12 @@ Plan plan_gemm(int M_tok, int N_out, int K, int splits_req) {
     if (s > KB) s = KB;
     p.splits = s < 1 ? 1 : s;
     const int sb = stage_bytes(BN);
-    const int tail = 1024 + (2 * 8 + 1) * 8 + 64;
+    const int tail = 1024 + kTailBytes + kColBytes;
     p.stages = (kSmemLimit - tail) / sb;
     if (p.stages > 8) p.stages = 8;
     const int part = BN * BM * 4;
     p.body = p.stages * sb > part ? p.stages * sb : part;
-    p.smem = (size_t)1024 + p.body + (2 * p.stages + 1) * 8 + 64;
+    p.smem = (size_t)1024 + p.body + kTailBytes + kColBytes;
     return p;
 }
 

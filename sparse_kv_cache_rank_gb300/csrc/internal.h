@@ -29,8 +29,8 @@ cudaError_t gemm_simt(const float *W, int N_out, int K, const float *X, int M_to
 // ---------------------------------------------------------------- row kernels
 template <class T>
 cudaError_t gather_rmsnorm(const T *H, SelRows sel, int B, int d, const T *gamma, float eps, T *Xn,
-                           float *proxy_cache, const float *proxy_cur, int r, unsigned *status,
-                           cudaStream_t st);
+                           float *proxy_cache, const float *proxy_cur, int r, const float *inv_freq,
+                           int half_hd, float2 *rope_cs, unsigned *status, cudaStream_t st);
 
 template <class T>
 cudaError_t rmsnorm_rows(const float *h1, int M, int d, const T *gamma, float eps, T *Xn2,

@@ -27,19 +27,26 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
 }
 
 // Xn[m] = RMSNorm(H[b, pos]) * gamma1 for the live selected rows, zeros otherwise;
-// proxy_cache[b, pos] <- proxy_cur[b, pos].
+// proxy_cache[b, pos] <- proxy_cur[b, pos];  rope_cs[m, i] = (cos, sin) of the rotary
+// angle pos * inv_freq[i] (fp32), used by the QKV epilogue.
 template <class T>
 __global__ void __launch_bounds__(256) k_gather_rmsnorm(const T *__restrict__ H, SelRows sel, int d,
                                                         const T *__restrict__ gamma, float eps,
                                                         T *__restrict__ Xn, float *proxy_cache,
                                                         const float *proxy_cur, int r,
-                                                        unsigned *status) {
+                                                        const float *inv_freq, int half_hd,
+                                                        float2 *rope_cs, unsigned *status) {
     __shared__ float red[33];
     const int m = blockIdx.x;
     int b, pos;
     sel.locate(m, b, pos);
     if (threadIdx.x == 0 && m % sel.k_max == 0 && sel.count[b] > sel.k_max)
         raise_status(status, DLLM_STATUS_COUNT_CLAMP);
+    if (rope_cs && threadIdx.x < half_hd) {
+        float sn = 0.f, cs = 1.f;
+        if (pos >= 0) sincosf((float)pos * inv_freq[threadIdx.x], &sn, &cs);
+        rope_cs[(size_t)m * half_hd + threadIdx.x] = make_float2(cs, sn);
+    }
     T *out = Xn + (size_t)m * d;
     if (pos < 0) {
         for (int e = threadIdx.x; e < d; e += 256) out[e] = from_f32<T>(0.f);
@@ -145,11 +152,12 @@ __global__ void k_rope_inv_freq(float *dst, int hd, float theta) {
 
 template <class T>
 cudaError_t gather_rmsnorm(const T *H, SelRows sel, int B, int d, const T *gamma, float eps, T *Xn,
-                           float *proxy_cache, const float *proxy_cur, int r, unsigned *status,
-                           cudaStream_t st) {
+                           float *proxy_cache, const float *proxy_cur, int r, const float *inv_freq,
+                           int half_hd, float2 *rope_cs, unsigned *status, cudaStream_t st) {
     const int M = B * sel.k_max;
     if (M <= 0) return cudaSuccess;
-    k_gather_rmsnorm<T><<<M, 256, 0, st>>>(H, sel, d, gamma, eps, Xn, proxy_cache, proxy_cur, r, status);
+    k_gather_rmsnorm<T><<<M, 256, 0, st>>>(H, sel, d, gamma, eps, Xn, proxy_cache, proxy_cur, r,
+                                           inv_freq, half_hd, rope_cs, status);
     return cudaGetLastError();
 }
 
@@ -189,7 +197,8 @@ cudaError_t rope_inv_freq(float *dst, int hd, float theta, cudaStream_t st) {
 
 #define DLLM_ROWOPS(T)                                                                           \
     template cudaError_t gather_rmsnorm<T>(const T *, SelRows, int, int, const T *, float, T *,  \
-                                           float *, const float *, int, unsigned *, cudaStream_t); \
+                                           float *, const float *, int, const float *, int, float2 *,   \
+                                           unsigned *, cudaStream_t);                                   \
     template cudaError_t rmsnorm_rows<T>(const float *, int, int, const T *, float, T *,         \
                                          cudaStream_t);                                          \
     template cudaError_t pack_rows_rope<T>(const T *, T *, int, int, int, cudaStream_t);         \

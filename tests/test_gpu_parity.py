@@ -231,3 +231,18 @@ def test_commit_no_valid_rows(B):
     valid = torch.zeros((2, 4), dtype=torch.uint8, device="cuda")
     tok, conf, ent, E, full = B.dllm_commit_entropy(logits, valid)
     assert (tok == -1).all().item() and (E == 0).all().item() and (full == 0).all().item()
+
+
+# --------------------------------------------------------------------------- plain GEMM
+@pytest.mark.parametrize("M,N_out,K,splits", [(1, 32, 64, 0), (37, 96, 192, 0), (164, 512, 1024, 1),
+                                              (164, 512, 1024, 4), (300, 384, 640, 0),
+                                              (513, 256, 2048, 8), (64, 4096, 4096, 0)])
+def test_gemm_bf16_parity(B, orc, M, N_out, K, splits):
+    """The engine under every projection: X W^T against the oracle's double-precision
+    projection (the proxy score computes exactly H . P), ragged M, K splits 1..8."""
+    g = synth.rng(3000 + M + K)
+    X = synth.round_bf16(g.standard_normal((M, K), dtype=np.float32))
+    W = synth.round_bf16((g.standard_normal((N_out, K)) * 0.05).astype(np.float32))
+    out = B.dllm_gemm_bf16(to_dev(X, torch.bfloat16), to_dev(W, torch.bfloat16), splits=splits)
+    ref, _ = orc.proxy_score(X[None], np.ascontiguousarray(W.T), np.ones((1, M, N_out), np.float32))
+    assert normwise_rel(to_np(out), ref[0]) < FP32_REDUCTION_RTOL
