@@ -9,10 +9,14 @@
 //   * SwiGLU gate j and up j are packed as rows 2j, 2j+1.
 // Token rows are the flattened selection m = b * k_max + s; a row is live when
 // s < min(count[b], k_max) and then refers to sequence position pos = idx[b, s].
-// The GEMM resolves (b, pos) once per token column (pos < 0: not live) and passes
-// it with every call; epilogues with kSel == false ignore it.  pre() is the one
-// global value an epilogue reads per output (residual input, h1); the GEMM issues
-// it for a batch of columns before consuming any, so those loads overlap.
+//
+// Interface of an epilogue E:
+//   E::kSel            the GEMM resolves (b, pos) of every token column (else b = 0, pos = -1)
+//   E::Feat feat(f)    per-weight-row constants, computed once per thread
+//   float2 pre(F, m, b, pos)            the global values one output needs (residual
+//                                       input, rotary cos/sin); the GEMM issues them for a
+//                                       batch of columns before consuming any
+//   operator()(F, m, b, pos, acc, pre)  writes the output(s)
 #pragma once
 
 #include "common.cuh"
@@ -38,15 +42,21 @@ struct SelRows {
     }
 };
 
+struct FeatRow {
+    int f;
+};
+
 // out[m, f] = acc (fp32), for f < n_valid.  Singular proxy and plain GEMM.
 struct EpiStoreF32 {
     static constexpr bool kSel = false;
+    using Feat = FeatRow;
     SelRows sel;
     float *out;
     int ld, n_valid;
-    __device__ __forceinline__ float pre(int, int, int, int) const { return 0.f; }
-    __device__ __forceinline__ void operator()(int f, int m, int, int, float acc, float) const {
-        if (f < n_valid) out[(size_t)m * ld + f] = acc;
+    __device__ __forceinline__ Feat feat(int f) const { return {f}; }
+    __device__ __forceinline__ float2 pre(const Feat &, int, int, int) const { return {0.f, 0.f}; }
+    __device__ __forceinline__ void operator()(const Feat &F, int m, int, int, float acc, float2) const {
+        if (F.f < n_valid) out[(size_t)m * ld + F.f] = acc;
     }
 };
 
@@ -62,27 +72,38 @@ struct EpiQKV {
     const float2 *rope_cs;
     int n_q, n_kv, hd, use_rope;
 
-    __device__ __forceinline__ float pre(int, int, int, int) const { return 0.f; }
-    __device__ __forceinline__ void operator()(int f, int m, int b, int pos, float acc, float) const {
-        const float partner = __shfl_xor_sync(0xffffffffu, acc, 1);
+    struct Feat {
+        int region;     // 0 Q, 1 K, 2 V
+        int col;        // head * hd + dim: output column inside Q / K / V
+        int i;          // rotary pair index
+        int odd;        // second half of the pair
+    };
+    __device__ __forceinline__ Feat feat(int f) const {
         const int dq = n_q * hd, dkv = n_kv * hd;
-        int region, g;
-        if (f < dq) { region = 0; g = f; }
-        else if (f < dq + dkv) { region = 1; g = f - dq; }
-        else { region = 2; g = f - dq - dkv; }
+        Feat F;
+        int g;
+        if (f < dq) { F.region = 0; g = f; }
+        else if (f < dq + dkv) { F.region = 1; g = f - dq; }
+        else { F.region = 2; g = f - dq - dkv; }
         const int head = g / hd, p = g - head * hd;
-        const int i = p >> 1, odd = p & 1;
-        const int dim = odd ? i + (hd >> 1) : i;
-        float out = acc;
-        if (use_rope && region < 2) {
-            const float2 cs = rope_cs[(size_t)m * (hd >> 1) + i];
-            out = odd ? (acc * cs.x + partner * cs.y) : (acc * cs.x - partner * cs.y);
-        }
-        if (region == 0) {
-            Q[(size_t)m * dq + (size_t)head * hd + dim] = from_f32<T>(out);
+        F.i = p >> 1;
+        F.odd = p & 1;
+        F.col = head * hd + (F.odd ? F.i + (hd >> 1) : F.i);
+        return F;
+    }
+    __device__ __forceinline__ float2 pre(const Feat &F, int m, int, int) const {
+        if (!use_rope || F.region == 2) return {1.f, 0.f};
+        return rope_cs[(size_t)m * (hd >> 1) + F.i];
+    }
+    __device__ __forceinline__ void operator()(const Feat &F, int m, int b, int pos, float acc,
+                                               float2 cs) const {
+        const float partner = __shfl_xor_sync(0xffffffffu, acc, 1);
+        const float out = F.odd ? fmaf(acc, cs.x, partner * cs.y) : fmaf(acc, cs.x, -partner * cs.y);
+        if (F.region == 0) {
+            Q[(size_t)m * (n_q * hd) + F.col] = from_f32<T>(out);
         } else if (pos >= 0) {
-            T *dst = region == 1 ? Kc : Vc;
-            dst[(((size_t)b * sel.N + pos) * n_kv + head) * hd + dim] = from_f32<T>(out);
+            T *dst = F.region == 1 ? Kc : Vc;
+            dst[((size_t)b * sel.N + pos) * (size_t)(n_kv * hd) + F.col] = from_f32<T>(out);
         }
     }
 };
@@ -91,15 +112,18 @@ struct EpiQKV {
 template <class T>
 struct EpiResidual {
     static constexpr bool kSel = true;
+    using Feat = FeatRow;
     SelRows sel;
     float *h1;          // [M, d]
     const T *H_in;      // [B, N, d]
     int d;
-    __device__ __forceinline__ float pre(int f, int, int b, int pos) const {
-        return pos >= 0 ? to_f32<T>(H_in[((size_t)b * sel.N + pos) * d + f]) : 0.f;
+    __device__ __forceinline__ Feat feat(int f) const { return {f}; }
+    __device__ __forceinline__ float2 pre(const Feat &F, int, int b, int pos) const {
+        return {pos >= 0 ? to_f32<T>(H_in[((size_t)b * sel.N + pos) * d + F.f]) : 0.f, 0.f};
     }
-    __device__ __forceinline__ void operator()(int f, int m, int, int pos, float acc, float hin) const {
-        h1[(size_t)m * d + f] = pos >= 0 ? hin + acc : 0.f;
+    __device__ __forceinline__ void operator()(const Feat &F, int m, int, int pos, float acc,
+                                               float2 hin) const {
+        h1[(size_t)m * d + F.f] = pos >= 0 ? hin.x + acc : 0.f;
     }
 };
 
@@ -107,13 +131,15 @@ struct EpiResidual {
 template <class T>
 struct EpiSwiGLU {
     static constexpr bool kSel = false;
+    using Feat = FeatRow;
     SelRows sel;
     T *U;               // [M, F]
     int F;
-    __device__ __forceinline__ float pre(int, int, int, int) const { return 0.f; }
-    __device__ __forceinline__ void operator()(int f, int m, int, int, float acc, float) const {
+    __device__ __forceinline__ Feat feat(int f) const { return {f}; }
+    __device__ __forceinline__ float2 pre(const Feat &, int, int, int) const { return {0.f, 0.f}; }
+    __device__ __forceinline__ void operator()(const Feat &Fr, int m, int, int, float acc, float2) const {
         const float partner = __shfl_xor_sync(0xffffffffu, acc, 1);
-        if ((f & 1) == 0) U[(size_t)m * F + (f >> 1)] = from_f32<T>(silu(acc) * partner);
+        if ((Fr.f & 1) == 0) U[(size_t)m * F + (Fr.f >> 1)] = from_f32<T>(silu(acc) * partner);
     }
 };
 
@@ -121,15 +147,18 @@ struct EpiSwiGLU {
 template <class T>
 struct EpiDownScatter {
     static constexpr bool kSel = true;
+    using Feat = FeatRow;
     SelRows sel;
     T *H_out;           // [B, N, d]
     const float *h1;    // [M, d]
     int d;
-    __device__ __forceinline__ float pre(int f, int m, int, int pos) const {
-        return pos >= 0 ? h1[(size_t)m * d + f] : 0.f;
+    __device__ __forceinline__ Feat feat(int f) const { return {f}; }
+    __device__ __forceinline__ float2 pre(const Feat &F, int m, int, int pos) const {
+        return {pos >= 0 ? h1[(size_t)m * d + F.f] : 0.f, 0.f};
     }
-    __device__ __forceinline__ void operator()(int f, int, int b, int pos, float acc, float h) const {
-        if (pos >= 0) H_out[((size_t)b * sel.N + pos) * d + f] = from_f32<T>(h + acc);
+    __device__ __forceinline__ void operator()(const Feat &F, int, int b, int pos, float acc,
+                                               float2 h) const {
+        if (pos >= 0) H_out[((size_t)b * sel.N + pos) * d + F.f] = from_f32<T>(h.x + acc);
     }
 };
 

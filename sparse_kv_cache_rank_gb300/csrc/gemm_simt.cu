@@ -56,8 +56,10 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const float *__restrict__ W, 
         if (Epi::kSel) epi.sel.locate(m, b, pos);
 #pragma unroll
         for (int g = 0; g < 2; ++g) {
-            const int f = f0 + g * 32 + lane;
-            if (f0 + g * 32 < N_out) epi(f, m, b, pos, acc[g][j], epi.pre(f, m, b, pos));
+            if (f0 + g * 32 < N_out) {
+                const typename Epi::Feat F = epi.feat(f0 + g * 32 + lane);
+                epi(F, m, b, pos, acc[g][j], epi.pre(F, m, b, pos));
+            }
         }
     }
 }

@@ -4,14 +4,19 @@
 // acc[f, m] = <W[f, :], X[m, :]>: the weight tile (128 rows of W) is the MMA's
 // A operand (M = 128) and a tile of BN token rows is its B operand (N = BN), so a
 // GEMM over few gathered tokens (the selected rows) wastes no MMA rows on padding.
-// Every CTA owns one (weight tile, token tile) pair and, when the tiles alone
-// cannot fill the GPU, a K slice of it: the CTAs of one K split form a
-// thread-block cluster and reduce their fp32 partial tiles through distributed
-// shared memory, then share the epilogue.  Weight bytes are read from HBM once.
+// Each CTA owns one (weight tile, token tile) pair, and, when the tiles alone cannot
+// fill the GPU, one K slice of it: the CTAs of one K split form a thread-block
+// cluster and reduce their fp32 partial tiles through distributed shared memory.
+// Weight bytes are read from HBM once (token tiles of one weight tile run side by
+// side and share it through L2).
 //
-// Roles (192 threads):  warp 0 lane 0  TMA producer (multi-stage ring)
-//                       warp 1         TMEM owner; lane 0 issues the MMAs
-//                       warps 2..5     TMEM -> shared partial tile -> epilogue
+// Roles (320 threads):  warp 0 lane 0   TMA producer (multi-stage ring)
+//                       warp 1          TMEM owner; lane 0 issues the MMAs
+//                       warps 2..9      epilogue, two warps per TMEM lane quarter,
+//                                       each taking half of the token columns
+// Without a K split the epilogue reads the accumulator straight from TMEM and the
+// CTA needs no shared memory beyond the ring, so two CTAs fit on an SM and one
+// CTA's epilogue overlaps the other's main loop.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -23,22 +28,41 @@ namespace {
 
 constexpr int BM = 128;                // weight rows per tile (MMA M)
 constexpr int BK = 64;                 // K per stage: one 128-byte swizzled row of bf16
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
 constexpr int kWBytes = BM * BK * 2;   // 16 KB
 constexpr int kSmemLimit = 232448;     // 227 KB dynamic shared memory per CTA
+constexpr int kSmemPair = 113 * 1024;  // budget per CTA when two share an SM
 constexpr int kTailBytes = 256;        // barriers, TMEM slot, abort flag
 constexpr int kColBytes = 2 * 256 * 4; // per-column (sequence, position)
 
 struct Shape {
     int M_tok, N_out, K;
     int BN, splits, stages;
-    int body_bytes;   // pipeline ring, reused for the fp32 partial tile [BN][128]
+    int body_bytes;   // pipeline ring (and, with a K split, the fp32 partial tile [BN][128])
 };
 
 __host__ __device__ inline int stage_bytes(int BN) { return kWBytes + BN * BK * 2; }
 
+// Applies the epilogue to 16 consecutive token columns c0.. of feature row F held in
+// v[]: the global values of all 16 outputs are requested before the first is written.
 template <class Epi>
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ void epi_16(const Epi &epi, const typename Epi::Feat &F, int m0, int c0,
+                                       int ncols, const int *col_b, const int *col_pos,
+                                       const float (&v)[16]) {
+    float2 pr[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int cc = min(c0 + j, ncols - 1);
+        pr[j] = epi.pre(F, m0 + cc, col_b[cc], col_pos[cc]);
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        if (c0 + j < ncols) epi(F, m0 + c0 + j, col_b[c0 + j], col_pos[c0 + j], v[j], pr[j]);
+}
+
+template <class Epi>
+__global__ void __launch_bounds__(kThreads, 2)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
               const Shape g, const Epi epi, unsigned *status) {
     extern __shared__ uint8_t smem_raw[];
@@ -62,6 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nkb = kb1 - kb0;
     const uint32_t tmem_cols = g.BN <= 32 ? 32u : g.BN <= 64 ? 64u : g.BN <= 128 ? 128u : 256u;
     const int sbytes = stage_bytes(g.BN);
+    const int ncols = min(g.BN, g.M_tok - m0);   // live token columns of this tile
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < g.stages; ++s) {
@@ -119,75 +144,84 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mma_commit(done);
         }
-    } else {   // ---------------- epilogue warps: TMEM -> partial tile [BN][128] fp32
-        const int q = warp & 3;   // TMEM lane quarter this warp may access
-        // while the main loop runs: resolve every token column's (sequence, position)
+    } else {
+        // ---------------- epilogue warps (2..9): resolve every token column's (sequence,
+        // position) while the main loop runs
         for (int c = threadIdx.x - 64; c < g.BN; c += kThreads - 64) {
             int b = 0, pos = -1;
-            if (Epi::kSel && m0 + c < g.M_tok) epi.sel.locate(m0 + c, b, pos);
+            if (Epi::kSel && c < ncols) epi.sel.locate(m0 + c, b, pos);
             col_b[c] = b;
             col_pos[c] = pos;
         }
+        named_bar_sync(1, kEpiWarps * 32);
         mbar_wait(done, 0, abort_flag, status);
         tc_fence_after();
-        float *part = reinterpret_cast<float *>(smem);
+        const int q = warp & 3;                  // TMEM lane quarter this warp may access
+        const int half = (warp - 2) >> 2;        // which half of the columns
         const int f = q * 32 + lane;
-        for (int c0 = 0; c0 < g.BN; c0 += 16) {
-            float v[16];
-            tmem_ld_x16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) part[(c0 + j) * BM + f] = v[j];
-        }
-    }
-    tc_fence_before();
-    if (g.splits > 1)
-        cluster_sync_all();
-    else
-        __syncthreads();
-
-    if (warp >= 2) {   // ---------------- K-split reduction + epilogue over this CTA's columns
-        const int q = warp & 3;
-        const int f = q * 32 + lane;
-        const int per = (g.BN + g.splits - 1) / g.splits;
-        const int c_begin = split * per;
-        const int c_end = min(min(g.BN, c_begin + per), g.M_tok - m0);
-        const float *part = reinterpret_cast<const float *>(smem);
-        const uint32_t part_s = smem_u32(smem) + (uint32_t)f * 4u;
-        if (n0 + q * 32 < g.N_out) {   // warp-uniform: N_out % 32 == 0
-            // 8 columns per batch: every shared / remote / global load of the batch is
-            // issued before the first one is consumed
-            for (int c = c_begin; c < c_end; c += 8) {
-                float acc[8], pre[8];
-                if (g.splits == 1) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[j] = part[min(c + j, c_end - 1) * BM + f];
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-                    for (int r = 0; r < g.splits; ++r) {
-                        const uint32_t base = mapa_shared(part_s, (uint32_t)r);
-                        float v[8];
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            v[j] = ld_dsmem_f32(base + (uint32_t)(min(c + j, c_end - 1) * BM) * 4u);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) acc[j] += v[j];
-                    }
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
+        const int nchunk = (g.BN + 15) / 16;
+        const int ch0 = half == 0 ? 0 : (nchunk + 1) / 2, ch1 = half == 0 ? (nchunk + 1) / 2 : nchunk;
+        if (g.splits == 1) {
+            // straight from TMEM
+            if (n0 + q * 32 < g.N_out) {   // warp-uniform: N_out % 32 == 0
+                const typename Epi::Feat F = epi.feat(n0 + f);
+                for (int ch = ch0; ch < ch1 && ch * 16 < ncols; ++ch) {
+                    float v[16];
+                    tmem_ld_x16(taddr + (uint32_t)(ch * 16), v);
+                    tmem_ld_wait();
+                    epi_16(epi, F, m0, ch * 16, ncols, col_b, col_pos, v);
                 }
+            }
+        } else {
+            // K split: fp32 partial tile [BN][128] into this CTA's shared memory
+            float *part = reinterpret_cast<float *>(smem);
+            for (int ch = ch0; ch < ch1; ++ch) {
+                float v[16];
+                tmem_ld_x16(taddr + (uint32_t)(ch * 16), v);
+                tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int cc = min(c + j, c_end - 1);
-                    pre[j] = epi.pre(n0 + f, m0 + cc, col_b[cc], col_pos[cc]);
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (c + j < c_end) epi(n0 + f, m0 + c + j, col_b[c + j], col_pos[c + j], acc[j], pre[j]);
+                for (int j = 0; j < 16; ++j) part[(ch * 16 + j) * BM + f] = v[j];
             }
         }
     }
-    if (g.splits > 1) cluster_sync_all();   // peers may still read this CTA's partial tile
-    __syncthreads();
+    tc_fence_before();
+    if (g.splits > 1) {
+        cluster_sync_all();
+        if (warp >= 2) {   // ---------------- reduce the cluster's partials, epilogue on my share
+            const int q = warp & 3;
+            const int half = (warp - 2) >> 2;
+            const int f = q * 32 + lane;
+            const int per = (((g.BN + g.splits - 1) / g.splits) + 15) / 16 * 16;
+            const int cb = split * per;
+            const int ce = min(min(g.BN, cb + per), ncols);
+            const int hper = (((ce - cb) + 1) / 2 + 15) / 16 * 16;
+            const int c_begin = cb + half * hper;
+            const int c_end = half == 0 ? min(ce, cb + hper) : ce;
+            const uint32_t part_s = smem_u32(smem) + (uint32_t)f * 4u;
+            if (n0 + q * 32 < g.N_out) {
+                const typename Epi::Feat F = epi.feat(n0 + f);
+                for (int c = c_begin; c < c_end; c += 16) {
+                    float acc[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+                    for (int r = 0; r < g.splits; ++r) {
+                        const uint32_t base = mapa_shared(part_s, (uint32_t)r);
+                        float v[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            v[j] = ld_dsmem_f32(base + (uint32_t)(min(c + j, c_end - 1) * BM) * 4u);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[j] += v[j];
+                    }
+                    epi_16(epi, F, m0, c, c_end, col_b, col_pos, acc);
+                }
+            }
+        }
+        cluster_sync_all();   // peers may still read this CTA's partial tile
+    } else {
+        __syncthreads();
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, tmem_cols);
@@ -234,30 +268,60 @@ struct Plan {
 
 int round16(int x) { return (x + 15) / 16 * 16; }
 
-Plan plan_gemm(int M_tok, int N_out, int K, int splits_req) {
-    const int sms = num_sms();
+Plan make_plan(int M_tok, int N_out, int K, int BN, int splits, int budget) {
     Plan p{};
-    p.w_tiles = (N_out + BM - 1) / BM;
-    const int KB = K / BK;
-    int BN = M_tok <= 256 ? round16(M_tok) : 256;
-    // smaller token tiles when even an 8-way K split would leave most SMs idle
-    while (BN > 64 && (long long)p.w_tiles * ((M_tok + BN - 1) / BN) * 8 < sms) BN = round16(BN / 2);
     p.BN = BN;
+    p.splits = splits;
+    p.w_tiles = (N_out + BM - 1) / BM;
     p.tok_tiles = (M_tok + BN - 1) / BN;
-    const long long tiles = (long long)p.tok_tiles * p.w_tiles;
-    int s = splits_req > 0 ? splits_req : (int)(sms / tiles);
-    s = s < 1 ? 1 : (s > 8 ? 8 : s);
-    while (s > 1 && KB / s < 2) --s;
-    if (s > KB) s = KB;
-    p.splits = s < 1 ? 1 : s;
     const int sb = stage_bytes(BN);
     const int tail = 1024 + kTailBytes + kColBytes;
-    p.stages = (kSmemLimit - tail) / sb;
+    const int part = splits > 1 ? BN * BM * 4 : 0;
+    p.stages = (budget - tail) / sb;
     if (p.stages > 8) p.stages = 8;
-    const int part = BN * BM * 4;
+    const int KB = K / BK;
+    if (p.stages > KB / splits + 1) p.stages = KB / splits + 1 > 2 ? KB / splits + 1 : 2;
     p.body = p.stages * sb > part ? p.stages * sb : part;
     p.smem = (size_t)1024 + p.body + kTailBytes + kColBytes;
     return p;
+}
+
+// Few tokens (the gathered rows of a step) make every projection a weight stream:
+// what matters is that every SM streams weights and that epilogues overlap main loops.
+//  * many weight tiles (>= half the SMs): no K split, two CTAs per SM; a second token
+//    tile when the weight tiles alone would leave SMs idle;
+//  * few weight tiles: a K split across a cluster sized to fill the SMs.
+// Many tokens (compute-bound): 256-column token tiles, K split only to fill the GPU.
+Plan plan_gemm(int M_tok, int N_out, int K, int splits_req) {
+    const int sms = num_sms();
+    const int w_tiles = (N_out + BM - 1) / BM;
+    const int KB = K / BK;
+    auto clamp_splits = [&](int s) {
+        s = s < 1 ? 1 : (s > 8 ? 8 : s);
+        while (s > 1 && KB / s < 2) --s;
+        return s;
+    };
+    if (splits_req > 0) {
+        const int BN = M_tok <= 256 ? round16(M_tok) : 256;
+        const int s = clamp_splits(splits_req);
+        return make_plan(M_tok, N_out, K, BN, s, s == 1 ? kSmemPair : kSmemLimit);
+    }
+    if (M_tok <= 256) {
+        if (2 * w_tiles >= sms) {
+            int BN = round16(M_tok);
+            if (w_tiles < sms && M_tok > 32) BN = round16((M_tok + 1) / 2);
+            return make_plan(M_tok, N_out, K, BN, 1, kSmemPair);
+        }
+        int BN = round16(M_tok);
+        const int tok_tiles = 1;
+        const int s = clamp_splits(sms / (w_tiles * tok_tiles));
+        return make_plan(M_tok, N_out, K, BN, s, s == 1 ? kSmemPair : kSmemLimit);
+    }
+    int BN = 256;
+    while (BN > 64 && (long long)w_tiles * ((M_tok + BN - 1) / BN) * 8 < sms) BN = round16(BN / 2);
+    const long long tiles = (long long)w_tiles * ((M_tok + BN - 1) / BN);
+    const int s = tiles >= sms ? 1 : clamp_splits((int)(sms / tiles));
+    return make_plan(M_tok, N_out, K, BN, s, s == 1 ? kSmemPair : kSmemLimit);
 }
 
 }  // namespace
@@ -275,8 +339,14 @@ cudaError_t gemm_tc(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, c
         return cudaErrorInvalidValue;
     Shape g{M_tok, N_out, K, p.BN, p.splits, p.stages, p.body};
     auto kern = k_gemm_tc<Epi>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem);
-    if (e != cudaSuccess) return e;
+    static bool configured[64] = {};   // per device: raise the shared-memory limit once
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = true;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.tok_tiles, p.w_tiles, p.splits);
     cfg.blockDim = dim3(kThreads);
