@@ -205,6 +205,23 @@ int dllm_commit_entropy(const float *logits, const uint8_t *valid, int B, int M,
                         size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * Around the layers of a denoising step ([EC] step 1: the forward pass; step 2:
+ * decode from the logits of the current block).
+ *
+ * dllm_embed: H[b, i] = E[tokens[b, i]] for every i (rows == NULL) or for the R
+ *   positions rows[b, 0..R) (entries outside [0, N) skipped); token ids outside
+ *   [0, V) give a zero row.  E [V, d], tokens [B, N] int32, H [B, N, d], dtype.
+ * dllm_rows_rmsnorm: out[b*R + j] = RMSNorm(H[b, rows[b, j]]) * gamma (zeros for
+ *   entries outside [0, N)): the final norm of the rows fed to the LM head.
+ *   H [B, N, d], rows [B, R] int32, gamma [d], out [B*R, d], dtype.
+ * ------------------------------------------------------------------------- */
+int dllm_embed(const void *E, const int32_t *tokens, const int32_t *rows, int R, void *H, int B,
+               int N, int d, int V, int dtype, void *stream);
+
+int dllm_rows_rmsnorm(const void *H, const int32_t *rows, int R, const void *gamma, float eps,
+                      void *out, int B, int N, int d, int dtype, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Plain product on the tensor cores, the engine under every bf16 projection above
  * (and the LM head of the vocabulary step: logits = RMSNorm(h) W_lm^T):
  *   out[m, f] = sum_k X[m, k] W[f, k]          (fp32 accumulation and output)
@@ -235,6 +252,12 @@ int dllm_gemm_bf16(const void *X, const void *W, float *out, int M, int N_out, i
 #define DLLM_KERNEL_DOWN 10
 #define DLLM_KERNEL_VOCAB 11
 #define DLLM_KERNEL_GEMM 12
+
+/* Launch mode of the library's kernels: with enable != 0 (the default) consecutive
+ * kernels on a stream use programmatic dependent launch (a kernel's prologue and its
+ * weight loads overlap the previous kernel's tail; it reads produced data only after
+ * that kernel has completed).  Returns the previous setting.  Host function. */
+int dllm_set_pdl(int enable);
 
 int dllm_timer_start(int kernel_id, int max_launches);
 int dllm_timer_stop(double *total_ms, int *launches);

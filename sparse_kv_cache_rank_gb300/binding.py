@@ -55,11 +55,16 @@ _SIGS = {
                                             C.c_void_p, C.c_int, C.c_void_p, C.c_void_p,
                                             C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
                                             C.c_int, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "dllm_set_pdl": (C.c_int, [C.c_int]),
     "dllm_timer_start": (C.c_int, [C.c_int, C.c_int]),
     "dllm_timer_stop": (C.c_int, [C.POINTER(C.c_double), C.POINTER(C.c_int)]),
     "dllm_launch_count": (C.c_ulonglong, []),
     "dllm_gemm_bf16": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                  C.c_int, C.c_void_p]),
+    "dllm_embed": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_void_p] + [C.c_int] * 5
+                   + [C.c_void_p]),
+    "dllm_rows_rmsnorm": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_void_p, C.c_float, C.c_void_p]
+                          + [C.c_int] * 4 + [C.c_void_p]),
     "dllm_commit_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
     "dllm_commit_entropy": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                       C.c_float, C.c_float] + [C.c_void_p] * 6 +
@@ -161,6 +166,11 @@ def dllm_launch_count() -> int:
     return int(lib().dllm_launch_count())
 
 
+def dllm_set_pdl(enable: bool) -> bool:
+    """Programmatic dependent launch between the library's kernels (default on)."""
+    return bool(lib().dllm_set_pdl(1 if enable else 0))
+
+
 # --------------------------------------------------------------------------- proxy
 def dllm_proxy_score(H, Pt, proxy_cache, proxy_cur=None, drift=None):
     """H [B,N,d] (bf16|f32), Pt [r,d] same dtype, proxy_cache [B,N,r] f32 ->
@@ -179,11 +189,30 @@ def dllm_proxy_score(H, Pt, proxy_cache, proxy_cur=None, drift=None):
     return proxy_cur, drift
 
 
-def build_proxy_matrix(w_v: torch.Tensor, gamma1: torch.Tensor, r: int) -> torch.Tensor:
+def build_proxy_matrix(w_v: torch.Tensor, gamma1: torch.Tensor, r: int, method: str = "svd",
+                       generator=None, oversample: int = 16, iters: int = 4) -> torch.Tensor:
     """One-time set-up (not part of the per-step path): Pt = (U_r S_r)^T of
-    diag(gamma1) W_V^T via a double-precision SVD on the device, returned in w_v's dtype."""
-    A = gamma1.double()[:, None] * w_v.double().t()
-    U, S, _ = torch.linalg.svd(A, full_matrices=False)
+    diag(gamma1) W_V^T in double precision on the device, returned in w_v's dtype.
+
+    method="svd": full SVD.  method="lowrank": randomized range finder with `iters`
+    subspace iterations and `oversample` extra columns, then the SVD of the small
+    projected matrix (top-r singular pairs up to the iteration's accuracy; used to set
+    up many large layers quickly when only throughput is measured)."""
+    A = gamma1.double()[:, None] * w_v.double().t()          # [d, d_kv]
+    if method == "svd":
+        U, S, _ = torch.linalg.svd(A, full_matrices=False)
+    elif method == "lowrank":
+        k = min(r + oversample, min(A.shape))
+        G = torch.randn(A.shape[1], k, generator=generator, device=A.device, dtype=torch.float32).double()
+        Y = A @ G
+        for _ in range(iters):
+            Q, _ = torch.linalg.qr(Y)
+            Y = A @ (A.t() @ Q)
+        Q, _ = torch.linalg.qr(Y)
+        Ub, S, _ = torch.linalg.svd(Q.t() @ A, full_matrices=False)
+        U = Q @ Ub
+    else:
+        raise DllmError(f"unknown method {method}")
     return (U[:, :r] * S[:r]).t().contiguous().to(w_v.dtype)
 
 
@@ -264,6 +293,30 @@ def dllm_sparse_layer_refresh(layer: Layer, H_in, idx, count, k_max: int, K_cach
                                            B, N, _ptr(ws), ws.numel(), _stream(H_in.device)),
            "dllm_sparse_layer_refresh")
     return K_cache, V_cache, H_out_cache
+
+
+# --------------------------------------------------------------------------- embedding, final norm
+def dllm_embed(E, tokens, H, rows=None):
+    """H[b, i] = E[tokens[b, i]] for all i, or for the positions rows[b, :] only."""
+    B, N, d = H.shape
+    V = E.shape[0]
+    R = 0 if rows is None else rows.shape[1]
+    _cuda(E, tokens, H, rows)
+    _check(lib().dllm_embed(_ptr(E), _ptr(tokens), _ptr(rows), R, _ptr(H), B, N, d, V,
+                            _dtype_code(H), _stream(H.device)), "dllm_embed")
+    return H
+
+
+def dllm_rows_rmsnorm(H, rows, gamma, eps: float = 1e-5, out=None):
+    """out [B*R, d] = RMSNorm(H[b, rows[b, j]]) * gamma."""
+    B, N, d = H.shape
+    R = rows.shape[1]
+    if out is None:
+        out = torch.empty((B * R, d), dtype=H.dtype, device=H.device)
+    _cuda(H, rows, gamma, out)
+    _check(lib().dllm_rows_rmsnorm(_ptr(H), _ptr(rows), R, _ptr(gamma), float(eps), _ptr(out), B, N,
+                                   d, _dtype_code(H), _stream(H.device)), "dllm_rows_rmsnorm")
+    return out
 
 
 # --------------------------------------------------------------------------- plain GEMM

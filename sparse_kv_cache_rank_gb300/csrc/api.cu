@@ -228,7 +228,7 @@ DLLM_EXPORT int dllm_proxy_score(const void *H, const void *Pt, const float *pro
     if (dtype == DLLM_BF16) {
         if (d % 64) return fail(DLLM_ERR_UNSUPPORTED, "bf16 path needs d % 64 == 0 (got %d)", d);
         Launch t(DLLM_KERNEL_PROXY_GEMM, st);
-        e = gemm_tc(static_cast<const bf16 *>(Pt), r, d, static_cast<const bf16 *>(H), rows, epi, 0,
+        e = gemm_tc(static_cast<const bf16 *>(Pt), r, d, static_cast<const bf16 *>(H), rows, epi, 0, true,
                     status_ptr(), st);
     } else {
         Launch t(DLLM_KERNEL_PROXY_GEMM, st);
@@ -379,19 +379,19 @@ int refresh_impl(const dllm_layer *W, const T *H_in, SelRows sel, int B, T *K_ca
     EpiSwiGLU<T> es{SelRows{}, U, F};
     EpiDownScatter<T> ed{sel, H_out, h1, d};
     if constexpr (sizeof(T) == 2) {
-        { Launch t(DLLM_KERNEL_QKV, st); CHECK_CUDA(gemm_tc(wqkv, dq + 2 * dkv, d, Xn, M, eq, 0, status, st), "qkv gemm"); }
+        { Launch t(DLLM_KERNEL_QKV, st); CHECK_CUDA(gemm_tc(wqkv, dq + 2 * dkv, d, Xn, M, eq, 0, true, status, st), "qkv gemm"); }
         {
-            const int na = attention_tc_splits(B, sel.k_max, W->n_q, sel.N) > 1 ? 2 : 1;
+            const int na = 1;
             Launch t(DLLM_KERNEL_ATTENTION, st, na);
             CHECK_CUDA(attention_tc(reinterpret_cast<const bf16 *>(Qc), reinterpret_cast<const bf16 *>(K_cache),
                                     reinterpret_cast<const bf16 *>(V_cache), reinterpret_cast<bf16 *>(Ac), sel, B,
                                     W->n_q, W->n_kv, W->hd, reinterpret_cast<float *>(ws + L.attn), status, st),
                        "attention");
         }
-        { Launch t(DLLM_KERNEL_OPROJ, st); CHECK_CUDA(gemm_tc(wo, d, dq, Ac, M, er, 0, status, st), "o gemm"); }
+        { Launch t(DLLM_KERNEL_OPROJ, st); CHECK_CUDA(gemm_tc(wo, d, dq, Ac, M, er, 0, true, status, st), "o gemm"); }
         { Launch t(DLLM_KERNEL_RMSNORM2, st); CHECK_CUDA(rmsnorm_rows<T>(h1, M, d, g2, W->eps, Xn2, st), "rmsnorm2"); }
-        { Launch t(DLLM_KERNEL_GATEUP, st); CHECK_CUDA(gemm_tc(wgu, 2 * F, d, Xn2, M, es, 0, status, st), "gate/up gemm"); }
-        { Launch t(DLLM_KERNEL_DOWN, st); CHECK_CUDA(gemm_tc(wdn, d, F, U, M, ed, 0, status, st), "down gemm"); }
+        { Launch t(DLLM_KERNEL_GATEUP, st); CHECK_CUDA(gemm_tc(wgu, 2 * F, d, Xn2, M, es, 0, true, status, st), "gate/up gemm"); }
+        { Launch t(DLLM_KERNEL_DOWN, st); CHECK_CUDA(gemm_tc(wdn, d, F, U, M, ed, 0, true, status, st), "down gemm"); }
     } else {
         { Launch t(DLLM_KERNEL_QKV, st); CHECK_CUDA(gemm_simt(wqkv, dq + 2 * dkv, d, Xn, M, eq, st), "qkv gemm"); }
         { Launch t(DLLM_KERNEL_ATTENTION, st); CHECK_CUDA(attention_simt<T>(Qc, K_cache, V_cache, Ac, sel, B, W->n_q, W->n_kv, W->hd, st), "attention"); }
@@ -438,6 +438,38 @@ DLLM_EXPORT int dllm_sparse_layer_refresh(const dllm_layer *W, const void *H_in,
                                proxy_cache, proxy_cur, r, w8, st);
 }
 
+// ------------------------------------------------------------------ embedding, final norm
+DLLM_EXPORT int dllm_embed(const void *E, const int32_t *tokens, const int32_t *rows, int R, void *H,
+                           int B, int N, int d, int V, int dtype, void *stream) {
+    CHECK_ARG(E && tokens && H, "null pointer");
+    CHECK_ARG(B > 0 && N > 0 && d > 0 && V > 0, "sizes must be positive");
+    CHECK_ARG(!rows || R >= 0, "R must be >= 0");
+    CHECK_ARG(dtype == DLLM_BF16 || dtype == DLLM_F32, "dtype must be DLLM_BF16 or DLLM_F32");
+    cudaStream_t st = as_stream(stream);
+    Launch t(DLLM_KERNEL_GATHER, st);
+    cudaError_t e = dtype == DLLM_BF16
+                        ? embed_rows(static_cast<const bf16 *>(E), tokens, rows, R, static_cast<bf16 *>(H), B, N, d, V, st)
+                        : embed_rows(static_cast<const float *>(E), tokens, rows, R, static_cast<float *>(H), B, N, d, V, st);
+    CHECK_CUDA(e, "embed launch");
+    return DLLM_OK;
+}
+
+DLLM_EXPORT int dllm_rows_rmsnorm(const void *H, const int32_t *rows, int R, const void *gamma,
+                                  float eps, void *out, int B, int N, int d, int dtype, void *stream) {
+    CHECK_ARG(H && rows && gamma && out, "null pointer");
+    CHECK_ARG(B > 0 && N > 0 && d > 0 && R >= 0, "bad sizes");
+    CHECK_ARG(dtype == DLLM_BF16 || dtype == DLLM_F32, "dtype must be DLLM_BF16 or DLLM_F32");
+    cudaStream_t st = as_stream(stream);
+    Launch t(DLLM_KERNEL_RMSNORM2, st);
+    cudaError_t e = dtype == DLLM_BF16
+                        ? rows_rmsnorm(static_cast<const bf16 *>(H), rows, R, static_cast<const bf16 *>(gamma), eps,
+                                       static_cast<bf16 *>(out), B, N, d, st)
+                        : rows_rmsnorm(static_cast<const float *>(H), rows, R, static_cast<const float *>(gamma), eps,
+                                       static_cast<float *>(out), B, N, d, st);
+    CHECK_CUDA(e, "rows rmsnorm launch");
+    return DLLM_OK;
+}
+
 // ------------------------------------------------------------------ plain GEMM
 DLLM_EXPORT int dllm_gemm_bf16(const void *X, const void *W, float *out, int M, int N_out, int K,
                                int splits, void *stream) {
@@ -450,7 +482,7 @@ DLLM_EXPORT int dllm_gemm_bf16(const void *X, const void *W, float *out, int M, 
     Launch t(DLLM_KERNEL_GEMM, st);
     EpiStoreF32 epi{SelRows{}, out, N_out, N_out};
     CHECK_CUDA(gemm_tc(static_cast<const bf16 *>(W), N_out, K, static_cast<const bf16 *>(X), M, epi,
-                       splits, status_ptr(), st),
+                       splits, false, status_ptr(), st),
                "gemm launch");
     return DLLM_OK;
 }
@@ -515,3 +547,16 @@ DLLM_EXPORT int dllm_timer_stop(double *total_ms, int *launches) {
 }
 
 DLLM_EXPORT unsigned long long dllm_launch_count(void) { return g_launches.load(); }
+
+// ------------------------------------------------------------------ launch options
+namespace dllm {
+namespace {
+std::atomic<int> g_pdl{1};
+}
+bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
+}  // namespace dllm
+
+DLLM_EXPORT int dllm_set_pdl(int enable) {
+    const int old = dllm::g_pdl.exchange(enable ? 1 : 0);
+    return old;
+}

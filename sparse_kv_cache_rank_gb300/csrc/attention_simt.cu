@@ -14,6 +14,8 @@ __global__ void __launch_bounds__(128) k_attention_simt(const T *__restrict__ Q,
                                                         const T *__restrict__ Vc, T *__restrict__ A,
                                                         SelRows sel, int n_q, int n_kv, float scale) {
     constexpr int hd = EPL * 32;
+    griddep_wait();
+    griddep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y * 4 + warp;
     const int m = blockIdx.x;
@@ -68,9 +70,9 @@ cudaError_t attention_simt(const T *Q, const T *Kc, const T *Vc, T *A, SelRows s
     dim3 grid(M, (n_q + 3) / 4);
     const float scale = 1.0f / sqrtf((float)hd);
     if (hd == 64)
-        k_attention_simt<T, 2><<<grid, 128, 0, st>>>(Q, Kc, Vc, A, sel, n_q, n_kv, scale);
+        launch_kernel(k_attention_simt<T, 2>, grid, dim3(128), 0, st, 1, Q, Kc, Vc, A, sel, n_q, n_kv, scale);
     else if (hd == 128)
-        k_attention_simt<T, 4><<<grid, 128, 0, st>>>(Q, Kc, Vc, A, sel, n_q, n_kv, scale);
+        launch_kernel(k_attention_simt<T, 4>, grid, dim3(128), 0, st, 1, Q, Kc, Vc, A, sel, n_q, n_kv, scale);
     else
         return cudaErrorInvalidValue;
     return cudaGetLastError();

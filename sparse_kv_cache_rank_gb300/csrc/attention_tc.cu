@@ -5,16 +5,18 @@
 // One CTA = 128 selected rows of one sequence (MMA M) x one query head x one
 // slice of the key range.  Per 128-key tile:
 //   S  = Q K^T          tcgen05.mma, Q and K K-major (head dim contiguous), fp32 in TMEM
-//   P  = exp2(S*c - m)  softmax warps, one thread per query row, bf16 into shared
-//                       memory in the 128-byte-swizzled K-major layout
+//   P  = exp2(S*c - m)  softmax warps, bf16 into shared memory in the 128-byte-swizzled
+//                       K-major layout
 //   PV = P V            tcgen05.mma, V read MN-major (head dim contiguous), fp32 in TMEM
 //   O  = O * corr + PV  in registers (streaming softmax)
-// K and V tiles are double-buffered by TMA; S is double-buffered in TMEM so the
-// next tile's Q K^T runs while the softmax of the current one is computed.
-// Rows of the key range beyond N are masked.  With several key slices, each CTA
-// writes (O, m, l) to the workspace and a combine kernel merges them.
+// K and V tiles are double-buffered by TMA; S is double-buffered in TMEM so the next
+// tile's Q K^T runs while the softmax of the current one is computed.  Keys beyond N
+// are masked.  With several key slices every CTA writes (O, m, l) to the workspace and
+// the last CTA of a (rows, head) tile to finish merges them (global counter; no second
+// launch and no waiting on other CTAs).
 //
-// Roles (192 threads): warp 0 TMA, warp 1 TMEM owner + MMA issuer, warps 2..5 softmax.
+// Roles (320 threads): warp 0 TMA, warp 1 TMEM owner + MMA issuer, warps 2..9 softmax:
+// two warps per TMEM lane quarter, thread = (query row, half of the key / head columns).
 #include <cudaTypedefs.h>
 
 #include "internal.h"
@@ -27,17 +29,19 @@ namespace {
 
 constexpr int AQ = 128;          // query rows per CTA
 constexpr int AKV = 128;         // keys per tile
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kSoftThreads = 256;
 constexpr int kChunk = 128 * 128;   // one 64-column (128-byte) box of 128 rows: 16 KB
 
 struct AttnArgs {
     const int32_t *count;
     int N, k_max, n_q, n_kv, B;
-    int kv_tiles, splits;
+    int kv_tiles, splits, q_tiles;
     float scale_log2;                 // log2(e) / sqrt(hd)
-    bf16 *A;                          // [B*k_max, n_q*hd] (splits == 1)
+    bf16 *A;                          // [B*k_max, n_q*hd]
     float *part_o;                    // [splits][B*k_max][n_q*hd]   (splits > 1)
     float *part_ml;                   // [splits][B*k_max][n_q][2]
+    int *counters;                    // [B * q_tiles * n_q], zero between launches
 };
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -52,6 +56,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int QB = NCH * kChunk;           // bytes of the Q tile
     constexpr int KB = NCH * kChunk;           // bytes of one K (or V) tile
     constexpr int PB = 2 * kChunk;             // P tile: 128 rows x 128 keys bf16
+    constexpr int OH = HD / 2;                 // head-dim columns per thread
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;
@@ -59,7 +64,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sK = sQ + QB;                     // [2][KB]
     uint8_t *sV = sK + 2 * KB;                 // [2][KB]
     uint8_t *sP = sV + 2 * KB;                 // [PB]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sP + PB);
+    float *xmax = reinterpret_cast<float *>(sP + PB);   // [2][128] partner exchange
+    float *xsum = xmax + 256;                            // [2][128]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(xsum + 256);
     uint64_t *q_full = bars + 0;
     uint64_t *k_full = bars + 1;               // [2]
     uint64_t *v_full = bars + 3;               // [2]
@@ -70,7 +77,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *pv_full = bars + 12;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *last_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
 
+    griddep_wait();
+    griddep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q0 = blockIdx.x * AQ;
     const int h = blockIdx.y;
@@ -85,21 +95,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nt = t1 - t0;
     const int dq = a.n_q * HD;
     const size_t row0 = (size_t)b * a.k_max + q0;   // flattened row of query 0
-    if (live <= 0 || nt <= 0) {                  // nothing to compute: outputs of dead rows
-        if (warp >= 2 && a.splits == 1) {
-            const int r = (warp & 3) * 32 + lane;
-            if (q0 + r < a.k_max && r < AQ) {
-                bf16 *dst = a.A + (row0 + r) * dq + (size_t)h * HD;
-                for (int e = 0; e < HD; ++e) dst[e] = __float2bfloat16_rn(0.f);
-            }
-        } else if (warp >= 2) {
-            const int r = (warp & 3) * 32 + lane;
+    const size_t rows_all = (size_t)a.B * a.k_max;
+    if (live <= 0) {   // no live query: zero outputs (a.A), nothing to merge
+        if (split == 0 && warp >= 2) {
+            const int r = (warp & 3) * 32 + lane, hf = (warp - 2) >> 2;
             if (q0 + r < a.k_max) {
-                const size_t pm = ((size_t)split * a.B * a.k_max + row0 + r);
-                a.part_ml[(pm * a.n_q + h) * 2 + 0] = -INFINITY;
-                a.part_ml[(pm * a.n_q + h) * 2 + 1] = 0.f;
-                float *po = a.part_o + pm * dq + (size_t)h * HD;
-                for (int e = 0; e < HD; ++e) po[e] = 0.f;
+                bf16 *dst = a.A + (row0 + r) * dq + (size_t)h * HD + hf * OH;
+                for (int e = 0; e < OH; ++e) dst[e] = __float2bfloat16_rn(0.f);
             }
         }
         return;
@@ -112,9 +114,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&v_full[i], 1);
             mbar_init(&kv_empty[i], 1);
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 128);
+            mbar_init(&s_free[i], kSoftThreads);
         }
-        mbar_init(p_full, 128);
+        mbar_init(p_full, kSoftThreads);
         mbar_init(pv_full, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -143,8 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int s = it & 1;
                 const uint32_t ph = (uint32_t)(it >> 1) & 1u;
                 if (!mbar_wait(&kv_empty[s], ph ^ 1u, abort_flag, status)) break;
-                const int j0 = (t0 + it) * AKV;
-                const int y = b * a.N + j0;
+                const int y = b * a.N + (t0 + it) * AKV;
                 mbar_arrive_expect_tx(&k_full[s], KB);
                 for (int c = 0; c < NCH; ++c)
                     tma_load_2d(sK + s * KB + c * kChunk, &tmK, &k_full[s], g * HD + c * 64, y);
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&s_full[s]);
                 return true;
             };
-            if (ok) ok = issue_s(0);
+            if (ok && nt > 0) ok = issue_s(0);
             for (int it = 0; ok && it < nt; ++it) {
                 if (it + 1 < nt && !issue_s(it + 1)) break;
                 const int s = it & 1;
@@ -203,61 +204,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&kv_empty[s]);
             }
         }
-    } else {   // ---------------- softmax warps: thread = query row
+    } else {   // ---------------- softmax warps: thread = (query row, half)
         const int q = warp & 3;
+        const int hf = (warp - 2) >> 2;              // key columns hf*64.., head dims hf*OH..
         const int r = q * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        float o[HD];
+        float o[OH];
 #pragma unroll
-        for (int e = 0; e < HD; ++e) o[e] = 0.f;
+        for (int e = 0; e < OH; ++e) o[e] = 0.f;
         float m_run = -INFINITY, l_run = 0.f;
-        uint8_t *prow = sP + (r >> 3) * 1024 + (r & 7) * 128;
+        uint8_t *prow = sP + hf * kChunk + (r >> 3) * 1024 + (r & 7) * 128;
         for (int it = 0; it < nt; ++it) {
             const int s = it & 1;
             const uint32_t ph = (uint32_t)(it >> 1) & 1u;
             if (!mbar_wait(&s_full[s], ph, abort_flag, status)) break;
             tc_fence_after();
-            const int j0 = (t0 + it) * AKV;
-            const int nvalid = a.N - j0;             // keys of this tile inside [0, N)
+            const int nvalid = a.N - (t0 + it) * AKV - hf * 64;   // keys of my half inside [0, N)
+            float v[64];
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 16)
+                tmem_ld_x16(tS[s] + lane_addr + (uint32_t)(hf * 64 + c0), slice16(v + c0));
+#pragma unroll
+            for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld_wait(slice16(v + c0));
+            tc_fence_before();
+            mbar_arrive(&s_free[s]);                    // S buffer may be overwritten now
             float mt = -INFINITY;
 #pragma unroll
-            for (int c0 = 0; c0 < AKV; c0 += 16) {
-                float v[16];
-                tmem_ld_x16(tS[s] + lane_addr + (uint32_t)c0, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (c0 + j < nvalid) mt = fmaxf(mt, v[j]);
-            }
+            for (int j = 0; j < 64; ++j)
+                if (j < nvalid) mt = fmaxf(mt, v[j]);
+            xmax[hf * 128 + r] = mt;
+            named_bar_sync(2 + q, 64);                 // the two warps of this lane quarter
+            mt = fmaxf(mt, xmax[(hf ^ 1) * 128 + r]);
             const float m_new = fmaxf(m_run, mt * a.scale_log2);
             const float corr = exp2f(m_run - m_new);
             float lsum = 0.f;
 #pragma unroll
-            for (int c0 = 0; c0 < AKV; c0 += 16) {
-                float v[16];
-                tmem_ld_x16(tS[s] + lane_addr + (uint32_t)c0, v);
-                tmem_ld_wait();
-                uint32_t pk[8];
+            for (int c0 = 0; c0 < 64; c0 += 8) {
+                uint32_t pk[4];
 #pragma unroll
-                for (int j = 0; j < 16; j += 2) {
-                    const float p0 = (c0 + j < nvalid) ? exp2f(v[j] * a.scale_log2 - m_new) : 0.f;
-                    const float p1 = (c0 + j + 1 < nvalid) ? exp2f(v[j + 1] * a.scale_log2 - m_new) : 0.f;
+                for (int j = 0; j < 8; j += 2) {
+                    const float p0 = (c0 + j < nvalid) ? exp2f(v[c0 + j] * a.scale_log2 - m_new) : 0.f;
+                    const float p1 = (c0 + j + 1 < nvalid) ? exp2f(v[c0 + j + 1] * a.scale_log2 - m_new) : 0.f;
                     const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
                     lsum += __low2float(pp) + __high2float(pp);
                     pk[j >> 1] = *reinterpret_cast<const uint32_t *>(&pp);
                 }
-                // 16 keys = two 16-byte units of this row in the swizzled K-major layout
-                const int chunk = c0 >> 6;
-                const int unit = (c0 & 63) >> 3;
-#pragma unroll
-                for (int hlf = 0; hlf < 2; ++hlf) {
-                    const int u = (unit + hlf) ^ (r & 7);
-                    uint4 val = make_uint4(pk[4 * hlf], pk[4 * hlf + 1], pk[4 * hlf + 2], pk[4 * hlf + 3]);
-                    *reinterpret_cast<uint4 *>(prow + chunk * kChunk + u * 16) = val;
-                }
+                const int u = (c0 >> 3) ^ (r & 7);       // 16-byte unit in the swizzled row
+                *reinterpret_cast<uint4 *>(prow + u * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
-            tc_fence_before();
-            mbar_arrive(&s_free[s]);
             fence_proxy_async_smem();
             mbar_arrive(p_full);
             l_run = l_run * corr + lsum;
@@ -265,30 +259,82 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(pv_full, (uint32_t)it & 1u, abort_flag, status)) break;
             tc_fence_after();
 #pragma unroll
-            for (int c0 = 0; c0 < HD; c0 += 16) {
-                float v[16];
-                tmem_ld_x16(tPV + lane_addr + (uint32_t)c0, v);
-                tmem_ld_wait();
+            for (int c0 = 0; c0 < OH; c0 += 16) {
+                float t[16];
+                tmem_ld_x16(tPV + lane_addr + (uint32_t)(hf * OH + c0), t);
+                tmem_ld_wait(t);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) o[c0 + j] = fmaf(o[c0 + j], corr, v[j]);
+                for (int j = 0; j < 16; ++j) o[c0 + j] = fmaf(o[c0 + j], corr, t[j]);
             }
         }
-        if (q0 + r < a.k_max) {
-            const size_t row = row0 + r;
-            if (a.splits == 1) {
-                const float inv = (r < live && l_run > 0.f) ? 1.0f / l_run : 0.f;
-                bf16 *dst = a.A + row * dq + (size_t)h * HD;
+        // combine the two halves' row sums
+        xsum[hf * 128 + r] = l_run;
+        named_bar_sync(2 + q, 64);
+        const float l_tot = l_run + xsum[(hf ^ 1) * 128 + r];
+        const bool row_ok = q0 + r < a.k_max;
+        const size_t row = row0 + r;
+        if (a.splits == 1) {
+            if (row_ok) {
+                const float inv = (r < live && l_tot > 0.f) ? 1.0f / l_tot : 0.f;
+                bf16 *dst = a.A + row * dq + (size_t)h * HD + hf * OH;
 #pragma unroll
-                for (int e = 0; e < HD; e += 2)
+                for (int e = 0; e < OH; e += 2)
                     *reinterpret_cast<__nv_bfloat162 *>(dst + e) = __floats2bfloat162_rn(o[e] * inv, o[e + 1] * inv);
-            } else {
-                const size_t pm = (size_t)split * a.B * a.k_max + row;
-                a.part_ml[(pm * a.n_q + h) * 2 + 0] = r < live ? m_run : -INFINITY;
-                a.part_ml[(pm * a.n_q + h) * 2 + 1] = r < live ? l_run : 0.f;
-                float *po = a.part_o + pm * dq + (size_t)h * HD;
+            }
+        } else {
+            if (row_ok) {
+                const size_t pm = (size_t)split * rows_all + row;
+                if (hf == 0) {
+                    a.part_ml[(pm * a.n_q + h) * 2 + 0] = (r < live && nt > 0) ? m_run : -INFINITY;
+                    a.part_ml[(pm * a.n_q + h) * 2 + 1] = (r < live && nt > 0) ? l_tot : 0.f;
+                }
+                float *po = a.part_o + pm * dq + (size_t)h * HD + hf * OH;
 #pragma unroll
-                for (int e = 0; e < HD; e += 4)
+                for (int e = 0; e < OH; e += 4)
                     *reinterpret_cast<float4 *>(po + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+            }
+            __threadfence();
+            named_bar_sync(1, kSoftThreads);
+            if (threadIdx.x == 64) {
+                int *ctr = a.counters + ((size_t)b * a.q_tiles + blockIdx.x) * a.n_q + h;
+                const int old = atomicAdd(ctr, 1);
+                const int last = old == a.splits - 1;
+                if (last) *ctr = 0;                    // ready for the next launch
+                *last_flag = last;
+            }
+            named_bar_sync(1, kSoftThreads);
+            if (*last_flag && row_ok) {                // merge every slice's (O, m, l)
+                __threadfence();
+                float M = -INFINITY;
+                for (int sp = 0; sp < a.splits; ++sp)
+                    M = fmaxf(M, __ldcg(&a.part_ml[(((size_t)sp * rows_all + row) * a.n_q + h) * 2]));
+                float acc[OH];
+#pragma unroll
+                for (int e = 0; e < OH; ++e) acc[e] = 0.f;
+                float den = 0.f;
+                if (M != -INFINITY) {
+                    for (int sp = 0; sp < a.splits; ++sp) {
+                        const size_t pm = (size_t)sp * rows_all + row;
+                        const float ms = __ldcg(&a.part_ml[(pm * a.n_q + h) * 2]);
+                        if (ms == -INFINITY) continue;
+                        const float w = exp2f(ms - M);
+                        den = fmaf(__ldcg(&a.part_ml[(pm * a.n_q + h) * 2 + 1]), w, den);
+                        const float *po = a.part_o + pm * dq + (size_t)h * HD + hf * OH;
+#pragma unroll
+                        for (int e = 0; e < OH; e += 4) {
+                            const float4 x = __ldcg(reinterpret_cast<const float4 *>(po + e));
+                            acc[e] = fmaf(x.x, w, acc[e]);
+                            acc[e + 1] = fmaf(x.y, w, acc[e + 1]);
+                            acc[e + 2] = fmaf(x.z, w, acc[e + 2]);
+                            acc[e + 3] = fmaf(x.w, w, acc[e + 3]);
+                        }
+                    }
+                }
+                const float inv = den > 0.f ? 1.0f / den : 0.f;
+                bf16 *dst = a.A + row * dq + (size_t)h * HD + hf * OH;
+#pragma unroll
+                for (int e = 0; e < OH; e += 2)
+                    *reinterpret_cast<__nv_bfloat162 *>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
             }
         }
     }
@@ -300,34 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// A[row, h] = sum_s O_s e^(m_s - M) / sum_s l_s e^(m_s - M) over the key slices.
-template <int HD>
-__global__ void __launch_bounds__(HD) k_attention_combine(const float *__restrict__ part_o,
-                                                          const float *__restrict__ part_ml,
-                                                          int splits, int rows, int n_q,
-                                                          bf16 *__restrict__ A) {
-    const int row = blockIdx.x, h = blockIdx.y, e = threadIdx.x;
-    const int dq = n_q * HD;
-    float M = -INFINITY;
-    for (int s = 0; s < splits; ++s)
-        M = fmaxf(M, part_ml[(((size_t)s * rows + row) * n_q + h) * 2]);
-    float num = 0.f, den = 0.f;
-    if (M != -INFINITY) {
-        for (int s = 0; s < splits; ++s) {
-            const size_t pm = (size_t)s * rows + row;
-            const float ms = part_ml[(pm * n_q + h) * 2];
-            if (ms == -INFINITY) continue;
-            const float w = exp2f(ms - M);
-            den = fmaf(part_ml[(pm * n_q + h) * 2 + 1], w, den);
-            num = fmaf(part_o[pm * dq + (size_t)h * HD + e], w, num);
-        }
-    }
-    A[(size_t)row * dq + (size_t)h * HD + e] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
-}
-
 template <int HD>
 size_t attn_smem() {
-    return 1024 + (size_t)(HD / 64) * kChunk * 5 + 2 * kChunk + 14 * 8 + 64;
+    return 1024 + (size_t)(HD / 64) * kChunk * 5 + 2 * kChunk + 512 * 4 + 16 * 8 + 64;
 }
 
 }  // namespace
@@ -346,7 +367,14 @@ size_t attention_tc_ws_bytes(int B, int k_max, int n_q, int hd, int N) {
     const int s = attention_tc_splits(B, k_max, n_q, N);
     if (s <= 1) return 0;
     const size_t rows = (size_t)B * k_max;
-    return (size_t)s * rows * n_q * hd * 4 + (size_t)s * rows * n_q * 2 * 4 + 512;
+    const size_t qt = (size_t)(k_max + AQ - 1) / AQ;
+    return (size_t)s * rows * n_q * hd * 4 + (size_t)s * rows * n_q * 2 * 4 + B * qt * n_q * 4 + 1024;
+}
+
+size_t attention_tc_counter_offset(int B, int k_max, int n_q, int hd, int N) {
+    const int s = attention_tc_splits(B, k_max, n_q, N);
+    const size_t rows = (size_t)B * k_max;
+    return ((size_t)s * rows * n_q * hd * 4 + (size_t)s * rows * n_q * 2 * 4 + 255) & ~size_t(255);
 }
 
 cudaError_t attention_tc(const bf16 *Q, const bf16 *Kc, const bf16 *Vc, bf16 *A, SelRows sel, int B,
@@ -369,32 +397,32 @@ cudaError_t attention_tc(const bf16 *Q, const bf16 *Kc, const bf16 *Vc, bf16 *A,
     a.B = B;
     a.kv_tiles = (sel.N + AKV - 1) / AKV;
     a.splits = attention_tc_splits(B, sel.k_max, n_q, sel.N);
+    a.q_tiles = (sel.k_max + AQ - 1) / AQ;
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
     a.A = A;
     if (a.splits > 1) {
         a.part_o = ws;
         a.part_ml = ws + (size_t)a.splits * M * dq;
+        a.counters = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(ws) +
+                                             attention_tc_counter_offset(B, sel.k_max, n_q, hd, sel.N));
     }
-    dim3 grid((sel.k_max + AQ - 1) / AQ, n_q, B * a.splits);
+    dim3 grid(a.q_tiles, n_q, B * a.splits);
     cudaError_t e;
+    if (a.splits > 1) {   // merge counters start at zero (the merging CTA resets its own)
+        e = cudaMemsetAsync(a.counters, 0, (size_t)B * a.q_tiles * n_q * sizeof(int), st);
+        if (e != cudaSuccess) return e;
+    }
     if (hd == 128) {
         const size_t sm = attn_smem<128>();
         e = cudaFuncSetAttribute(k_attention_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         if (e != cudaSuccess) return e;
-        k_attention_tc<128><<<grid, kThreads, sm, st>>>(tq, tk, tv, a, status);
+        e = launch_kernel(k_attention_tc<128>, grid, dim3(kThreads), sm, st, 1, tq, tk, tv, a, status);
     } else {
         const size_t sm = attn_smem<64>();
         e = cudaFuncSetAttribute(k_attention_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         if (e != cudaSuccess) return e;
-        k_attention_tc<64><<<grid, kThreads, sm, st>>>(tq, tk, tv, a, status);
+        e = launch_kernel(k_attention_tc<64>, grid, dim3(kThreads), sm, st, 1, tq, tk, tv, a, status);
     }
-    e = cudaGetLastError();
-    if (e != cudaSuccess || a.splits == 1) return e;
-    dim3 g2(M, n_q);
-    if (hd == 128)
-        k_attention_combine<128><<<g2, 128, 0, st>>>(a.part_o, a.part_ml, a.splits, M, n_q, A);
-    else
-        k_attention_combine<64><<<g2, 64, 0, st>>>(a.part_o, a.part_ml, a.splits, M, n_q, A);
     return cudaGetLastError();
 }
 

@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(256) k_gemm_simt(const float *__restrict__ W, 
                                                    const float *__restrict__ X, int M_tok, const Epi epi) {
     __shared__ float Ws[TK][TF + 1];
     __shared__ float Xs[TK][TM + 1];
+    griddep_wait();
+    griddep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * TM, f0 = blockIdx.y * TF;
     float acc[2][8];
@@ -72,8 +74,7 @@ cudaError_t gemm_simt(const float *W, int N_out, int K, const float *X, int M_to
     if (M_tok <= 0 || N_out <= 0) return cudaSuccess;
     if (N_out % 32 != 0) return cudaErrorInvalidValue;
     dim3 grid((M_tok + TM - 1) / TM, (N_out + TF - 1) / TF);
-    k_gemm_simt<Epi><<<grid, 256, 0, st>>>(W, N_out, K, X, M_tok, epi);
-    return cudaGetLastError();
+    return launch_kernel(k_gemm_simt<Epi>, grid, dim3(256), 0, st, 1, W, N_out, K, X, M_tok, epi);
 }
 
 template cudaError_t gemm_simt<EpiStoreF32>(const float *, int, int, const float *, int,

@@ -39,6 +39,7 @@ constexpr int kColBytes = 2 * 256 * 4; // per-column (sequence, position)
 struct Shape {
     int M_tok, N_out, K;
     int BN, splits, stages;
+    int w_const;      // weights are never written on the device: stream them before the wait
     int body_bytes;   // pipeline ring (and, with a K split, the fp32 partial tile [BN][128])
 };
 
@@ -108,10 +109,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    griddep_launch();
     if (warp == 0) {
         if (lane == 0) {   // ---------------- TMA producer
-            int issued = 0;
-            for (int it = 0; it < nkb; ++it) {
+            // weights never change on the device: the first ring stages stream their
+            // weight tiles while the previous kernel is still draining
+            const int pre = g.w_const ? (nkb < g.stages ? nkb : g.stages) : 0;
+            for (int it = 0; it < pre; ++it) {
+                mbar_arrive_expect_tx(&full[it], (uint32_t)sbytes);
+                tma_load_2d(smem + it * sbytes, &tmW, &full[it], (kb0 + it) * BK, n0);
+            }
+            griddep_wait();
+            for (int it = 0; it < pre; ++it)
+                tma_load_2d(smem + it * sbytes + kWBytes, &tmX, &full[it], (kb0 + it) * BK, m0);
+            int issued = pre;
+            for (int it = pre; it < nkb; ++it) {
                 const int s = it % g.stages;
                 const uint32_t ph = (uint32_t)(it / g.stages) & 1u;
                 if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status)) break;
@@ -147,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     } else {
         // ---------------- epilogue warps (2..9): resolve every token column's (sequence,
         // position) while the main loop runs
+        griddep_wait();
         for (int c = threadIdx.x - 64; c < g.BN; c += kThreads - 64) {
             int b = 0, pos = -1;
             if (Epi::kSel && c < ncols) epi.sel.locate(m0 + c, b, pos);
@@ -169,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int ch = ch0; ch < ch1 && ch * 16 < ncols; ++ch) {
                     float v[16];
                     tmem_ld_x16(taddr + (uint32_t)(ch * 16), v);
-                    tmem_ld_wait();
+                    tmem_ld_wait(v);
                     epi_16(epi, F, m0, ch * 16, ncols, col_b, col_pos, v);
                 }
             }
@@ -179,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int ch = ch0; ch < ch1; ++ch) {
                 float v[16];
                 tmem_ld_x16(taddr + (uint32_t)(ch * 16), v);
-                tmem_ld_wait();
+                tmem_ld_wait(v);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) part[(ch * 16 + j) * BM + f] = v[j];
             }
@@ -328,7 +341,7 @@ Plan plan_gemm(int M_tok, int N_out, int K, int splits_req) {
 
 template <class Epi>
 cudaError_t gemm_tc(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, const Epi &epi,
-                    int splits, unsigned *status, cudaStream_t st) {
+                    int splits, bool w_const, unsigned *status, cudaStream_t st) {
     if (M_tok <= 0 || N_out <= 0) return cudaSuccess;
     if (K % BK != 0 || N_out % 32 != 0) return cudaErrorInvalidValue;
     const Plan p = plan_gemm(M_tok, N_out, K, splits);
@@ -337,7 +350,7 @@ cudaError_t gemm_tc(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, c
     if (!make_tmap(&tmW, W, (uint64_t)N_out, (uint64_t)K, BM) ||
         !make_tmap(&tmX, X, (uint64_t)M_tok, (uint64_t)K, (uint32_t)p.BN))
         return cudaErrorInvalidValue;
-    Shape g{M_tok, N_out, K, p.BN, p.splits, p.stages, p.body};
+    Shape g{M_tok, N_out, K, p.BN, p.splits, p.stages, w_const ? 1 : 0, p.body};
     auto kern = k_gemm_tc<Epi>;
     static bool configured[64] = {};   // per device: raise the shared-memory limit once
     int dev = 0;
@@ -347,33 +360,22 @@ cudaError_t gemm_tc(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, c
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.tok_tiles, p.w_tiles, p.splits);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = p.smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = p.splits;
-    cfg.attrs = attr;
-    cfg.numAttrs = p.splits > 1 ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, tmW, tmX, g, epi, status);
+    return launch_kernel(kern, dim3(p.tok_tiles, p.w_tiles, p.splits), dim3(kThreads), p.smem, st,
+                         p.splits, tmW, tmX, g, epi, status);
 }
 
 template cudaError_t gemm_tc<EpiStoreF32>(const bf16 *, int, int, const bf16 *, int,
-                                          const EpiStoreF32 &, int, unsigned *, cudaStream_t);
+                                          const EpiStoreF32 &, int, bool, unsigned *, cudaStream_t);
 template cudaError_t gemm_tc<EpiQKV<bf16>>(const bf16 *, int, int, const bf16 *, int,
-                                           const EpiQKV<bf16> &, int, unsigned *, cudaStream_t);
+                                           const EpiQKV<bf16> &, int, bool, unsigned *, cudaStream_t);
 template cudaError_t gemm_tc<EpiResidual<bf16>>(const bf16 *, int, int, const bf16 *, int,
-                                                const EpiResidual<bf16> &, int, unsigned *,
+                                                const EpiResidual<bf16> &, int, bool, unsigned *,
                                                 cudaStream_t);
 template cudaError_t gemm_tc<EpiSwiGLU<bf16>>(const bf16 *, int, int, const bf16 *, int,
-                                              const EpiSwiGLU<bf16> &, int, unsigned *,
+                                              const EpiSwiGLU<bf16> &, int, bool, unsigned *,
                                               cudaStream_t);
 template cudaError_t gemm_tc<EpiDownScatter<bf16>>(const bf16 *, int, int, const bf16 *, int,
-                                                   const EpiDownScatter<bf16> &, int, unsigned *,
+                                                   const EpiDownScatter<bf16> &, int, bool, unsigned *,
                                                    cudaStream_t);
 
 }  // namespace dllm

@@ -5,11 +5,44 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "epilogues.cuh"
 
 namespace dllm {
 
 int num_sms();   // SMs of the current device (cached per device)
+
+bool pdl_enabled();   // programmatic dependent launch of the step's kernels (default on)
+
+// Launches `kern` with the step's launch attributes: programmatic stream
+// serialization (when enabled) and, for cluster_z > 1, a 1 x 1 x cluster_z cluster.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, int cluster_z, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (cluster_z > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 1;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = cluster_z;
+        ++n;
+    }
+    if (pdl_enabled()) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- GEMMs
 // acc[f, m] = <W[f, :K], X[m, :K]>, W [N_out, K] and X [M_tok, K] row-major,
@@ -19,7 +52,7 @@ int num_sms();   // SMs of the current device (cached per device)
 // `splits` = 0 picks the K split (cluster size) automatically.
 template <class Epi>
 cudaError_t gemm_tc(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, const Epi &epi,
-                    int splits, unsigned *status, cudaStream_t st);
+                    int splits, bool w_const, unsigned *status, cudaStream_t st);
 
 // CUDA cores (fp32 FMA): any K.
 template <class Epi>
@@ -47,6 +80,14 @@ cudaError_t pack_rows_interleave(const T *a, const T *b, T *dst, int rows, int c
                                  cudaStream_t st);
 
 cudaError_t rope_inv_freq(float *dst, int hd, float theta, cudaStream_t st);
+
+template <class T>
+cudaError_t embed_rows(const T *E, const int32_t *tokens, const int32_t *rows, int R, T *H, int B,
+                       int N, int d, int V, cudaStream_t st);
+
+template <class T>
+cudaError_t rows_rmsnorm(const T *H, const int32_t *rows, int R, const T *gamma, float eps, T *out,
+                         int B, int N, int d, cudaStream_t st);
 
 // ---------------------------------------------------------------- attention
 // A[m, h*hd:(h+1)*hd] = softmax(Q_h K_g^T / sqrt(hd)) V_g over all N rows of the

@@ -37,6 +37,8 @@ __global__ void __launch_bounds__(256) k_gather_rmsnorm(const T *__restrict__ H,
                                                         const float *inv_freq, int half_hd,
                                                         float2 *rope_cs, unsigned *status) {
     __shared__ float red[33];
+    griddep_wait();
+    griddep_launch();
     const int m = blockIdx.x;
     int b, pos;
     sel.locate(m, b, pos);
@@ -74,6 +76,8 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float *__restrict__ 
                                                       const T *__restrict__ gamma, float eps,
                                                       T *__restrict__ Xn2) {
     __shared__ float red[33];
+    griddep_wait();
+    griddep_launch();
     const float *row = h1 + (size_t)blockIdx.x * d;
     float ss = 0.f;
     for (int e = threadIdx.x; e < d; e += 256) ss = fmaf(row[e], row[e], ss);
@@ -90,6 +94,8 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float *__restrict__ 
 __global__ void __launch_bounds__(256) k_cosine_drift(const float *__restrict__ cur,
                                                       const float *__restrict__ cached,
                                                       float *__restrict__ drift, long rows, int r) {
+    griddep_wait();
+    griddep_launch();
     const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -156,7 +162,7 @@ cudaError_t gather_rmsnorm(const T *H, SelRows sel, int B, int d, const T *gamma
                            int half_hd, float2 *rope_cs, unsigned *status, cudaStream_t st) {
     const int M = B * sel.k_max;
     if (M <= 0) return cudaSuccess;
-    k_gather_rmsnorm<T><<<M, 256, 0, st>>>(H, sel, d, gamma, eps, Xn, proxy_cache, proxy_cur, r,
+    return launch_kernel(k_gather_rmsnorm<T>, dim3(M), dim3(256), 0, st, 1, H, sel, d, gamma, eps, Xn, proxy_cache, proxy_cur, r,
                                            inv_freq, half_hd, rope_cs, status);
     return cudaGetLastError();
 }
@@ -165,14 +171,14 @@ template <class T>
 cudaError_t rmsnorm_rows(const float *h1, int M, int d, const T *gamma, float eps, T *Xn2,
                          cudaStream_t st) {
     if (M <= 0) return cudaSuccess;
-    k_rmsnorm_rows<T><<<M, 256, 0, st>>>(h1, d, gamma, eps, Xn2);
+    return launch_kernel(k_rmsnorm_rows<T>, dim3(M), dim3(256), 0, st, 1, h1, d, gamma, eps, Xn2);
     return cudaGetLastError();
 }
 
 cudaError_t cosine_drift(const float *cur, const float *cached, float *drift, long rows, int r,
                          cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
-    k_cosine_drift<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(cur, cached, drift, rows, r);
+    return launch_kernel(k_cosine_drift, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, st, 1, cur, cached, drift, rows, r);
     return cudaGetLastError();
 }
 
@@ -206,5 +212,84 @@ cudaError_t rope_inv_freq(float *dst, int hd, float theta, cudaStream_t st) {
 DLLM_ROWOPS(float)
 DLLM_ROWOPS(bf16)
 #undef DLLM_ROWOPS
+
+}  // namespace dllm
+
+// ---------------------------------------------------------------------------
+// Token embedding lookup and the final RMSNorm of chosen rows (decode loop around
+// the refresh: the inputs of layer 0 and the rows fed to the LM head).
+namespace dllm {
+namespace {
+
+template <class T>
+__global__ void __launch_bounds__(256) k_embed(const T *__restrict__ E, const int32_t *__restrict__ tokens,
+                                               const int32_t *__restrict__ rows, int R, T *__restrict__ H,
+                                               int N, int d, int V) {
+    griddep_wait();
+    griddep_launch();
+    const int b = blockIdx.y;
+    int i = blockIdx.x;
+    if (rows) {
+        i = rows[(size_t)b * R + blockIdx.x];
+        if (i < 0 || i >= N) return;
+    }
+    const int tok = tokens[(size_t)b * N + i];
+    T *dst = H + ((size_t)b * N + i) * d;
+    if (tok < 0 || tok >= V) {
+        for (int e = threadIdx.x; e < d; e += 256) dst[e] = from_f32<T>(0.f);
+        return;
+    }
+    const T *src = E + (size_t)tok * d;
+    for (int e = threadIdx.x; e < d; e += 256) dst[e] = src[e];
+}
+
+template <class T>
+__global__ void __launch_bounds__(256) k_rows_rmsnorm(const T *__restrict__ H, const int32_t *__restrict__ rows,
+                                                      int R, const T *__restrict__ gamma, float eps,
+                                                      T *__restrict__ out, int N, int d) {
+    __shared__ float red[33];
+    griddep_wait();
+    griddep_launch();
+    const int b = blockIdx.y, j = blockIdx.x;
+    const int i = rows[(size_t)b * R + j];
+    T *o = out + ((size_t)b * R + j) * d;
+    if (i < 0 || i >= N) {
+        for (int e = threadIdx.x; e < d; e += 256) o[e] = from_f32<T>(0.f);
+        return;
+    }
+    const T *row = H + ((size_t)b * N + i) * d;
+    float ss = 0.f;
+    for (int e = threadIdx.x; e < d; e += 256) {
+        const float x = to_f32<T>(row[e]);
+        ss = fmaf(x, x, ss);
+    }
+    ss = block_sum<256>(ss, red);
+    const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+    for (int e = threadIdx.x; e < d; e += 256) o[e] = from_f32<T>(to_f32<T>(row[e]) * inv * to_f32<T>(gamma[e]));
+}
+
+}  // namespace
+
+template <class T>
+cudaError_t embed_rows(const T *E, const int32_t *tokens, const int32_t *rows, int R, T *H, int B,
+                       int N, int d, int V, cudaStream_t st) {
+    const int nr = rows ? R : N;
+    if (B <= 0 || nr <= 0) return cudaSuccess;
+    return launch_kernel(k_embed<T>, dim3(nr, B), dim3(256), 0, st, 1, E, tokens, rows, R, H, N, d, V);
+    return cudaGetLastError();
+}
+
+template <class T>
+cudaError_t rows_rmsnorm(const T *H, const int32_t *rows, int R, const T *gamma, float eps, T *out,
+                         int B, int N, int d, cudaStream_t st) {
+    if (B <= 0 || R <= 0) return cudaSuccess;
+    return launch_kernel(k_rows_rmsnorm<T>, dim3(R, B), dim3(256), 0, st, 1, H, rows, R, gamma, eps, out, N, d);
+    return cudaGetLastError();
+}
+
+template cudaError_t embed_rows<float>(const float *, const int32_t *, const int32_t *, int, float *, int, int, int, int, cudaStream_t);
+template cudaError_t embed_rows<bf16>(const bf16 *, const int32_t *, const int32_t *, int, bf16 *, int, int, int, int, cudaStream_t);
+template cudaError_t rows_rmsnorm<float>(const float *, const int32_t *, int, const float *, float, float *, int, int, int, cudaStream_t);
+template cudaError_t rows_rmsnorm<bf16>(const bf16 *, const int32_t *, int, const bf16 *, float, bf16 *, int, int, int, cudaStream_t);
 
 }  // namespace dllm

@@ -55,6 +55,8 @@ __global__ void __launch_bounds__(kT) k_select_topk(const float *__restrict__ dr
     __shared__ uint32_t hist[256];
     __shared__ uint32_t wsum[33];
     __shared__ uint32_t sh_prefix, sh_rem;
+    griddep_wait();
+    griddep_launch();
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
     const float *dr = drift + (size_t)b * N;
@@ -111,16 +113,32 @@ __global__ void __launch_bounds__(kT) k_select_topk(const float *__restrict__ dr
                 if (kk != 0 && (kk & mask) == prefix) atomicAdd(&hist[(kk >> shift) & 255u], 1u);
             }
             __syncthreads();
-            if (tid == 0) {
-                uint32_t cum = 0;
-                for (int dg = 255; dg >= 0; --dg) {
-                    const uint32_t h = hist[dg];
-                    if (cum + h >= rem) {
-                        sh_prefix = prefix | ((uint32_t)dg << shift);
-                        sh_rem = rem - cum;
-                        break;
+            if (tid < 32) {
+                // lane l owns digits 255-8l .. 248-8l (descending); suffix counts by a
+                // warp scan find the digit holding the rem-th largest key
+                uint32_t h[8], own = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    h[j] = hist[255 - 8 * tid - j];
+                    own += h[j];
+                }
+                uint32_t incl = own;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (tid >= o) incl += y;
+                }
+                uint32_t cum = incl - own;   // keys in higher digits than this lane's
+                if (cum < rem && rem <= incl) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (cum + h[j] >= rem) {
+                            sh_prefix = prefix | ((uint32_t)(255 - 8 * tid - j) << shift);
+                            sh_rem = rem - cum;
+                            break;
+                        }
+                        cum += h[j];
                     }
-                    cum += h;
                 }
             }
             __syncthreads();
@@ -168,7 +186,7 @@ cudaError_t select_topk(const float *drift, const int32_t *forced, int F, int k,
     cudaError_t e = cudaFuncSetAttribute(k_select_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    k_select_topk<<<B, kT, smem, st>>>(drift, forced, F, k, min_drift, idx, count, N);
+    return launch_kernel(k_select_topk, dim3(B), dim3(kT), smem, st, 1, drift, forced, F, k, min_drift, idx, count, N);
     return cudaGetLastError();
 }
 

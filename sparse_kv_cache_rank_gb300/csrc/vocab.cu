@@ -43,6 +43,8 @@ constexpr int kT1 = 256;
 __global__ void __launch_bounds__(kT1) k_row_stats(const float *__restrict__ logits,
                                                    const uint8_t *__restrict__ valid, int V,
                                                    int slices, RowState *__restrict__ part) {
+    griddep_wait();
+    griddep_launch();
     const int row = blockIdx.y, sl = blockIdx.x;
     if (!valid[row]) return;
     const int chunk = (V + slices - 1) / slices;
@@ -91,6 +93,8 @@ __global__ void __launch_bounds__(1024) k_commit(const RowState *__restrict__ pa
                                                  float conf_thresh, float tau, int32_t *token,
                                                  float *conf, float *entropy, float *max_entropy,
                                                  int32_t *full_next) {
+    griddep_wait();
+    griddep_launch();
     const int b = blockIdx.x, m = threadIdx.x;
     __shared__ float s_conf[32];
     __shared__ int s_row[32];
@@ -181,15 +185,14 @@ cudaError_t commit_entropy(const float *logits, const uint8_t *valid, int B, int
     RowState *part = reinterpret_cast<RowState *>(ws);
     if (rows > 0) {
         const int slices = slices_for(rows, V);
-        k_row_stats<<<dim3(slices, rows), kT1, 0, st>>>(logits, valid, V, slices, part);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_kernel(k_row_stats, dim3(slices, rows), dim3(kT1), 0, st, 1, logits, valid, V, slices, part);
         if (e != cudaSuccess) return e;
         const int threads = ((M + 31) / 32) * 32;
-        k_commit<<<B, threads, 0, st>>>(part, slices, valid, M, conf_thresh, tau, token, conf, entropy,
+        return launch_kernel(k_commit, dim3(B), dim3(threads), 0, st, 1, part, slices, valid, M, conf_thresh, tau, token, conf, entropy,
                                         max_entropy, full_next);
     } else {
         const int threads = 32;
-        k_commit<<<B, threads, 0, st>>>(part, 1, valid, 0, conf_thresh, tau, token, conf, entropy,
+        return launch_kernel(k_commit, dim3(B), dim3(threads), 0, st, 1, part, 1, valid, 0, conf_thresh, tau, token, conf, entropy,
                                         max_entropy, full_next);
     }
     return cudaGetLastError();
