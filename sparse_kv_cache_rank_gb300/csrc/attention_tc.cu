@@ -357,7 +357,9 @@ int attention_tc_splits(int B, int k_max, int n_q, int N) {
     const int qt = (k_max + AQ - 1) / AQ;
     const long long base = (long long)qt * n_q * B;
     const int kv_tiles = (N + AKV - 1) / AKV;
-    int s = (int)((num_sms() + base - 1) / base);
+    // one CTA per SM (the ring and TMEM need the whole SM): as many key slices as keep
+    // the grid within a single wave
+    int s = (int)(num_sms() / base);
     if (s > kv_tiles) s = kv_tiles;
     if (s > 16) s = 16;
     return s < 1 ? 1 : s;

@@ -46,7 +46,7 @@ class _Layer:
 class DecodeStack:
     def __init__(self, shape: LayerShape, seed: int, device, rho: RhoSchedule | None = None,
                  uniform_rho: float | None = None, k_recent: int = 8, conf_thresh: float = 0.9,
-                 tau: float = 2.0, proxy_method: str = "lowrank"):
+                 tau: float = 2.0, proxy_method: str = "lowrank", keep_weights: bool = False):
         self.sh = sh = shape
         self.dev = device
         self.rho = rho or RhoSchedule()
@@ -62,6 +62,7 @@ class DecodeStack:
 
         d, dq, dkv, F, Bn, N = sh.d, sh.d_q, sh.d_kv, sh.F, sh.B, sh.N
         self.layers = []
+        self.weights = [] if keep_weights else None
         for _ in range(sh.layers):
             w = {"w_q": randn(dq, d, std=0.02), "w_k": randn(dkv, d, std=0.02),
                  "w_v": randn(dkv, d, std=0.02), "w_o": randn(d, dq, std=0.02),
@@ -70,6 +71,8 @@ class DecodeStack:
                  "gamma2": torch.ones(d, device=device, dtype=bf)}
             layer = B.dllm_pack_layer(w, sh.n_q, sh.n_kv, sh.hd, eps=sh.eps, rope_theta=sh.rope_theta)
             Pt = B.build_proxy_matrix(w["w_v"], w["gamma1"], sh.r, method=proxy_method, generator=gen)
+            if keep_weights:
+                self.weights.append(w)
             del w
             K = torch.empty((Bn, N, sh.n_kv, sh.hd), device=device, dtype=bf)
             self.layers.append(_Layer(layer, Pt, K, torch.empty_like(K),
@@ -154,6 +157,7 @@ class DecodeStack:
             H = L.O
         X = B.dllm_rows_rmsnorm(H, self.block_rows, self.gamma_f, sh.eps)
         logits = B.dllm_gemm_bf16(X, self.W_lm).view(sh.B, sh.block, sh.V)
+        self.logits = logits
         return B.dllm_commit_entropy(logits, self.valid, self.conf_thresh, self.tau)
 
     def count_rows(self, full: bool):
