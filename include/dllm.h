@@ -205,6 +205,31 @@ int dllm_commit_entropy(const float *logits, const uint8_t *valid, int B, int M,
                         size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * dllm_commit_entropy without a workspace.  (No counterpart on the pages: this is an
+ * interface variant, not a step of the method.)
+ *
+ * For callers that cannot allocate device memory themselves -- for example code that
+ * only receives device buffers from a host application and has no cudaMalloc or
+ * caching allocator of its own -- this entry point keeps its scratch (one softmax
+ * state per row slice) in a fixed device array inside the library instead of a
+ * caller workspace, and allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine.  The array holds 16384 states (256 KB) and stays resident on every
+ * GPU that loads the library until the process exits; shapes that need more (roughly
+ * B*M rows x ceil(V/2048) slices, capped by the GPU size) are rejected with
+ * DLLM_ERR_UNSUPPORTED and a message.  Outputs, arguments and results are those of
+ * dllm_commit_entropy.
+ * The first call on a device looks up the array's device address (once per device,
+ * with that device current); make that first call before any stream capture.  All
+ * calls share the one array and it keeps the previous call's contents (each call
+ * writes every state it reads, so nothing needs clearing); calls whose kernels could
+ * overlap on the GPU (different streams without ordering) race on it.
+ * ------------------------------------------------------------------------- */
+int dllm_commit_entropy_noalloc(const float *logits, const uint8_t *valid, int B, int M, int V,
+                                float conf_thresh, float tau, int32_t *token, float *conf,
+                                float *entropy, float *max_entropy, int32_t *full_next,
+                                void *stream);
+
+/* ---------------------------------------------------------------------------
  * Around the layers of a denoising step ([EC] step 1: the forward pass; step 2:
  * decode from the logits of the current block).
  *

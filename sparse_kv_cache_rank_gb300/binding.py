@@ -65,6 +65,8 @@ _SIGS = {
                    + [C.c_void_p]),
     "dllm_rows_rmsnorm": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_void_p, C.c_float, C.c_void_p]
                           + [C.c_int] * 4 + [C.c_void_p]),
+    "dllm_commit_entropy_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
+                                              C.c_float, C.c_float] + [C.c_void_p] * 6),
     "dllm_commit_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
     "dllm_commit_entropy": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                       C.c_float, C.c_float] + [C.c_void_p] * 6 +
@@ -355,4 +357,25 @@ def dllm_commit_entropy(logits, valid, conf_thresh: float = 0.9, tau: float = 2.
                                      float(tau), _ptr(tok), _ptr(conf), _ptr(ent), _ptr(E),
                                      _ptr(full), _ptr(ws), ws.numel(), _stream(dev)),
            "dllm_commit_entropy")
+    return out
+
+
+def dllm_commit_entropy_noalloc(logits, valid, conf_thresh: float = 0.9, tau: float = 2.0, out=None):
+    """dllm_commit_entropy for callers that cannot allocate device memory: the library
+    keeps the scratch in its own fixed device array (no workspace argument).  The caller
+    still provides the output tensors (allocated here when `out` is None)."""
+    B, M, V = logits.shape
+    dev = logits.device
+    if out is None:
+        out = (torch.empty((B, M), dtype=torch.int32, device=dev),
+               torch.empty((B, M), dtype=torch.float32, device=dev),
+               torch.empty((B, M), dtype=torch.float32, device=dev),
+               torch.empty((B,), dtype=torch.float32, device=dev),
+               torch.empty((B,), dtype=torch.int32, device=dev))
+    tok, conf, ent, E, full = out
+    _cuda(logits, valid, *out)
+    _check(lib().dllm_commit_entropy_noalloc(_ptr(logits), _ptr(valid), B, M, V, float(conf_thresh),
+                                             float(tau), _ptr(tok), _ptr(conf), _ptr(ent), _ptr(E),
+                                             _ptr(full), _stream(dev)),
+           "dllm_commit_entropy_noalloc")
     return out

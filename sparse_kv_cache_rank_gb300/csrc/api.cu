@@ -560,3 +560,26 @@ DLLM_EXPORT int dllm_set_pdl(int enable) {
     const int old = dllm::g_pdl.exchange(enable ? 1 : 0);
     return old;
 }
+
+// ------------------------------------------------------------------ allocation-free vocabulary step
+DLLM_EXPORT int dllm_commit_entropy_noalloc(const float *logits, const uint8_t *valid, int B, int M,
+                                            int V, float conf_thresh, float tau, int32_t *token,
+                                            float *conf, float *entropy, float *max_entropy,
+                                            int32_t *full_next, void *stream) {
+    CHECK_ARG(max_entropy && full_next, "null pointer");
+    CHECK_ARG(B > 0 && M >= 0 && V > 0, "sizes must be positive");
+    CHECK_ARG(M <= 1024, "M must be <= 1024 (got %d)", M);
+    if (M > 0) CHECK_ARG(logits && valid && token && conf && entropy, "null pointer");
+    const size_t states = commit_noalloc_states(B, M, V);
+    if (states > (size_t)commit_noalloc_max_states())
+        return fail(DLLM_ERR_UNSUPPORTED,
+                    "B*M = %d rows need %zu scratch states; the allocation-free entry point holds %d "
+                    "(use dllm_commit_entropy with a workspace)",
+                    B * M, states, commit_noalloc_max_states());
+    cudaStream_t st = as_stream(stream);
+    Launch t(DLLM_KERNEL_VOCAB, st, 2);
+    CHECK_CUDA(commit_entropy_noalloc(logits, valid, B, M, V, conf_thresh, tau, token, conf, entropy,
+                                      max_entropy, full_next, st),
+               "commit launch");
+    return DLLM_OK;
+}

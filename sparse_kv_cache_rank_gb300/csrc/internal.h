@@ -115,3 +115,13 @@ cudaError_t commit_entropy(const float *logits, const uint8_t *valid, int B, int
                            cudaStream_t st);
 
 }  // namespace dllm
+
+namespace dllm {
+// Allocation-free vocabulary step (scratch in a device array of the library).
+int commit_noalloc_max_states();
+size_t commit_noalloc_states(int B, int M, int V);
+cudaError_t commit_entropy_noalloc(const float *logits, const uint8_t *valid, int B, int M, int V,
+                                   float conf_thresh, float tau, int32_t *token, float *conf,
+                                   float *entropy, float *max_entropy, int32_t *full_next,
+                                   cudaStream_t st);
+}  // namespace dllm

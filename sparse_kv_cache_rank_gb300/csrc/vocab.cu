@@ -9,6 +9,7 @@
 // Pass 2 (one CTA per sequence) merges the slices of each row and applies the commit
 // rule and the full-refresh decision.
 #include <cfloat>
+#include <mutex>
 
 #include "internal.h"
 
@@ -196,6 +197,61 @@ cudaError_t commit_entropy(const float *logits, const uint8_t *valid, int B, int
                                         max_entropy, full_next);
     }
     return cudaGetLastError();
+}
+
+}  // namespace dllm
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the vocabulary step, for callers that cannot allocate
+// device memory (no cudaMalloc and no caching allocator on their side, e.g. code that
+// only ever receives buffers from a host application).  Its scratch (one softmax state
+// per row slice) lives in this file-scope device array instead of a caller workspace;
+// every GPU that loads the library keeps the array until the process exits.
+namespace dllm {
+namespace {
+
+constexpr int kNoAllocStates = 16384;   // 16384 row-slice states x 16 bytes = 256 KB
+__device__ __align__(256) RowState g_commit_scratch[kNoAllocStates];
+
+// Device address of the scratch array on the current device (resolved once per device).
+cudaError_t noalloc_scratch(RowState **out) {
+    static RowState *addr[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_commit_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = static_cast<RowState *>(p);
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+int commit_noalloc_max_states() { return kNoAllocStates; }
+
+size_t commit_noalloc_states(int B, int M, int V) {
+    const int rows = B * M;
+    return (size_t)rows * slices_for(rows, V);
+}
+
+cudaError_t commit_entropy_noalloc(const float *logits, const uint8_t *valid, int B, int M, int V,
+                                   float conf_thresh, float tau, int32_t *token, float *conf,
+                                   float *entropy, float *max_entropy, int32_t *full_next,
+                                   cudaStream_t st) {
+    RowState *scratch = nullptr;
+    cudaError_t e = noalloc_scratch(&scratch);
+    if (e != cudaSuccess) return e;
+    // every state the commit kernel reads is written by the row kernel of this call,
+    // so nothing has to be cleared between calls
+    return commit_entropy(logits, valid, B, M, V, conf_thresh, tau, token, conf, entropy, max_entropy,
+                          full_next, scratch, st);
 }
 
 }  // namespace dllm
