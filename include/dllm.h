@@ -83,10 +83,15 @@ int dllm_check_status(unsigned *status_out, int reset);
  *   proxy_cur   [B, N, r]  fp32 out
  *   drift       [B, N]     fp32 out
  * Requirements: r % 32 == 0, r <= 1024; d % 64 == 0 for DLLM_BF16.
- * No workspace.
+ * Workspace: dllm_proxy_workspace_bytes() (fp32 partial proxies of independent K slices,
+ * summed in a fixed order, so identical inputs always give identical proxies); 0 bytes
+ * when the shape needs no K split.
  * ------------------------------------------------------------------------- */
+size_t dllm_proxy_workspace_bytes(int B, int N, int d, int r, int dtype);
+
 int dllm_proxy_score(const void *H, const void *Pt, const float *proxy_cache, float *proxy_cur,
-                     float *drift, int B, int N, int d, int r, int dtype, void *stream);
+                     float *drift, int B, int N, int d, int r, int dtype, void *ws,
+                     size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
  * Selection.  [SPA] "1. ...": the rows with the lowest proxy similarity (largest

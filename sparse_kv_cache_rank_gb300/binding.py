@@ -39,7 +39,8 @@ _SIGS = {
     "dllm_last_error": (C.c_char_p, []),
     "dllm_version": (C.c_int, []),
     "dllm_check_status": (C.c_int, [C.POINTER(C.c_uint), C.c_int]),
-    "dllm_proxy_score": (C.c_int, [C.c_void_p] * 5 + [C.c_int] * 5 + [C.c_void_p]),
+    "dllm_proxy_score": (C.c_int, [C.c_void_p] * 5 + [C.c_int] * 5 + [C.c_void_p, C.c_size_t, C.c_void_p]),
+    "dllm_proxy_workspace_bytes": (C.c_size_t, [C.c_int] * 5),
     "dllm_select_topk": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_float,
                                    C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p]),
     "dllm_layer_rho": (C.c_double, [C.c_int] + [C.c_double] * 5),
@@ -174,7 +175,7 @@ def dllm_set_pdl(enable: bool) -> bool:
 
 
 # --------------------------------------------------------------------------- proxy
-def dllm_proxy_score(H, Pt, proxy_cache, proxy_cur=None, drift=None):
+def dllm_proxy_score(H, Pt, proxy_cache, proxy_cur=None, drift=None, ws=None):
     """H [B,N,d] (bf16|f32), Pt [r,d] same dtype, proxy_cache [B,N,r] f32 ->
     (proxy_cur [B,N,r] f32, drift [B,N] f32)."""
     B, N, d = H.shape
@@ -186,8 +187,12 @@ def dllm_proxy_score(H, Pt, proxy_cache, proxy_cur=None, drift=None):
     if drift is None:
         drift = torch.empty((B, N), dtype=torch.float32, device=H.device)
     _cuda(H, Pt, proxy_cache, proxy_cur, drift)
+    need = int(lib().dllm_proxy_workspace_bytes(B, N, d, r, _dtype_code(H)))
+    if ws is None and need > 0:
+        ws = _workspace(need, H.device, "proxy")
     _check(lib().dllm_proxy_score(_ptr(H), _ptr(Pt), _ptr(proxy_cache), _ptr(proxy_cur), _ptr(drift),
-                                  B, N, d, r, _dtype_code(H), _stream(H.device)), "dllm_proxy_score")
+                                  B, N, d, r, _dtype_code(H), _ptr(ws), 0 if ws is None else ws.numel(),
+                                  _stream(H.device)), "dllm_proxy_score")
     return proxy_cur, drift
 
 

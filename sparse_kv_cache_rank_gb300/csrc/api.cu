@@ -211,9 +211,22 @@ DLLM_EXPORT int dllm_check_status(unsigned *status_out, int reset) {
 }
 
 // ------------------------------------------------------------------ proxy score
+namespace {
+int proxy_slices(int B, int N, int d, int r, int dtype) {
+    if (dtype != DLLM_BF16 || B <= 0 || N <= 0 || d % 64 || r % 32) return 1;
+    return gemm_tc_slices_count(B * N, r, d);
+}
+}  // namespace
+
+DLLM_EXPORT size_t dllm_proxy_workspace_bytes(int B, int N, int d, int r, int dtype) {
+    if (B <= 0 || N <= 0 || d <= 0 || r <= 0) return 0;
+    const int s = proxy_slices(B, N, d, r, dtype);
+    return s > 1 ? (size_t)s * B * N * r * sizeof(float) + 256 : 0;
+}
+
 DLLM_EXPORT int dllm_proxy_score(const void *H, const void *Pt, const float *proxy_cache,
                                  float *proxy_cur, float *drift, int B, int N, int d, int r,
-                                 int dtype, void *stream) {
+                                 int dtype, void *ws, size_t ws_bytes, void *stream) {
     CHECK_ARG(H && Pt && proxy_cache && proxy_cur && drift, "null pointer");
     CHECK_ARG(B > 0 && N > 0 && d > 0 && r > 0, "sizes must be positive (B=%d N=%d d=%d r=%d)", B, N, d, r);
     CHECK_ARG(r <= 1024, "r must be <= 1024");
@@ -223,21 +236,30 @@ DLLM_EXPORT int dllm_proxy_score(const void *H, const void *Pt, const float *pro
     if (r % 32) return fail(DLLM_ERR_UNSUPPORTED, "r must be a multiple of 32 (got %d)", r);
     cudaStream_t st = as_stream(stream);
     const int rows = B * N;
-    EpiStoreF32 epi{SelRows{}, proxy_cur, r, r};
     cudaError_t e;
+    const int nparts = proxy_slices(B, N, d, r, dtype);
+    float *parts = proxy_cur;
+    if (nparts > 1) {   // K slices write fp32 partials; the cosine kernel sums them in order
+        const size_t need = dllm_proxy_workspace_bytes(B, N, d, r, dtype);
+        if (!ws || ws_bytes < need)
+            return fail(DLLM_ERR_WORKSPACE, "workspace holds %zu bytes, %zu needed", ws_bytes, need);
+        parts = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255));
+    }
     if (dtype == DLLM_BF16) {
         if (d % 64) return fail(DLLM_ERR_UNSUPPORTED, "bf16 path needs d % 64 == 0 (got %d)", d);
         Launch t(DLLM_KERNEL_PROXY_GEMM, st);
-        e = gemm_tc(static_cast<const bf16 *>(Pt), r, d, static_cast<const bf16 *>(H), rows, epi, 0, true,
-                    status_ptr(), st);
+        e = gemm_tc_slices(static_cast<const bf16 *>(Pt), r, d, static_cast<const bf16 *>(H), rows, parts,
+                           true, status_ptr(), st);
     } else {
         Launch t(DLLM_KERNEL_PROXY_GEMM, st);
+        EpiStoreF32 epi{SelRows{}, proxy_cur, r, r};
         e = gemm_simt(static_cast<const float *>(Pt), r, d, static_cast<const float *>(H), rows, epi, st);
     }
     CHECK_CUDA(e, "proxy projection launch");
     {
         Launch t(DLLM_KERNEL_COSINE, st);
-        CHECK_CUDA(cosine_drift(proxy_cur, proxy_cache, drift, rows, r, st), "cosine drift launch");
+        CHECK_CUDA(cosine_drift(parts, nparts, proxy_cache, proxy_cur, drift, rows, r, st),
+                   "cosine drift launch");
     }
     return DLLM_OK;
 }

@@ -213,11 +213,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < OH; ++e) o[e] = 0.f;
         float m_run = -INFINITY, l_run = 0.f;
+        float corr_prev = 1.f;   // rescale factor of the PV product still in flight
         uint8_t *prow = sP + hf * kChunk + (r >> 3) * 1024 + (r & 7) * 128;
-        for (int it = 0; it < nt; ++it) {
+        // O <- O * corr + PV of the previous tile (its MMA overlapped this tile's softmax)
+        auto fold_pv = [&](int tile) -> bool {
+            if (!mbar_wait(pv_full, (uint32_t)tile & 1u, abort_flag, status)) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < OH; c0 += 16) {
+                float t[16];
+                tmem_ld_x16(tPV + lane_addr + (uint32_t)(hf * OH + c0), t);
+                tmem_ld_wait(t);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) o[c0 + j] = fmaf(o[c0 + j], corr_prev, t[j]);
+            }
+            return true;
+        };
+        bool ok = true;
+        for (int it = 0; it < nt && ok; ++it) {
             const int s = it & 1;
             const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-            if (!mbar_wait(&s_full[s], ph, abort_flag, status)) break;
+            if (!mbar_wait(&s_full[s], ph, abort_flag, status)) { ok = false; break; }
             tc_fence_after();
             const int nvalid = a.N - (t0 + it) * AKV - hf * 64;   // keys of my half inside [0, N)
             float v[64];
@@ -238,35 +254,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float m_new = fmaxf(m_run, mt * a.scale_log2);
             const float corr = exp2f(m_run - m_new);
             float lsum = 0.f;
+            uint32_t pk[32];                           // P of this tile, bf16 pairs
+#pragma unroll
+            for (int j = 0; j < 64; j += 2) {
+                const float p0 = (j < nvalid) ? exp2f(v[j] * a.scale_log2 - m_new) : 0.f;
+                const float p1 = (j + 1 < nvalid) ? exp2f(v[j + 1] * a.scale_log2 - m_new) : 0.f;
+                const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
+                lsum += __low2float(pp) + __high2float(pp);
+                pk[j >> 1] = *reinterpret_cast<const uint32_t *>(&pp);
+            }
+            // the P buffer is free once the previous tile's PV product has completed
+            if (it > 0 && !(ok = fold_pv(it - 1))) break;
 #pragma unroll
             for (int c0 = 0; c0 < 64; c0 += 8) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int j = 0; j < 8; j += 2) {
-                    const float p0 = (c0 + j < nvalid) ? exp2f(v[c0 + j] * a.scale_log2 - m_new) : 0.f;
-                    const float p1 = (c0 + j + 1 < nvalid) ? exp2f(v[c0 + j + 1] * a.scale_log2 - m_new) : 0.f;
-                    const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
-                    lsum += __low2float(pp) + __high2float(pp);
-                    pk[j >> 1] = *reinterpret_cast<const uint32_t *>(&pp);
-                }
                 const int u = (c0 >> 3) ^ (r & 7);       // 16-byte unit in the swizzled row
-                *reinterpret_cast<uint4 *>(prow + u * 16) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                *reinterpret_cast<uint4 *>(prow + u * 16) =
+                    make_uint4(pk[c0 / 2], pk[c0 / 2 + 1], pk[c0 / 2 + 2], pk[c0 / 2 + 3]);
             }
             fence_proxy_async_smem();
             mbar_arrive(p_full);
             l_run = l_run * corr + lsum;
             m_run = m_new;
-            if (!mbar_wait(pv_full, (uint32_t)it & 1u, abort_flag, status)) break;
-            tc_fence_after();
-#pragma unroll
-            for (int c0 = 0; c0 < OH; c0 += 16) {
-                float t[16];
-                tmem_ld_x16(tPV + lane_addr + (uint32_t)(hf * OH + c0), t);
-                tmem_ld_wait(t);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) o[c0 + j] = fmaf(o[c0 + j], corr, t[j]);
-            }
+            corr_prev = corr;
         }
+        if (ok && nt > 0) fold_pv(nt - 1);
         // combine the two halves' row sums
         xsum[hf * 128 + r] = l_run;
         named_bar_sync(2 + q, 64);

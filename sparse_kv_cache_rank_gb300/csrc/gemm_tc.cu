@@ -40,7 +40,9 @@ struct Shape {
     int M_tok, N_out, K;
     int BN, splits, stages;
     int w_const;      // weights are never written on the device: stream them before the wait
-    int body_bytes;   // pipeline ring (and, with a K split, the fp32 partial tile [BN][128])
+    int indep;        // K slices are independent CTAs (no cluster): slice z writes token rows
+                      // z * M_tok + m of the epilogue's output (partial sums, reduced later)
+    int body_bytes;   // pipeline ring (and, with a cluster K split, the fp32 partial tile [BN][128])
 };
 
 __host__ __device__ inline int stage_bytes(int BN) { return kWBytes + BN * BK * 2; }
@@ -80,7 +82,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * g.BN;
     const int n0 = blockIdx.y * BM;
-    const int split = g.splits > 1 ? (int)cluster_ctarank() : 0;
+    const int split = g.indep ? (int)blockIdx.z : (g.splits > 1 ? (int)cluster_ctarank() : 0);
+    const bool cluster_split = g.splits > 1 && !g.indep;
     const int KB = g.K / BK;
     const int kb0 = (int)((long long)split * KB / g.splits);
     const int kb1 = (int)((long long)(split + 1) * KB / g.splits);
@@ -175,15 +178,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
         const int nchunk = (g.BN + 15) / 16;
         const int ch0 = half == 0 ? 0 : (nchunk + 1) / 2, ch1 = half == 0 ? (nchunk + 1) / 2 : nchunk;
-        if (g.splits == 1) {
-            // straight from TMEM
+        if (!cluster_split) {
+            // straight from TMEM (independent K slices write rows split * M_tok + m)
+            const int moff = g.indep ? split * g.M_tok : 0;
             if (n0 + q * 32 < g.N_out) {   // warp-uniform: N_out % 32 == 0
                 const typename Epi::Feat F = epi.feat(n0 + f);
                 for (int ch = ch0; ch < ch1 && ch * 16 < ncols; ++ch) {
                     float v[16];
                     tmem_ld_x16(taddr + (uint32_t)(ch * 16), v);
                     tmem_ld_wait(v);
-                    epi_16(epi, F, m0, ch * 16, ncols, col_b, col_pos, v);
+                    epi_16(epi, F, m0 + moff, ch * 16, ncols, col_b, col_pos, v);
                 }
             }
         } else {
@@ -199,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     }
     tc_fence_before();
-    if (g.splits > 1) {
+    if (cluster_split) {
         cluster_sync_all();
         if (warp >= 2) {   // ---------------- reduce the cluster's partials, epilogue on my share
             const int q = warp & 3;
@@ -281,7 +285,7 @@ struct Plan {
 
 int round16(int x) { return (x + 15) / 16 * 16; }
 
-Plan make_plan(int M_tok, int N_out, int K, int BN, int splits, int budget) {
+Plan make_plan(int M_tok, int N_out, int K, int BN, int splits, int budget, bool smem_partial) {
     Plan p{};
     p.BN = BN;
     p.splits = splits;
@@ -289,7 +293,7 @@ Plan make_plan(int M_tok, int N_out, int K, int BN, int splits, int budget) {
     p.tok_tiles = (M_tok + BN - 1) / BN;
     const int sb = stage_bytes(BN);
     const int tail = 1024 + kTailBytes + kColBytes;
-    const int part = splits > 1 ? BN * BM * 4 : 0;
+    const int part = smem_partial ? BN * BM * 4 : 0;
     p.stages = (budget - tail) / sb;
     if (p.stages > 8) p.stages = 8;
     const int KB = K / BK;
@@ -317,40 +321,48 @@ Plan plan_gemm(int M_tok, int N_out, int K, int splits_req) {
     if (splits_req > 0) {
         const int BN = M_tok <= 256 ? round16(M_tok) : 256;
         const int s = clamp_splits(splits_req);
-        return make_plan(M_tok, N_out, K, BN, s, s == 1 ? kSmemPair : kSmemLimit);
+        return make_plan(M_tok, N_out, K, BN, s, s == 1 ? kSmemPair : kSmemLimit, s > 1);
     }
     if (M_tok <= 256) {
         if (2 * w_tiles >= sms) {
             int BN = round16(M_tok);
             if (w_tiles < sms && M_tok > 32) BN = round16((M_tok + 1) / 2);
-            return make_plan(M_tok, N_out, K, BN, 1, kSmemPair);
+            return make_plan(M_tok, N_out, K, BN, 1, kSmemPair, false);
         }
         int BN = round16(M_tok);
         const int tok_tiles = 1;
         const int s = clamp_splits(sms / (w_tiles * tok_tiles));
-        return make_plan(M_tok, N_out, K, BN, s, s == 1 ? kSmemPair : kSmemLimit);
+        return make_plan(M_tok, N_out, K, BN, s, s == 1 ? kSmemPair : kSmemLimit, s > 1);
     }
     int BN = 256;
     while (BN > 64 && (long long)w_tiles * ((M_tok + BN - 1) / BN) * 8 < sms) BN = round16(BN / 2);
     const long long tiles = (long long)w_tiles * ((M_tok + BN - 1) / BN);
     const int s = tiles >= sms ? 1 : clamp_splits((int)(sms / tiles));
-    return make_plan(M_tok, N_out, K, BN, s, s == 1 ? kSmemPair : kSmemLimit);
+    return make_plan(M_tok, N_out, K, BN, s, s == 1 ? kSmemPair : kSmemLimit, s > 1);
 }
 
-}  // namespace
+// Independent K slices (no cluster), each writing its own fp32 partial output: token
+// tiles of 64 rows (128 beyond 2048 tokens), slices sized to two CTAs per SM.
+Plan plan_slices(int M_tok, int N_out, int K) {
+    const int sms = num_sms();
+    const int KB = K / BK;
+    const int BN = M_tok <= 256 ? round16(M_tok) : (M_tok <= 2048 ? 64 : 128);
+    const long long tiles = (long long)((N_out + BM - 1) / BM) * ((M_tok + BN - 1) / BN);
+    int s = (int)(2 * sms / tiles);
+    s = s < 1 ? 1 : (s > 8 ? 8 : s);
+    while (s > 1 && KB / s < 2) --s;
+    return make_plan(M_tok, N_out, K, BN, s, kSmemPair, false);
+}
 
 template <class Epi>
-cudaError_t gemm_tc(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, const Epi &epi,
-                    int splits, bool w_const, unsigned *status, cudaStream_t st) {
-    if (M_tok <= 0 || N_out <= 0) return cudaSuccess;
-    if (K % BK != 0 || N_out % 32 != 0) return cudaErrorInvalidValue;
-    const Plan p = plan_gemm(M_tok, N_out, K, splits);
+cudaError_t launch_plan(const Plan &p, bool indep, const bf16 *W, int N_out, int K, const bf16 *X,
+                        int M_tok, const Epi &epi, bool w_const, unsigned *status, cudaStream_t st) {
     if (p.stages < 2) return cudaErrorInvalidValue;
     CUtensorMap tmW, tmX;
     if (!make_tmap(&tmW, W, (uint64_t)N_out, (uint64_t)K, BM) ||
         !make_tmap(&tmX, X, (uint64_t)M_tok, (uint64_t)K, (uint32_t)p.BN))
         return cudaErrorInvalidValue;
-    Shape g{M_tok, N_out, K, p.BN, p.splits, p.stages, w_const ? 1 : 0, p.body};
+    Shape g{M_tok, N_out, K, p.BN, p.splits, p.stages, w_const ? 1 : 0, indep ? 1 : 0, p.body};
     auto kern = k_gemm_tc<Epi>;
     static bool configured[64] = {};   // per device: raise the shared-memory limit once
     int dev = 0;
@@ -361,7 +373,32 @@ cudaError_t gemm_tc(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, c
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
     return launch_kernel(kern, dim3(p.tok_tiles, p.w_tiles, p.splits), dim3(kThreads), p.smem, st,
-                         p.splits, tmW, tmX, g, epi, status);
+                         indep ? 1 : p.splits, tmW, tmX, g, epi, status);
+}
+
+}  // namespace
+
+template <class Epi>
+cudaError_t gemm_tc(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, const Epi &epi,
+                    int splits, bool w_const, unsigned *status, cudaStream_t st) {
+    if (M_tok <= 0 || N_out <= 0) return cudaSuccess;
+    if (K % BK != 0 || N_out % 32 != 0) return cudaErrorInvalidValue;
+    return launch_plan(plan_gemm(M_tok, N_out, K, splits), false, W, N_out, K, X, M_tok, epi, w_const,
+                       status, st);
+}
+
+int gemm_tc_slices_count(int M_tok, int N_out, int K) {
+    if (M_tok <= 0 || N_out <= 0 || K % BK != 0) return 1;
+    return plan_slices(M_tok, N_out, K).splits;
+}
+
+cudaError_t gemm_tc_slices(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, float *parts,
+                           bool w_const, unsigned *status, cudaStream_t st) {
+    if (M_tok <= 0 || N_out <= 0) return cudaSuccess;
+    if (K % BK != 0 || N_out % 32 != 0) return cudaErrorInvalidValue;
+    const Plan p = plan_slices(M_tok, N_out, K);
+    EpiStoreF32 epi{SelRows{}, parts, N_out, N_out};
+    return launch_plan(p, true, W, N_out, K, X, M_tok, epi, w_const, status, st);
 }
 
 template cudaError_t gemm_tc<EpiStoreF32>(const bf16 *, int, int, const bf16 *, int,

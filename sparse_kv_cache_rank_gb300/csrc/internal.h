@@ -54,6 +54,12 @@ template <class Epi>
 cudaError_t gemm_tc(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, const Epi &epi,
                     int splits, bool w_const, unsigned *status, cudaStream_t st);
 
+// Independent K slices: parts[z * M_tok + m, f] = partial sum of slice z (fp32), for a
+// later fixed-order reduction; gemm_tc_slices_count() tells how many slices it uses.
+int gemm_tc_slices_count(int M_tok, int N_out, int K);
+cudaError_t gemm_tc_slices(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, float *parts,
+                           bool w_const, unsigned *status, cudaStream_t st);
+
 // CUDA cores (fp32 FMA): any K.
 template <class Epi>
 cudaError_t gemm_simt(const float *W, int N_out, int K, const float *X, int M_tok, const Epi &epi,
@@ -69,8 +75,10 @@ template <class T>
 cudaError_t rmsnorm_rows(const float *h1, int M, int d, const T *gamma, float eps, T *Xn2,
                          cudaStream_t st);
 
-cudaError_t cosine_drift(const float *cur, const float *cached, float *drift, long rows, int r,
-                         cudaStream_t st);
+// cur = sum of nparts partial proxies (parts[z * rows * r ...], fixed order; when
+// nparts == 1, parts is cur itself), then drift = 1 - cos(cur, cached).  r <= 1024.
+cudaError_t cosine_drift(const float *parts, int nparts, const float *cached, float *cur,
+                         float *drift, long rows, int r, cudaStream_t st);
 
 template <class T>
 cudaError_t pack_rows_rope(const T *src, T *dst, int rows, int cols, int hd, cudaStream_t st);

@@ -90,16 +90,29 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float *__restrict__ 
 // drift = 1 - cos(cur, cached), evaluated as |cur/|cur| - cached/|cached||^2 / 2, which
 // equals 1 - cos for unit vectors and keeps the small drifts of nearly unchanged rows
 // free of the cancellation in 1 - dot/norm.  Identical inputs give exactly 0; both
-// norms zero -> 0, one zero -> 1; clamped to [0, 2].  One warp per row.
-__global__ void __launch_bounds__(256) k_cosine_drift(const float *__restrict__ cur,
+// norms zero -> 0, one zero -> 1; clamped to [0, 2].  One warp per row.  With
+// nparts > 1 the proxy is first summed from the K-slice partials in slice order (the
+// same order every call, so identical inputs still give identical proxies).
+__global__ void __launch_bounds__(256) k_cosine_drift(const float *__restrict__ parts, int nparts,
                                                       const float *__restrict__ cached,
+                                                      float *__restrict__ cur,
                                                       float *__restrict__ drift, long rows, int r) {
     griddep_wait();
     griddep_launch();
     const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
-    const float *a = cur + row * r, *c = cached + row * r;
+    float *a = cur + row * r;
+    const float *c = cached + row * r;
+    if (nparts > 1) {
+        const size_t stride = (size_t)rows * r;
+        for (int e = lane; e < r; e += 32) {
+            const float *p = parts + row * r + e;
+            float x = p[0];
+            for (int z = 1; z < nparts; ++z) x += p[z * stride];
+            a[e] = x;
+        }
+    }
     float na = 0.f, nc = 0.f;
     for (int e = lane; e < r; e += 32) {
         na = fmaf(a[e], a[e], na);
@@ -175,11 +188,11 @@ cudaError_t rmsnorm_rows(const float *h1, int M, int d, const T *gamma, float ep
     return cudaGetLastError();
 }
 
-cudaError_t cosine_drift(const float *cur, const float *cached, float *drift, long rows, int r,
-                         cudaStream_t st) {
+cudaError_t cosine_drift(const float *parts, int nparts, const float *cached, float *cur,
+                         float *drift, long rows, int r, cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
-    return launch_kernel(k_cosine_drift, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, st, 1, cur, cached, drift, rows, r);
-    return cudaGetLastError();
+    return launch_kernel(k_cosine_drift, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, st, 1, parts,
+                         nparts, cached, cur, drift, rows, r);
 }
 
 template <class T>
