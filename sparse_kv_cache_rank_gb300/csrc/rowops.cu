@@ -105,11 +105,21 @@ __global__ void __launch_bounds__(256) k_cosine_drift(const float *__restrict__ 
     float *a = cur + row * r;
     const float *c = cached + row * r;
     if (nparts > 1) {
+        // all partial loads of a batch are issued before the first add (slice order kept)
         const size_t stride = (size_t)rows * r;
+#pragma unroll 4
         for (int e = lane; e < r; e += 32) {
             const float *p = parts + row * r + e;
-            float x = p[0];
-            for (int z = 1; z < nparts; ++z) x += p[z * stride];
+            float x = 0.f;
+            int z = 0;
+            for (; z + 8 <= nparts; z += 8) {
+                float t[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) t[u] = __ldcg(p + (size_t)(z + u) * stride);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x += t[u];
+            }
+            for (; z < nparts; ++z) x += __ldcg(p + (size_t)z * stride);
             a[e] = x;
         }
     }

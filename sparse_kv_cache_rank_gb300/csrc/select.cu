@@ -86,9 +86,9 @@ __global__ void __launch_bounds__(kT) k_select_topk(const float *__restrict__ dr
         }
         key[i] = kk;
     }
-    uint32_t tot_f, tot_e;
-    block_scan(nf, wsum, &tot_f);
-    block_scan(ne, wsum, &tot_e);
+    uint32_t tot_fe;   // both counts in one scan (N <= 16384 < 2^16)
+    block_scan((nf << 16) | ne, wsum, &tot_fe);
+    const uint32_t tot_f = tot_fe >> 16, tot_e = tot_fe & 0xFFFFu;
     long long budget = (long long)N - tot_f;
     if ((long long)k < budget) budget = k;
     if (budget < 0) budget = 0;
@@ -108,9 +108,17 @@ __global__ void __launch_bounds__(kT) k_select_topk(const float *__restrict__ dr
         for (int shift = 24; shift >= 0; shift -= 8) {
             for (int i = tid; i < 256; i += kT) hist[i] = 0;
             __syncthreads();
-            for (int i = i0; i < i1; ++i) {
-                const uint32_t kk = key[i];
-                if (kk != 0 && (kk & mask) == prefix) atomicAdd(&hist[(kk >> shift) & 255u], 1u);
+            // warp-aggregated counts: most keys share their leading digits, so one
+            // atomic per distinct digit per warp instead of one per key
+            for (int c = 0; c < C; ++c) {
+                const int i = i0 + c;
+                uint32_t dg = 256u;   // no digit
+                if (i < i1) {
+                    const uint32_t kk = key[i];
+                    if (kk != 0 && (kk & mask) == prefix) dg = (kk >> shift) & 255u;
+                }
+                const uint32_t same = __match_any_sync(0xffffffffu, dg);
+                if (dg < 256u && (threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(&hist[dg], (uint32_t)__popc(same));
             }
             __syncthreads();
             if (tid < 32) {
