@@ -210,6 +210,22 @@ int dllm_commit_entropy(const float *logits, const uint8_t *valid, int B, int M,
                         size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * [SPA] "3. Sparse execution", the attention of the selected queries alone (the same
+ * kernels dllm_sparse_layer_refresh runs after the K/V scatter):
+ *   A[m, h] = softmax(Q[m, h] K_cache[b, :, g]^T / sqrt(hd)) V_cache[b, :, g]
+ * over all N rows, non-causal, g = h / (n_q / n_kv), for every flattened row
+ * m = b * k_max + s that is live (s < min(count[b], k_max) and idx[b, s] in [0, N));
+ * other rows of A get zeros.  Q and A [B*k_max, n_q*hd]; K_cache, V_cache [B, N, n_kv, hd];
+ * idx [B, N], count [B] int32 as written by dllm_select_topk; dtype as the caches.
+ * Requirements: hd in {64, 128}; k_max <= N.
+ * ------------------------------------------------------------------------- */
+size_t dllm_attention_workspace_bytes(int B, int N, int k_max, int n_q, int hd, int dtype);
+
+int dllm_attention(const void *Q, const void *K_cache, const void *V_cache, void *A,
+                   const int32_t *idx, const int32_t *count, int k_max, int B, int N, int n_q,
+                   int n_kv, int hd, int dtype, void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
  * dllm_commit_entropy without a workspace.  (No counterpart on the pages: this is an
  * interface variant, not a step of the method.)
  *

@@ -62,6 +62,8 @@ _SIGS = {
     "dllm_launch_count": (C.c_ulonglong, []),
     "dllm_gemm_bf16": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                  C.c_int, C.c_void_p]),
+    "dllm_attention_workspace_bytes": (C.c_size_t, [C.c_int] * 6),
+    "dllm_attention": (C.c_int, [C.c_void_p] * 6 + [C.c_int] * 8 + [C.c_void_p, C.c_size_t, C.c_void_p]),
     "dllm_embed": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_void_p] + [C.c_int] * 5
                    + [C.c_void_p]),
     "dllm_rows_rmsnorm": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_void_p, C.c_float, C.c_void_p]
@@ -300,6 +302,25 @@ def dllm_sparse_layer_refresh(layer: Layer, H_in, idx, count, k_max: int, K_cach
                                            B, N, _ptr(ws), ws.numel(), _stream(H_in.device)),
            "dllm_sparse_layer_refresh")
     return K_cache, V_cache, H_out_cache
+
+
+# --------------------------------------------------------------------------- attention alone
+def dllm_attention(Q, K_cache, V_cache, idx, count, k_max: int, A=None, ws=None):
+    """Q [B*k_max, n_q*hd], caches [B, N, n_kv, hd] -> A [B*k_max, n_q*hd] (zeros for rows
+    that are not live)."""
+    Bn, N, n_kv, hd = K_cache.shape
+    n_q = Q.shape[1] // hd
+    if A is None:
+        A = torch.empty_like(Q)
+    _cuda(Q, K_cache, V_cache, A, idx, count)
+    dt = _dtype_code(Q)
+    need = int(lib().dllm_attention_workspace_bytes(Bn, N, int(k_max), n_q, hd, dt))
+    if ws is None and need > 0:
+        ws = _workspace(need, Q.device, "attention")
+    _check(lib().dllm_attention(_ptr(Q), _ptr(K_cache), _ptr(V_cache), _ptr(A), _ptr(idx), _ptr(count),
+                                int(k_max), Bn, N, n_q, n_kv, hd, dt, _ptr(ws),
+                                0 if ws is None else ws.numel(), _stream(Q.device)), "dllm_attention")
+    return A
 
 
 # --------------------------------------------------------------------------- embedding, final norm

@@ -460,6 +460,45 @@ DLLM_EXPORT int dllm_sparse_layer_refresh(const dllm_layer *W, const void *H_in,
                                proxy_cache, proxy_cur, r, w8, st);
 }
 
+// ------------------------------------------------------------------ attention alone
+DLLM_EXPORT size_t dllm_attention_workspace_bytes(int B, int N, int k_max, int n_q, int hd, int dtype) {
+    if (B <= 0 || N <= 0 || k_max <= 0 || n_q <= 0 || dtype != DLLM_BF16) return 0;
+    return attention_tc_ws_bytes(B, k_max, n_q, hd, N) + 256;
+}
+
+DLLM_EXPORT int dllm_attention(const void *Q, const void *K_cache, const void *V_cache, void *A,
+                               const int32_t *idx, const int32_t *count, int k_max, int B, int N,
+                               int n_q, int n_kv, int hd, int dtype, void *ws, size_t ws_bytes,
+                               void *stream) {
+    CHECK_ARG(Q && K_cache && V_cache && A && idx && count, "null pointer");
+    CHECK_ARG(B > 0 && N > 0 && n_q > 0 && n_kv > 0, "sizes must be positive");
+    CHECK_ARG(k_max > 0 && k_max <= N, "k_max must be in [1, N]");
+    CHECK_ARG(n_q % n_kv == 0, "n_q must be a multiple of n_kv");
+    CHECK_ARG(dtype == DLLM_BF16 || dtype == DLLM_F32, "dtype must be DLLM_BF16 or DLLM_F32");
+    if (hd != 64 && hd != 128) return fail(DLLM_ERR_UNSUPPORTED, "hd must be 64 or 128 (got %d)", hd);
+    CHECK_ARG(aligned16(Q) && aligned16(K_cache) && aligned16(V_cache) && aligned16(A),
+              "arrays must be 16-byte aligned");
+    const size_t need = dllm_attention_workspace_bytes(B, N, k_max, n_q, hd, dtype);
+    if (need > 0 && (!ws || ws_bytes < need))
+        return fail(DLLM_ERR_WORKSPACE, "workspace holds %zu bytes, %zu needed", ws_bytes, need);
+    SelRows sel{idx, count, k_max, N};
+    cudaStream_t st = as_stream(stream);
+    Launch t(DLLM_KERNEL_ATTENTION, st);
+    cudaError_t e;
+    if (dtype == DLLM_BF16) {
+        float *w = need ? reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255)) : nullptr;
+        e = attention_tc(static_cast<const bf16 *>(Q), static_cast<const bf16 *>(K_cache),
+                         static_cast<const bf16 *>(V_cache), static_cast<bf16 *>(A), sel, B, n_q, n_kv, hd,
+                         w, status_ptr(), st);
+    } else {
+        e = attention_simt(static_cast<const float *>(Q), static_cast<const float *>(K_cache),
+                           static_cast<const float *>(V_cache), static_cast<float *>(A), sel, B, n_q, n_kv,
+                           hd, st);
+    }
+    CHECK_CUDA(e, "attention launch");
+    return DLLM_OK;
+}
+
 // ------------------------------------------------------------------ embedding, final norm
 DLLM_EXPORT int dllm_embed(const void *E, const int32_t *tokens, const int32_t *rows, int R, void *H,
                            int B, int N, int d, int V, int dtype, void *stream) {

@@ -104,29 +104,44 @@ __global__ void __launch_bounds__(256) k_cosine_drift(const float *__restrict__ 
     if (row >= rows) return;
     float *a = cur + row * r;
     const float *c = cached + row * r;
-    if (nparts > 1) {
-        // all partial loads of a batch are issued before the first add (slice order kept)
-        const size_t stride = (size_t)rows * r;
-#pragma unroll 4
-        for (int e = lane; e < r; e += 32) {
-            const float *p = parts + row * r + e;
-            float x = 0.f;
-            int z = 0;
-            for (; z + 8 <= nparts; z += 8) {
-                float t[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) t[u] = __ldcg(p + (size_t)(z + u) * stride);
-#pragma unroll
-                for (int u = 0; u < 8; ++u) x += t[u];
-            }
-            for (; z < nparts; ++z) x += __ldcg(p + (size_t)z * stride);
-            a[e] = x;
-        }
-    }
+    // float4 chunks (r % 32 == 0); for each chunk every partial load is issued before
+    // the first add, and the adds run in slice order
+    const int nch = r >> 2;
+    const size_t stride4 = (size_t)rows * nch;
+    const float4 *p4 = reinterpret_cast<const float4 *>(parts) + (size_t)row * nch;
+    float4 *a4 = reinterpret_cast<float4 *>(a);
+    const float4 *c4 = reinterpret_cast<const float4 *>(c);
     float na = 0.f, nc = 0.f;
-    for (int e = lane; e < r; e += 32) {
-        na = fmaf(a[e], a[e], na);
-        nc = fmaf(c[e], c[e], nc);
+    for (int ch = lane; ch < nch; ch += 32) {
+        float4 x;
+        const float4 cc = c4[ch];
+        if (nparts > 1) {
+            float4 t[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (u < nparts) t[u] = __ldcg(p4 + (size_t)u * stride4 + ch);
+            x = t[0];
+#pragma unroll
+            for (int u = 1; u < 8; ++u)
+                if (u < nparts) {
+                    x.x += t[u].x;
+                    x.y += t[u].y;
+                    x.z += t[u].z;
+                    x.w += t[u].w;
+                }
+            for (int z = 8; z < nparts; ++z) {
+                const float4 y = __ldcg(p4 + (size_t)z * stride4 + ch);
+                x.x += y.x;
+                x.y += y.y;
+                x.z += y.z;
+                x.w += y.w;
+            }
+            a4[ch] = x;
+        } else {
+            x = a4[ch];
+        }
+        na = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, na))));
+        nc = fmaf(cc.x, cc.x, fmaf(cc.y, cc.y, fmaf(cc.z, cc.z, fmaf(cc.w, cc.w, nc))));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -141,10 +156,14 @@ __global__ void __launch_bounds__(256) k_cosine_drift(const float *__restrict__ 
     } else {
         const float ia = 1.0f / sqrtf(na), ic = 1.0f / sqrtf(nc);
         float s = 0.f;
-        for (int e = lane; e < r; e += 32) {
+        for (int ch = lane; ch < nch; ch += 32) {   // the chunks this lane summed above
+            const float4 x = a4[ch], cc = c4[ch];
             // separately rounded products (no FMA contraction): equal inputs give t == 0
-            const float t = __fsub_rn(__fmul_rn(a[e], ia), __fmul_rn(c[e], ic));
-            s = fmaf(t, t, s);
+            const float t0 = __fsub_rn(__fmul_rn(x.x, ia), __fmul_rn(cc.x, ic));
+            const float t1 = __fsub_rn(__fmul_rn(x.y, ia), __fmul_rn(cc.y, ic));
+            const float t2 = __fsub_rn(__fmul_rn(x.z, ia), __fmul_rn(cc.z, ic));
+            const float t3 = __fsub_rn(__fmul_rn(x.w, ia), __fmul_rn(cc.w, ic));
+            s = fmaf(t0, t0, fmaf(t1, t1, fmaf(t2, t2, fmaf(t3, t3, s))));
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);

@@ -2,7 +2,7 @@
 // identification via singular proxy" and "2. Adaptive budget allocation") united
 // with the always-recomputed rows (EntropyCache, "How EntropyCache works", step 3).
 //
-// One CTA of 1024 threads per sequence, keys in shared memory.  The k-th largest
+// One CTA per sequence (256 threads up to N = 4096, 1024 above), keys in shared memory.  The k-th largest
 // drift is found exactly by a 4-pass radix select on order-preserving 32-bit keys
 // (256-bin shared histograms); rows above it are taken, rows equal to it are taken
 // in index order until the budget is met (lower row index wins ties), and the union
@@ -12,12 +12,14 @@
 namespace dllm {
 namespace {
 
-constexpr int kT = 1024;
+constexpr int kTMax = 1024;
 constexpr int kMaxN = 16384;
 
 // Exclusive block scan of one value per thread; returns the exclusive prefix and
 // writes the block total to *total.  All threads must call it.
+template <int kT>
 __device__ uint32_t block_scan(uint32_t v, uint32_t *wsum, uint32_t *total) {
+    constexpr int kWarps = kT / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint32_t x = v;
 #pragma unroll
@@ -28,7 +30,7 @@ __device__ uint32_t block_scan(uint32_t v, uint32_t *wsum, uint32_t *total) {
     if (lane == 31) wsum[warp] = x;
     __syncthreads();
     if (warp == 0) {
-        uint32_t w = wsum[lane];
+        uint32_t w = lane < kWarps ? wsum[lane] : 0u;
         uint32_t s = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -45,6 +47,7 @@ __device__ uint32_t block_scan(uint32_t v, uint32_t *wsum, uint32_t *total) {
     return r;
 }
 
+template <int kT>
 __global__ void __launch_bounds__(kT) k_select_topk(const float *__restrict__ drift,
                                                     const int32_t *__restrict__ forced, int F, int k,
                                                     float min_drift, int32_t *__restrict__ idx,
@@ -87,7 +90,7 @@ __global__ void __launch_bounds__(kT) k_select_topk(const float *__restrict__ dr
         key[i] = kk;
     }
     uint32_t tot_fe;   // both counts in one scan (N <= 16384 < 2^16)
-    block_scan((nf << 16) | ne, wsum, &tot_fe);
+    block_scan<kT>((nf << 16) | ne, wsum, &tot_fe);
     const uint32_t tot_f = tot_fe >> 16, tot_e = tot_fe & 0xFFFFu;
     long long budget = (long long)N - tot_f;
     if ((long long)k < budget) budget = k;
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(kT) k_select_topk(const float *__restrict__ dr
     if (rem > 0)
         for (int i = i0; i < i1; ++i) neq += (key[i] == T);
     uint32_t tot_eq;
-    uint32_t eq_before = block_scan(neq, wsum, &tot_eq);
+    uint32_t eq_before = block_scan<kT>(neq, wsum, &tot_eq);
     uint32_t nsel = 0;
     for (int i = i0; i < i1; ++i) {
         const uint32_t kk = key[i];
@@ -176,7 +179,7 @@ __global__ void __launch_bounds__(kT) k_select_topk(const float *__restrict__ dr
         nsel += s;
     }
     uint32_t total;
-    uint32_t out = block_scan(nsel, wsum, &total);
+    uint32_t out = block_scan<kT>(nsel, wsum, &total);
     int32_t *row = idx + (size_t)b * N;
     for (int i = i0; i < i1; ++i)
         if (flag[i] == 2) row[out++] = i;
@@ -191,11 +194,19 @@ cudaError_t select_topk(const float *drift, const int32_t *forced, int F, int k,
     if (B <= 0 || N <= 0) return cudaSuccess;
     if (N > kMaxN) return cudaErrorInvalidValue;
     const size_t smem = (size_t)N * 5;
-    cudaError_t e = cudaFuncSetAttribute(k_select_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    // fewer threads (cheaper block barriers) while each still handles <= 16 rows
+    if (N <= 4096) {
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(k_select_topk<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+        }
+        return launch_kernel(k_select_topk<256>, dim3(B), dim3(256), smem, st, 1, drift, forced, F, k,
+                             min_drift, idx, count, N);
+    }
+    cudaError_t e = cudaFuncSetAttribute(k_select_topk<kTMax>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_kernel(k_select_topk, dim3(B), dim3(kT), smem, st, 1, drift, forced, F, k, min_drift, idx, count, N);
-    return cudaGetLastError();
+    return launch_kernel(k_select_topk<kTMax>, dim3(B), dim3(kTMax), smem, st, 1, drift, forced, F, k,
+                         min_drift, idx, count, N);
 }
 
 }  // namespace dllm

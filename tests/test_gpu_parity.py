@@ -246,3 +246,68 @@ def test_gemm_bf16_parity(B, orc, M, N_out, K, splits):
     out = B.dllm_gemm_bf16(to_dev(X, torch.bfloat16), to_dev(W, torch.bfloat16), splits=splits)
     ref, _ = orc.proxy_score(X[None], np.ascontiguousarray(W.T), np.ones((1, M, N_out), np.float32))
     assert normwise_rel(to_np(out), ref[0]) < FP32_REDUCTION_RTOL
+
+
+def _sampled_layer_parity(B, orc, sh, seed, n_sample=8):
+    c = layer_case(orc, sh, seed, consistent=False, svd_proxy=False)
+    k = orc.budget(sh.rho, sh.N)
+    H = to_dev(c.H_cur, torch.bfloat16)
+    _, drift = B.dllm_proxy_score(H, to_dev(c.P.T.copy(), torch.bfloat16), to_dev(c.pc0))
+    idx, cnt = B.dllm_select_topk(drift, None, k)
+    mask = np.zeros((sh.B, sh.N), np.uint8)
+    for b in range(sh.B):
+        I = to_np(idx)[b, :to_np(cnt)[b]]
+        mask[b, I[synth.rng(seed + b).permutation(len(I))[:n_sample]]] = 1
+    g, o = _step(B, orc, c, k, None, out_mask=mask)
+    _compare_step(c, g, o, None, k, out_mask=mask)
+    for b in range(sh.B):
+        assert set(c.hot[b].tolist()) <= set(g["idx"][b, :g["cnt"][b]].tolist())
+
+
+def test_refresh_dream_layer_sampled(B, orc):
+    """Dream-7B-shaped (Qwen2.5-7B layout) layer: d=3584, 28 query / 4 KV heads x 128
+    (GQA group 7), F=18944, r=128, 16% of N=2048 -> k=328 per sequence; batch 2
+    (the configuration's batch 8 changes only the number of independent sequences)."""
+    sh = dataclasses.replace(synth.DREAM_STACK, name="dream7b-layer-b2", B=2, layers=1, V=0)
+    _sampled_layer_parity(B, orc, sh, 70)
+
+
+def test_refresh_long_context_point(B, orc):
+    """Long-context sweep point: LLaDA-8B-shaped layer at N=8192 with a 5% update ratio."""
+    sh = dataclasses.replace(synth.LLADA_LAYER, name="llada8b-N8192-rho0.05", N=8192, rho=0.05,
+                             prompt=4096)
+    _sampled_layer_parity(B, orc, sh, 71, n_sample=6)
+
+
+# --------------------------------------------------------------------------- attention alone
+@pytest.mark.parametrize("Bq,N,k_max,n_q,n_kv,hd,live", [
+    (1, 1024, 164, 32, 32, 128, 164), (2, 333, 150, 4, 2, 64, 150), (1, 2048, 328, 28, 4, 128, 300),
+    (3, 200, 37, 8, 8, 128, 37), (1, 129, 129, 2, 1, 64, 100)])
+def test_attention_parity(B, orc, Bq, N, k_max, n_q, n_kv, hd, live):
+    """Selected queries over the whole cache, non-causal, GQA, ragged key tiles and
+    partially live query tiles, against the oracle's attention of every live row."""
+    g = synth.rng(400 + N + k_max)
+    dq, dkv = n_q * hd, n_kv * hd
+    Q = synth.round_bf16(g.standard_normal((Bq * k_max, dq), dtype=np.float32))
+    K = synth.round_bf16(g.standard_normal((Bq, N, dkv), dtype=np.float32))
+    V = synth.round_bf16(g.standard_normal((Bq, N, dkv), dtype=np.float32))
+    idx = np.full((Bq, N), -1, np.int32)
+    cnt = np.zeros(Bq, np.int32)
+    for b in range(Bq):
+        nb = max(1, live - 3 * b)
+        idx[b, :nb] = np.sort(g.permutation(N)[:nb])
+        cnt[b] = nb
+    A = B.dllm_attention(to_dev(Q, torch.bfloat16), to_dev(K.reshape(Bq, N, n_kv, hd), torch.bfloat16),
+                         to_dev(V.reshape(Bq, N, n_kv, hd), torch.bfloat16), to_dev(idx), to_dev(cnt), k_max)
+    A = to_np(A)
+    L = orc.Layer({"w_q": np.zeros((dq, dq), np.float32), "w_k": np.zeros((dkv, dq), np.float32),
+                   "w_v": np.zeros((dkv, dq), np.float32), "w_o": np.zeros((dq, dq), np.float32),
+                   "w_g": np.zeros((32, dq), np.float32), "w_u": np.zeros((32, dq), np.float32),
+                   "w_d": np.zeros((dq, 32), np.float32), "gamma1": np.ones(dq, np.float32),
+                   "gamma2": np.ones(dq, np.float32)}, n_q, n_kv, hd)
+    for b in range(Bq):
+        rows = np.arange(b * k_max, b * k_max + cnt[b])
+        ref = orc.attention_rows(L, Q[rows], K[b], V[b])
+        assert_close_layer(A[rows], ref, "bf16", f"attention b={b}")
+        dead = np.arange(b * k_max + cnt[b], (b + 1) * k_max)
+        assert (A[dead] == 0).all()
