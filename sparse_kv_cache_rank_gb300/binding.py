@@ -63,7 +63,7 @@ _SIGS = {
     "dllm_gemm_bf16": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                  C.c_int, C.c_void_p]),
     "dllm_attention_workspace_bytes": (C.c_size_t, [C.c_int] * 6),
-    "dllm_attention": (C.c_int, [C.c_void_p] * 6 + [C.c_int] * 8 + [C.c_void_p, C.c_size_t, C.c_void_p]),
+    "dllm_attention": (C.c_int, [C.c_void_p] * 6 + [C.c_int] * 7 + [C.c_void_p, C.c_size_t, C.c_void_p]),
     "dllm_embed": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_void_p] + [C.c_int] * 5
                    + [C.c_void_p]),
     "dllm_rows_rmsnorm": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_void_p, C.c_float, C.c_void_p]
