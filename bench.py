@@ -47,6 +47,10 @@ def parse():
                     help="skip the 32-layer LLaDA-8B-shaped stack measurement")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="approximate budget of the CPU-oracle sample")
+    ap.add_argument("--profile-step", action="store_true",
+                    help="profiling mode: set up the layer workload, warm up, then run ONE layer "
+                         "step inside a cudaProfilerStart/Stop range (for ncu --profile-from-start off); "
+                         "prints a short JSON line, no measurement")
     return ap.parse_args()
 
 
@@ -489,9 +493,30 @@ def reference(args):
     }), flush=True)
 
 
+def profile_step(args):
+    """One warmed-up layer step inside a profiler range: the launches an external
+    profiler captures are exactly those of one timed bench step."""
+    import torch
+    from sparse_kv_cache_rank_gb300 import binding as B
+    from sparse_kv_cache_rank_gb300 import synth
+    dev = torch.device("cuda", 0)
+    wl = LayerWorkload(synth.LLADA_LAYER, 1234, dev)
+    for _ in range(max(args.warmup, 3)):
+        wl.step()
+    torch.cuda.synchronize(dev)
+    torch.cuda.profiler.start()
+    wl.step()
+    torch.cuda.synchronize(dev)
+    torch.cuda.profiler.stop()
+    B.check_status()
+    print(json.dumps({"profile_step": "llada8b-layer", "rows": int(wl.cnt.sum())}), flush=True)
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.profile_step:
+        profile_step(args)
+    elif args.impl == "reference":
         reference(args)
     else:
         native(args)

@@ -390,8 +390,13 @@ int refresh_impl(const dllm_layer *W, const T *H_in, SelRows sel, int B, T *K_ca
     // a3: gather + RMSNorm, proxy cache update
     {
         Launch t(DLLM_KERNEL_GATHER, st);
+        int *zero_ptr = nullptr;
+        int zero_n = 0;
+        if (sizeof(T) == 2)
+            attention_tc_counters(reinterpret_cast<float *>(ws + L.attn), B, sel.k_max, W->n_q, W->hd,
+                                  sel.N, &zero_ptr, &zero_n);
         CHECK_CUDA(gather_rmsnorm<T>(H_in, sel, B, d, g1, W->eps, Xn, proxy_cache, proxy_cur, r,
-                                     W->rope_inv_freq, W->hd / 2, rope_cs, status, st),
+                                     W->rope_inv_freq, W->hd / 2, rope_cs, zero_ptr, zero_n, status, st),
                    "gather launch");
     }
     // a4: QKV projection, rotary embedding, K/V scattered into the cache
@@ -407,7 +412,8 @@ int refresh_impl(const dllm_layer *W, const T *H_in, SelRows sel, int B, T *K_ca
             Launch t(DLLM_KERNEL_ATTENTION, st, na);
             CHECK_CUDA(attention_tc(reinterpret_cast<const bf16 *>(Qc), reinterpret_cast<const bf16 *>(K_cache),
                                     reinterpret_cast<const bf16 *>(V_cache), reinterpret_cast<bf16 *>(Ac), sel, B,
-                                    W->n_q, W->n_kv, W->hd, reinterpret_cast<float *>(ws + L.attn), status, st),
+                                    W->n_q, W->n_kv, W->hd, reinterpret_cast<float *>(ws + L.attn), true,
+                                    status, st),
                        "attention");
         }
         { Launch t(DLLM_KERNEL_OPROJ, st); CHECK_CUDA(gemm_tc(wo, d, dq, Ac, M, er, 0, true, status, st), "o gemm"); }
@@ -489,7 +495,7 @@ DLLM_EXPORT int dllm_attention(const void *Q, const void *K_cache, const void *V
         float *w = need ? reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255)) : nullptr;
         e = attention_tc(static_cast<const bf16 *>(Q), static_cast<const bf16 *>(K_cache),
                          static_cast<const bf16 *>(V_cache), static_cast<bf16 *>(A), sel, B, n_q, n_kv, hd,
-                         w, status_ptr(), st);
+                         w, false, status_ptr(), st);
     } else {
         e = attention_simt(static_cast<const float *>(Q), static_cast<const float *>(K_cache),
                            static_cast<const float *>(V_cache), static_cast<float *>(A), sel, B, n_q, n_kv,

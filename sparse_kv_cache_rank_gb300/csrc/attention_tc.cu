@@ -391,7 +391,8 @@ size_t attention_tc_counter_offset(int B, int k_max, int n_q, int hd, int N) {
 }
 
 cudaError_t attention_tc(const bf16 *Q, const bf16 *Kc, const bf16 *Vc, bf16 *A, SelRows sel, int B,
-                         int n_q, int n_kv, int hd, float *ws, unsigned *status, cudaStream_t st) {
+                         int n_q, int n_kv, int hd, float *ws, bool counters_zeroed, unsigned *status,
+                         cudaStream_t st) {
     const int M = B * sel.k_max;
     if (M <= 0) return cudaSuccess;
     if (hd != 64 && hd != 128) return cudaErrorInvalidValue;
@@ -421,22 +422,32 @@ cudaError_t attention_tc(const bf16 *Q, const bf16 *Kc, const bf16 *Vc, bf16 *A,
     }
     dim3 grid(a.q_tiles, n_q, B * a.splits);
     cudaError_t e;
-    if (a.splits > 1) {   // merge counters start at zero (the merging CTA resets its own)
+    if (a.splits > 1 && !counters_zeroed) {   // merge counters start at zero
         e = cudaMemsetAsync(a.counters, 0, (size_t)B * a.q_tiles * n_q * sizeof(int), st);
         if (e != cudaSuccess) return e;
     }
-    if (hd == 128) {
-        const size_t sm = attn_smem<128>();
-        e = cudaFuncSetAttribute(k_attention_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    static bool configured[2][64] = {};   // per head size and device: raise the smem limit once
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int hv = hd == 128 ? 1 : 0;
+    if (dev < 0 || dev >= 64 || !configured[hv][dev]) {
+        e = hv ? cudaFuncSetAttribute(k_attention_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem<128>())
+               : cudaFuncSetAttribute(k_attention_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem<64>());
         if (e != cudaSuccess) return e;
-        e = launch_kernel(k_attention_tc<128>, grid, dim3(kThreads), sm, st, 1, tq, tk, tv, a, status);
-    } else {
-        const size_t sm = attn_smem<64>();
-        e = cudaFuncSetAttribute(k_attention_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        if (e != cudaSuccess) return e;
-        e = launch_kernel(k_attention_tc<64>, grid, dim3(kThreads), sm, st, 1, tq, tk, tv, a, status);
+        if (dev >= 0 && dev < 64) configured[hv][dev] = true;
     }
-    return cudaGetLastError();
+    if (hv)
+        return launch_kernel(k_attention_tc<128>, grid, dim3(kThreads), attn_smem<128>(), st, 1, tq, tk, tv, a, status);
+    return launch_kernel(k_attention_tc<64>, grid, dim3(kThreads), attn_smem<64>(), st, 1, tq, tk, tv, a, status);
+}
+
+void attention_tc_counters(float *ws, int B, int k_max, int n_q, int hd, int N, int **ptr, int *n) {
+    *ptr = nullptr;
+    *n = 0;
+    if (!ws || attention_tc_splits(B, k_max, n_q, N) <= 1) return;
+    *ptr = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(ws) +
+                                   attention_tc_counter_offset(B, k_max, n_q, hd, N));
+    *n = B * ((k_max + AQ - 1) / AQ) * n_q;
 }
 
 }  // namespace dllm

@@ -263,16 +263,45 @@ PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 }  // namespace
 
 // Row-major bf16 matrix [rows, cols], boxes of 64 columns x box_rows rows, 128-byte swizzle.
+// Encoded maps are cached per host thread (a step re-encodes the same few operands
+// every call; the descriptor depends only on these four values and the device).
 bool make_tmap(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    struct Entry {
+        const void *base;
+        uint64_t rows, cols;
+        uint32_t box_rows;
+        int dev;
+        CUtensorMap map;
+    };
+    constexpr int kSlots = 64;
+    thread_local Entry cache[kSlots] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t h = (reinterpret_cast<uint64_t>(base) >> 8) ^ (rows * 0x9E3779B97F4A7C15ull) ^
+                       (cols << 7) ^ ((uint64_t)box_rows << 3) ^ (uint64_t)dev;
+    Entry &e = cache[(h ^ (h >> 29)) % kSlots];
+    if (e.base == base && e.rows == rows && e.cols == cols && e.box_rows == box_rows && e.dev == dev &&
+        base != nullptr) {
+        *tm = e.map;
+        return true;
+    }
     auto enc = tmap_encoder();
     if (!enc) return false;
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * 2};
     cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    if (enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    e.base = base;
+    e.rows = rows;
+    e.cols = cols;
+    e.box_rows = box_rows;
+    e.dev = dev;
+    e.map = *tm;
+    return true;
 }
 
 namespace {
