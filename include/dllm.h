@@ -218,6 +218,8 @@ int dllm_commit_entropy(const float *logits, const uint8_t *valid, int B, int M,
  * other rows of A get zeros.  Q and A [B*k_max, n_q*hd]; K_cache, V_cache [B, N, n_kv, hd];
  * idx [B, N], count [B] int32 as written by dllm_select_topk; dtype as the caches.
  * Requirements: hd in {64, 128}; k_max <= N.
+ * Workspace: dllm_attention_workspace_bytes() bytes (currently 0 for every shape: the
+ * key-range split is merged on chip); ws may then be NULL.
  * ------------------------------------------------------------------------- */
 size_t dllm_attention_workspace_bytes(int B, int N, int k_max, int n_q, int hd, int dtype);
 

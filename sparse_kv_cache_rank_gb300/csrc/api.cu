@@ -129,7 +129,7 @@ PackLayout pack_layout(int d, int n_q, int n_kv, int hd, int F, int dtype) {
 }
 
 struct RefreshWs {
-    size_t xn, q, a, h1, xn2, u, rope, attn, total;
+    size_t xn, q, a, h1, xn2, u, rope, total;
 };
 
 RefreshWs refresh_ws(const dllm_layer *W, int B, int N, int k_max) {
@@ -151,8 +151,7 @@ RefreshWs refresh_ws(const dllm_layer *W, int B, int N, int k_max) {
     off = align256(off + M * W->F * el);
     r.rope = off;
     off = align256(off + M * (size_t)(W->hd / 2) * sizeof(float2));
-    r.attn = off;
-    if (W->dtype == DLLM_BF16) off = align256(off + attention_tc_ws_bytes(B, k_max, W->n_q, W->hd, N));
+    (void)N;
     r.total = off + 256;   // room to align the caller's base
     return r;
 }
@@ -390,13 +389,8 @@ int refresh_impl(const dllm_layer *W, const T *H_in, SelRows sel, int B, T *K_ca
     // a3: gather + RMSNorm, proxy cache update
     {
         Launch t(DLLM_KERNEL_GATHER, st);
-        int *zero_ptr = nullptr;
-        int zero_n = 0;
-        if (sizeof(T) == 2)
-            attention_tc_counters(reinterpret_cast<float *>(ws + L.attn), B, sel.k_max, W->n_q, W->hd,
-                                  sel.N, &zero_ptr, &zero_n);
         CHECK_CUDA(gather_rmsnorm<T>(H_in, sel, B, d, g1, W->eps, Xn, proxy_cache, proxy_cur, r,
-                                     W->rope_inv_freq, W->hd / 2, rope_cs, zero_ptr, zero_n, status, st),
+                                     W->rope_inv_freq, W->hd / 2, rope_cs, status, st),
                    "gather launch");
     }
     // a4: QKV projection, rotary embedding, K/V scattered into the cache
@@ -412,8 +406,7 @@ int refresh_impl(const dllm_layer *W, const T *H_in, SelRows sel, int B, T *K_ca
             Launch t(DLLM_KERNEL_ATTENTION, st, na);
             CHECK_CUDA(attention_tc(reinterpret_cast<const bf16 *>(Qc), reinterpret_cast<const bf16 *>(K_cache),
                                     reinterpret_cast<const bf16 *>(V_cache), reinterpret_cast<bf16 *>(Ac), sel, B,
-                                    W->n_q, W->n_kv, W->hd, reinterpret_cast<float *>(ws + L.attn), true,
-                                    status, st),
+                                    W->n_q, W->n_kv, W->hd, status, st),
                        "attention");
         }
         { Launch t(DLLM_KERNEL_OPROJ, st); CHECK_CUDA(gemm_tc(wo, d, dq, Ac, M, er, 0, true, status, st), "o gemm"); }
@@ -468,8 +461,8 @@ DLLM_EXPORT int dllm_sparse_layer_refresh(const dllm_layer *W, const void *H_in,
 
 // ------------------------------------------------------------------ attention alone
 DLLM_EXPORT size_t dllm_attention_workspace_bytes(int B, int N, int k_max, int n_q, int hd, int dtype) {
-    if (B <= 0 || N <= 0 || k_max <= 0 || n_q <= 0 || dtype != DLLM_BF16) return 0;
-    return attention_tc_ws_bytes(B, k_max, n_q, hd, N) + 256;
+    (void)B; (void)N; (void)k_max; (void)n_q; (void)hd; (void)dtype;
+    return 0;   // the key-range split is merged on chip
 }
 
 DLLM_EXPORT int dllm_attention(const void *Q, const void *K_cache, const void *V_cache, void *A,
@@ -492,10 +485,9 @@ DLLM_EXPORT int dllm_attention(const void *Q, const void *K_cache, const void *V
     Launch t(DLLM_KERNEL_ATTENTION, st);
     cudaError_t e;
     if (dtype == DLLM_BF16) {
-        float *w = need ? reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255)) : nullptr;
         e = attention_tc(static_cast<const bf16 *>(Q), static_cast<const bf16 *>(K_cache),
                          static_cast<const bf16 *>(V_cache), static_cast<bf16 *>(A), sel, B, n_q, n_kv, hd,
-                         w, false, status_ptr(), st);
+                         status_ptr(), st);
     } else {
         e = attention_simt(static_cast<const float *>(Q), static_cast<const float *>(K_cache),
                            static_cast<const float *>(V_cache), static_cast<float *>(A), sel, B, n_q, n_kv,

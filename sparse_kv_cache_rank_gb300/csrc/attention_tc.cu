@@ -11,9 +11,9 @@
 //   O  = O * corr + PV  in registers (streaming softmax)
 // K and V tiles are double-buffered by TMA; S is double-buffered in TMEM so the next
 // tile's Q K^T runs while the softmax of the current one is computed.  Keys beyond N
-// are masked.  With several key slices every CTA writes (O, m, l) to the workspace and
-// the last CTA of a (rows, head) tile to finish merges them (global counter; no second
-// launch and no waiting on other CTAs).
+// are masked.  With several key slices, the slices of one (rows, head) tile run as a
+// thread-block cluster: each keeps its (O, m, l) in shared memory and the CTAs merge
+// disjoint row ranges through distributed shared memory (no workspace, no second launch).
 //
 // Roles (320 threads): warp 0 TMA, warp 1 TMEM owner + MMA issuer, warps 2..9 softmax:
 // two warps per TMEM lane quarter, thread = (query row, half of the key / head columns).
@@ -39,9 +39,6 @@ struct AttnArgs {
     int kv_tiles, splits, q_tiles;
     float scale_log2;                 // log2(e) / sqrt(hd)
     bf16 *A;                          // [B*k_max, n_q*hd]
-    float *part_o;                    // [splits][B*k_max][n_q*hd]   (splits > 1)
-    float *part_ml;                   // [splits][B*k_max][n_q][2]
-    int *counters;                    // [B * q_tiles * n_q], zero between launches
 };
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -77,7 +74,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *pv_full = bars + 12;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    volatile int *last_flag = reinterpret_cast<volatile int *>(tmem_slot + 2);
 
     griddep_wait();
     griddep_launch();
@@ -95,8 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nt = t1 - t0;
     const int dq = a.n_q * HD;
     const size_t row0 = (size_t)b * a.k_max + q0;   // flattened row of query 0
-    const size_t rows_all = (size_t)a.B * a.k_max;
-    if (live <= 0) {   // no live query: zero outputs (a.A), nothing to merge
+    if (live <= 0) {   // no live query (the same in every slice of the cluster): zero outputs
         if (split == 0 && warp >= 2) {
             const int r = (warp & 3) * 32 + lane, hf = (warp - 2) >> 2;
             if (q0 + r < a.k_max) {
@@ -128,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_slot, 512);
         tmem_relinquish();
     }
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -293,61 +289,79 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<__nv_bfloat162 *>(dst + e) = __floats2bfloat162_rn(o[e] * inv, o[e + 1] * inv);
             }
         } else {
-            if (row_ok) {
-                const size_t pm = (size_t)split * rows_all + row;
-                if (hf == 0) {
-                    a.part_ml[(pm * a.n_q + h) * 2 + 0] = (r < live && nt > 0) ? m_run : -INFINITY;
-                    a.part_ml[(pm * a.n_q + h) * 2 + 1] = (r < live && nt > 0) ? l_tot : 0.f;
-                }
-                float *po = a.part_o + pm * dq + (size_t)h * HD + hf * OH;
+            // this key slice's (O, m, l) into the CTA's own shared memory, over the Q tile
+            // and K ring: every copy into them has landed and every MMA reading them is done
+            float *sO = reinterpret_cast<float *>(smem);   // [128 rows][HD]
+            float *sML = sO + AQ * HD;                      // [128 rows][m, l]
+            float *po = sO + r * HD + hf * OH;
 #pragma unroll
-                for (int e = 0; e < OH; e += 4)
-                    *reinterpret_cast<float4 *>(po + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-            }
-            __threadfence();
-            named_bar_sync(1, kSoftThreads);
-            if (threadIdx.x == 64) {
-                int *ctr = a.counters + ((size_t)b * a.q_tiles + blockIdx.x) * a.n_q + h;
-                const int old = atomicAdd(ctr, 1);
-                const int last = old == a.splits - 1;
-                if (last) *ctr = 0;                    // ready for the next launch
-                *last_flag = last;
-            }
-            named_bar_sync(1, kSoftThreads);
-            if (*last_flag && row_ok) {                // merge every slice's (O, m, l)
-                __threadfence();
-                float M = -INFINITY;
-                for (int sp = 0; sp < a.splits; ++sp)
-                    M = fmaxf(M, __ldcg(&a.part_ml[(((size_t)sp * rows_all + row) * a.n_q + h) * 2]));
-                float acc[OH];
-#pragma unroll
-                for (int e = 0; e < OH; ++e) acc[e] = 0.f;
-                float den = 0.f;
-                if (M != -INFINITY) {
-                    for (int sp = 0; sp < a.splits; ++sp) {
-                        const size_t pm = (size_t)sp * rows_all + row;
-                        const float ms = __ldcg(&a.part_ml[(pm * a.n_q + h) * 2]);
-                        if (ms == -INFINITY) continue;
-                        const float w = exp2f(ms - M);
-                        den = fmaf(__ldcg(&a.part_ml[(pm * a.n_q + h) * 2 + 1]), w, den);
-                        const float *po = a.part_o + pm * dq + (size_t)h * HD + hf * OH;
-#pragma unroll
-                        for (int e = 0; e < OH; e += 4) {
-                            const float4 x = __ldcg(reinterpret_cast<const float4 *>(po + e));
-                            acc[e] = fmaf(x.x, w, acc[e]);
-                            acc[e + 1] = fmaf(x.y, w, acc[e + 1]);
-                            acc[e + 2] = fmaf(x.z, w, acc[e + 2]);
-                            acc[e + 3] = fmaf(x.w, w, acc[e + 3]);
-                        }
-                    }
-                }
-                const float inv = den > 0.f ? 1.0f / den : 0.f;
-                bf16 *dst = a.A + row * dq + (size_t)h * HD + hf * OH;
-#pragma unroll
-                for (int e = 0; e < OH; e += 2)
-                    *reinterpret_cast<__nv_bfloat162 *>(dst + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+            for (int e = 0; e < OH; e += 4)
+                *reinterpret_cast<float4 *>(po + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+            if (hf == 0) {
+                const bool has = r < live && nt > 0;
+                sML[2 * r] = has ? m_run : -INFINITY;
+                sML[2 * r + 1] = has ? l_tot : 0.f;
             }
         }
+    }
+    __syncwarp();
+    if (a.splits > 1) {
+        // The key slices of one (rows, head) tile are the CTAs of a cluster: CTA rank k
+        // merges rows [k*128/S, (k+1)*128/S) of every slice's partial through distributed
+        // shared memory.
+        cluster_sync_all();
+        if (warp >= 2) {
+            const int S = a.splits;
+            const int rk = (int)cluster_ctarank();
+            const int per = (AQ + S - 1) / S;
+            const int rb = rk * per, re = min(AQ, rb + per);
+            const int tid = threadIdx.x - 64;
+            float *wts = xmax;   // [per][S] slice weights 2^(m_s - M)   (per * S <= 256)
+            float *inv = xsum;   // [per]   1 / sum_s l_s 2^(m_s - M)
+            const uint32_t sO = smem_u32(smem);
+            const uint32_t sML = sO + (uint32_t)(AQ * HD * 4);
+            if (tid < re - rb) {
+                const int rr = rb + tid;
+                float M = -INFINITY;
+                for (int sp = 0; sp < S; ++sp)
+                    M = fmaxf(M, ld_dsmem_f32(mapa_shared(sML + (uint32_t)(8 * rr), (uint32_t)sp)));
+                float den = 0.f;
+                for (int sp = 0; sp < S; ++sp) {
+                    const uint32_t base = mapa_shared(sML + (uint32_t)(8 * rr), (uint32_t)sp);
+                    const float ms = ld_dsmem_f32(base);
+                    const float w = (M == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - M);
+                    den = fmaf(ld_dsmem_f32(base + 4), w, den);
+                    wts[tid * S + sp] = w;
+                }
+                inv[tid] = den > 0.f ? 1.0f / den : 0.f;
+            }
+            __syncwarp();
+            named_bar_sync(1, kSoftThreads);
+            constexpr int D4 = HD / 4;
+            for (int it = tid; it < (re - rb) * D4; it += kSoftThreads) {
+                const int lr = it / D4, d4 = it - lr * D4;
+                const int rr = rb + lr;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int sp = 0; sp < S; ++sp) {
+                    const float w = wts[lr * S + sp];
+                    if (w == 0.f) continue;
+                    const float4 v = ld_dsmem_f32x4(mapa_shared(sO + (uint32_t)((rr * HD + d4 * 4) * 4), (uint32_t)sp));
+                    acc.x = fmaf(v.x, w, acc.x);
+                    acc.y = fmaf(v.y, w, acc.y);
+                    acc.z = fmaf(v.z, w, acc.z);
+                    acc.w = fmaf(v.w, w, acc.w);
+                }
+                if (q0 + rr < a.k_max) {
+                    const float iv = inv[lr];
+                    __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(
+                        a.A + (row0 + rr) * dq + (size_t)h * HD + d4 * 4);
+                    dst[0] = __floats2bfloat162_rn(acc.x * iv, acc.y * iv);
+                    dst[1] = __floats2bfloat162_rn(acc.z * iv, acc.w * iv);
+                }
+            }
+        }
+        __syncwarp();
+        cluster_sync_all();   // peers may still read this CTA's partial
     }
     tc_fence_before();
     __syncthreads();
@@ -369,30 +383,15 @@ int attention_tc_splits(int B, int k_max, int n_q, int N) {
     const long long base = (long long)qt * n_q * B;
     const int kv_tiles = (N + AKV - 1) / AKV;
     // one CTA per SM (the ring and TMEM need the whole SM): as many key slices as keep
-    // the grid within a single wave
+    // the grid within a single wave; the slices of a tile form a cluster (at most 8)
     int s = (int)(num_sms() / base);
     if (s > kv_tiles) s = kv_tiles;
-    if (s > 16) s = 16;
+    if (s > 8) s = 8;
     return s < 1 ? 1 : s;
 }
 
-size_t attention_tc_ws_bytes(int B, int k_max, int n_q, int hd, int N) {
-    const int s = attention_tc_splits(B, k_max, n_q, N);
-    if (s <= 1) return 0;
-    const size_t rows = (size_t)B * k_max;
-    const size_t qt = (size_t)(k_max + AQ - 1) / AQ;
-    return (size_t)s * rows * n_q * hd * 4 + (size_t)s * rows * n_q * 2 * 4 + B * qt * n_q * 4 + 1024;
-}
-
-size_t attention_tc_counter_offset(int B, int k_max, int n_q, int hd, int N) {
-    const int s = attention_tc_splits(B, k_max, n_q, N);
-    const size_t rows = (size_t)B * k_max;
-    return ((size_t)s * rows * n_q * hd * 4 + (size_t)s * rows * n_q * 2 * 4 + 255) & ~size_t(255);
-}
-
 cudaError_t attention_tc(const bf16 *Q, const bf16 *Kc, const bf16 *Vc, bf16 *A, SelRows sel, int B,
-                         int n_q, int n_kv, int hd, float *ws, bool counters_zeroed, unsigned *status,
-                         cudaStream_t st) {
+                         int n_q, int n_kv, int hd, unsigned *status, cudaStream_t st) {
     const int M = B * sel.k_max;
     if (M <= 0) return cudaSuccess;
     if (hd != 64 && hd != 128) return cudaErrorInvalidValue;
@@ -414,40 +413,22 @@ cudaError_t attention_tc(const bf16 *Q, const bf16 *Kc, const bf16 *Vc, bf16 *A,
     a.q_tiles = (sel.k_max + AQ - 1) / AQ;
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
     a.A = A;
-    if (a.splits > 1) {
-        a.part_o = ws;
-        a.part_ml = ws + (size_t)a.splits * M * dq;
-        a.counters = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(ws) +
-                                             attention_tc_counter_offset(B, sel.k_max, n_q, hd, sel.N));
-    }
     dim3 grid(a.q_tiles, n_q, B * a.splits);
-    cudaError_t e;
-    if (a.splits > 1 && !counters_zeroed) {   // merge counters start at zero
-        e = cudaMemsetAsync(a.counters, 0, (size_t)B * a.q_tiles * n_q * sizeof(int), st);
-        if (e != cudaSuccess) return e;
-    }
     static bool configured[2][64] = {};   // per head size and device: raise the smem limit once
     int dev = 0;
     cudaGetDevice(&dev);
     const int hv = hd == 128 ? 1 : 0;
     if (dev < 0 || dev >= 64 || !configured[hv][dev]) {
-        e = hv ? cudaFuncSetAttribute(k_attention_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem<128>())
-               : cudaFuncSetAttribute(k_attention_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem<64>());
+        cudaError_t e = hv ? cudaFuncSetAttribute(k_attention_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem<128>())
+                           : cudaFuncSetAttribute(k_attention_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem<64>());
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[hv][dev] = true;
     }
     if (hv)
-        return launch_kernel(k_attention_tc<128>, grid, dim3(kThreads), attn_smem<128>(), st, 1, tq, tk, tv, a, status);
-    return launch_kernel(k_attention_tc<64>, grid, dim3(kThreads), attn_smem<64>(), st, 1, tq, tk, tv, a, status);
-}
-
-void attention_tc_counters(float *ws, int B, int k_max, int n_q, int hd, int N, int **ptr, int *n) {
-    *ptr = nullptr;
-    *n = 0;
-    if (!ws || attention_tc_splits(B, k_max, n_q, N) <= 1) return;
-    *ptr = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(ws) +
-                                   attention_tc_counter_offset(B, k_max, n_q, hd, N));
-    *n = B * ((k_max + AQ - 1) / AQ) * n_q;
+        return launch_kernel(k_attention_tc<128>, grid, dim3(kThreads), attn_smem<128>(), st, a.splits, tq, tk,
+                             tv, a, status);
+    return launch_kernel(k_attention_tc<64>, grid, dim3(kThreads), attn_smem<64>(), st, a.splits, tq, tk, tv,
+                         a, status);
 }
 
 }  // namespace dllm

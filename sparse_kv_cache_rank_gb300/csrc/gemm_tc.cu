@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         tmem_alloc(tmem_slot, tmem_cols);
         tmem_relinquish();
     }
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -169,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             col_b[c] = b;
             col_pos[c] = pos;
         }
+        __syncwarp();
         named_bar_sync(1, kEpiWarps * 32);
         mbar_wait(done, 0, abort_flag, status);
         tc_fence_after();
@@ -202,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
         }
     }
+    __syncwarp();   // each warp converged before the block-wide / cluster-wide barrier
     tc_fence_before();
     if (cluster_split) {
         cluster_sync_all();
@@ -235,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
         }
+        __syncwarp();
         cluster_sync_all();   // peers may still read this CTA's partial tile
     } else {
         __syncthreads();

@@ -69,8 +69,7 @@ cudaError_t gemm_simt(const float *W, int N_out, int K, const float *X, int M_to
 template <class T>
 cudaError_t gather_rmsnorm(const T *H, SelRows sel, int B, int d, const T *gamma, float eps, T *Xn,
                            float *proxy_cache, const float *proxy_cur, int r, const float *inv_freq,
-                           int half_hd, float2 *rope_cs, int *zero_ptr, int zero_n, unsigned *status,
-                           cudaStream_t st);
+                           int half_hd, float2 *rope_cs, unsigned *status, cudaStream_t st);
 
 template <class T>
 cudaError_t rmsnorm_rows(const float *h1, int M, int d, const T *gamma, float eps, T *Xn2,
@@ -105,16 +104,11 @@ template <class T>
 cudaError_t attention_simt(const T *Q, const T *Kc, const T *Vc, T *A, SelRows sel, int B,
                            int n_q, int n_kv, int hd, cudaStream_t st);
 
-// Tensor cores (bf16, hd in {64, 128}); `ws` holds the split-KV partials
-// (attention_tc_ws_bytes, may be 0 when a single key slice is used).
+// Tensor cores (bf16, hd in {64, 128}); the key range is split over a cluster of up to
+// 8 CTAs (attention_tc_splits) merged through distributed shared memory: no workspace.
 int attention_tc_splits(int B, int k_max, int n_q, int N);
-size_t attention_tc_ws_bytes(int B, int k_max, int n_q, int hd, int N);
-// counters_zeroed: the split-merge counters inside ws (attention_tc_counters) were
-// zeroed by an earlier kernel on the stream; otherwise a memset runs first.
 cudaError_t attention_tc(const bf16 *Q, const bf16 *Kc, const bf16 *Vc, bf16 *A, SelRows sel, int B,
-                         int n_q, int n_kv, int hd, float *ws, bool counters_zeroed, unsigned *status,
-                         cudaStream_t st);
-void attention_tc_counters(float *ws, int B, int k_max, int n_q, int hd, int N, int **ptr, int *n);
+                         int n_q, int n_kv, int hd, unsigned *status, cudaStream_t st);
 
 // ---------------------------------------------------------------- selection
 cudaError_t select_topk(const float *drift, const int32_t *forced, int F, int k, float min_drift,

@@ -35,14 +35,11 @@ __global__ void __launch_bounds__(256) k_gather_rmsnorm(const T *__restrict__ H,
                                                         T *__restrict__ Xn, float *proxy_cache,
                                                         const float *proxy_cur, int r,
                                                         const float *inv_freq, int half_hd,
-                                                        float2 *rope_cs, int *zero_ptr, int zero_n,
-                                                        unsigned *status) {
+                                                        float2 *rope_cs, unsigned *status) {
     __shared__ float red[33];
     griddep_wait();
     griddep_launch();
     const int m = blockIdx.x;
-    if (m == 0)   // scratch counters of a later kernel of the step start at zero
-        for (int i = threadIdx.x; i < zero_n; i += 256) zero_ptr[i] = 0;
     int b, pos;
     sel.locate(m, b, pos);
     if (threadIdx.x == 0 && m % sel.k_max == 0 && sel.count[b] > sel.k_max)
@@ -204,12 +201,11 @@ __global__ void k_rope_inv_freq(float *dst, int hd, float theta) {
 template <class T>
 cudaError_t gather_rmsnorm(const T *H, SelRows sel, int B, int d, const T *gamma, float eps, T *Xn,
                            float *proxy_cache, const float *proxy_cur, int r, const float *inv_freq,
-                           int half_hd, float2 *rope_cs, int *zero_ptr, int zero_n, unsigned *status,
-                           cudaStream_t st) {
+                           int half_hd, float2 *rope_cs, unsigned *status, cudaStream_t st) {
     const int M = B * sel.k_max;
     if (M <= 0) return cudaSuccess;
     return launch_kernel(k_gather_rmsnorm<T>, dim3(M), dim3(256), 0, st, 1, H, sel, d, gamma, eps, Xn,
-                         proxy_cache, proxy_cur, r, inv_freq, half_hd, rope_cs, zero_ptr, zero_n, status);
+                         proxy_cache, proxy_cur, r, inv_freq, half_hd, rope_cs, status);
 }
 
 template <class T>
@@ -249,7 +245,7 @@ cudaError_t rope_inv_freq(float *dst, int hd, float theta, cudaStream_t st) {
 #define DLLM_ROWOPS(T)                                                                           \
     template cudaError_t gather_rmsnorm<T>(const T *, SelRows, int, int, const T *, float, T *,  \
                                            float *, const float *, int, const float *, int, float2 *,   \
-                                           int *, int, unsigned *, cudaStream_t);                       \
+                                           unsigned *, cudaStream_t);                                   \
     template cudaError_t rmsnorm_rows<T>(const float *, int, int, const T *, float, T *,         \
                                          cudaStream_t);                                          \
     template cudaError_t pack_rows_rope<T>(const T *, T *, int, int, int, cudaStream_t);         \

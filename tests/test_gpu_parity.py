@@ -236,10 +236,15 @@ def test_commit_no_valid_rows(B):
 # --------------------------------------------------------------------------- plain GEMM
 @pytest.mark.parametrize("M,N_out,K,splits", [(1, 32, 64, 0), (37, 96, 192, 0), (164, 512, 1024, 1),
                                               (164, 512, 1024, 4), (300, 384, 640, 0),
-                                              (513, 256, 2048, 8), (64, 4096, 4096, 0)])
+                                              (513, 256, 2048, 8), (64, 4096, 4096, 0),
+                                              (164, 384, 12288, 0), (256, 1024, 4096, 0),
+                                              (200, 2080, 1024, 0), (16, 128, 256, 0),
+                                              (96, 160 * 128 + 96, 256, 0)])
 def test_gemm_bf16_parity(B, orc, M, N_out, K, splits):
     """The engine under every projection: X W^T against the oracle's double-precision
-    projection (the proxy score computes exactly H . P), ragged M, K splits 1..8."""
+    projection (the proxy score computes exactly H . P), ragged M, K splits 1..8, long K
+    over few weight tiles (automatic cluster split), a ragged last weight tile (2080 rows),
+    tiny grids, and more weight tiles than SMs."""
     g = synth.rng(3000 + M + K)
     X = synth.round_bf16(g.standard_normal((M, K), dtype=np.float32))
     W = synth.round_bf16((g.standard_normal((N_out, K)) * 0.05).astype(np.float32))
