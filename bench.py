@@ -33,6 +33,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "sparse-refresh denoise steps/s & tokens/s (LLaDA-8B shape); % of roofline"
+# dram__bytes_read.sum + dram__bytes_write.sum per launch, LLaDA-8B layer at k = 164
+# (profiles/gemm_attention_llada8b_full.md); to be re-taken whenever these kernels change
+NCU_TRAFFIC_BYTES = {"gateup": 206.35e6, "qkv": 105.15e6, "down": 110.41e6, "attention": 18.19e6}
 UNIT = "steps/s"
 
 
@@ -299,7 +302,9 @@ def native(args):
     else:
         roof = {"bound": "hbm", "achieved": dom_bytes / dom_s / 1e9, "peak": bw, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    # DRAM bytes (read + write) per launch from the committed full ncu capture
+    # (profiles/gemm_attention_llada8b_full.md); None for a kernel not captured there
+    roof["traffic"] = NCU_TRAFFIC_BYTES.get(dominant)
     roof["kernel"] = dominant
     roof["peak_source"] = src
     step_roof_s = sum(max(b / (bw * 1e9), f / (tc * 1e12)) for b, f in work.values())

@@ -354,7 +354,9 @@ Plan plan_gemm(int M_tok, int N_out, int K, int splits_req) {
     if (splits_req > 0) {
         const int BN = M_tok <= 256 ? round16(M_tok) : 256;
         const int s = clamp_splits(splits_req);
-        return make_plan(M_tok, N_out, K, BN, s, s == 1 ? kSmemPair : kSmemLimit, s > 1);
+        // two CTAs per SM whenever the fp32 partial tile of a K split fits their share
+        const bool pair = s == 1 || BN * BM * 4 + 1024 + kTailBytes + kColBytes <= kSmemPair;
+        return make_plan(M_tok, N_out, K, BN, s, pair ? kSmemPair : kSmemLimit, s > 1);
     }
     if (M_tok <= 256) {
         if (2 * w_tiles >= sms) {
