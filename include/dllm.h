@@ -57,6 +57,8 @@ extern "C" {
 /* Device status bits (dllm_check_status). */
 #define DLLM_STATUS_TIMEOUT 1u     /* a kernel's bounded mbarrier wait ran out          */
 #define DLLM_STATUS_COUNT_CLAMP 2u /* count[b] > k_max: extra rows were ignored         */
+#define DLLM_STATUS_SMEM_LAYOUT 4u /* a GEMM found its shared memory misaligned and      */
+                                   /* skipped its work (outputs not written)             */
 
 /* Message of the last failed call on this thread ("" if none). */
 const char *dllm_last_error(void);
@@ -66,7 +68,8 @@ int dllm_version(void);
 
 /* Reads (and with reset != 0 clears) the device status word of the current device.
  * Synchronises the device.  Returns DLLM_ERR_TIMEOUT if the timeout bit is set,
- * DLLM_OK otherwise; *status_out (optional) receives all bits. */
+ * DLLM_ERR_CUDA if the shared-memory layout bit is set, DLLM_OK otherwise;
+ * *status_out (optional) receives all bits. */
 int dllm_check_status(unsigned *status_out, int reset);
 
 /* ---------------------------------------------------------------------------

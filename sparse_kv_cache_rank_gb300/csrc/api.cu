@@ -206,6 +206,8 @@ DLLM_EXPORT int dllm_check_status(unsigned *status_out, int reset) {
     }
     if (status_out) *status_out = v;
     if (v & DLLM_STATUS_TIMEOUT) return fail(DLLM_ERR_TIMEOUT, "a kernel wait timed out (status 0x%x)", v);
+    if (v & DLLM_STATUS_SMEM_LAYOUT)
+        return fail(DLLM_ERR_CUDA, "a GEMM found its shared memory misaligned and skipped its work (status 0x%x)", v);
     return DLLM_OK;
 }
 

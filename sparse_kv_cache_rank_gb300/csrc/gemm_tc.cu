@@ -34,7 +34,7 @@ constexpr int kWBytes = BM * BK * 2;   // 16 KB
 constexpr int kSmemLimit = 232448;     // 227 KB dynamic shared memory per CTA
 constexpr int kSmemPair = 113 * 1024;  // budget per CTA when two share an SM
 constexpr int kTailBytes = 256;        // barriers, TMEM slot, abort flag
-constexpr int kColBytes = 2 * 256 * 4; // per-column (sequence, position)
+                                       // then per token column (sequence, position): 8 * BN bytes
 
 struct Shape {
     int M_tok, N_out, K;
@@ -43,9 +43,15 @@ struct Shape {
     int indep;        // K slices are independent CTAs (no cluster): slice z writes token rows
                       // z * M_tok + m of the epilogue's output (partial sums, reduced later)
     int body_bytes;   // pipeline ring (and, with a cluster K split, the fp32 partial tile [BN][128])
+    int xrows;        // token rows staged per K block (<= BN; the MMA's N = BN columns past xrows
+                      // read whatever follows in shared memory and are never stored)
+    int base_aligned; // no alignment slack was reserved: the dynamic shared memory must start
+                      // on a 1024-byte boundary (else the kernel reports it and does nothing)
+    int col_bytes;    // per token column (sequence, position) after the body, >= 8 * BN and
+                      // >= the bytes the MMA reads past the last stage; barriers follow
 };
 
-__host__ __device__ inline int stage_bytes(int BN) { return kWBytes + BN * BK * 2; }
+__host__ __device__ inline int stage_bytes(int xrows) { return kWBytes + xrows * BK * 2; }
 
 // Applies the epilogue to 16 consecutive token columns c0.. of feature row F held in
 // v[]: the global values of all 16 outputs are requested before the first is written.
@@ -71,13 +77,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;   // 1024-byte aligned: required by the 128-byte swizzle
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + g.body_bytes);
+    if (g.base_aligned && pad != 0) {  // the plan left no room to align: do nothing, loudly
+        griddep_wait();
+        if (threadIdx.x == 0) raise_status(status, DLLM_STATUS_SMEM_LAYOUT);
+        return;
+    }
+    int *col_b = reinterpret_cast<int *>(smem + g.body_bytes);   // [BN] then col_pos [BN]
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + g.body_bytes + g.col_bytes);
     uint64_t *empty = full + g.stages;
     uint64_t *done = empty + g.stages;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    int *col_b = reinterpret_cast<int *>(smem + g.body_bytes + kTailBytes);   // [BN]
-    int *col_pos = col_b + 256;                                                // [BN]
+    int *col_pos = col_b + g.BN;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * g.BN;
@@ -89,7 +100,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int kb1 = (int)((long long)(split + 1) * KB / g.splits);
     const int nkb = kb1 - kb0;
     const uint32_t tmem_cols = g.BN <= 32 ? 32u : g.BN <= 64 ? 64u : g.BN <= 128 ? 128u : 256u;
-    const int sbytes = stage_bytes(g.BN);
+    const int sbytes = stage_bytes(g.xrows);
     const int ncols = min(g.BN, g.M_tok - m0);   // live token columns of this tile
 
     if (threadIdx.x == 0) {
@@ -312,7 +323,7 @@ namespace {
 
 struct Plan {
     int BN, splits, stages, tok_tiles, w_tiles;
-    int body;
+    int body, xrows, base_aligned, col_bytes;
     size_t smem;
 };
 
@@ -324,15 +335,31 @@ Plan make_plan(int M_tok, int N_out, int K, int BN, int splits, int budget, bool
     p.splits = splits;
     p.w_tiles = (N_out + BM - 1) / BM;
     p.tok_tiles = (M_tok + BN - 1) / BN;
-    const int sb = stage_bytes(BN);
-    const int tail = 1024 + kTailBytes + kColBytes;
+    // one token tile: stage only the rows that exist, rounded up to the 8-row swizzle atom
+    const int r8 = (M_tok + 7) / 8 * 8;
+    p.xrows = p.tok_tiles == 1 && r8 < BN ? r8 : BN;
+    const int sb = stage_bytes(p.xrows);
+    const int over = (BN - p.xrows) * BK * 2;   // read by the MMA past the last stage
+    p.col_bytes = 8 * BN > over ? 8 * BN : over;
+    const int tail = p.col_bytes + kTailBytes;
     const int part = smem_partial ? BN * BM * 4 : 0;
-    p.stages = (budget - tail) / sb;
-    if (p.stages > 8) p.stages = 8;
     const int KB = K / BK;
-    if (p.stages > KB / splits + 1) p.stages = KB / splits + 1 > 2 ? KB / splits + 1 : 2;
+    auto fit = [&](int slack) {
+        int st = (budget - slack - tail) / sb;
+        if (st > 8) st = 8;
+        if (st > KB / splits + 1) st = KB / splits + 1 > 2 ? KB / splits + 1 : 2;
+        return st;
+    };
+    p.stages = fit(1024);
+    p.base_aligned = 0;
+    // one stage more when only the 1 KB alignment slack stands in the way (not in a
+    // cluster: a CTA that finds its base misaligned returns alone)
+    if (!smem_partial && splits == 1 && fit(0) > p.stages) {
+        p.stages = fit(0);
+        p.base_aligned = 1;
+    }
     p.body = p.stages * sb > part ? p.stages * sb : part;
-    p.smem = (size_t)1024 + p.body + kTailBytes + kColBytes;
+    p.smem = (size_t)(p.base_aligned ? 0 : 1024) + p.body + tail;
     return p;
 }
 
@@ -355,7 +382,7 @@ Plan plan_gemm(int M_tok, int N_out, int K, int splits_req) {
         const int BN = M_tok <= 256 ? round16(M_tok) : 256;
         const int s = clamp_splits(splits_req);
         // two CTAs per SM whenever the fp32 partial tile of a K split fits their share
-        const bool pair = s == 1 || BN * BM * 4 + 1024 + kTailBytes + kColBytes <= kSmemPair;
+        const bool pair = s == 1 || BN * BM * 4 + 1024 + kTailBytes + 8 * BN <= kSmemPair;
         return make_plan(M_tok, N_out, K, BN, s, pair ? kSmemPair : kSmemLimit, s > 1);
     }
     if (M_tok <= 256) {
@@ -395,9 +422,10 @@ cudaError_t launch_plan(const Plan &p, bool indep, const bf16 *W, int N_out, int
     if (p.stages < 2) return cudaErrorInvalidValue;
     CUtensorMap tmW, tmX;
     if (!make_tmap(&tmW, W, (uint64_t)N_out, (uint64_t)K, BM) ||
-        !make_tmap(&tmX, X, (uint64_t)M_tok, (uint64_t)K, (uint32_t)p.BN))
+        !make_tmap(&tmX, X, (uint64_t)M_tok, (uint64_t)K, (uint32_t)p.xrows))
         return cudaErrorInvalidValue;
-    Shape g{M_tok, N_out, K, p.BN, p.splits, p.stages, w_const ? 1 : 0, indep ? 1 : 0, p.body};
+    Shape g{M_tok, N_out, K, p.BN, p.splits, p.stages, w_const ? 1 : 0, indep ? 1 : 0, p.body,
+            p.xrows, p.base_aligned, p.col_bytes};
     auto kern = k_gemm_tc<Epi>;
     static bool configured[64] = {};   // per device: raise the shared-memory limit once
     int dev = 0;
