@@ -365,8 +365,8 @@ Plan make_plan(int M_tok, int N_out, int K, int BN, int splits, int budget, bool
 
 // Few tokens (the gathered rows of a step) make every projection a weight stream:
 // what matters is that every SM streams weights and that epilogues overlap main loops.
-//  * many weight tiles (>= half the SMs): no K split, two CTAs per SM; a second token
-//    tile when the weight tiles alone would leave SMs idle;
+//  * many weight tiles (>= half the SMs): two CTAs per SM; no K split when the weight
+//    tiles fill the SMs, else a K split over a cluster sized to about two CTAs per SM;
 //  * few weight tiles: a K split across a cluster sized to fill the SMs.
 // Many tokens (compute-bound): 256-column token tiles, K split only to fill the GPU.
 Plan plan_gemm(int M_tok, int N_out, int K, int splits_req) {
@@ -387,8 +387,15 @@ Plan plan_gemm(int M_tok, int N_out, int K, int splits_req) {
     }
     if (M_tok <= 256) {
         if (2 * w_tiles >= sms) {
-            int BN = round16(M_tok);
-            if (w_tiles < sms && M_tok > 32) BN = round16((M_tok + 1) / 2);
+            const int BN = round16(M_tok);
+            if (w_tiles < sms && M_tok > 32) {
+                // fewer weight tiles than SMs: a K split over a cluster, two CTAs per SM, so
+                // that every SM streams weights (each weight byte is still read once)
+                int s = clamp_splits(2 * sms / w_tiles);
+                s = s > 4 ? 4 : s;
+                if (s > 1 && BN * BM * 4 + 1024 + kTailBytes + 8 * BN <= kSmemPair)
+                    return make_plan(M_tok, N_out, K, BN, s, kSmemPair, true);
+            }
             return make_plan(M_tok, N_out, K, BN, 1, kSmemPair, false);
         }
         int BN = round16(M_tok);
