@@ -41,6 +41,14 @@ struct AttnArgs {
     bf16 *A;                          // [B*k_max, n_q*hd]
 };
 
+// 2^x by the SFU's approximate base-2 exponential (relative error ~2^-22, subnormal
+// results flushed to zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -67,12 +75,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *q_full = bars + 0;
     uint64_t *k_full = bars + 1;               // [2]
     uint64_t *v_full = bars + 3;               // [2]
-    uint64_t *kv_empty = bars + 5;             // [2]
+    uint64_t *k_empty = bars + 5;              // [2] K tile read by its S product
     uint64_t *s_full = bars + 7;               // [2]
     uint64_t *s_free = bars + 9;               // [2]
     uint64_t *p_full = bars + 11;
     uint64_t *pv_full = bars + 12;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
+    uint64_t *v_empty = bars + 13;             // [2] V tile read by its PV product
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     griddep_wait();
@@ -107,7 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&k_full[i], 1);
             mbar_init(&v_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&s_free[i], kSoftThreads);
         }
@@ -131,31 +141,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS[2] = {tmem, tmem + 128};
     const uint32_t tPV = tmem + 256;
 
+    // softmax threads' results for the key-split merge: (O row half, m, l) of the row
+    float o[OH];
+    float m_fin = -INFINITY, l_fin = 0.f;
     if (warp == 0) {
-        if (lane == 0) {   // ---------------- TMA producer
+        // ---------------- TMA producers: lane 0 loads Q and the K tiles, lane 1 the V tiles;
+        // a K buffer is refilled as soon as its Q K^T product is done, a V buffer after
+        // its P V product
+        if (lane == 0) {
             mbar_arrive_expect_tx(q_full, QB);
             for (int c = 0; c < NCH; ++c)
                 tma_load_2d(sQ + c * kChunk, &tmQ, q_full, h * HD + c * 64, (int)row0);
+        }
+        if (lane < 2) {
+            const bool isK = lane == 0;
+            uint64_t *fullb = isK ? k_full : v_full;
+            uint64_t *emptyb = isK ? k_empty : v_empty;
+            uint8_t *buf = isK ? sK : sV;
+            const CUtensorMap *tm = isK ? &tmK : &tmV;
             int issued = 0;
             for (int it = 0; it < nt; ++it) {
                 const int s = it & 1;
                 const uint32_t ph = (uint32_t)(it >> 1) & 1u;
-                if (!mbar_wait(&kv_empty[s], ph ^ 1u, abort_flag, status)) break;
+                if (!mbar_wait(&emptyb[s], ph ^ 1u, abort_flag, status)) break;
                 const int y = b * a.N + (t0 + it) * AKV;
-                mbar_arrive_expect_tx(&k_full[s], KB);
+                mbar_arrive_expect_tx(&fullb[s], KB);
                 for (int c = 0; c < NCH; ++c)
-                    tma_load_2d(sK + s * KB + c * kChunk, &tmK, &k_full[s], g * HD + c * 64, y);
-                mbar_arrive_expect_tx(&v_full[s], KB);
-                for (int c = 0; c < NCH; ++c)
-                    tma_load_2d(sV + s * KB + c * kChunk, &tmV, &v_full[s], g * HD + c * 64, y);
+                    tma_load_2d(buf + s * KB + c * kChunk, tm, &fullb[s], g * HD + c * 64, y);
                 ++issued;
             }
-            if (*abort_flag) {
-                mbar_drain(q_full, 0);
-                for (int it = issued > 2 ? issued - 2 : 0; it < issued; ++it) {
-                    mbar_drain(&k_full[it & 1], (uint32_t)(it >> 1) & 1u);
-                    mbar_drain(&v_full[it & 1], (uint32_t)(it >> 1) & 1u);
-                }
+            if (*abort_flag) {   // every issued copy must land before the CTA can exit
+                if (isK) mbar_drain(q_full, 0);
+                for (int it = issued > 2 ? issued - 2 : 0; it < issued; ++it)
+                    mbar_drain(&fullb[it & 1], (uint32_t)(it >> 1) & 1u);
             }
         }
     } else if (warp == 1) {
@@ -177,6 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              smem_desc_sw128(ak + s * KB + off, 16, 1024), id_s, kk > 0);
                 }
                 mma_commit(&s_full[s]);
+                mma_commit(&k_empty[s]);   // the K buffer may be refilled
                 return true;
             };
             if (ok && nt > 0) ok = issue_s(0);
@@ -197,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              smem_desc_sw128(av + s * KB + offv, kChunk, 1024), id_pv, kk > 0);
                 }
                 mma_commit(pv_full);
-                mma_commit(&kv_empty[s]);
+                mma_commit(&v_empty[s]);
             }
         }
     } else {   // ---------------- softmax warps: thread = (query row, half)
@@ -205,7 +224,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hf = (warp - 2) >> 2;              // key columns hf*64.., head dims hf*OH..
         const int r = q * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        float o[OH];
 #pragma unroll
         for (int e = 0; e < OH; ++e) o[e] = 0.f;
         float m_run = -INFINITY, l_run = 0.f;
@@ -240,25 +258,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld_wait(slice16(v + c0));
             tc_fence_before();
             mbar_arrive(&s_free[s]);                    // S buffer may be overwritten now
-            float mt = -INFINITY;
+            if (nvalid < 64) {   // keys past N (last tile only): out of the max and the sum
 #pragma unroll
-            for (int j = 0; j < 64; ++j)
-                if (j < nvalid) mt = fmaxf(mt, v[j]);
+                for (int j = 0; j < 64; ++j)
+                    if (j >= nvalid) v[j] = -INFINITY;
+            }
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int j = 0; j < 64; ++j) mq[j & 3] = fmaxf(mq[j & 3], v[j]);
+            float mt = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
             xmax[hf * 128 + r] = mt;
             named_bar_sync(2 + q, 64);                 // the two warps of this lane quarter
             mt = fmaxf(mt, xmax[(hf ^ 1) * 128 + r]);
             const float m_new = fmaxf(m_run, mt * a.scale_log2);
-            const float corr = exp2f(m_run - m_new);
-            float lsum = 0.f;
+            const float corr = ex2_approx(m_run - m_new);
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
             uint32_t pk[32];                           // P of this tile, bf16 pairs
 #pragma unroll
-            for (int j = 0; j < 64; j += 2) {
-                const float p0 = (j < nvalid) ? exp2f(v[j] * a.scale_log2 - m_new) : 0.f;
-                const float p1 = (j + 1 < nvalid) ? exp2f(v[j + 1] * a.scale_log2 - m_new) : 0.f;
+            for (int j = 0; j < 64; j += 2) {          // 2^(-inf) = 0 for the masked keys
+                const float p0 = ex2_approx(fmaf(v[j], a.scale_log2, -m_new));
+                const float p1 = ex2_approx(fmaf(v[j + 1], a.scale_log2, -m_new));
                 const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
-                lsum += __low2float(pp) + __high2float(pp);
+                ls[(j >> 1) & 3] += __low2float(pp) + __high2float(pp);
                 pk[j >> 1] = *reinterpret_cast<const uint32_t *>(&pp);
             }
+            const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
             // the P buffer is free once the previous tile's PV product has completed
             if (it > 0 && !(ok = fold_pv(it - 1))) break;
 #pragma unroll
@@ -280,6 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float l_tot = l_run + xsum[(hf ^ 1) * 128 + r];
         const bool row_ok = q0 + r < a.k_max;
         const size_t row = row0 + r;
+        m_fin = (r < live && nt > 0) ? m_run : -INFINITY;
+        l_fin = (r < live && nt > 0) ? l_tot : 0.f;
         if (a.splits == 1) {
             if (row_ok) {
                 const float inv = (r < live && l_tot > 0.f) ? 1.0f / l_tot : 0.f;
@@ -288,71 +314,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < OH; e += 2)
                     *reinterpret_cast<__nv_bfloat162 *>(dst + e) = __floats2bfloat162_rn(o[e] * inv, o[e + 1] * inv);
             }
-        } else {
-            // this key slice's (O, m, l) into the CTA's own shared memory, over the Q tile
-            // and K ring: every copy into them has landed and every MMA reading them is done
-            float *sO = reinterpret_cast<float *>(smem);   // [128 rows][HD]
-            float *sML = sO + AQ * HD;                      // [128 rows][m, l]
-            float *po = sO + r * HD + hf * OH;
-#pragma unroll
-            for (int e = 0; e < OH; e += 4)
-                *reinterpret_cast<float4 *>(po + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-            if (hf == 0) {
-                const bool has = r < live && nt > 0;
-                sML[2 * r] = has ? m_run : -INFINITY;
-                sML[2 * r + 1] = has ? l_tot : 0.f;
-            }
         }
     }
     __syncwarp();
     if (a.splits > 1) {
-        // The key slices of one (rows, head) tile are the CTAs of a cluster: CTA rank k
-        // merges rows [k*128/S, (k+1)*128/S) of every slice's partial through distributed
-        // shared memory.
+        // The key slices of one (rows, head) tile are the CTAs of a cluster; CTA rank k
+        // owns rows [k*per, (k+1)*per).  Once every CTA is past its main loop (first
+        // barrier), each pushes its (O, m, l) of every row into the owner's shared memory
+        // (remote stores, over the owner's idle Q tile and K ring); after the second
+        // barrier every owner merges its rows from local memory.
+        const int S = a.splits;
+        const int per = (AQ + S - 1) / S;
+        const uint32_t my = cluster_ctarank();
+        float *rO = reinterpret_cast<float *>(smem);   // [S senders][per rows][HD]
+        float *rML = rO + (size_t)S * per * HD;         // [S senders][per rows][m, l]
         cluster_sync_all();
         if (warp >= 2) {
-            const int S = a.splits;
-            const int rk = (int)cluster_ctarank();
-            const int per = (AQ + S - 1) / S;
-            const int rb = rk * per, re = min(AQ, rb + per);
-            const int tid = threadIdx.x - 64;
-            float *wts = xmax;   // [per][S] slice weights 2^(m_s - M)   (per * S <= 256)
-            float *inv = xsum;   // [per]   1 / sum_s l_s 2^(m_s - M)
-            const uint32_t sO = smem_u32(smem);
-            const uint32_t sML = sO + (uint32_t)(AQ * HD * 4);
-            if (tid < re - rb) {
-                const int rr = rb + tid;
-                float M = -INFINITY;
-                for (int sp = 0; sp < S; ++sp)
-                    M = fmaxf(M, ld_dsmem_f32(mapa_shared(sML + (uint32_t)(8 * rr), (uint32_t)sp)));
-                float den = 0.f;
-                for (int sp = 0; sp < S; ++sp) {
-                    const uint32_t base = mapa_shared(sML + (uint32_t)(8 * rr), (uint32_t)sp);
-                    const float ms = ld_dsmem_f32(base);
-                    const float w = (M == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - M);
-                    den = fmaf(ld_dsmem_f32(base + 4), w, den);
-                    wts[tid * S + sp] = w;
-                }
-                inv[tid] = den > 0.f ? 1.0f / den : 0.f;
+            const int q = warp & 3, hf = (warp - 2) >> 2, r = q * 32 + lane;
+            const int owner = r / per, lr = r - owner * per;
+            const uint32_t dO = mapa_shared(smem_u32(rO + ((size_t)(my * per + lr) * HD + hf * OH)), (uint32_t)owner);
+#pragma unroll
+            for (int e = 0; e < OH; e += 4)
+                st_dsmem_f32x4(dO + (uint32_t)(e * 4), make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]));
+            if (hf == 0) {
+                const uint32_t dM = mapa_shared(smem_u32(rML + (size_t)(my * per + lr) * 2), (uint32_t)owner);
+                st_dsmem_f32(dM, m_fin);
+                st_dsmem_f32(dM + 4, l_fin);
             }
-            __syncwarp();
-            named_bar_sync(1, kSoftThreads);
+        }
+        __syncwarp();
+        cluster_sync_all();   // every push has landed; nothing remote is touched after this
+        if (warp >= 2) {
+            const int tid = threadIdx.x - 64;
+            const int rb = (int)my * per;
+            const int nrows = min(per, AQ - rb);
             constexpr int D4 = HD / 4;
-            for (int it = tid; it < (re - rb) * D4; it += kSoftThreads) {
+            for (int it = tid; it < nrows * D4; it += kSoftThreads) {
                 const int lr = it / D4, d4 = it - lr * D4;
-                const int rr = rb + lr;
+                float M = -INFINITY;
+                for (int sp = 0; sp < S; ++sp) M = fmaxf(M, rML[(sp * per + lr) * 2]);
                 float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int sp = 0; sp < S; ++sp) {
-                    const float w = wts[lr * S + sp];
-                    if (w == 0.f) continue;
-                    const float4 v = ld_dsmem_f32x4(mapa_shared(sO + (uint32_t)((rr * HD + d4 * 4) * 4), (uint32_t)sp));
-                    acc.x = fmaf(v.x, w, acc.x);
-                    acc.y = fmaf(v.y, w, acc.y);
-                    acc.z = fmaf(v.z, w, acc.z);
-                    acc.w = fmaf(v.w, w, acc.w);
+                float den = 0.f;
+                if (M != -INFINITY) {
+                    for (int sp = 0; sp < S; ++sp) {
+                        const float ms = rML[(sp * per + lr) * 2];
+                        if (ms == -INFINITY) continue;
+                        const float w = ex2_approx(ms - M);
+                        den = fmaf(rML[(sp * per + lr) * 2 + 1], w, den);
+                        const float4 x = *reinterpret_cast<const float4 *>(rO + ((size_t)(sp * per + lr) * HD + d4 * 4));
+                        acc.x = fmaf(x.x, w, acc.x);
+                        acc.y = fmaf(x.y, w, acc.y);
+                        acc.z = fmaf(x.z, w, acc.z);
+                        acc.w = fmaf(x.w, w, acc.w);
+                    }
                 }
+                const int rr = rb + lr;
                 if (q0 + rr < a.k_max) {
-                    const float iv = inv[lr];
+                    const float iv = den > 0.f ? 1.0f / den : 0.f;
                     __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(
                         a.A + (row0 + rr) * dq + (size_t)h * HD + d4 * 4);
                     dst[0] = __floats2bfloat162_rn(acc.x * iv, acc.y * iv);
@@ -360,8 +378,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        __syncwarp();
-        cluster_sync_all();   // peers may still read this CTA's partial
     }
     tc_fence_before();
     __syncthreads();
