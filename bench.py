@@ -50,6 +50,10 @@ def parse():
                     help="skip the 32-layer LLaDA-8B-shaped stack measurement")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="approximate budget of the CPU-oracle sample")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other layer configurations (tiny fp32, Dream-shaped, long context)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="all 36 long-context points (N x batch x update ratio) instead of 9")
     ap.add_argument("--profile-step", action="store_true",
                     help="profiling mode: set up the layer workload, warm up, then run ONE layer "
                          "step inside a cudaProfilerStart/Stop range (for ncu --profile-from-start off); "
@@ -138,13 +142,18 @@ def layer_kernel_work(sh, M):
 
 # --------------------------------------------------------------------------- native arm
 class LayerWorkload:
+    """One layer's resident state for repeated sparse refresh steps: weights (N(0, 0.02)),
+    two drifted inputs that alternate step to step, caches from a full refresh of the
+    previous input, and the forced rows (the current block's masked rows and the k_recent
+    decoded before them) when the shape has a vocabulary block."""
+
     def __init__(self, sh, seed, dev):
         import torch
         from sparse_kv_cache_rank_gb300 import binding as B
         self.B_ = B
         self.sh = sh
         self.dev = dev
-        bf = torch.bfloat16
+        bf = torch.float32 if sh.dtype == "f32" else torch.bfloat16
         gen = torch.Generator(device=dev)
         gen.manual_seed(seed)
 
@@ -189,7 +198,14 @@ class LayerWorkload:
         self.idx = torch.empty((Bn, N), device=dev, dtype=torch.int32)
         self.cnt = torch.empty((Bn,), device=dev, dtype=torch.int32)
         self.k = B.dllm_layer_budget(sh.rho, N)
-        need = B.dllm_refresh_workspace_bytes(self.layer, Bn, N, self.k)
+        self.forced = None
+        self.k_max = self.k
+        if sh.V and sh.k_recent:   # the block after the prompt: 8 decoded + the rest masked
+            rows = torch.arange(sh.prompt - sh.k_recent, sh.prompt + sh.block - sh.k_recent,
+                                device=dev, dtype=torch.int32)
+            self.forced = rows.repeat(Bn, 1).contiguous()
+            self.k_max = min(N, self.k + rows.numel())
+        need = B.dllm_refresh_workspace_bytes(self.layer, Bn, N, self.k_max)
         self.ws = torch.empty(need, device=dev, dtype=torch.uint8)
         self.H_prev = H_prev
         self.s = 0
@@ -201,8 +217,8 @@ class LayerWorkload:
             H = self.H[self.s & 1]
         self.s += 1
         B.dllm_proxy_score(H, self.Pt, self.pc, proxy_cur=self.cur, drift=self.drift)
-        B.dllm_select_topk(self.drift, None, self.k, idx=self.idx, count=self.cnt)
-        B.dllm_sparse_layer_refresh(self.layer, H, self.idx, self.cnt, self.k, self.K, self.V, self.O,
+        B.dllm_select_topk(self.drift, self.forced, self.k, idx=self.idx, count=self.cnt)
+        B.dllm_sparse_layer_refresh(self.layer, H, self.idx, self.cnt, self.k_max, self.K, self.V, self.O,
                                     self.pc, self.cur, ws=self.ws)
 
 
@@ -332,10 +348,13 @@ def native(args):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
-    if not args.no_stack:
+    if not args.no_stack or not args.no_configs:
         del wl
         torch.cuda.empty_cache()
+    if not args.no_stack:
         result["stack"] = stack_measure(dev, args.steps, args.warmup)
+    if not args.no_configs:
+        result["configs"] = config_points(dev, args.sweep)
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:
@@ -403,6 +422,48 @@ def stack_measure(dev, steps, warmup, decode_steps=48):
                         "timing": "wall clock incl. one device->host read and host commit per step"},
         "setup_s": setup_s,
     }
+
+
+def layer_point(sh, dev, steps, warmup, seed=77):
+    """Layer-steps/s of one configuration (CUDA events over `steps` resident steps)."""
+    import torch
+    wl = LayerWorkload(sh, seed, dev)
+    for _ in range(max(warmup, 3)):
+        wl.step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        wl.step()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    dt = e0.elapsed_time(e1) / 1e3 / steps
+    rows = int(wl.cnt.sum().item())
+    res = {"B": sh.B, "N": sh.N, "rho": sh.rho, "rows_per_step": rows, "dtype": sh.dtype,
+           "steps_per_s": 1.0 / dt, "ms_per_step": dt * 1e3, "tokens_per_s": sh.B * sh.N / dt,
+           "refreshed_rows_per_s": rows / dt}
+    del wl
+    torch.cuda.empty_cache()
+    return res
+
+
+def config_points(dev, full_sweep):
+    """The other layer configurations: the tiny fp32 layer (forced block rows), the
+    Dream-7B-shaped layer (batch 8, GQA) and the long-context LLaDA-8B-shaped points
+    (all 36 with full_sweep, else batch 1 at 5% / 16% / 100%)."""
+    import dataclasses
+    from sparse_kv_cache_rank_gb300 import synth
+    out = {"tiny_fp32": layer_point(synth.TINY, dev, 100, 5)}
+    dream = dataclasses.replace(synth.DREAM_STACK, name="dream7b-layer", layers=1, V=0)
+    out["dream7b_layer"] = layer_point(dream, dev, 20, 3)
+    pts = []
+    for sh in synth.sweep_shapes():
+        if not full_sweep and (sh.B != 1 or sh.rho == 0.5):
+            continue
+        pts.append(layer_point(sh, dev, 20, 3))
+    out["long_context"] = pts
+    return out
 
 
 # --------------------------------------------------------------------------- oracle legs
