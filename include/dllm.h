@@ -213,6 +213,24 @@ int dllm_commit_entropy(const float *logits, const uint8_t *valid, int B, int M,
                         size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * LM head fused with the vocabulary step ([EC] step 2, [TSPD] "Input features"): the
+ * same outputs as dllm_commit_entropy on logits = X W_lm^T, without materialising the
+ * logits.  The product runs on the tensor cores and reduces each 128-row tile of the
+ * vocabulary to one online-softmax state (max, argmax, sum of exponentials, their
+ * weighted sum) per row, which the commit step merges in a fixed order.
+ *   X [B*M, d] bf16 (the block rows after the final RMSNorm, as dllm_rows_rmsnorm
+ *   writes them), W_lm [V, d] bf16, valid [B, M] uint8; outputs as dllm_commit_entropy.
+ * Requirements: M <= 1024, d % 64 == 0, V % 32 == 0.  Workspace:
+ * dllm_lmhead_workspace_bytes(B, M, V) bytes (16 bytes per row and vocabulary tile).
+ * ------------------------------------------------------------------------- */
+size_t dllm_lmhead_workspace_bytes(int B, int M, int V);
+
+int dllm_lmhead_commit(const void *X, const void *W_lm, const uint8_t *valid, int B, int M, int V,
+                       int d, float conf_thresh, float tau, int32_t *token, float *conf,
+                       float *entropy, float *max_entropy, int32_t *full_next, void *ws,
+                       size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
  * [SPA] "3. Sparse execution", the attention of the selected queries alone (the same
  * kernels dllm_sparse_layer_refresh runs after the K/V scatter):
  *   A[m, h] = softmax(Q[m, h] K_cache[b, :, g]^T / sqrt(hd)) V_cache[b, :, g]

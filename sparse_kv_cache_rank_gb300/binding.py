@@ -71,6 +71,9 @@ _SIGS = {
     "dllm_commit_entropy_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                               C.c_float, C.c_float] + [C.c_void_p] * 6),
     "dllm_commit_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
+    "dllm_lmhead_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
+    "dllm_lmhead_commit": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p] + [C.c_int] * 4 +
+                           [C.c_float, C.c_float] + [C.c_void_p] * 6 + [C.c_size_t, C.c_void_p]),
     "dllm_commit_entropy": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                       C.c_float, C.c_float] + [C.c_void_p] * 6 +
                             [C.c_size_t, C.c_void_p]),
@@ -383,6 +386,32 @@ def dllm_commit_entropy(logits, valid, conf_thresh: float = 0.9, tau: float = 2.
                                      float(tau), _ptr(tok), _ptr(conf), _ptr(ent), _ptr(E),
                                      _ptr(full), _ptr(ws), ws.numel(), _stream(dev)),
            "dllm_commit_entropy")
+    return out
+
+
+def dllm_lmhead_commit(X, W_lm, valid, conf_thresh: float = 0.9, tau: float = 2.0, out=None, ws=None):
+    """X [B*M, d] bf16 (normalised block rows), W_lm [V, d] bf16, valid [B, M] uint8 ->
+    the outputs of dllm_commit_entropy on X W_lm^T, without materialising the logits."""
+    B, M = valid.shape
+    V, d = W_lm.shape
+    if X.shape != (B * M, d) or X.dtype != torch.bfloat16 or W_lm.dtype != torch.bfloat16:
+        raise DllmError("X [B*M, d] and W_lm [V, d] must be bf16")
+    dev = X.device
+    if out is None:
+        out = (torch.empty((B, M), dtype=torch.int32, device=dev),
+               torch.empty((B, M), dtype=torch.float32, device=dev),
+               torch.empty((B, M), dtype=torch.float32, device=dev),
+               torch.empty((B,), dtype=torch.float32, device=dev),
+               torch.empty((B,), dtype=torch.int32, device=dev))
+    tok, conf, ent, E, full = out
+    _cuda(X, W_lm, valid, *out)
+    need = int(lib().dllm_lmhead_workspace_bytes(B, M, V))
+    if ws is None:
+        ws = _workspace(need, dev, "lmhead")
+    _check(lib().dllm_lmhead_commit(_ptr(X), _ptr(W_lm), _ptr(valid), B, M, V, d, float(conf_thresh),
+                                    float(tau), _ptr(tok), _ptr(conf), _ptr(ent), _ptr(E), _ptr(full),
+                                    _ptr(ws), ws.numel(), _stream(dev)),
+           "dllm_lmhead_commit")
     return out
 
 

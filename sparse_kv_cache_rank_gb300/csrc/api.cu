@@ -573,6 +573,45 @@ DLLM_EXPORT int dllm_commit_entropy(const float *logits, const uint8_t *valid, i
     return DLLM_OK;
 }
 
+// ------------------------------------------------------------------ fused LM head + commit
+namespace {
+int vocab_tiles(int V) { return (V + 127) / 128; }
+}  // namespace
+
+DLLM_EXPORT size_t dllm_lmhead_workspace_bytes(int B, int M, int V) {
+    if (B <= 0 || M <= 0 || V <= 0) return 0;
+    return (size_t)B * M * vocab_tiles(V) * sizeof(VocabState) + 256;
+}
+
+DLLM_EXPORT int dllm_lmhead_commit(const void *X, const void *W_lm, const uint8_t *valid, int B, int M,
+                                   int V, int d, float conf_thresh, float tau, int32_t *token, float *conf,
+                                   float *entropy, float *max_entropy, int32_t *full_next, void *ws,
+                                   size_t ws_bytes, void *stream) {
+    CHECK_ARG(X && W_lm && valid && token && conf && entropy && max_entropy && full_next, "null pointer");
+    CHECK_ARG(B > 0 && M > 0 && V > 0 && d > 0, "sizes must be positive");
+    CHECK_ARG(M <= 1024, "M must be <= 1024 (got %d)", M);
+    CHECK_ARG(aligned16(X) && aligned16(W_lm), "arrays must be 16-byte aligned");
+    if (d % 64 || V % 32) return fail(DLLM_ERR_UNSUPPORTED, "needs d %% 64 == 0 and V %% 32 == 0");
+    const size_t need = dllm_lmhead_workspace_bytes(B, M, V);
+    if (!ws || ws_bytes < need)
+        return fail(DLLM_ERR_WORKSPACE, "workspace holds %zu bytes, %zu needed", ws_bytes, need);
+    VocabState *part = reinterpret_cast<VocabState *>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255));
+    cudaStream_t st = as_stream(stream);
+    const int tiles = vocab_tiles(V);
+    {
+        Launch t(DLLM_KERNEL_GEMM, st);
+        EpiVocabStats epi{SelRows{}, part, tiles};
+        CHECK_CUDA(gemm_tc(static_cast<const bf16 *>(W_lm), V, d, static_cast<const bf16 *>(X), B * M, epi, 1,
+                           true, status_ptr(), st),
+                   "lm head launch");
+    }
+    Launch t(DLLM_KERNEL_VOCAB, st);
+    CHECK_CUDA(commit_from_states(part, tiles, valid, B, M, conf_thresh, tau, token, conf, entropy, max_entropy,
+                                  full_next, st),
+               "commit launch");
+    return DLLM_OK;
+}
+
 // ------------------------------------------------------------------ measurement support
 DLLM_EXPORT int dllm_timer_start(int kernel_id, int max_launches) {
     CHECK_ARG(kernel_id >= DLLM_KERNEL_PROXY_GEMM && kernel_id <= DLLM_KERNEL_GEMM, "unknown kernel id %d", kernel_id);

@@ -49,6 +49,7 @@ struct FeatRow {
 // out[m, f] = acc (fp32), for f < n_valid.  Singular proxy and plain GEMM.
 struct EpiStoreF32 {
     static constexpr bool kSel = false;
+    static constexpr bool kTileReduce = false;
     using Feat = FeatRow;
     SelRows sel;
     float *out;
@@ -66,6 +67,7 @@ struct EpiStoreF32 {
 template <class T>
 struct EpiQKV {
     static constexpr bool kSel = true;
+    static constexpr bool kTileReduce = false;
     SelRows sel;
     T *Q;               // [M, n_q*hd]
     T *Kc, *Vc;         // [B, N, n_kv, hd]
@@ -112,6 +114,7 @@ struct EpiQKV {
 template <class T>
 struct EpiResidual {
     static constexpr bool kSel = true;
+    static constexpr bool kTileReduce = false;
     using Feat = FeatRow;
     SelRows sel;
     float *h1;          // [M, d]
@@ -131,6 +134,7 @@ struct EpiResidual {
 template <class T>
 struct EpiSwiGLU {
     static constexpr bool kSel = false;
+    static constexpr bool kTileReduce = false;
     using Feat = FeatRow;
     SelRows sel;
     T *U;               // [M, F]
@@ -147,6 +151,7 @@ struct EpiSwiGLU {
 template <class T>
 struct EpiDownScatter {
     static constexpr bool kSel = true;
+    static constexpr bool kTileReduce = false;
     using Feat = FeatRow;
     SelRows sel;
     T *H_out;           // [B, N, d]
@@ -160,6 +165,48 @@ struct EpiDownScatter {
                                                float2 h) const {
         if (pos >= 0) H_out[((size_t)b * sel.N + pos) * d + F.f] = from_f32<T>(h.x + acc);
     }
+};
+
+// Online softmax state of a set of logits l_i (EntropyCache, "How EntropyCache works",
+// step 2; TSPD "Input features"): m = max, a = its lowest index, s = sum e^(l - m),
+// t = sum (l - m) e^(l - m); then p_max = 1/s and entropy = ln s - t/s.  States of
+// disjoint sets merge exactly under a change of reference maximum.  s == 0: empty set.
+struct VocabState {
+    float m, s, t;
+    int a;
+};
+
+__device__ __forceinline__ VocabState vocab_merge(VocabState x, VocabState y) {
+    if (y.s == 0.f) return x;
+    if (x.s == 0.f) return y;
+    if (y.m > x.m || (y.m == x.m && y.a < x.a)) {
+        const VocabState tmp = x;
+        x = y;
+        y = tmp;
+    }
+    // x holds the larger maximum (lower index on equal maxima)
+    const float c = expf(y.m - x.m);
+    VocabState r;
+    r.m = x.m;
+    r.a = x.a;
+    r.s = x.s + y.s * c;
+    r.t = x.t + c * (y.t + (y.m - x.m) * y.s);
+    return r;
+}
+
+// LM head fused with the vocabulary statistics: instead of storing logits, the GEMM
+// reduces each weight tile (128 vocabulary rows) to one VocabState per token row:
+// part[m * tiles + tile].  Rows at or past V are not part of any state.
+struct EpiVocabStats {
+    static constexpr bool kSel = false;
+    static constexpr bool kTileReduce = true;
+    using Feat = FeatRow;
+    SelRows sel;
+    VocabState *part;   // [M_tok][tiles]
+    int tiles;
+    __device__ __forceinline__ Feat feat(int f) const { return {f}; }
+    __device__ __forceinline__ float2 pre(const Feat &, int, int, int) const { return {0.f, 0.f}; }
+    __device__ __forceinline__ void operator()(const Feat &, int, int, int, float, float2) const {}
 };
 
 }  // namespace dllm

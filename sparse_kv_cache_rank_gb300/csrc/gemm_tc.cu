@@ -191,7 +191,41 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
         const int nchunk = (g.BN + 15) / 16;
         const int ch0 = half == 0 ? 0 : (nchunk + 1) / 2, ch1 = half == 0 ? (nchunk + 1) / 2 : nchunk;
-        if (!cluster_split) {
+        if constexpr (Epi::kTileReduce) {
+            // one softmax state per token column over this tile's 128 weight rows: a
+            // butterfly over the 32 rows of each warp, then the 4 lane quarters in order
+            // (the ring is idle once `done` has completed)
+            VocabState *red = reinterpret_cast<VocabState *>(smem);   // [4][BN]
+            const bool rows_ok = n0 + q * 32 < g.N_out;                // warp-uniform
+            for (int ch = ch0; ch < ch1; ++ch) {
+                float v[16];
+                tmem_ld_x16(taddr + (uint32_t)(ch * 16), v);
+                tmem_ld_wait(v);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    VocabState st = rows_ok ? VocabState{v[j], 1.f, 0.f, n0 + f}
+                                            : VocabState{-INFINITY, 0.f, 0.f, INT_MAX};
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        VocabState y;
+                        y.m = __shfl_xor_sync(0xffffffffu, st.m, o);
+                        y.s = __shfl_xor_sync(0xffffffffu, st.s, o);
+                        y.t = __shfl_xor_sync(0xffffffffu, st.t, o);
+                        y.a = __shfl_xor_sync(0xffffffffu, st.a, o);
+                        st = (lane & o) ? vocab_merge(y, st) : vocab_merge(st, y);
+                    }
+                    if (lane == 0) red[q * g.BN + ch * 16 + j] = st;
+                }
+            }
+            __syncwarp();
+            named_bar_sync(1, kEpiWarps * 32);
+            for (int c = threadIdx.x - 64; c < ncols; c += kEpiWarps * 32) {
+                VocabState r = red[c];
+#pragma unroll
+                for (int qq = 1; qq < 4; ++qq) r = vocab_merge(r, red[qq * g.BN + c]);
+                epi.part[(size_t)(m0 + c) * epi.tiles + blockIdx.y] = r;
+            }
+        } else if (!cluster_split) {
             // straight from TMEM (independent K slices write rows split * M_tok + m)
             const int moff = g.indep ? split * g.M_tok : 0;
             if (n0 + q * 32 < g.N_out) {   // warp-uniform: N_out % 32 == 0
@@ -473,6 +507,8 @@ cudaError_t gemm_tc_slices(const bf16 *W, int N_out, int K, const bf16 *X, int M
 
 template cudaError_t gemm_tc<EpiStoreF32>(const bf16 *, int, int, const bf16 *, int,
                                           const EpiStoreF32 &, int, bool, unsigned *, cudaStream_t);
+template cudaError_t gemm_tc<EpiVocabStats>(const bf16 *, int, int, const bf16 *, int,
+                                            const EpiVocabStats &, int, bool, unsigned *, cudaStream_t);
 template cudaError_t gemm_tc<EpiQKV<bf16>>(const bf16 *, int, int, const bf16 *, int,
                                            const EpiQKV<bf16> &, int, bool, unsigned *, cudaStream_t);
 template cudaError_t gemm_tc<EpiResidual<bf16>>(const bf16 *, int, int, const bf16 *, int,

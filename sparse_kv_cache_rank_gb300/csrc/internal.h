@@ -116,6 +116,10 @@ cudaError_t select_topk(const float *drift, const int32_t *forced, int F, int k,
 
 // ---------------------------------------------------------------- vocabulary
 size_t commit_ws_bytes(int B, int M, int V);
+// The commit step from per-slice states part[(b * M + m) * slices + i] (M <= 1024).
+cudaError_t commit_from_states(const VocabState *part, int slices, const uint8_t *valid, int B, int M,
+                               float conf_thresh, float tau, int32_t *token, float *conf, float *entropy,
+                               float *max_entropy, int32_t *full_next, cudaStream_t st);
 cudaError_t commit_entropy(const float *logits, const uint8_t *valid, int B, int M, int V,
                            float conf_thresh, float tau, int32_t *token, float *conf,
                            float *entropy, float *max_entropy, int32_t *full_next, void *ws,

@@ -16,28 +16,9 @@
 namespace dllm {
 namespace {
 
-struct RowState {
-    float m, s, t;
-    int a;
-};
+using RowState = VocabState;
 
-__device__ __forceinline__ RowState merge(RowState x, RowState y) {
-    if (y.s == 0.f) return x;
-    if (x.s == 0.f) return y;
-    RowState r;
-    if (y.m > x.m || (y.m == x.m && y.a < x.a)) {
-        RowState tmp = x;
-        x = y;
-        y = tmp;
-    }
-    // x holds the larger maximum (lower index on equal maxima)
-    const float c = expf(y.m - x.m);
-    r.m = x.m;
-    r.a = x.a;
-    r.s = x.s + y.s * c;
-    r.t = x.t + c * (y.t + (y.m - x.m) * y.s);
-    return r;
-}
+__device__ __forceinline__ RowState merge(RowState x, RowState y) { return vocab_merge(x, y); }
 
 constexpr int kT1 = 256;
 
@@ -100,14 +81,36 @@ __global__ void __launch_bounds__(1024) k_commit(const RowState *__restrict__ pa
     __shared__ float s_conf[32];
     __shared__ int s_row[32];
     __shared__ unsigned s_emax;
+    __shared__ RowState s_state[1024];
     if (m == 0) s_emax = 0u;
+    // each row's slices merged by one warp: lane-strided in slice order, then a butterfly
+    // (a fixed order, so results repeat exactly)
+    {
+        const int warp = m >> 5, lane = m & 31, nwarps = blockDim.x >> 5;
+        for (int row = warp; row < M; row += nwarps) {
+            RowState r{-INFINITY, 0.f, 0.f, INT_MAX};
+            if (valid[(size_t)b * M + row]) {
+                const RowState *ps = part + ((size_t)b * M + row) * slices;
+                for (int i = lane; i < slices; i += 32) r = merge(r, ps[i]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    RowState y;
+                    y.m = __shfl_xor_sync(0xffffffffu, r.m, o);
+                    y.s = __shfl_xor_sync(0xffffffffu, r.s, o);
+                    y.t = __shfl_xor_sync(0xffffffffu, r.t, o);
+                    y.a = __shfl_xor_sync(0xffffffffu, r.a, o);
+                    r = (lane & o) ? merge(y, r) : merge(r, y);
+                }
+            }
+            if (lane == 0) s_state[row] = r;
+        }
+    }
+    __syncthreads();
     const bool live = m < M && valid[(size_t)b * M + m];
     float p = 0.f, H = 0.f;
     int am = -1;
     if (live) {
-        const RowState *ps = part + ((size_t)b * M + m) * slices;
-        RowState r = ps[0];
-        for (int i = 1; i < slices; ++i) r = merge(r, ps[i]);
+        const RowState r = s_state[m];
         p = 1.0f / r.s;
         H = fmaxf(logf(r.s) - r.t / r.s, 0.f);
         am = r.a;
@@ -177,6 +180,19 @@ size_t commit_ws_bytes(int B, int M, int V) {
     return (size_t)rows * slices_for(rows, V) * sizeof(RowState);
 }
 
+cudaError_t commit_from_states(const VocabState *part, int slices, const uint8_t *valid, int B, int M,
+                               float conf_thresh, float tau, int32_t *token, float *conf, float *entropy,
+                               float *max_entropy, int32_t *full_next, cudaStream_t st) {
+    if (B <= 0 || M <= 0) return cudaSuccess;
+    // enough warps that each merges few rows (M <= 1024 threads for the per-row step)
+    int threads = ((M + 31) / 32) * 32;
+    const int want = 32 * (slices < 32 ? slices : 32);
+    if (threads < want) threads = want;
+    if (threads > 1024) threads = 1024;
+    return launch_kernel(k_commit, dim3(B), dim3(threads), 0, st, 1, part, slices, valid, M, conf_thresh, tau,
+                         token, conf, entropy, max_entropy, full_next);
+}
+
 cudaError_t commit_entropy(const float *logits, const uint8_t *valid, int B, int M, int V,
                            float conf_thresh, float tau, int32_t *token, float *conf,
                            float *entropy, float *max_entropy, int32_t *full_next, void *ws,
@@ -188,9 +204,8 @@ cudaError_t commit_entropy(const float *logits, const uint8_t *valid, int B, int
         const int slices = slices_for(rows, V);
         cudaError_t e = launch_kernel(k_row_stats, dim3(slices, rows), dim3(kT1), 0, st, 1, logits, valid, V, slices, part);
         if (e != cudaSuccess) return e;
-        const int threads = ((M + 31) / 32) * 32;
-        return launch_kernel(k_commit, dim3(B), dim3(threads), 0, st, 1, part, slices, valid, M, conf_thresh, tau, token, conf, entropy,
-                                        max_entropy, full_next);
+        return commit_from_states(part, slices, valid, B, M, conf_thresh, tau, token, conf, entropy,
+                                  max_entropy, full_next, st);
     } else {
         const int threads = 32;
         return launch_kernel(k_commit, dim3(B), dim3(threads), 0, st, 1, part, 1, valid, 0, conf_thresh, tau, token, conf, entropy,

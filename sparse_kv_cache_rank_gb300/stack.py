@@ -46,7 +46,8 @@ class _Layer:
 class DecodeStack:
     def __init__(self, shape: LayerShape, seed: int, device, rho: RhoSchedule | None = None,
                  uniform_rho: float | None = None, k_recent: int = 8, conf_thresh: float = 0.9,
-                 tau: float = 2.0, proxy_method: str = "lowrank", keep_weights: bool = False):
+                 tau: float = 2.0, proxy_method: str = "lowrank", keep_weights: bool = False,
+                 keep_logits: bool = False):
         self.sh = sh = shape
         self.dev = device
         self.rho = rho or RhoSchedule()
@@ -63,6 +64,8 @@ class DecodeStack:
         d, dq, dkv, F, Bn, N = sh.d, sh.d_q, sh.d_kv, sh.F, sh.B, sh.N
         self.layers = []
         self.weights = [] if keep_weights else None
+        self.keep_logits = keep_logits   # materialise the block's logits (else the fused LM head)
+        self.logits = None
         for _ in range(sh.layers):
             w = {"w_q": randn(dq, d, std=0.02), "w_k": randn(dkv, d, std=0.02),
                  "w_v": randn(dkv, d, std=0.02), "w_o": randn(d, dq, std=0.02),
@@ -156,9 +159,12 @@ class DecodeStack:
                                             L.O, L.pc, L.cur, ws=self.ws)
             H = L.O
         X = B.dllm_rows_rmsnorm(H, self.block_rows, self.gamma_f, sh.eps)
-        logits = B.dllm_gemm_bf16(X, self.W_lm).view(sh.B, sh.block, sh.V)
-        self.logits = logits
-        return B.dllm_commit_entropy(logits, self.valid, self.conf_thresh, self.tau)
+        if self.keep_logits:
+            logits = B.dllm_gemm_bf16(X, self.W_lm).view(sh.B, sh.block, sh.V)
+            self.logits = logits
+            return B.dllm_commit_entropy(logits, self.valid, self.conf_thresh, self.tau)
+        # LM head fused with the softmax statistics (the logits are never stored)
+        return B.dllm_lmhead_commit(X, self.W_lm, self.valid, self.conf_thresh, self.tau)
 
     def count_rows(self, full: bool):
         """Rows refreshed per layer by one step (synchronises; for reporting)."""

@@ -72,6 +72,34 @@ def test_lmhead_and_commit_parity(B, orc):
     np.testing.assert_array_equal(to_np(full), f_o)
 
 
+@pytest.mark.parametrize("Bq,M,V,d,scale", [(1, 32, 4096, 512, 0.1), (2, 24, 4160, 256, 0.5),
+                                             (1, 32, 126464, 512, 0.05), (2, 8, 1024, 128, 3.0)])
+def test_lmhead_commit_fused(B, orc, Bq, M, V, d, scale):
+    """The LM head fused with the vocabulary statistics gives the unfused path's decisions:
+    argmax and committed tokens exactly, confidence and entropy within the fp32 reduction
+    tolerance (against the oracle's statistics of the same logits), with invalid rows, a
+    ragged last vocabulary tile (V = 4160) and the LLaDA vocabulary."""
+    g = synth.rng(71 + M + V)
+    X = synth.round_bf16(g.standard_normal((Bq * M, d), dtype=np.float32))
+    W = synth.round_bf16((g.standard_normal((V, d)) * scale / np.sqrt(d) * 8).astype(np.float32))
+    valid = (g.random((Bq, M)) > 0.2).astype(np.uint8)
+    valid[:, 0] = 1
+    Xd, Wd, vd = to_dev(X, torch.bfloat16), to_dev(W, torch.bfloat16), to_dev(valid)
+    logits = B.dllm_gemm_bf16(Xd, Wd).view(Bq, M, V)
+    tok_u, conf_u, ent_u, E_u, full_u = B.dllm_commit_entropy(logits, vd)
+    tok, conf, ent, E, full = B.dllm_lmhead_commit(Xd, Wd, vd)
+    am, pm, H = orc.vocab_stats(to_np(logits))
+    live = valid.astype(bool)
+    np.testing.assert_allclose(to_np(conf)[live], pm[live], rtol=FP32_REDUCTION_RTOL, atol=1e-9)
+    np.testing.assert_allclose(to_np(ent)[live], H[live], rtol=FP32_REDUCTION_RTOL, atol=1e-6)
+    t_o, E_o, f_o = orc.commit_rule(am, to_np(conf), to_np(ent), valid)
+    np.testing.assert_array_equal(to_np(tok), t_o)
+    np.testing.assert_array_equal(to_np(full), f_o)
+    np.testing.assert_array_equal(to_np(tok), to_np(tok_u))
+    again = B.dllm_lmhead_commit(Xd, Wd, vd)
+    assert all(torch.equal(a, b) for a, b in zip(again, (tok, conf, ent, E, full)))
+
+
 TINY_STACK = synth.LayerShape("tiny-stack", B=1, N=96, d=256, n_q=4, n_kv=2, hd=64, F=256, r=64,
                               rho=0.25, dtype="bf16", V=512, prompt=64, block=32, layers=2)
 
@@ -81,7 +109,8 @@ def test_full_step_equals_dense_forward(B, orc):
     followed by the final norm and the LM head of the block rows."""
     from sparse_kv_cache_rank_gb300.stack import DecodeStack
     sh = TINY_STACK
-    st = DecodeStack(sh, 62, torch.device("cuda"), k_recent=4, keep_weights=True, proxy_method="svd")
+    st = DecodeStack(sh, 62, torch.device("cuda"), k_recent=4, keep_weights=True, proxy_method="svd",
+                     keep_logits=True)
     st.forward(True)
     torch.cuda.synchronize()
     H = to_np(st.H0)
