@@ -49,6 +49,8 @@ struct Shape {
                       // on a 1024-byte boundary (else the kernel reports it and does nothing)
     int col_bytes;    // per token column (sequence, position) after the body, >= 8 * BN and
                       // >= the bytes the MMA reads past the last stage; barriers follow
+    int w_stream;     // the weights are larger than a fraction of L2 and read once per call:
+                      // their lines are loaded with an evict-first policy
 };
 
 __host__ __device__ inline int stage_bytes(int xrows) { return kWBytes + xrows * BK * 2; }
@@ -129,10 +131,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) {   // ---------------- TMA producer
             // weights never change on the device: the first ring stages stream their
             // weight tiles while the previous kernel is still draining
+            const uint64_t pol = l2_policy_evict_first();
+            auto load_w = [&](void *dst, uint64_t *bar, int kb) {
+                if (g.w_stream) tma_load_2d_hint(dst, &tmW, bar, kb * BK, n0, pol);
+                else tma_load_2d(dst, &tmW, bar, kb * BK, n0);
+            };
             const int pre = g.w_const ? (nkb < g.stages ? nkb : g.stages) : 0;
             for (int it = 0; it < pre; ++it) {
                 mbar_arrive_expect_tx(&full[it], (uint32_t)sbytes);
-                tma_load_2d(smem + it * sbytes, &tmW, &full[it], (kb0 + it) * BK, n0);
+                load_w(smem + it * sbytes, &full[it], kb0 + it);
             }
             griddep_wait();
             for (int it = 0; it < pre; ++it)
@@ -144,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status)) break;
                 uint8_t *sw = smem + s * sbytes;
                 mbar_arrive_expect_tx(&full[s], (uint32_t)sbytes);
-                tma_load_2d(sw, &tmW, &full[s], (kb0 + it) * BK, n0);
+                load_w(sw, &full[s], kb0 + it);
                 tma_load_2d(sw + kWBytes, &tmX, &full[s], (kb0 + it) * BK, m0);
                 ++issued;
             }
@@ -465,8 +472,10 @@ cudaError_t launch_plan(const Plan &p, bool indep, const bf16 *W, int N_out, int
     if (!make_tmap(&tmW, W, (uint64_t)N_out, (uint64_t)K, BM) ||
         !make_tmap(&tmX, X, (uint64_t)M_tok, (uint64_t)K, (uint32_t)p.xrows))
         return cudaErrorInvalidValue;
+    // a weight matrix beyond 1/8 of L2 is streamed, not reused: evict-first lines
+    const int w_stream = (size_t)N_out * (size_t)K * 2 > (size_t)16 << 20 ? 1 : 0;
     Shape g{M_tok, N_out, K, p.BN, p.splits, p.stages, w_const ? 1 : 0, indep ? 1 : 0, p.body,
-            p.xrows, p.base_aligned, p.col_bytes};
+            p.xrows, p.base_aligned, p.col_bytes, w_stream};
     auto kern = k_gemm_tc<Epi>;
     static bool configured[64] = {};   // per device: raise the shared-memory limit once
     int dev = 0;
