@@ -211,14 +211,16 @@ class LayerWorkload:
         self.s = 0
         torch.cuda.synchronize(dev)
 
-    def step(self, H=None):
+    def step(self, H=None, idx=None, cnt=None):
         B = self.B_
         if H is None:
             H = self.H[self.s & 1]
+        idx = self.idx if idx is None else idx
+        cnt = self.cnt if cnt is None else cnt
         self.s += 1
         B.dllm_proxy_score(H, self.Pt, self.pc, proxy_cur=self.cur, drift=self.drift)
-        B.dllm_select_topk(self.drift, self.forced, self.k, idx=self.idx, count=self.cnt)
-        B.dllm_sparse_layer_refresh(self.layer, H, self.idx, self.cnt, self.k_max, self.K, self.V, self.O,
+        B.dllm_select_topk(self.drift, self.forced, self.k, idx=idx, count=cnt)
+        B.dllm_sparse_layer_refresh(self.layer, H, idx, cnt, self.k_max, self.K, self.V, self.O,
                                     self.pc, self.cur, ws=self.ws)
 
 
@@ -295,36 +297,52 @@ def native(args):
 
     # end to end through the same calls with host buffers: every step copies its input
     # from pinned host memory and reads its result (the selection) back, inside the timed
-    # region.  The input copies run on a second stream into two device buffers, so the
-    # copy for step s+1 overlaps the compute of step s.
+    # region.  Inputs and selections are double-buffered and every copy runs on a second
+    # stream: after step s, that stream reads back step s's selection and uploads the input
+    # of step s + 2 into the freed buffers, so the compute stream carries only the step's
+    # kernels and one event wait per step.
     Hh = [wl.H[0].cpu().pin_memory(), wl.H[1].cpu().pin_memory()]
     Hd = [torch.empty_like(wl.H[0]), torch.empty_like(wl.H[0])]
-    idx_h = torch.empty(wl.idx.shape, dtype=torch.int32).pin_memory()
-    cnt_h = torch.empty(wl.cnt.shape, dtype=torch.int32).pin_memory()
+    idx_d = [torch.empty_like(wl.idx), torch.empty_like(wl.idx)]
+    cnt_d = [torch.empty_like(wl.cnt), torch.empty_like(wl.cnt)]
+    idx_h = [torch.empty(wl.idx.shape, dtype=torch.int32).pin_memory() for _ in range(2)]
+    cnt_h = [torch.empty(wl.cnt.shape, dtype=torch.int32).pin_memory() for _ in range(2)]
     main = torch.cuda.current_stream(dev)
     cs = torch.cuda.Stream(dev)
-    copied = [torch.cuda.Event(), torch.cuda.Event()]
-    consumed = [torch.cuda.Event(), torch.cuda.Event()]
+    ready = [torch.cuda.Event(), torch.cuda.Event()]   # input of the step in Hd[b] is resident
+    done = [torch.cuda.Event(), torch.cuda.Event()]    # the step using buffers b has finished
+    read_back = torch.cuda.Event()
 
-    def issue_copy(s):
+    def read_result(s):
         b = s & 1
+        cs.wait_event(done[b])
+        idx_h[b].copy_(idx_d[b], non_blocking=True)
+        cnt_h[b].copy_(cnt_d[b], non_blocking=True)
+
+    def stage(s):   # on the copy stream: step s - 2's result out, step s's input in
         with torch.cuda.stream(cs):
-            cs.wait_event(consumed[b])          # the step two back has read this buffer
-            Hd[b].copy_(Hh[s & 1], non_blocking=True)
-            copied[b].record(cs)
+            if s >= 2:
+                read_result(s - 2)
+            Hd[s & 1].copy_(Hh[s & 1], non_blocking=True)
+            ready[s & 1].record(cs)
 
     def e2e_steps(n, start_event=None):
         if start_event is not None:
             cs.wait_event(start_event)
-        issue_copy(0)
+        stage(0)
+        stage(1)
         for s in range(n):
-            if s + 1 < n:
-                issue_copy(s + 1)
-            main.wait_event(copied[s & 1])
-            wl.step(Hd[s & 1])
-            consumed[s & 1].record(main)
-            idx_h.copy_(wl.idx, non_blocking=True)
-            cnt_h.copy_(wl.cnt, non_blocking=True)
+            b = s & 1
+            main.wait_event(ready[b])
+            wl.step(Hd[b], idx=idx_d[b], cnt=cnt_d[b])
+            done[b].record(main)
+            if s + 2 < n:
+                stage(s + 2)
+        with torch.cuda.stream(cs):
+            for s in range(max(n - 2, 0), n):
+                read_result(s)
+            read_back.record(cs)
+        main.wait_event(read_back)
 
     e2e_steps(2)
     torch.cuda.synchronize(dev)
