@@ -35,7 +35,8 @@ if ROOT not in sys.path:
 METRIC = "sparse-refresh denoise steps/s & tokens/s (LLaDA-8B shape); % of roofline"
 # dram__bytes_read.sum + dram__bytes_write.sum per launch, LLaDA-8B layer at k = 164
 # (profiles/gemm_attention_llada8b_full.md); to be re-taken whenever these kernels change
-NCU_TRAFFIC_BYTES = {"attention": 18.18e6}
+NCU_TRAFFIC_BYTES = {"gateup": 205.85e6, "qkv": 106.14e6, "down": 110.35e6, "oproj": 36.30e6,
+                     "attention": 18.18e6}
 UNIT = "steps/s"
 
 
