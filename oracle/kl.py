@@ -10,13 +10,15 @@ D_i = KL(A_i^t || A_i^{t-1}), and the attention used for it is a proxy attention
 from compressed representations (same section, sparse updates).
 
 Reading used here (the page gives no formula for A beyond this): the attention
-distribution of row i is the softmax over all N rows j of the sequence (bidirectional,
-j = i included) of the scaled dot product of proxies, <s_i, s_j> / sqrt(r), where s are
-the singular proxies of the rows ("Singular proxies for adaptive caching in diffusion
-language models", 1. Update identification via singular proxy); A^t uses the proxies of
-the current step and A^{t-1} the cached ones.  Then
+distribution of row i is the softmax, over the other N - 1 rows j != i of the sequence
+(bidirectional), of the scaled dot product of proxies <s_i, s_j> / sqrt(r), where s are the
+singular proxies of the rows ("Singular proxies for adaptive caching in diffusion language
+models", 1. Update identification via singular proxy); A^t uses the proxies of the current
+step and A^{t-1} the cached ones.  The row itself is left out because with the same proxy
+as query and key its own logit |s_i|^2 / sqrt(r) dwarfs the others and every distribution
+would be one-hot on itself.  Then
 
-    D_i = sum_j A_i^t(j) (ln A_i^t(j) - ln A_i^{t-1}(j)).
+    D_i = sum_{j != i} A_i^t(j) (ln A_i^t(j) - ln A_i^{t-1}(j)),   D_i = 0 when N = 1.
 
 fp64 throughout; numpy's matmul is the only library step.
 """
@@ -44,9 +46,18 @@ def kl_drift(cur, cached):
     cached = np.asarray(cached, dtype=np.float64)
     if cur.shape != cached.shape or cur.ndim != 3:
         raise ValueError("cur and cached must both be [B, N, r]")
-    out = np.empty(cur.shape[:2])
-    for b in range(cur.shape[0]):
-        lp = log_softmax_rows(proxy_attention_logits(cur[b]))
-        lq = log_softmax_rows(proxy_attention_logits(cached[b]))
+    B, N, _ = cur.shape
+    out = np.zeros((B, N))
+    if N < 2:
+        return out
+    off = ~np.eye(N, dtype=bool)
+    for b in range(B):
+        x = proxy_attention_logits(cur[b])
+        y = proxy_attention_logits(cached[b])
+        # the N - 1 other rows of every row (row i's own column removed)
+        x = x[off].reshape(N, N - 1)
+        y = y[off].reshape(N, N - 1)
+        lp = log_softmax_rows(x)
+        lq = log_softmax_rows(y)
         out[b] = (np.exp(lp) * (lp - lq)).sum(axis=-1)
     return out
