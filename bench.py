@@ -402,6 +402,7 @@ def native(args):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+    result["next_rows"] = {"kl_drift": kl_drift_measure(wl, args.steps, args.warmup)}
     if not args.no_stack or not args.no_configs:
         del wl
         torch.cuda.empty_cache()
@@ -504,6 +505,38 @@ def layer_point(sh, dev, steps, warmup, seed=77):
     del wl
     torch.cuda.empty_cache()
     return res
+
+
+# fp32 FMA rate of the GPU: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz (maximum SM clock)
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def kl_drift_measure(wl, steps, warmup):
+    """The attention-distribution drift (KL of proxy-attention rows, this step against the
+    cached proxies) on the layer's proxies: B x N x N x r scores for each of the two steps,
+    fp32 on the CUDA cores.  CUDA events around `steps` back-to-back launches."""
+    import torch
+    B_ = wl.B_
+    Bn, N, r = wl.cur.shape
+    out = torch.empty((Bn, N), dtype=torch.float32, device=wl.dev)
+    for _ in range(max(warmup, 3)):
+        B_.dllm_kl_drift(wl.cur, wl.pc, out)
+    torch.cuda.synchronize(wl.dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        B_.dllm_kl_drift(wl.cur, wl.pc, out)
+    e1.record()
+    torch.cuda.synchronize(wl.dev)
+    s = e0.elapsed_time(e1) / 1e3 / steps
+    flops = 2 * 2 * Bn * N * N * r          # two score products of 2 N^2 r FLOP each
+    achieved = flops / s / 1e12
+    return {"workload": f"B={Bn} N={N} r={r}", "us_per_launch": s * 1e6, "flop": flops,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS,
+                         "unit": "TFLOP/s", "frac": achieved / FP32_PEAK_TFLOPS,
+                         "peak_source": "fp32 FMA lanes x maximum SM clock"},
+            "timing": "CUDA events around back-to-back launches, outside the timed region"}
 
 
 def config_points(dev, full_sweep):

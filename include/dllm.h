@@ -97,6 +97,25 @@ int dllm_proxy_score(const void *H, const void *Pt, const float *proxy_cache, fl
                      size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * [POL] "2. A. Polestar-Cache", drift measurement: the drift of a row between
+ * consecutive steps is the KL divergence of its attention distributions,
+ * D_i = KL(A_i^t || A_i^{t-1}) -- an alternative score to the cosine of
+ * dllm_proxy_score, selected on in the same way (dllm_select_topk).  The page gives
+ * no formula for A; the attention here is row-granular proxy attention over the
+ * other rows of the sequence:
+ *   A^t_i(j)     = softmax over j != i of <proxy_cur[b,i], proxy_cur[b,j]> / sqrt(r)
+ *   A^{t-1}_i(j) = the same with proxy_cache
+ *   drift[b, i]  = sum_{j != i} A^t_i(j) ln(A^t_i(j) / A^{t-1}_i(j));  0 when N == 1.
+ * Identical proxies give exactly 0.  fp32 arithmetic (CUDA cores).
+ *   proxy_cur, proxy_cache [B, N, r] fp32 (as produced and kept by dllm_proxy_score);
+ *   drift [B, N] fp32 out.
+ * Requirements: r % 32 == 0, B <= 65535.  No workspace.  Caller-owned arrays; errors:
+ * DLLM_ERR_ARG for null pointers or non-positive sizes, DLLM_ERR_UNSUPPORTED for r.
+ * ------------------------------------------------------------------------- */
+int dllm_kl_drift(const float *proxy_cur, const float *proxy_cache, float *drift, int B, int N,
+                  int r, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Selection.  [SPA] "1. ...": the rows with the lowest proxy similarity (largest
  * drift) are recomputed, [SPA] "2. Adaptive budget allocation": at most k of them
  * per layer; [EC] step 3: the current masked tokens and the k most recently decoded
@@ -321,6 +340,7 @@ int dllm_gemm_bf16(const void *X, const void *W, float *out, int M, int N_out, i
 #define DLLM_KERNEL_DOWN 10
 #define DLLM_KERNEL_VOCAB 11
 #define DLLM_KERNEL_GEMM 12
+#define DLLM_KERNEL_KL_DRIFT 13
 
 /* Launch mode of the library's kernels: with enable != 0 (the default) consecutive
  * kernels on a stream use programmatic dependent launch (a kernel's prologue and its

@@ -41,6 +41,7 @@ _SIGS = {
     "dllm_check_status": (C.c_int, [C.POINTER(C.c_uint), C.c_int]),
     "dllm_proxy_score": (C.c_int, [C.c_void_p] * 5 + [C.c_int] * 5 + [C.c_void_p, C.c_size_t, C.c_void_p]),
     "dllm_proxy_workspace_bytes": (C.c_size_t, [C.c_int] * 5),
+    "dllm_kl_drift": (C.c_int, [C.c_void_p] * 3 + [C.c_int] * 3 + [C.c_void_p]),
     "dllm_select_topk": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_float,
                                    C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p]),
     "dllm_layer_rho": (C.c_double, [C.c_int] + [C.c_double] * 5),
@@ -156,7 +157,8 @@ def check_status(reset: bool = True) -> int:
 
 # --------------------------------------------------------------------------- measurement
 KERNELS = {"proxy_gemm": 1, "cosine": 2, "select": 3, "gather": 4, "qkv": 5, "attention": 6,
-           "oproj": 7, "rmsnorm2": 8, "gateup": 9, "down": 10, "vocab": 11, "gemm": 12}
+           "oproj": 7, "rmsnorm2": 8, "gateup": 9, "down": 10, "vocab": 11, "gemm": 12,
+           "kl_drift": 13}
 
 
 def dllm_timer_start(kernel: str, max_launches: int) -> None:
@@ -199,6 +201,20 @@ def dllm_proxy_score(H, Pt, proxy_cache, proxy_cur=None, drift=None, ws=None):
                                   B, N, d, r, _dtype_code(H), _ptr(ws), 0 if ws is None else ws.numel(),
                                   _stream(H.device)), "dllm_proxy_score")
     return proxy_cur, drift
+
+
+def dllm_kl_drift(proxy_cur, proxy_cache, drift=None):
+    """proxy_cur, proxy_cache [B,N,r] f32 -> drift [B,N] f32 = KL of the rows' proxy-attention
+    distributions (this step against the cached proxies)."""
+    B, N, r = proxy_cur.shape
+    if proxy_cache.shape != (B, N, r) or proxy_cur.dtype != torch.float32 or proxy_cache.dtype != torch.float32:
+        raise DllmError("proxy_cur and proxy_cache must both be [B, N, r] float32")
+    if drift is None:
+        drift = torch.empty((B, N), dtype=torch.float32, device=proxy_cur.device)
+    _cuda(proxy_cur, proxy_cache, drift)
+    _check(lib().dllm_kl_drift(_ptr(proxy_cur), _ptr(proxy_cache), _ptr(drift), B, N, r,
+                               _stream(proxy_cur.device)), "dllm_kl_drift")
+    return drift
 
 
 def build_proxy_matrix(w_v: torch.Tensor, gamma1: torch.Tensor, r: int, method: str = "svd",

@@ -265,6 +265,18 @@ DLLM_EXPORT int dllm_proxy_score(const void *H, const void *Pt, const float *pro
     return DLLM_OK;
 }
 
+DLLM_EXPORT int dllm_kl_drift(const float *proxy_cur, const float *proxy_cache, float *drift,
+                              int B, int N, int r, void *stream) {
+    CHECK_ARG(proxy_cur && proxy_cache && drift, "null pointer");
+    CHECK_ARG(B > 0 && N > 0 && r > 0, "sizes must be positive (B=%d N=%d r=%d)", B, N, r);
+    CHECK_ARG(B <= 65535, "B must be <= 65535");
+    if (r % 32) return fail(DLLM_ERR_UNSUPPORTED, "r must be a multiple of 32 (got %d)", r);
+    cudaStream_t st = as_stream(stream);
+    Launch t(DLLM_KERNEL_KL_DRIFT, st);
+    CHECK_CUDA(kl_drift(proxy_cur, proxy_cache, drift, B, N, r, st), "KL drift launch");
+    return DLLM_OK;
+}
+
 // ------------------------------------------------------------------ selection
 DLLM_EXPORT int dllm_select_topk(const float *drift, const int32_t *forced, int F, int k,
                                  float min_drift, int32_t *idx, int32_t *count, int B, int N,
@@ -614,7 +626,7 @@ DLLM_EXPORT int dllm_lmhead_commit(const void *X, const void *W_lm, const uint8_
 
 // ------------------------------------------------------------------ measurement support
 DLLM_EXPORT int dllm_timer_start(int kernel_id, int max_launches) {
-    CHECK_ARG(kernel_id >= DLLM_KERNEL_PROXY_GEMM && kernel_id <= DLLM_KERNEL_GEMM, "unknown kernel id %d", kernel_id);
+    CHECK_ARG(kernel_id >= DLLM_KERNEL_PROXY_GEMM && kernel_id <= DLLM_KERNEL_KL_DRIFT, "unknown kernel id %d", kernel_id);
     CHECK_ARG(max_launches > 0 && max_launches <= 1 << 16, "max_launches must be in [1, 65536]");
     std::lock_guard<std::mutex> lock(g_timer.mu);
     CHECK_ARG(g_timer.armed == 0, "a timer is already armed");

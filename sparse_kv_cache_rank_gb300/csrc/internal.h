@@ -80,6 +80,12 @@ cudaError_t rmsnorm_rows(const float *h1, int M, int d, const T *gamma, float ep
 cudaError_t cosine_drift(const float *parts, int nparts, const float *cached, float *cur,
                          float *drift, long rows, int r, cudaStream_t st);
 
+// KL divergence of proxy-attention rows between two steps (kl.cu): drift [B, N] from
+// cur, cache [B, N, r] fp32; r % 32 == 0.  Key slices per query tile (a cluster along z):
+int kl_drift_slices(int B, int N);
+cudaError_t kl_drift(const float *cur, const float *cache, float *drift, int B, int N, int r,
+                     cudaStream_t st);
+
 template <class T>
 cudaError_t pack_rows_rope(const T *src, T *dst, int rows, int cols, int hd, cudaStream_t st);
 

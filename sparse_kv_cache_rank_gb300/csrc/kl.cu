@@ -1,0 +1,307 @@
+// kl.cu -- drift of a row as the KL divergence between its attention distributions at two
+// consecutive steps ("Polestar: drift-aware cache correction and token commit", 2. A,
+// Polestar-Cache, drift measurement: D_i = KL(A_i^t || A_i^{t-1})), over row-granular proxy
+// attention: A_i(j) = softmax_j(<s_i, s_j> / sqrt(r)) over the other rows j != i of the
+// sequence, with the singular proxies of this step (A^t) and the cached ones (A^{t-1}).  The
+// row's own column is left out: with the same proxy as query and key its logit |s_i|^2 /
+// sqrt(r) would dominate and every distribution would be one-hot on itself.
+//
+// With x_j = <cur_i, cur_j> / sqrt(r), y_j = <cache_i, cache_j> / sqrt(r), p = softmax(x):
+//     D_i = sum_j p_j (x_j - y_j) - (LSE(x) - LSE(y)),   LSE(x) = m_x + ln sum_j e^(x_j - m_x),
+// and D_i = 0 for a sequence of one row.
+// One pass over the keys keeps, per row, the running maxima m_x, m_y, the sums
+// Z_x = sum e^(x - m_x), Z_y = sum e^(y - m_y) and W = sum e^(x - m_x) (x - y), rescaled
+// whenever a maximum grows.  Identical proxies give x == y bit for bit, hence W = 0,
+// Z_x == Z_y and D = 0 exactly.
+//
+// fp32 on the CUDA cores: the drift is made of score differences that bf16 tensor-core
+// scores would swamp.  One CTA (16 warps) = 64 query rows x one slice of the 128-row key
+// tiles; thread (ty, tx) owns rows 4 ty .. 4 ty + 3 and key columns 4 tx .. 4 tx + 3 of both
+// score tiles, so one warp holds four whole rows of a tile.  The query tile (both steps, all
+// r dimensions) stays in shared memory, transposed; the key tiles stream through a two-chunk
+// ring of 32 dimensions each, the next chunk's global loads held in registers while the
+// current chunk is multiplied.  The shared memory (~134 KB at r = 128) keeps one CTA per SM,
+// so the key slices spread over the SMs.  The key slices of one query tile are the CTAs of a
+// thread-block cluster (along z); CTA rank k merges rows [k 64/S, (k+1) 64/S) of every
+// slice's state through distributed shared memory, in slice order.
+#include <math.h>
+
+#include "internal.h"
+
+namespace dllm {
+namespace {
+
+constexpr int kQ = 64;           // query rows per CTA
+constexpr int kK = 128;          // key rows per tile
+constexpr int kR = 32;           // proxy dimensions per staged chunk
+constexpr int kPq = kQ + 4;      // padded rows of the transposed chunks (16-byte aligned)
+constexpr int kPk = kK + 4;
+constexpr int kThreads = 512;    // 16 x 32 threads, 4 x 4 scores each
+constexpr int kMaxSlices = 8;
+constexpr int kMaxR = 256;
+
+// dynamic shared memory: query tile [2 steps][r][kPq], key ring [2 buffers][2 steps][kR][kPk]
+__host__ __device__ inline size_t kl_smem_bytes(int r) {
+    return ((size_t)2 * r * kPq + (size_t)4 * kR * kPk) * 4;
+}
+
+struct RowState {
+    float mx, zx, w, my, zy;
+};
+
+// Chunk [row0, row0 + ROWS) x [c0, c0 + 32) of a [N, r] matrix as ROWS / 16 values per
+// thread (dimension = lane, rows warp + 16 i; rows past N are zero), and its transposed
+// store dst[c * P + row].
+template <int ROWS>
+__device__ __forceinline__ void load_chunk(float (&v)[ROWS / 16], const float *__restrict__ src, int row0,
+                                           int N, int r, int c0) {
+    const int c = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int i = 0; i < ROWS / 16; ++i) {
+        const int row = row0 + w + 16 * i;
+        v[i] = row < N ? src[(size_t)row * r + c0 + c] : 0.f;
+    }
+}
+template <int ROWS, int P>
+__device__ __forceinline__ void store_chunk(float *dst, const float (&v)[ROWS / 16]) {
+    const int c = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int i = 0; i < ROWS / 16; ++i) dst[c * P + w + 16 * i] = v[i];
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_kl_drift(const float *__restrict__ cur, const float *__restrict__ cache, float *__restrict__ drift,
+               int N, int r, int S) {
+    extern __shared__ __align__(16) float smf[];
+    float *qc = smf;                    // [r][kPq] this step's query proxies, transposed
+    float *qp = qc + (size_t)r * kPq;   // [r][kPq] the cached ones
+    float *ring = qp + (size_t)r * kPq; // [2 buffers][2 steps][kR][kPk]
+    __shared__ RowState st[kQ];
+
+    griddep_wait();
+    griddep_launch();
+    const int b = blockIdx.y;
+    const int q0 = blockIdx.x * kQ;
+    const int slice = (int)blockIdx.z;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const float *cb = cur + (size_t)b * N * r;
+    const float *pb = cache + (size_t)b * N * r;
+    const float scale = 1.f / sqrtf((float)r);
+
+    const int nkt = (N + kK - 1) / kK;
+    const int kt0 = (int)((long long)slice * nkt / S), kt1 = (int)((long long)(slice + 1) * nkt / S);
+    const int nch = r / kR;
+    const int nit = (kt1 - kt0) * nch;
+
+    // the query tile (four chunks' loads in flight before they are stored) and the first key chunk
+    for (int c0 = 0; c0 < r; c0 += 4 * kR) {
+        float v[4][kQ / 16];
+        const int n = (r - c0) / kR < 4 ? (r - c0) / kR : 4;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (k < n) load_chunk<kQ>(v[k], cb, q0, N, r, c0 + k * kR);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (k < n) store_chunk<kQ, kPq>(qc + (size_t)(c0 + k * kR) * kPq, v[k]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (k < n) load_chunk<kQ>(v[k], pb, q0, N, r, c0 + k * kR);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            if (k < n) store_chunk<kQ, kPq>(qp + (size_t)(c0 + k * kR) * kPq, v[k]);
+    }
+    float pc_[kK / 16], pp_[kK / 16];
+    if (nit > 0) {
+        load_chunk<kK>(pc_, cb, kt0 * kK, N, r, 0);
+        load_chunk<kK>(pp_, pb, kt0 * kK, N, r, 0);
+        store_chunk<kK, kPk>(ring, pc_);
+        store_chunk<kK, kPk>(ring + kR * kPk, pp_);
+    }
+    __syncthreads();
+
+    float mx[4], zx[4], w[4], my[4], zy[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+        mx[a] = -INFINITY;
+        my[a] = -INFINITY;
+        zx[a] = 0.f;
+        zy[a] = 0.f;
+        w[a] = 0.f;
+    }
+    float x[4][4], y[4][4];
+    for (int it = 0; it < nit; ++it) {
+        const int kt = kt0 + it / nch, ch = it % nch;
+        const int k0 = kt * kK;
+        if (ch == 0) {
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    x[a][e] = 0.f;
+                    y[a][e] = 0.f;
+                }
+        }
+        if (it + 1 < nit) {   // next chunk's loads in flight during this chunk's products
+            const int nk0 = (kt0 + (it + 1) / nch) * kK, nc0 = ((it + 1) % nch) * kR;
+            load_chunk<kK>(pc_, cb, nk0, N, r, nc0);
+            load_chunk<kK>(pp_, pb, nk0, N, r, nc0);
+        }
+        const float *kcb = ring + (size_t)(it & 1) * 2 * kR * kPk;
+        const float *kpb = kcb + kR * kPk;
+        const float *qcb = qc + (size_t)ch * kR * kPq;
+        const float *qpb = qp + (size_t)ch * kR * kPq;
+#pragma unroll 8
+        for (int c = 0; c < kR; ++c) {
+            const float4 ac = *reinterpret_cast<const float4 *>(qcb + c * kPq + ty * 4);
+            const float4 ap = *reinterpret_cast<const float4 *>(qpb + c * kPq + ty * 4);
+            const float4 bc = *reinterpret_cast<const float4 *>(kcb + c * kPk + tx * 4);
+            const float4 bp = *reinterpret_cast<const float4 *>(kpb + c * kPk + tx * 4);
+            const float av[4] = {ac.x, ac.y, ac.z, ac.w}, pv[4] = {ap.x, ap.y, ap.z, ap.w};
+            const float bv[4] = {bc.x, bc.y, bc.z, bc.w}, qv[4] = {bp.x, bp.y, bp.z, bp.w};
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    x[a][e] = fmaf(av[a], bv[e], x[a][e]);
+                    y[a][e] = fmaf(pv[a], qv[e], y[a][e]);
+                }
+        }
+        if (it + 1 < nit) {   // the other buffer was last read in iteration it - 1
+            float *nb = ring + (size_t)((it + 1) & 1) * 2 * kR * kPk;
+            store_chunk<kK, kPk>(nb, pc_);
+            store_chunk<kK, kPk>(nb + kR * kPk, pp_);
+        }
+        __syncthreads();
+        if (ch != nch - 1) continue;
+        // online update of the 4 rows over this tile's live key columns (j < N, j != i)
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+            const int qi = q0 + ty * 4 + a;
+            float tmx = -INFINITY, tmy = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[a][e] *= scale;
+                y[a][e] *= scale;
+                const int j = k0 + tx * 4 + e;
+                if (j < N && j != qi) {
+                    tmx = fmaxf(tmx, x[a][e]);
+                    tmy = fmaxf(tmy, y[a][e]);
+                }
+            }
+            tmx = warp_max(tmx);   // -inf only if the tile's one live key is the row itself
+            tmy = warp_max(tmy);
+            const float nmx = fmaxf(mx[a], tmx), nmy = fmaxf(my[a], tmy);
+            float sx = 0.f, sw = 0.f, sy = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = k0 + tx * 4 + e;
+                if (j < N && j != qi) {
+                    const float ex = expf(x[a][e] - nmx);
+                    sx += ex;
+                    sw = fmaf(ex, x[a][e] - y[a][e], sw);
+                    sy += expf(y[a][e] - nmy);
+                }
+            }
+            sx = warp_sum(sx);
+            sw = warp_sum(sw);
+            sy = warp_sum(sy);
+            // rescale of the running sums: 0 when they were empty, 1 when the maximum held
+            // (also while no live key has been seen, where both maxima are still -inf)
+            const float cx = mx[a] == nmx ? 1.f : expf(mx[a] - nmx);
+            const float cy = my[a] == nmy ? 1.f : expf(my[a] - nmy);
+            zx[a] = fmaf(zx[a], cx, sx);
+            w[a] = fmaf(w[a], cx, sw);
+            zy[a] = fmaf(zy[a], cy, sy);
+            mx[a] = nmx;
+            my[a] = nmy;
+        }
+    }
+    if (tx == 0)
+#pragma unroll
+        for (int a = 0; a < 4; ++a) st[ty * 4 + a] = RowState{mx[a], zx[a], w[a], my[a], zy[a]};
+
+    // merge the slices in order: rows [slice * 64 / S, (slice + 1) * 64 / S) of this tile
+    if (S > 1) {
+        __syncwarp();
+        cluster_sync_all();
+    } else {
+        __syncthreads();
+    }
+    const int r0 = slice * kQ / S, r1 = (slice + 1) * kQ / S;
+    const int row = r0 + (int)threadIdx.x;
+    if (row < r1 && q0 + row < N) {
+        float Mx = -INFINITY, My = -INFINITY;
+        RowState part[kMaxSlices];
+        for (int s = 0; s < S; ++s) {
+            if (S > 1) {
+                const uint32_t a = mapa_shared(smem_u32(&st[row]), (uint32_t)s);
+                part[s].mx = ld_dsmem_f32(a);
+                part[s].zx = ld_dsmem_f32(a + 4);
+                part[s].w = ld_dsmem_f32(a + 8);
+                part[s].my = ld_dsmem_f32(a + 12);
+                part[s].zy = ld_dsmem_f32(a + 16);
+            } else {
+                part[s] = st[row];
+            }
+            if (part[s].zx > 0.f) {
+                Mx = fmaxf(Mx, part[s].mx);
+                My = fmaxf(My, part[s].my);
+            }
+        }
+        float Zx = 0.f, W = 0.f, Zy = 0.f;
+        for (int s = 0; s < S; ++s) {
+            if (!(part[s].zx > 0.f)) continue;   // a slice without keys
+            const float cx = expf(part[s].mx - Mx), cy = expf(part[s].my - My);
+            Zx = fmaf(part[s].zx, cx, Zx);
+            W = fmaf(part[s].w, cx, W);
+            Zy = fmaf(part[s].zy, cy, Zy);
+        }
+        drift[(size_t)b * N + q0 + row] = Zx > 0.f ? W / Zx - (Mx - My) - (logf(Zx) - logf(Zy)) : 0.f;
+    }
+    if (S > 1) {
+        __syncwarp();
+        cluster_sync_all();   // peers may still read this CTA's states
+    }
+}
+
+}  // namespace
+
+int kl_drift_slices(int B, int N) {
+    const int nqt = (N + kQ - 1) / kQ, nkt = (N + kK - 1) / kK;
+    const long long tiles = (long long)nqt * B;
+    int s = (int)((num_sms() + tiles - 1) / tiles);
+    s = s < 1 ? 1 : (s > kMaxSlices ? kMaxSlices : s);
+    return s > nkt ? nkt : s;
+}
+
+cudaError_t kl_drift(const float *cur, const float *cache, float *drift, int B, int N, int r,
+                     cudaStream_t st) {
+    if (B <= 0 || N <= 0) return cudaSuccess;
+    if (r <= 0 || r % kR != 0 || r > kMaxR || B > 65535) return cudaErrorInvalidValue;
+    static bool configured[64] = {};   // per device: raise the dynamic shared-memory limit once
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        const cudaError_t e = cudaFuncSetAttribute(k_kl_drift, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)kl_smem_bytes(kMaxR));
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = true;
+    }
+    const int S = kl_drift_slices(B, N);
+    const dim3 grid((unsigned)((N + kQ - 1) / kQ), (unsigned)B, (unsigned)S);
+    return launch_kernel(k_kl_drift, grid, dim3(kThreads), kl_smem_bytes(r), st, S, cur, cache, drift, N,
+                         r, S);
+}
+
+}  // namespace dllm
