@@ -109,11 +109,16 @@ int dllm_proxy_score(const void *H, const void *Pt, const float *proxy_cache, fl
  * Identical proxies give exactly 0.  fp32 arithmetic (CUDA cores).
  *   proxy_cur, proxy_cache [B, N, r] fp32 (as produced and kept by dllm_proxy_score);
  *   drift [B, N] fp32 out.
- * Requirements: r % 32 == 0, B <= 65535.  No workspace.  Caller-owned arrays; errors:
- * DLLM_ERR_ARG for null pointers or non-positive sizes, DLLM_ERR_UNSUPPORTED for r.
+ * Workspace: dllm_kl_drift_workspace_bytes(B, N) bytes (per-row states of the key slices,
+ * merged in a fixed order, so identical inputs always give identical results).
+ * Requirements: r % 32 == 0, r <= 256, B <= 65535.  Caller-owned arrays; errors:
+ * DLLM_ERR_ARG for null pointers or non-positive sizes, DLLM_ERR_UNSUPPORTED for r,
+ * DLLM_ERR_WORKSPACE for a missing or short workspace.
  * ------------------------------------------------------------------------- */
+size_t dllm_kl_drift_workspace_bytes(int B, int N);
+
 int dllm_kl_drift(const float *proxy_cur, const float *proxy_cache, float *drift, int B, int N,
-                  int r, void *stream);
+                  int r, void *ws, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
  * Selection.  [SPA] "1. ...": the rows with the lowest proxy similarity (largest

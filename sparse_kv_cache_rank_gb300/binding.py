@@ -41,7 +41,8 @@ _SIGS = {
     "dllm_check_status": (C.c_int, [C.POINTER(C.c_uint), C.c_int]),
     "dllm_proxy_score": (C.c_int, [C.c_void_p] * 5 + [C.c_int] * 5 + [C.c_void_p, C.c_size_t, C.c_void_p]),
     "dllm_proxy_workspace_bytes": (C.c_size_t, [C.c_int] * 5),
-    "dllm_kl_drift": (C.c_int, [C.c_void_p] * 3 + [C.c_int] * 3 + [C.c_void_p]),
+    "dllm_kl_drift_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int]),
+    "dllm_kl_drift": (C.c_int, [C.c_void_p] * 3 + [C.c_int] * 3 + [C.c_void_p, C.c_size_t, C.c_void_p]),
     "dllm_select_topk": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_float,
                                    C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p]),
     "dllm_layer_rho": (C.c_double, [C.c_int] + [C.c_double] * 5),
@@ -212,7 +213,9 @@ def dllm_kl_drift(proxy_cur, proxy_cache, drift=None):
     if drift is None:
         drift = torch.empty((B, N), dtype=torch.float32, device=proxy_cur.device)
     _cuda(proxy_cur, proxy_cache, drift)
-    _check(lib().dllm_kl_drift(_ptr(proxy_cur), _ptr(proxy_cache), _ptr(drift), B, N, r,
+    need = int(lib().dllm_kl_drift_workspace_bytes(B, N))
+    ws = _workspace(need, proxy_cur.device, "kl")
+    _check(lib().dllm_kl_drift(_ptr(proxy_cur), _ptr(proxy_cache), _ptr(drift), B, N, r, _ptr(ws), ws.numel(),
                                _stream(proxy_cur.device)), "dllm_kl_drift")
     return drift
 

@@ -265,15 +265,20 @@ DLLM_EXPORT int dllm_proxy_score(const void *H, const void *Pt, const float *pro
     return DLLM_OK;
 }
 
-DLLM_EXPORT int dllm_kl_drift(const float *proxy_cur, const float *proxy_cache, float *drift,
-                              int B, int N, int r, void *stream) {
+DLLM_EXPORT size_t dllm_kl_drift_workspace_bytes(int B, int N) { return kl_drift_workspace_bytes(B, N); }
+
+DLLM_EXPORT int dllm_kl_drift(const float *proxy_cur, const float *proxy_cache, float *drift, int B,
+                              int N, int r, void *ws, size_t ws_bytes, void *stream) {
     CHECK_ARG(proxy_cur && proxy_cache && drift, "null pointer");
     CHECK_ARG(B > 0 && N > 0 && r > 0, "sizes must be positive (B=%d N=%d r=%d)", B, N, r);
     CHECK_ARG(B <= 65535, "B must be <= 65535");
-    if (r % 32) return fail(DLLM_ERR_UNSUPPORTED, "r must be a multiple of 32 (got %d)", r);
+    if (r % 32 || r > 256) return fail(DLLM_ERR_UNSUPPORTED, "r must be a multiple of 32 up to 256 (got %d)", r);
+    const size_t need = kl_drift_workspace_bytes(B, N);
+    if (!ws || ws_bytes < need)
+        return fail(DLLM_ERR_WORKSPACE, "workspace holds %zu bytes, %zu needed", ws_bytes, need);
     cudaStream_t st = as_stream(stream);
-    Launch t(DLLM_KERNEL_KL_DRIFT, st);
-    CHECK_CUDA(kl_drift(proxy_cur, proxy_cache, drift, B, N, r, st), "KL drift launch");
+    Launch t(DLLM_KERNEL_KL_DRIFT, st, 2);
+    CHECK_CUDA(kl_drift(proxy_cur, proxy_cache, drift, B, N, r, ws, st), "KL drift launch");
     return DLLM_OK;
 }
 

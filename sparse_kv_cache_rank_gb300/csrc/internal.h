@@ -81,9 +81,11 @@ cudaError_t cosine_drift(const float *parts, int nparts, const float *cached, fl
                          float *drift, long rows, int r, cudaStream_t st);
 
 // KL divergence of proxy-attention rows between two steps (kl.cu): drift [B, N] from
-// cur, cache [B, N, r] fp32; r % 32 == 0.  Key slices per query tile (a cluster along z):
+// cur, cache [B, N, r] fp32; r % 32 == 0, r <= 256.  Per-slice row states go to ws
+// (kl_drift_workspace_bytes), merged by a second kernel.
 int kl_drift_slices(int B, int N);
-cudaError_t kl_drift(const float *cur, const float *cache, float *drift, int B, int N, int r,
+size_t kl_drift_workspace_bytes(int B, int N);
+cudaError_t kl_drift(const float *cur, const float *cache, float *drift, int B, int N, int r, void *ws,
                      cudaStream_t st);
 
 template <class T>

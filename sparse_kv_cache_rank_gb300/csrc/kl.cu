@@ -21,9 +21,10 @@
 // r dimensions) stays in shared memory, transposed; the key tiles stream through a two-chunk
 // ring of 32 dimensions each, the next chunk's global loads held in registers while the
 // current chunk is multiplied.  The shared memory (~134 KB at r = 128) keeps one CTA per SM,
-// so the key slices spread over the SMs.  The key slices of one query tile are the CTAs of a
-// thread-block cluster (along z); CTA rank k merges rows [k 64/S, (k+1) 64/S) of every
-// slice's state through distributed shared memory, in slice order.
+// and the number of key slices is chosen so that every CTA runs in one wave.  Each slice
+// writes its per-row (m_x, Z_x, W, m_y, Z_y) to the workspace; a second kernel merges the
+// slices of every row in slice order.  (Merging inside a thread-block cluster instead left
+// some 8-CTA clusters for a second wave.)
 #include <math.h>
 
 #include "internal.h"
@@ -37,7 +38,7 @@ constexpr int kR = 32;           // proxy dimensions per staged chunk
 constexpr int kPq = kQ + 4;      // padded rows of the transposed chunks (16-byte aligned)
 constexpr int kPk = kK + 4;
 constexpr int kThreads = 512;    // 16 x 32 threads, 4 x 4 scores each
-constexpr int kMaxSlices = 8;
+constexpr int kMaxSlices = 32;
 constexpr int kMaxR = 256;
 
 // dynamic shared memory: query tile [2 steps][r][kPq], key ring [2 buffers][2 steps][kR][kPk]
@@ -81,13 +82,12 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    k_kl_drift(const float *__restrict__ cur, const float *__restrict__ cache, float *__restrict__ drift,
-               int N, int r, int S) {
+    k_kl_slices(const float *__restrict__ cur, const float *__restrict__ cache, RowState *__restrict__ part,
+                int B, int N, int r, int S) {
     extern __shared__ __align__(16) float smf[];
     float *qc = smf;                    // [r][kPq] this step's query proxies, transposed
     float *qp = qc + (size_t)r * kPq;   // [r][kPq] the cached ones
     float *ring = qp + (size_t)r * kPq; // [2 buffers][2 steps][kR][kPk]
-    __shared__ RowState st[kQ];
 
     griddep_wait();
     griddep_launch();
@@ -229,79 +229,77 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tx == 0)
 #pragma unroll
-        for (int a = 0; a < 4; ++a) st[ty * 4 + a] = RowState{mx[a], zx[a], w[a], my[a], zy[a]};
+        for (int a = 0; a < 4; ++a) {
+            const int qi = q0 + ty * 4 + a;
+            if (qi < N) part[((size_t)slice * B + b) * N + qi] = RowState{mx[a], zx[a], w[a], my[a], zy[a]};
+        }
+}
 
-    // merge the slices in order: rows [slice * 64 / S, (slice + 1) * 64 / S) of this tile
-    if (S > 1) {
-        __syncwarp();
-        cluster_sync_all();
-    } else {
-        __syncthreads();
-    }
-    const int r0 = slice * kQ / S, r1 = (slice + 1) * kQ / S;
-    const int row = r0 + (int)threadIdx.x;
-    if (row < r1 && q0 + row < N) {
-        float Mx = -INFINITY, My = -INFINITY;
-        RowState part[kMaxSlices];
-        for (int s = 0; s < S; ++s) {
-            if (S > 1) {
-                const uint32_t a = mapa_shared(smem_u32(&st[row]), (uint32_t)s);
-                part[s].mx = ld_dsmem_f32(a);
-                part[s].zx = ld_dsmem_f32(a + 4);
-                part[s].w = ld_dsmem_f32(a + 8);
-                part[s].my = ld_dsmem_f32(a + 12);
-                part[s].zy = ld_dsmem_f32(a + 16);
-            } else {
-                part[s] = st[row];
-            }
-            if (part[s].zx > 0.f) {
-                Mx = fmaxf(Mx, part[s].mx);
-                My = fmaxf(My, part[s].my);
-            }
+// D of every row from its S slice states, merged in slice order.
+__global__ void __launch_bounds__(256)
+    k_kl_merge(const RowState *__restrict__ part, float *__restrict__ drift, long rows, int S) {
+    griddep_wait();
+    griddep_launch();
+    const long t = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= rows) return;
+    float Mx = -INFINITY, My = -INFINITY;
+    for (int s = 0; s < S; ++s) {
+        const RowState p = part[(size_t)s * rows + t];
+        if (p.zx > 0.f) {
+            Mx = fmaxf(Mx, p.mx);
+            My = fmaxf(My, p.my);
         }
-        float Zx = 0.f, W = 0.f, Zy = 0.f;
-        for (int s = 0; s < S; ++s) {
-            if (!(part[s].zx > 0.f)) continue;   // a slice without keys
-            const float cx = expf(part[s].mx - Mx), cy = expf(part[s].my - My);
-            Zx = fmaf(part[s].zx, cx, Zx);
-            W = fmaf(part[s].w, cx, W);
-            Zy = fmaf(part[s].zy, cy, Zy);
-        }
-        drift[(size_t)b * N + q0 + row] = Zx > 0.f ? W / Zx - (Mx - My) - (logf(Zx) - logf(Zy)) : 0.f;
     }
-    if (S > 1) {
-        __syncwarp();
-        cluster_sync_all();   // peers may still read this CTA's states
+    float Zx = 0.f, W = 0.f, Zy = 0.f;
+    for (int s = 0; s < S; ++s) {
+        const RowState p = part[(size_t)s * rows + t];
+        if (!(p.zx > 0.f)) continue;   // a slice without keys for this row
+        const float cx = expf(p.mx - Mx), cy = expf(p.my - My);
+        Zx = fmaf(p.zx, cx, Zx);
+        W = fmaf(p.w, cx, W);
+        Zy = fmaf(p.zy, cy, Zy);
     }
+    drift[t] = Zx > 0.f ? W / Zx - (Mx - My) - (logf(Zx) - logf(Zy)) : 0.f;
 }
 
 }  // namespace
 
+// Key slices per query tile: as many as keep every CTA (one per SM) in one wave.
 int kl_drift_slices(int B, int N) {
     const int nqt = (N + kQ - 1) / kQ, nkt = (N + kK - 1) / kK;
     const long long tiles = (long long)nqt * B;
-    int s = (int)((num_sms() + tiles - 1) / tiles);
+    int s = (int)(num_sms() / tiles);
     s = s < 1 ? 1 : (s > kMaxSlices ? kMaxSlices : s);
     return s > nkt ? nkt : s;
 }
 
-cudaError_t kl_drift(const float *cur, const float *cache, float *drift, int B, int N, int r,
+size_t kl_drift_workspace_bytes(int B, int N) {
+    if (B <= 0 || N <= 0) return 0;
+    return (size_t)kl_drift_slices(B, N) * B * N * sizeof(RowState) + 256;
+}
+
+cudaError_t kl_drift(const float *cur, const float *cache, float *drift, int B, int N, int r, void *ws,
                      cudaStream_t st) {
     if (B <= 0 || N <= 0) return cudaSuccess;
-    if (r <= 0 || r % kR != 0 || r > kMaxR || B > 65535) return cudaErrorInvalidValue;
+    if (r <= 0 || r % kR != 0 || r > kMaxR || B > 65535 || !ws) return cudaErrorInvalidValue;
     static bool configured[64] = {};   // per device: raise the dynamic shared-memory limit once
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        const cudaError_t e = cudaFuncSetAttribute(k_kl_drift, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        const cudaError_t e = cudaFuncSetAttribute(k_kl_slices, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    (int)kl_smem_bytes(kMaxR));
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
     const int S = kl_drift_slices(B, N);
+    RowState *part = reinterpret_cast<RowState *>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255));
     const dim3 grid((unsigned)((N + kQ - 1) / kQ), (unsigned)B, (unsigned)S);
-    return launch_kernel(k_kl_drift, grid, dim3(kThreads), kl_smem_bytes(r), st, S, cur, cache, drift, N,
-                         r, S);
+    cudaError_t e = launch_kernel(k_kl_slices, grid, dim3(kThreads), kl_smem_bytes(r), st, 1, cur, cache, part,
+                                  B, N, r, S);
+    if (e != cudaSuccess) return e;
+    const long rows = (long)B * N;
+    return launch_kernel(k_kl_merge, dim3((unsigned)((rows + 255) / 256)), dim3(256), 0, st, 1,
+                         (const RowState *)part, drift, rows, S);
 }
 
 }  // namespace dllm
