@@ -15,9 +15,10 @@
 // Z_x == Z_y and D = 0 exactly.
 //
 // fp32 on the CUDA cores: the drift is made of score differences that bf16 tensor-core
-// scores would swamp.  One CTA (16 warps) = 64 query rows x one slice of the 128-row key
-// tiles; thread (ty, tx) owns rows 4 ty .. 4 ty + 3 and key columns 4 tx .. 4 tx + 3 of both
-// score tiles, so one warp holds four whole rows of a tile.  The query tile (both steps, all
+// scores would swamp.  One CTA (8 warps) = 64 query rows x one slice of the 128-row key
+// tiles; thread (ty, tx) owns rows 8 ty .. 8 ty + 7 and key columns 4 tx .. 4 tx + 3 of both
+// score tiles (64 FMA per 6 shared-memory loads), so one warp holds eight whole rows of a
+// tile.  The query tile (both steps, all
 // r dimensions) stays in shared memory, transposed; the key tiles stream through a two-chunk
 // ring of 32 dimensions each, the next chunk's global loads held in registers while the
 // current chunk is multiplied.  The shared memory (~134 KB at r = 128) keeps one CTA per SM,
@@ -37,7 +38,9 @@ constexpr int kK = 128;          // key rows per tile
 constexpr int kR = 32;           // proxy dimensions per staged chunk
 constexpr int kPq = kQ + 4;      // padded rows of the transposed chunks (16-byte aligned)
 constexpr int kPk = kK + 4;
-constexpr int kThreads = 512;    // 16 x 32 threads, 4 x 4 scores each
+constexpr int kThreads = 256;    // 8 x 32 threads, 8 x 4 scores each
+constexpr int kWarps = kThreads / 32;
+constexpr int kRows = kQ / kWarps;   // query rows per thread (and per warp)
 constexpr int kMaxSlices = 32;
 constexpr int kMaxR = 256;
 
@@ -50,24 +53,24 @@ struct RowState {
     float mx, zx, w, my, zy;
 };
 
-// Chunk [row0, row0 + ROWS) x [c0, c0 + 32) of a [N, r] matrix as ROWS / 16 values per
-// thread (dimension = lane, rows warp + 16 i; rows past N are zero), and its transposed
+// Chunk [row0, row0 + ROWS) x [c0, c0 + 32) of a [N, r] matrix as ROWS / kWarps values per
+// thread (dimension = lane, rows warp + kWarps i; rows past N are zero), and its transposed
 // store dst[c * P + row].
 template <int ROWS>
-__device__ __forceinline__ void load_chunk(float (&v)[ROWS / 16], const float *__restrict__ src, int row0,
+__device__ __forceinline__ void load_chunk(float (&v)[ROWS / kWarps], const float *__restrict__ src, int row0,
                                            int N, int r, int c0) {
     const int c = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
-    for (int i = 0; i < ROWS / 16; ++i) {
-        const int row = row0 + w + 16 * i;
+    for (int i = 0; i < ROWS / kWarps; ++i) {
+        const int row = row0 + w + kWarps * i;
         v[i] = row < N ? src[(size_t)row * r + c0 + c] : 0.f;
     }
 }
 template <int ROWS, int P>
-__device__ __forceinline__ void store_chunk(float *dst, const float (&v)[ROWS / 16]) {
+__device__ __forceinline__ void store_chunk(float *dst, const float (&v)[ROWS / kWarps]) {
     const int c = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
-    for (int i = 0; i < ROWS / 16; ++i) dst[c * P + w + 16 * i] = v[i];
+    for (int i = 0; i < ROWS / kWarps; ++i) dst[c * P + w + kWarps * i] = v[i];
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -106,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // the query tile (four chunks' loads in flight before they are stored) and the first key chunk
     for (int c0 = 0; c0 < r; c0 += 4 * kR) {
-        float v[4][kQ / 16];
+        float v[4][kQ / kWarps];
         const int n = (r - c0) / kR < 4 ? (r - c0) / kR : 4;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 4; ++k)
             if (k < n) store_chunk<kQ, kPq>(qp + (size_t)(c0 + k * kR) * kPq, v[k]);
     }
-    float pc_[kK / 16], pp_[kK / 16];
+    float pc_[kK / kWarps], pp_[kK / kWarps];
     if (nit > 0) {
         load_chunk<kK>(pc_, cb, kt0 * kK, N, r, 0);
         load_chunk<kK>(pp_, pb, kt0 * kK, N, r, 0);
@@ -130,22 +133,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
 
-    float mx[4], zx[4], w[4], my[4], zy[4];
+    float mx[kRows], zx[kRows], w[kRows], my[kRows], zy[kRows];
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
+    for (int a = 0; a < kRows; ++a) {
         mx[a] = -INFINITY;
         my[a] = -INFINITY;
         zx[a] = 0.f;
         zy[a] = 0.f;
         w[a] = 0.f;
     }
-    float x[4][4], y[4][4];
+    float x[kRows][4], y[kRows][4];
     for (int it = 0; it < nit; ++it) {
         const int kt = kt0 + it / nch, ch = it % nch;
         const int k0 = kt * kK;
         if (ch == 0) {
 #pragma unroll
-            for (int a = 0; a < 4; ++a)
+            for (int a = 0; a < kRows; ++a)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     x[a][e] = 0.f;
@@ -163,14 +166,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float *qpb = qp + (size_t)ch * kR * kPq;
 #pragma unroll 8
         for (int c = 0; c < kR; ++c) {
-            const float4 ac = *reinterpret_cast<const float4 *>(qcb + c * kPq + ty * 4);
-            const float4 ap = *reinterpret_cast<const float4 *>(qpb + c * kPq + ty * 4);
+            const float4 ac0 = *reinterpret_cast<const float4 *>(qcb + c * kPq + ty * kRows);
+            const float4 ac1 = *reinterpret_cast<const float4 *>(qcb + c * kPq + ty * kRows + 4);
+            const float4 ap0 = *reinterpret_cast<const float4 *>(qpb + c * kPq + ty * kRows);
+            const float4 ap1 = *reinterpret_cast<const float4 *>(qpb + c * kPq + ty * kRows + 4);
             const float4 bc = *reinterpret_cast<const float4 *>(kcb + c * kPk + tx * 4);
             const float4 bp = *reinterpret_cast<const float4 *>(kpb + c * kPk + tx * 4);
-            const float av[4] = {ac.x, ac.y, ac.z, ac.w}, pv[4] = {ap.x, ap.y, ap.z, ap.w};
+            const float av[kRows] = {ac0.x, ac0.y, ac0.z, ac0.w, ac1.x, ac1.y, ac1.z, ac1.w};
+            const float pv[kRows] = {ap0.x, ap0.y, ap0.z, ap0.w, ap1.x, ap1.y, ap1.z, ap1.w};
             const float bv[4] = {bc.x, bc.y, bc.z, bc.w}, qv[4] = {bp.x, bp.y, bp.z, bp.w};
 #pragma unroll
-            for (int a = 0; a < 4; ++a)
+            for (int a = 0; a < kRows; ++a)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     x[a][e] = fmaf(av[a], bv[e], x[a][e]);
@@ -184,10 +190,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
         if (ch != nch - 1) continue;
-        // online update of the 4 rows over this tile's live key columns (j < N, j != i)
+        // online update of the thread's rows over this tile's live key columns (j < N, j != i)
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const int qi = q0 + ty * 4 + a;
+        for (int a = 0; a < kRows; ++a) {
+            const int qi = q0 + ty * kRows + a;
             float tmx = -INFINITY, tmy = -INFINITY;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -229,8 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (tx == 0)
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-            const int qi = q0 + ty * 4 + a;
+        for (int a = 0; a < kRows; ++a) {
+            const int qi = q0 + ty * kRows + a;
             if (qi < N) part[((size_t)slice * B + b) * N + qi] = RowState{mx[a], zx[a], w[a], my[a], zy[a]};
         }
 }
