@@ -402,7 +402,8 @@ def native(args):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
-    result["next_rows"] = {"kl_drift": kl_drift_measure(wl, args.steps, args.warmup)}
+    result["next_rows"] = {"kl_drift": kl_drift_measure(wl, args.steps, args.warmup),
+                           "confidence_extrapolation": ce_measure(dev, args.steps, args.warmup)}
     if not args.no_stack or not args.no_configs:
         del wl
         torch.cuda.empty_cache()
@@ -507,6 +508,36 @@ def layer_point(sh, dev, steps, warmup, seed=77):
     return res
 
 
+GRAPH_TIMING = ("a CUDA graph of back-to-back calls (the library's launches, captured once), "
+                "CUDA events around its replays, outside the timed region")
+
+
+def _graph_time(call, steps, warmup, dev):
+    """Seconds per call: `steps` calls captured in a CUDA graph, replayed after warm-up, so
+    the host's per-call cost does not hide the device time of small kernels."""
+    import torch
+    for _ in range(max(warmup, 3)):
+        call()
+    torch.cuda.synchronize(dev)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for _ in range(steps):
+            call()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(3):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / 1e3 / (3 * steps)
+
+
 # fp32 FMA rate of the GPU: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz (maximum SM clock)
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
@@ -519,24 +550,39 @@ def kl_drift_measure(wl, steps, warmup):
     B_ = wl.B_
     Bn, N, r = wl.cur.shape
     out = torch.empty((Bn, N), dtype=torch.float32, device=wl.dev)
-    for _ in range(max(warmup, 3)):
-        B_.dllm_kl_drift(wl.cur, wl.pc, out)
-    torch.cuda.synchronize(wl.dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        B_.dllm_kl_drift(wl.cur, wl.pc, out)
-    e1.record()
-    torch.cuda.synchronize(wl.dev)
-    s = e0.elapsed_time(e1) / 1e3 / steps
+    s = _graph_time(lambda: B_.dllm_kl_drift(wl.cur, wl.pc, out), steps, warmup, wl.dev)
     flops = 2 * 2 * Bn * N * N * r          # two score products of 2 N^2 r FLOP each
     achieved = flops / s / 1e12
     return {"workload": f"B={Bn} N={N} r={r}", "us_per_launch": s * 1e6, "flop": flops,
             "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_PEAK_TFLOPS,
                          "unit": "TFLOP/s", "frac": achieved / FP32_PEAK_TFLOPS,
                          "peak_source": "fp32 FMA lanes x maximum SM clock"},
-            "timing": "CUDA events around back-to-back launches, outside the timed region"}
+            "timing": GRAPH_TIMING}
+
+
+def ce_measure(dev, steps, warmup):
+    """Confidence extrapolation step (Kalman predict + update of every token's confidence
+    state and the early-commit decision) on the LLaDA block (B = 1, M = 32) and on 64
+    sequences x 1024 positions; CUDA events around back-to-back launches."""
+    import torch
+    from sparse_kv_cache_rank_gb300 import binding as B_
+    out = {}
+    for name, (Bn, M) in {"block": (1, 32), "wide": (64, 1024)}.items():
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(7)
+        conf = torch.rand((Bn, M), generator=gen, device=dev)
+        state = torch.zeros((Bn, M, 5), device=dev)
+        ones = torch.ones((Bn, M), dtype=torch.uint8, device=dev)
+        committed = (torch.rand((Bn, M), generator=gen, device=dev) < 0.5).to(torch.uint8)
+        early = torch.empty((Bn, M), dtype=torch.uint8, device=dev)
+        B_.dllm_ce_step(conf, torch.zeros_like(ones), ones, committed, state, early)
+        s = _graph_time(lambda: B_.dllm_ce_step(conf, ones, ones, committed, state, early), steps, warmup, dev)
+        nbytes = Bn * M * (4 + 3 + 2 * 20 + 1)   # conf, flags, state in and out, decision
+        out[name] = {"workload": f"B={Bn} M={M}", "us_per_launch": s * 1e6, "bytes": nbytes,
+                     "gb_per_s": nbytes / s / 1e9,
+                     "note": "latency-bound at these sizes (one CTA per sequence, O(M) work)",
+                     "timing": GRAPH_TIMING}
+    return out
 
 
 def config_points(dev, full_sweep):

@@ -121,6 +121,29 @@ int dllm_kl_drift(const float *proxy_cur, const float *proxy_cache, float *drift
                   int r, void *ws, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * [TSPD] "2. Confidence Extrapolation (CE)": the top-1 confidence of every token is a
+ * noisy observation of a latent (level, velocity) state, filtered like a Kalman filter;
+ * near-future confidence is forecast with its uncertainty and a token is committed early
+ * when a conservative lower bound of the forecast exceeds a minimum threshold, within a
+ * look-ahead horizon bounded by the left context already fixed.  The page gives no
+ * equations or constants; this call takes the textbook constant-velocity filter:
+ *   seen[b,m] != 0:  predict l- = l + v, P- = F P F^T + diag(q_l, q_v) (F = [[1,1],[0,1]]),
+ *                    update with c = conf[b,m]: S = P-00 + R, K = (P-00, P-10)/S,
+ *                    l = l- + K0 (c - l-), v = v + K1 (c - l-), P = (I - K [1 0]) P-;
+ *   seen[b,m] == 0:  l = c, v = 0, P = diag(R, p_v0) (first observation);
+ *   H = min(h_max, #{m' < m : committed[b,m'] != 0});
+ *   early[b,m] = undecided[b,m] && exists h in 1..H with
+ *                l + h v - z sqrt(P00 + 2h P01 + h^2 P11) >= c_min.
+ *   conf [B, M] fp32 (dllm_commit_entropy's conf); seen, undecided, committed [B, M] uint8;
+ *   state [B, M, 5] fp32 (l, v, P00, P01, P11), read when seen and written for every
+ *   position; early [B, M] uint8 out.
+ * Requirements: M <= 1024, R > 0, noise levels >= 0, 0 <= h_max <= 1024.  No workspace.
+ * ------------------------------------------------------------------------- */
+int dllm_ce_step(const float *conf, const uint8_t *seen, const uint8_t *undecided,
+                 const uint8_t *committed, float *state, uint8_t *early, int B, int M, float q_l,
+                 float q_v, float R, float p_v0, float z, int h_max, float c_min, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Selection.  [SPA] "1. ...": the rows with the lowest proxy similarity (largest
  * drift) are recomputed, [SPA] "2. Adaptive budget allocation": at most k of them
  * per layer; [EC] step 3: the current masked tokens and the k most recently decoded
@@ -346,6 +369,7 @@ int dllm_gemm_bf16(const void *X, const void *W, float *out, int M, int N_out, i
 #define DLLM_KERNEL_VOCAB 11
 #define DLLM_KERNEL_GEMM 12
 #define DLLM_KERNEL_KL_DRIFT 13
+#define DLLM_KERNEL_CE 14
 
 /* Launch mode of the library's kernels: with enable != 0 (the default) consecutive
  * kernels on a stream use programmatic dependent launch (a kernel's prologue and its

@@ -43,6 +43,7 @@ _SIGS = {
     "dllm_proxy_workspace_bytes": (C.c_size_t, [C.c_int] * 5),
     "dllm_kl_drift_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int]),
     "dllm_kl_drift": (C.c_int, [C.c_void_p] * 3 + [C.c_int] * 3 + [C.c_void_p, C.c_size_t, C.c_void_p]),
+    "dllm_ce_step": (C.c_int, [C.c_void_p] * 6 + [C.c_int] * 2 + [C.c_float] * 5 + [C.c_int, C.c_float, C.c_void_p]),
     "dllm_select_topk": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_float,
                                    C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p]),
     "dllm_layer_rho": (C.c_double, [C.c_int] + [C.c_double] * 5),
@@ -159,7 +160,7 @@ def check_status(reset: bool = True) -> int:
 # --------------------------------------------------------------------------- measurement
 KERNELS = {"proxy_gemm": 1, "cosine": 2, "select": 3, "gather": 4, "qkv": 5, "attention": 6,
            "oproj": 7, "rmsnorm2": 8, "gateup": 9, "down": 10, "vocab": 11, "gemm": 12,
-           "kl_drift": 13}
+           "kl_drift": 13, "ce": 14}
 
 
 def dllm_timer_start(kernel: str, max_launches: int) -> None:
@@ -218,6 +219,25 @@ def dllm_kl_drift(proxy_cur, proxy_cache, drift=None):
     _check(lib().dllm_kl_drift(_ptr(proxy_cur), _ptr(proxy_cache), _ptr(drift), B, N, r, _ptr(ws), ws.numel(),
                                _stream(proxy_cur.device)), "dllm_kl_drift")
     return drift
+
+
+def dllm_ce_step(conf, seen, undecided, committed, state, early=None, q_l=1e-3, q_v=1e-3, R=1e-2,
+                 p_v0=1e-2, z=1.645, h_max=4, c_min=0.9):
+    """Confidence extrapolation step: conf [B,M] f32, seen/undecided/committed [B,M] uint8,
+    state [B,M,5] f32 (updated in place) -> early [B,M] uint8."""
+    B, M = conf.shape
+    if state.shape != (B, M, 5) or state.dtype != torch.float32 or conf.dtype != torch.float32:
+        raise DllmError("conf [B, M] and state [B, M, 5] must be float32")
+    for t in (seen, undecided, committed):
+        if t.shape != (B, M) or t.dtype != torch.uint8:
+            raise DllmError("seen, undecided, committed must be [B, M] uint8")
+    if early is None:
+        early = torch.empty((B, M), dtype=torch.uint8, device=conf.device)
+    _cuda(conf, seen, undecided, committed, state, early)
+    _check(lib().dllm_ce_step(_ptr(conf), _ptr(seen), _ptr(undecided), _ptr(committed), _ptr(state),
+                              _ptr(early), B, M, float(q_l), float(q_v), float(R), float(p_v0), float(z),
+                              int(h_max), float(c_min), _stream(conf.device)), "dllm_ce_step")
+    return early
 
 
 def build_proxy_matrix(w_v: torch.Tensor, gamma1: torch.Tensor, r: int, method: str = "svd",

@@ -282,6 +282,22 @@ DLLM_EXPORT int dllm_kl_drift(const float *proxy_cur, const float *proxy_cache, 
     return DLLM_OK;
 }
 
+DLLM_EXPORT int dllm_ce_step(const float *conf, const uint8_t *seen, const uint8_t *undecided,
+                             const uint8_t *committed, float *state, uint8_t *early, int B, int M,
+                             float q_l, float q_v, float R, float p_v0, float z, int h_max, float c_min,
+                             void *stream) {
+    CHECK_ARG(conf && seen && undecided && committed && state && early, "null pointer");
+    CHECK_ARG(B > 0 && M > 0, "sizes must be positive (B=%d M=%d)", B, M);
+    CHECK_ARG(M <= 1024, "M must be <= 1024 (got %d)", M);
+    CHECK_ARG(q_l >= 0.f && q_v >= 0.f && R > 0.f && p_v0 >= 0.f && z >= 0.f, "noise levels must be >= 0, R > 0");
+    CHECK_ARG(h_max >= 0 && h_max <= 1024, "h_max must be in [0, 1024]");
+    cudaStream_t st = as_stream(stream);
+    Launch t(DLLM_KERNEL_CE, st);
+    const CEParams p{q_l, q_v, R, p_v0, z, c_min, h_max};
+    CHECK_CUDA(ce_step(conf, seen, undecided, committed, state, early, B, M, p, st), "CE step launch");
+    return DLLM_OK;
+}
+
 // ------------------------------------------------------------------ selection
 DLLM_EXPORT int dllm_select_topk(const float *drift, const int32_t *forced, int F, int k,
                                  float min_drift, int32_t *idx, int32_t *count, int B, int N,
@@ -631,7 +647,7 @@ DLLM_EXPORT int dllm_lmhead_commit(const void *X, const void *W_lm, const uint8_
 
 // ------------------------------------------------------------------ measurement support
 DLLM_EXPORT int dllm_timer_start(int kernel_id, int max_launches) {
-    CHECK_ARG(kernel_id >= DLLM_KERNEL_PROXY_GEMM && kernel_id <= DLLM_KERNEL_KL_DRIFT, "unknown kernel id %d", kernel_id);
+    CHECK_ARG(kernel_id >= DLLM_KERNEL_PROXY_GEMM && kernel_id <= DLLM_KERNEL_CE, "unknown kernel id %d", kernel_id);
     CHECK_ARG(max_launches > 0 && max_launches <= 1 << 16, "max_launches must be in [1, 65536]");
     std::lock_guard<std::mutex> lock(g_timer.mu);
     CHECK_ARG(g_timer.armed == 0, "a timer is already armed");

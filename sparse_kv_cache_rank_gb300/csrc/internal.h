@@ -80,6 +80,16 @@ cudaError_t rmsnorm_rows(const float *h1, int M, int d, const T *gamma, float ep
 cudaError_t cosine_drift(const float *parts, int nparts, const float *cached, float *cur,
                          float *drift, long rows, int r, cudaStream_t st);
 
+// Confidence extrapolation (ce.cu): one predict + update of every token's (level,
+// velocity) Kalman state and the early-commit decision; M <= 1024 positions per sequence.
+struct CEParams {
+    float q_l, q_v, R, p_v0, z, c_min;
+    int h_max;
+};
+cudaError_t ce_step(const float *conf, const uint8_t *seen, const uint8_t *undecided,
+                    const uint8_t *committed, float *state, uint8_t *early, int B, int M,
+                    const CEParams &p, cudaStream_t st);
+
 // KL divergence of proxy-attention rows between two steps (kl.cu): drift [B, N] from
 // cur, cache [B, N, r] fp32; r % 32 == 0, r <= 256.  Per-slice row states go to ws
 // (kl_drift_workspace_bytes), merged by a second kernel.
