@@ -403,7 +403,8 @@ def native(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     result["next_rows"] = {"kl_drift": kl_drift_measure(wl, args.steps, args.warmup),
-                           "confidence_extrapolation": ce_measure(dev, args.steps, args.warmup)}
+                           "confidence_extrapolation": ce_measure(dev, args.steps, args.warmup),
+                           "drift_aware_commit": polestar_measure(dev, args.steps, args.warmup)}
     if not args.no_stack or not args.no_configs:
         del wl
         torch.cuda.empty_cache()
@@ -581,6 +582,33 @@ def ce_measure(dev, steps, warmup):
         out[name] = {"workload": f"B={Bn} M={M}", "us_per_launch": s * 1e6, "bytes": nbytes,
                      "gb_per_s": nbytes / s / 1e9,
                      "note": "latency-bound at these sizes (one CTA per sequence, O(M) work)",
+                     "timing": GRAPH_TIMING}
+    return out
+
+
+def polestar_measure(dev, steps, warmup):
+    """Drift-aware commit (drift delta against each token's drift history, dynamic threshold,
+    suffix rule) over the 256 generated positions of the LLaDA stack (B = 1) and over
+    64 x 1024 tokens."""
+    import torch
+    from sparse_kv_cache_rank_gb300 import binding as B_
+    out = {}
+    for name, (Bn, M) in {"generation": (1, 256), "wide": (64, 1024)}.items():
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(11)
+        drift = torch.rand((Bn, M), generator=gen, device=dev)
+        conf = torch.rand((Bn, M), generator=gen, device=dev)
+        ones = torch.ones((Bn, M), dtype=torch.uint8, device=dev)
+        suffix = torch.zeros_like(ones)
+        suffix[:, 32:] = 1
+        sel = (torch.rand((Bn, M), generator=gen, device=dev) < 0.3).to(torch.uint8)
+        hist = torch.zeros((Bn, M, 2), device=dev)
+        commit = torch.empty_like(ones)
+        s = _graph_time(lambda: B_.dllm_polestar_commit(drift, conf, ones, suffix, sel, hist, commit),
+                        steps, warmup, dev)
+        nbytes = Bn * M * (4 + 4 + 3 + 2 * 8 + 1)
+        out[name] = {"workload": f"B={Bn} M={M}", "us_per_launch": s * 1e6, "bytes": nbytes,
+                     "gb_per_s": nbytes / s / 1e9, "note": "elementwise, latency-bound at these sizes",
                      "timing": GRAPH_TIMING}
     return out
 

@@ -144,6 +144,25 @@ int dllm_ce_step(const float *conf, const uint8_t *seen, const uint8_t *undecide
                  float q_v, float R, float p_v0, float z, int h_max, float c_min, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * [POL] "2. B. Polestar-Commit": a token of the current block is committed when its drift
+ * delta (its drift minus the historical mean of its drift) exceeds the confidence-
+ * conditioned threshold alpha (tau_s - c)^2; suffix tokens are committed when the drift
+ * score selects them and their confidence reaches tau_s.  The page gives no alpha, tau_s or
+ * history; this call takes the mean of the token's earlier drifts:
+ *   current block (suffix == 0): commit = undecided && count >= 1 &&
+ *                                 drift - sum / count > alpha (tau_s - conf)^2
+ *   suffix (suffix != 0):        commit = undecided && selected && conf >= tau_s
+ *   then history = (sum + drift, count + 1) for every token.
+ *   drift, conf [B, M] fp32 (the step's drift score and top-1 confidence);
+ *   undecided, suffix, selected [B, M] uint8; history [B, M, 2] fp32 (sum, count; zero to
+ *   start), 8-byte aligned, updated in place; commit [B, M] uint8 out.
+ * No workspace.
+ * ------------------------------------------------------------------------- */
+int dllm_polestar_commit(const float *drift, const float *conf, const uint8_t *undecided,
+                         const uint8_t *suffix, const uint8_t *selected, float *history, uint8_t *commit,
+                         int B, int M, float alpha, float tau_s, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Selection.  [SPA] "1. ...": the rows with the lowest proxy similarity (largest
  * drift) are recomputed, [SPA] "2. Adaptive budget allocation": at most k of them
  * per layer; [EC] step 3: the current masked tokens and the k most recently decoded
@@ -370,6 +389,7 @@ int dllm_gemm_bf16(const void *X, const void *W, float *out, int M, int N_out, i
 #define DLLM_KERNEL_GEMM 12
 #define DLLM_KERNEL_KL_DRIFT 13
 #define DLLM_KERNEL_CE 14
+#define DLLM_KERNEL_POLESTAR 15
 
 /* Launch mode of the library's kernels: with enable != 0 (the default) consecutive
  * kernels on a stream use programmatic dependent launch (a kernel's prologue and its

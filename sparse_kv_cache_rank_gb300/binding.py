@@ -44,6 +44,7 @@ _SIGS = {
     "dllm_kl_drift_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int]),
     "dllm_kl_drift": (C.c_int, [C.c_void_p] * 3 + [C.c_int] * 3 + [C.c_void_p, C.c_size_t, C.c_void_p]),
     "dllm_ce_step": (C.c_int, [C.c_void_p] * 6 + [C.c_int] * 2 + [C.c_float] * 5 + [C.c_int, C.c_float, C.c_void_p]),
+    "dllm_polestar_commit": (C.c_int, [C.c_void_p] * 7 + [C.c_int] * 2 + [C.c_float] * 2 + [C.c_void_p]),
     "dllm_select_topk": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_float,
                                    C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p]),
     "dllm_layer_rho": (C.c_double, [C.c_int] + [C.c_double] * 5),
@@ -160,7 +161,7 @@ def check_status(reset: bool = True) -> int:
 # --------------------------------------------------------------------------- measurement
 KERNELS = {"proxy_gemm": 1, "cosine": 2, "select": 3, "gather": 4, "qkv": 5, "attention": 6,
            "oproj": 7, "rmsnorm2": 8, "gateup": 9, "down": 10, "vocab": 11, "gemm": 12,
-           "kl_drift": 13, "ce": 14}
+           "kl_drift": 13, "ce": 14, "polestar": 15}
 
 
 def dllm_timer_start(kernel: str, max_launches: int) -> None:
@@ -238,6 +239,24 @@ def dllm_ce_step(conf, seen, undecided, committed, state, early=None, q_l=1e-3, 
                               _ptr(early), B, M, float(q_l), float(q_v), float(R), float(p_v0), float(z),
                               int(h_max), float(c_min), _stream(conf.device)), "dllm_ce_step")
     return early
+
+
+def dllm_polestar_commit(drift, conf, undecided, suffix, selected, history, commit=None, alpha=1.0, tau_s=0.9):
+    """Drift-aware commit: drift, conf [B,M] f32; undecided, suffix, selected [B,M] uint8;
+    history [B,M,2] f32 (updated in place) -> commit [B,M] uint8."""
+    B, M = drift.shape
+    if conf.shape != (B, M) or history.shape != (B, M, 2) or history.dtype != torch.float32:
+        raise DllmError("conf [B, M] f32 and history [B, M, 2] f32 expected")
+    for t in (undecided, suffix, selected):
+        if t.shape != (B, M) or t.dtype != torch.uint8:
+            raise DllmError("undecided, suffix, selected must be [B, M] uint8")
+    if commit is None:
+        commit = torch.empty((B, M), dtype=torch.uint8, device=drift.device)
+    _cuda(drift, conf, undecided, suffix, selected, history, commit)
+    _check(lib().dllm_polestar_commit(_ptr(drift), _ptr(conf), _ptr(undecided), _ptr(suffix), _ptr(selected),
+                                      _ptr(history), _ptr(commit), B, M, float(alpha), float(tau_s),
+                                      _stream(drift.device)), "dllm_polestar_commit")
+    return commit
 
 
 def build_proxy_matrix(w_v: torch.Tensor, gamma1: torch.Tensor, r: int, method: str = "svd",

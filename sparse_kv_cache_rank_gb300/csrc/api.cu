@@ -48,6 +48,7 @@ int cuda_fail(cudaError_t e, const char *what) {
     } while (0)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned8(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -295,6 +296,21 @@ DLLM_EXPORT int dllm_ce_step(const float *conf, const uint8_t *seen, const uint8
     Launch t(DLLM_KERNEL_CE, st);
     const CEParams p{q_l, q_v, R, p_v0, z, c_min, h_max};
     CHECK_CUDA(ce_step(conf, seen, undecided, committed, state, early, B, M, p, st), "CE step launch");
+    return DLLM_OK;
+}
+
+DLLM_EXPORT int dllm_polestar_commit(const float *drift, const float *conf, const uint8_t *undecided,
+                                     const uint8_t *suffix, const uint8_t *selected, float *history,
+                                     uint8_t *commit, int B, int M, float alpha, float tau_s, void *stream) {
+    CHECK_ARG(drift && conf && undecided && suffix && selected && history && commit, "null pointer");
+    CHECK_ARG(B > 0 && M > 0, "sizes must be positive (B=%d M=%d)", B, M);
+    CHECK_ARG(aligned8(history), "history must be 8-byte aligned");
+    CHECK_ARG(alpha >= 0.f, "alpha must be >= 0");
+    cudaStream_t st = as_stream(stream);
+    Launch t(DLLM_KERNEL_POLESTAR, st);
+    CHECK_CUDA(polestar_commit(drift, conf, undecided, suffix, selected, history, commit, (long)B * M, alpha,
+                               tau_s, st),
+               "drift-aware commit launch");
     return DLLM_OK;
 }
 
@@ -647,7 +663,7 @@ DLLM_EXPORT int dllm_lmhead_commit(const void *X, const void *W_lm, const uint8_
 
 // ------------------------------------------------------------------ measurement support
 DLLM_EXPORT int dllm_timer_start(int kernel_id, int max_launches) {
-    CHECK_ARG(kernel_id >= DLLM_KERNEL_PROXY_GEMM && kernel_id <= DLLM_KERNEL_CE, "unknown kernel id %d", kernel_id);
+    CHECK_ARG(kernel_id >= DLLM_KERNEL_PROXY_GEMM && kernel_id <= DLLM_KERNEL_POLESTAR, "unknown kernel id %d", kernel_id);
     CHECK_ARG(max_launches > 0 && max_launches <= 1 << 16, "max_launches must be in [1, 65536]");
     std::lock_guard<std::mutex> lock(g_timer.mu);
     CHECK_ARG(g_timer.armed == 0, "a timer is already armed");

@@ -90,6 +90,11 @@ cudaError_t ce_step(const float *conf, const uint8_t *seen, const uint8_t *undec
                     const uint8_t *committed, float *state, uint8_t *early, int B, int M,
                     const CEParams &p, cudaStream_t st);
 
+// Drift-aware commit (polestar.cu): n = B * M tokens, history [n][2] (sum, count) fp32.
+cudaError_t polestar_commit(const float *drift, const float *conf, const uint8_t *undecided,
+                            const uint8_t *suffix, const uint8_t *selected, float *history, uint8_t *commit,
+                            long n, float alpha, float tau_s, cudaStream_t st);
+
 // KL divergence of proxy-attention rows between two steps (kl.cu): drift [B, N] from
 // cur, cache [B, N, r] fp32; r % 32 == 0, r <= 256.  Per-slice row states go to ws
 // (kl_drift_workspace_bytes), merged by a second kernel.
