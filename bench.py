@@ -404,7 +404,8 @@ def native(args):
         result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
     result["next_rows"] = {"kl_drift": kl_drift_measure(wl, args.steps, args.warmup),
                            "confidence_extrapolation": ce_measure(dev, args.steps, args.warmup),
-                           "drift_aware_commit": polestar_measure(dev, args.steps, args.warmup)}
+                           "drift_aware_commit": polestar_measure(dev, args.steps, args.warmup),
+                           "cluster_proxy": cluster_measure(dev, args.steps, args.warmup)}
     if not args.no_stack or not args.no_configs:
         del wl
         torch.cuda.empty_cache()
@@ -611,6 +612,43 @@ def polestar_measure(dev, steps, warmup):
                      "gb_per_s": nbytes / s / 1e9, "note": "elementwise, latency-bound at these sizes",
                      "timing": GRAPH_TIMING}
     return out
+
+
+def cluster_measure(dev, steps, warmup):
+    """Cluster-granular proxy over a local window of the LLaDA stack (prefix, current and
+    suffix blocks: 96 rows x d = 4096 hidden states, K = 16 clusters, 4 Lloyd rounds): k-means,
+    residuals, NVFP4 quantisation of the residuals, selection of the 4 most drifted
+    clusters' rows."""
+    import torch
+    from sparse_kv_cache_rank_gb300 import binding as B_
+    Bn, N, D, K = 1, 96, 4096, 16
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+    X = torch.randn((Bn, N, D), generator=gen, device=dev)
+    C0 = X[:, :K].clone()
+    C = C0.clone()
+    Cprev = C0.clone()
+    assign = torch.empty((Bn, N), dtype=torch.int32, device=dev)
+    xnorm = torch.empty((Bn, N), device=dev)
+    R = torch.empty_like(X)
+    codes = torch.empty((Bn * N, D // 2), dtype=torch.uint8, device=dev)
+    scales = torch.empty((Bn * N, D // 16), dtype=torch.uint8, device=dev)
+    idx = torch.empty((Bn, N), dtype=torch.int32, device=dev)
+    cnt = torch.empty((Bn,), dtype=torch.int32, device=dev)
+
+    def pipeline():
+        C.copy_(C0)
+        B_.dllm_spherical_kmeans(X, C, 4, assign, xnorm)
+        B_.dllm_cluster_residual(X, C, assign, xnorm, R)
+        B_.dllm_nvfp4_quantize(R, 1e-3, codes, scales)
+        B_.dllm_cluster_select(C, Cprev, assign, 4, idx, cnt)
+
+    s = _graph_time(pipeline, steps, warmup, dev)
+    nbytes = Bn * N * D * 4
+    return {"workload": f"B={Bn} window={N} rows d={D} K={K} iters=4 kc=4", "us_per_step": s * 1e6,
+            "launches_per_step": 2 * 4 + 2 + 3, "window_bytes": nbytes,
+            "compressed_bytes": Bn * N * (D // 2 + D // 16),
+            "note": "launch-bound at a 96-row window (13 small launches)", "timing": GRAPH_TIMING}
 
 
 def config_points(dev, full_sweep):

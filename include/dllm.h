@@ -163,6 +163,39 @@ int dllm_polestar_commit(const float *drift, const float *conf, const uint8_t *u
                          int B, int M, float alpha, float tau_s, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * [POL] "2. A. Polestar-Cache", local window and clustering / sparse updates: the hidden
+ * states of a local window are clustered with spherical k-means, their residuals are
+ * quantised with NVFP4 into a compressed proxy, and the top-k drifted clusters are
+ * refreshed.  The page names the steps, not their equations; these calls take:
+ *
+ * dllm_spherical_kmeans: X [B, N, D] fp32 rows; C [B, K, D] fp32 initial centroids,
+ *   normalised to unit length, then `iters` Lloyd rounds (a_i = argmax_k <x_i, c_k>, the
+ *   lowest k on ties; c_k = normalise(sum of x_i / |x_i| over its members, in row order),
+ *   an empty cluster keeps its centroid) and a final assignment; assign [B, N] int32 and
+ *   xnorm [B, N] fp32 (|x_i|) out.  D % 4 == 0, D <= 8192, K <= 256, X and C
+ *   16-byte aligned.
+ * dllm_cluster_residual: R [B, N, D] = x_i - xnorm_i c_{assign_i} (an assignment outside
+ *   [0, K) leaves the row whole).
+ * dllm_nvfp4_quantize: R [rows, D] fp32 (16-byte aligned, D % 16 == 0), tensor scale g > 0;
+ *   per 16-element block scales [rows, D/16] = E4M3(amax / (6 g)) and codes [rows, D/2]
+ *   (8-byte aligned) = E2M1(x / (scale g)), two per byte, element 2j in the low nibble
+ *   (sign << 3 | magnitude index into {0, .5, 1, 1.5, 2, 3, 4, 6}); both rounded to
+ *   nearest even with saturation by the device conversions; code 0 when the scale is 0.
+ * dllm_cluster_select: drift_k = 1 - cos(C_now[b,k], C_prev[b,k]) (0 for two zero rows, 1
+ *   for one); the kc clusters with the largest drift (lower k on ties); idx [B, N] receives
+ *   their member rows ascending, then -1; count [B] their number (the same output as
+ *   dllm_select_topk, for dllm_sparse_layer_refresh).  K <= 256.
+ * No workspace.
+ * ------------------------------------------------------------------------- */
+int dllm_spherical_kmeans(const float *X, float *C, int32_t *assign, float *xnorm, int B, int N, int D, int K,
+                          int iters, void *stream);
+int dllm_cluster_residual(const float *X, const float *C, const int32_t *assign, const float *xnorm, float *R,
+                          int B, int N, int D, int K, void *stream);
+int dllm_nvfp4_quantize(const float *R, float g, uint8_t *codes, uint8_t *scales, long rows, int D, void *stream);
+int dllm_cluster_select(const float *C_now, const float *C_prev, const int32_t *assign, int kc, int32_t *idx,
+                        int32_t *count, int B, int N, int D, int K, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Selection.  [SPA] "1. ...": the rows with the lowest proxy similarity (largest
  * drift) are recomputed, [SPA] "2. Adaptive budget allocation": at most k of them
  * per layer; [EC] step 3: the current masked tokens and the k most recently decoded
@@ -390,6 +423,7 @@ int dllm_gemm_bf16(const void *X, const void *W, float *out, int M, int N_out, i
 #define DLLM_KERNEL_KL_DRIFT 13
 #define DLLM_KERNEL_CE 14
 #define DLLM_KERNEL_POLESTAR 15
+#define DLLM_KERNEL_CLUSTER 16
 
 /* Launch mode of the library's kernels: with enable != 0 (the default) consecutive
  * kernels on a stream use programmatic dependent launch (a kernel's prologue and its

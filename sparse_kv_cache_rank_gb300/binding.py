@@ -45,6 +45,10 @@ _SIGS = {
     "dllm_kl_drift": (C.c_int, [C.c_void_p] * 3 + [C.c_int] * 3 + [C.c_void_p, C.c_size_t, C.c_void_p]),
     "dllm_ce_step": (C.c_int, [C.c_void_p] * 6 + [C.c_int] * 2 + [C.c_float] * 5 + [C.c_int, C.c_float, C.c_void_p]),
     "dllm_polestar_commit": (C.c_int, [C.c_void_p] * 7 + [C.c_int] * 2 + [C.c_float] * 2 + [C.c_void_p]),
+    "dllm_spherical_kmeans": (C.c_int, [C.c_void_p] * 4 + [C.c_int] * 5 + [C.c_void_p]),
+    "dllm_cluster_residual": (C.c_int, [C.c_void_p] * 5 + [C.c_int] * 4 + [C.c_void_p]),
+    "dllm_nvfp4_quantize": (C.c_int, [C.c_void_p, C.c_float, C.c_void_p, C.c_void_p, C.c_long, C.c_int, C.c_void_p]),
+    "dllm_cluster_select": (C.c_int, [C.c_void_p] * 3 + [C.c_int] + [C.c_void_p] * 2 + [C.c_int] * 4 + [C.c_void_p]),
     "dllm_select_topk": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_float,
                                    C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p]),
     "dllm_layer_rho": (C.c_double, [C.c_int] + [C.c_double] * 5),
@@ -161,7 +165,7 @@ def check_status(reset: bool = True) -> int:
 # --------------------------------------------------------------------------- measurement
 KERNELS = {"proxy_gemm": 1, "cosine": 2, "select": 3, "gather": 4, "qkv": 5, "attention": 6,
            "oproj": 7, "rmsnorm2": 8, "gateup": 9, "down": 10, "vocab": 11, "gemm": 12,
-           "kl_drift": 13, "ce": 14, "polestar": 15}
+           "kl_drift": 13, "ce": 14, "polestar": 15, "cluster": 16}
 
 
 def dllm_timer_start(kernel: str, max_launches: int) -> None:
@@ -257,6 +261,61 @@ def dllm_polestar_commit(drift, conf, undecided, suffix, selected, history, comm
                                       _ptr(history), _ptr(commit), B, M, float(alpha), float(tau_s),
                                       _stream(drift.device)), "dllm_polestar_commit")
     return commit
+
+
+def dllm_spherical_kmeans(X, C, iters: int, assign=None, xnorm=None):
+    """X [B,N,D] f32, C [B,K,D] f32 (initial; refined in place) -> (assign [B,N] int32, xnorm [B,N] f32)."""
+    B, N, D = X.shape
+    K = C.shape[1]
+    if C.shape != (B, K, D) or X.dtype != torch.float32 or C.dtype != torch.float32:
+        raise DllmError("X [B, N, D] and C [B, K, D] must be float32")
+    if assign is None:
+        assign = torch.empty((B, N), dtype=torch.int32, device=X.device)
+    if xnorm is None:
+        xnorm = torch.empty((B, N), dtype=torch.float32, device=X.device)
+    _cuda(X, C, assign, xnorm)
+    _check(lib().dllm_spherical_kmeans(_ptr(X), _ptr(C), _ptr(assign), _ptr(xnorm), B, N, D, K, int(iters),
+                                       _stream(X.device)), "dllm_spherical_kmeans")
+    return assign, xnorm
+
+
+def dllm_cluster_residual(X, C, assign, xnorm, R=None):
+    B, N, D = X.shape
+    K = C.shape[1]
+    if R is None:
+        R = torch.empty_like(X)
+    _cuda(X, C, assign, xnorm, R)
+    _check(lib().dllm_cluster_residual(_ptr(X), _ptr(C), _ptr(assign), _ptr(xnorm), _ptr(R), B, N, D, K,
+                                       _stream(X.device)), "dllm_cluster_residual")
+    return R
+
+
+def dllm_nvfp4_quantize(R, g: float, codes=None, scales=None):
+    """R [rows, D] f32 -> (codes [rows, D/2] uint8, scales [rows, D/16] uint8)."""
+    R2 = R.reshape(-1, R.shape[-1])
+    rows, D = R2.shape
+    if codes is None:
+        codes = torch.empty((rows, D // 2), dtype=torch.uint8, device=R.device)
+    if scales is None:
+        scales = torch.empty((rows, D // 16), dtype=torch.uint8, device=R.device)
+    _cuda(R2, codes, scales)
+    _check(lib().dllm_nvfp4_quantize(_ptr(R2), float(g), _ptr(codes), _ptr(scales), rows, D, _stream(R.device)),
+           "dllm_nvfp4_quantize")
+    return codes, scales
+
+
+def dllm_cluster_select(C_now, C_prev, assign, kc: int, idx=None, count=None):
+    """-> (idx [B,N] int32 ascending member rows of the kc most drifted clusters, -1 padded; count [B])."""
+    B, K, D = C_now.shape
+    N = assign.shape[1]
+    if idx is None:
+        idx = torch.empty((B, N), dtype=torch.int32, device=C_now.device)
+    if count is None:
+        count = torch.empty((B,), dtype=torch.int32, device=C_now.device)
+    _cuda(C_now, C_prev, assign, idx, count)
+    _check(lib().dllm_cluster_select(_ptr(C_now), _ptr(C_prev), _ptr(assign), int(kc), _ptr(idx), _ptr(count),
+                                     B, N, D, K, _stream(C_now.device)), "dllm_cluster_select")
+    return idx, count
 
 
 def build_proxy_matrix(w_v: torch.Tensor, gamma1: torch.Tensor, r: int, method: str = "svd",

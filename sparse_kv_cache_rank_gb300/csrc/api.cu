@@ -314,6 +314,54 @@ DLLM_EXPORT int dllm_polestar_commit(const float *drift, const float *conf, cons
     return DLLM_OK;
 }
 
+DLLM_EXPORT int dllm_spherical_kmeans(const float *X, float *C, int32_t *assign, float *xnorm, int B, int N,
+                                      int D, int K, int iters, void *stream) {
+    CHECK_ARG(X && C && assign && xnorm, "null pointer");
+    CHECK_ARG(B > 0 && N > 0 && D > 0 && K > 0 && iters >= 0, "sizes must be positive, iters >= 0");
+    CHECK_ARG(B <= 65535, "B must be <= 65535");
+    if (D > 8192 || D % 4 || K > 256)
+        return fail(DLLM_ERR_UNSUPPORTED, "D must be a multiple of 4 up to 8192 and K <= 256 (D=%d K=%d)", D, K);
+    CHECK_ARG(aligned16(X) && aligned16(C), "X and C must be 16-byte aligned");
+    cudaStream_t st = as_stream(stream);
+    Launch t(DLLM_KERNEL_CLUSTER, st, 2 * iters + 2);
+    CHECK_CUDA(spherical_kmeans(X, C, assign, xnorm, B, N, D, K, iters, st), "k-means launch");
+    return DLLM_OK;
+}
+
+DLLM_EXPORT int dllm_cluster_residual(const float *X, const float *C, const int32_t *assign, const float *xnorm,
+                                      float *R, int B, int N, int D, int K, void *stream) {
+    CHECK_ARG(X && C && assign && xnorm && R, "null pointer");
+    CHECK_ARG(B > 0 && N > 0 && D > 0 && K > 0, "sizes must be positive");
+    cudaStream_t st = as_stream(stream);
+    Launch t(DLLM_KERNEL_CLUSTER, st);
+    CHECK_CUDA(cluster_residual(X, C, assign, xnorm, R, B, N, D, K, st), "residual launch");
+    return DLLM_OK;
+}
+
+DLLM_EXPORT int dllm_nvfp4_quantize(const float *R, float g, uint8_t *codes, uint8_t *scales, long rows, int D,
+                                    void *stream) {
+    CHECK_ARG(R && codes && scales, "null pointer");
+    CHECK_ARG(rows > 0 && D > 0, "sizes must be positive");
+    CHECK_ARG(g > 0.f && isfinite(g), "the tensor scale g must be positive and finite");
+    CHECK_ARG(aligned16(R) && aligned8(codes), "R must be 16-byte and codes 8-byte aligned");
+    if (D % 16) return fail(DLLM_ERR_UNSUPPORTED, "D must be a multiple of 16 (got %d)", D);
+    cudaStream_t st = as_stream(stream);
+    Launch t(DLLM_KERNEL_CLUSTER, st);
+    CHECK_CUDA(nvfp4_quantize(R, g, codes, scales, rows, D, st), "NVFP4 launch");
+    return DLLM_OK;
+}
+
+DLLM_EXPORT int dllm_cluster_select(const float *C_now, const float *C_prev, const int32_t *assign, int kc,
+                                    int32_t *idx, int32_t *count, int B, int N, int D, int K, void *stream) {
+    CHECK_ARG(C_now && C_prev && assign && idx && count, "null pointer");
+    CHECK_ARG(B > 0 && N > 0 && D > 0 && K > 0 && kc >= 0, "sizes must be positive, kc >= 0");
+    if (K > 256) return fail(DLLM_ERR_UNSUPPORTED, "K must be <= 256 (got %d)", K);
+    cudaStream_t st = as_stream(stream);
+    Launch t(DLLM_KERNEL_CLUSTER, st);
+    CHECK_CUDA(cluster_select(C_now, C_prev, assign, kc, idx, count, B, N, D, K, st), "cluster select launch");
+    return DLLM_OK;
+}
+
 // ------------------------------------------------------------------ selection
 DLLM_EXPORT int dllm_select_topk(const float *drift, const int32_t *forced, int F, int k,
                                  float min_drift, int32_t *idx, int32_t *count, int B, int N,
@@ -663,7 +711,7 @@ DLLM_EXPORT int dllm_lmhead_commit(const void *X, const void *W_lm, const uint8_
 
 // ------------------------------------------------------------------ measurement support
 DLLM_EXPORT int dllm_timer_start(int kernel_id, int max_launches) {
-    CHECK_ARG(kernel_id >= DLLM_KERNEL_PROXY_GEMM && kernel_id <= DLLM_KERNEL_POLESTAR, "unknown kernel id %d", kernel_id);
+    CHECK_ARG(kernel_id >= DLLM_KERNEL_PROXY_GEMM && kernel_id <= DLLM_KERNEL_CLUSTER, "unknown kernel id %d", kernel_id);
     CHECK_ARG(max_launches > 0 && max_launches <= 1 << 16, "max_launches must be in [1, 65536]");
     std::lock_guard<std::mutex> lock(g_timer.mu);
     CHECK_ARG(g_timer.armed == 0, "a timer is already armed");

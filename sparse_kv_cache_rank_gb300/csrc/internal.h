@@ -95,6 +95,19 @@ cudaError_t polestar_commit(const float *drift, const float *conf, const uint8_t
                             const uint8_t *suffix, const uint8_t *selected, float *history, uint8_t *commit,
                             long n, float alpha, float tau_s, cudaStream_t st);
 
+// Cluster-granular proxy (cluster.cu): spherical k-means over [B, N, D] rows with K
+// centroids per sequence (C normalised first, `iters` Lloyd rounds, final assignment and
+// row norms); residuals against the centroid direction; NVFP4 quantisation of [rows, D]
+// (D % 16 == 0); selection of the kc most drifted clusters' rows (K <= 256).
+cudaError_t spherical_kmeans(const float *X, float *C, int32_t *assign, float *xnorm, int B, int N, int D, int K,
+                             int iters, cudaStream_t st);
+cudaError_t cluster_residual(const float *X, const float *C, const int32_t *assign, const float *xnorm, float *R,
+                             int B, int N, int D, int K, cudaStream_t st);
+cudaError_t nvfp4_quantize(const float *R, float g, uint8_t *codes, uint8_t *scales, long rows, int D,
+                           cudaStream_t st);
+cudaError_t cluster_select(const float *Cn, const float *Cp, const int32_t *assign, int kc, int32_t *idx,
+                           int32_t *count, int B, int N, int D, int K, cudaStream_t st);
+
 // KL divergence of proxy-attention rows between two steps (kl.cu): drift [B, N] from
 // cur, cache [B, N, r] fp32; r % 32 == 0, r <= 256.  Per-slice row states go to ws
 // (kl_drift_workspace_bytes), merged by a second kernel.
