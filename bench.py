@@ -59,6 +59,9 @@ def parse():
                     help="profiling mode: set up the layer workload, warm up, then run ONE layer "
                          "step inside a cudaProfilerStart/Stop range (for ncu --profile-from-start off); "
                          "prints a short JSON line, no measurement")
+    ap.add_argument("--profile-kl", action="store_true",
+                    help="profiling mode: ONE KL drift call on the layer workload's proxies inside a "
+                         "cudaProfilerStart/Stop range; prints a short JSON line, no measurement")
     return ap.parse_args()
 
 
@@ -781,10 +784,33 @@ def profile_step(args):
     print(json.dumps({"profile_step": "llada8b-layer", "rows": int(wl.cnt.sum())}), flush=True)
 
 
+def profile_kl(args):
+    """One warmed-up KL drift call on the layer step's proxies inside a profiler range."""
+    import torch
+    from sparse_kv_cache_rank_gb300 import binding as B
+    from sparse_kv_cache_rank_gb300 import synth
+    dev = torch.device("cuda", 0)
+    wl = LayerWorkload(synth.LLADA_LAYER, 1234, dev)
+    for _ in range(max(args.warmup, 3)):
+        wl.step()
+    out = torch.empty(wl.drift.shape, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        B.dllm_kl_drift(wl.cur, wl.pc, out)
+    torch.cuda.synchronize(dev)
+    torch.cuda.profiler.start()
+    B.dllm_kl_drift(wl.cur, wl.pc, out)
+    torch.cuda.synchronize(dev)
+    torch.cuda.profiler.stop()
+    B.check_status()
+    print(json.dumps({"profile_kl": "llada8b-layer proxies", "N": int(wl.cur.shape[1])}), flush=True)
+
+
 def main():
     args = parse()
     if args.profile_step:
         profile_step(args)
+    elif args.profile_kl:
+        profile_kl(args)
     elif args.impl == "reference":
         reference(args)
     else:
