@@ -63,7 +63,8 @@ extern "C" {
 /* Message of the last failed call on this thread ("" if none). */
 const char *dllm_last_error(void);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor): 1.10 adds the NEXT-row calls (KL drift,
+ * drift-aware commit, confidence extrapolation, cluster-granular proxy). */
 int dllm_version(void);
 
 /* Reads (and with reset != 0 clears) the device status word of the current device.

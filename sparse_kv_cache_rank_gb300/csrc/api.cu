@@ -195,7 +195,7 @@ using namespace dllm;
 
 DLLM_EXPORT const char *dllm_last_error(void) { return t_err.c_str(); }
 
-DLLM_EXPORT int dllm_version(void) { return 100; }
+DLLM_EXPORT int dllm_version(void) { return 110; }
 
 DLLM_EXPORT int dllm_check_status(unsigned *status_out, int reset) {
     CHECK_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
