@@ -182,6 +182,8 @@ int dllm_polestar_commit(const float *drift, const float *conf, const uint8_t *u
  *   (8-byte aligned) = E2M1(x / (scale g)), two per byte, element 2j in the low nibble
  *   (sign << 3 | magnitude index into {0, .5, 1, 1.5, 2, 3, 4, 6}); both rounded to
  *   nearest even with saturation by the device conversions; code 0 when the scale is 0.
+ * dllm_nvfp4_dequantize: out [rows, D] fp32 (16-byte aligned) = E2M1(code) * E4M3(scale) * g,
+ *   the first product exact, one rounding by the multiplication with g.
  * dllm_cluster_select: drift_k = 1 - cos(C_now[b,k], C_prev[b,k]) (0 for two zero rows, 1
  *   for one); the kc clusters with the largest drift (lower k on ties); idx [B, N] receives
  *   their member rows ascending, then -1; count [B] their number (the same output as
@@ -193,6 +195,8 @@ int dllm_spherical_kmeans(const float *X, float *C, int32_t *assign, float *xnor
 int dllm_cluster_residual(const float *X, const float *C, const int32_t *assign, const float *xnorm, float *R,
                           int B, int N, int D, int K, void *stream);
 int dllm_nvfp4_quantize(const float *R, float g, uint8_t *codes, uint8_t *scales, long rows, int D, void *stream);
+int dllm_nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales, float g, float *out, long rows, int D,
+                          void *stream);
 int dllm_cluster_select(const float *C_now, const float *C_prev, const int32_t *assign, int kc, int32_t *idx,
                         int32_t *count, int B, int N, int D, int K, void *stream);
 

@@ -48,6 +48,7 @@ _SIGS = {
     "dllm_spherical_kmeans": (C.c_int, [C.c_void_p] * 4 + [C.c_int] * 5 + [C.c_void_p]),
     "dllm_cluster_residual": (C.c_int, [C.c_void_p] * 5 + [C.c_int] * 4 + [C.c_void_p]),
     "dllm_nvfp4_quantize": (C.c_int, [C.c_void_p, C.c_float, C.c_void_p, C.c_void_p, C.c_long, C.c_int, C.c_void_p]),
+    "dllm_nvfp4_dequantize": (C.c_int, [C.c_void_p, C.c_void_p, C.c_float, C.c_void_p, C.c_long, C.c_int, C.c_void_p]),
     "dllm_cluster_select": (C.c_int, [C.c_void_p] * 3 + [C.c_int] + [C.c_void_p] * 2 + [C.c_int] * 4 + [C.c_void_p]),
     "dllm_select_topk": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_float,
                                    C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_void_p]),
@@ -302,6 +303,18 @@ def dllm_nvfp4_quantize(R, g: float, codes=None, scales=None):
     _check(lib().dllm_nvfp4_quantize(_ptr(R2), float(g), _ptr(codes), _ptr(scales), rows, D, _stream(R.device)),
            "dllm_nvfp4_quantize")
     return codes, scales
+
+
+def dllm_nvfp4_dequantize(codes, scales, g: float, out=None):
+    """codes [rows, D/2] uint8, scales [rows, D/16] uint8 -> out [rows, D] f32."""
+    rows, half = codes.shape
+    D = half * 2
+    if out is None:
+        out = torch.empty((rows, D), dtype=torch.float32, device=codes.device)
+    _cuda(codes, scales, out)
+    _check(lib().dllm_nvfp4_dequantize(_ptr(codes), _ptr(scales), float(g), _ptr(out), rows, D,
+                                       _stream(codes.device)), "dllm_nvfp4_dequantize")
+    return out
 
 
 def dllm_cluster_select(C_now, C_prev, assign, kc: int, idx=None, count=None):

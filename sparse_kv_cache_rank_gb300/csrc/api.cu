@@ -351,6 +351,19 @@ DLLM_EXPORT int dllm_nvfp4_quantize(const float *R, float g, uint8_t *codes, uin
     return DLLM_OK;
 }
 
+DLLM_EXPORT int dllm_nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales, float g, float *out, long rows,
+                                      int D, void *stream) {
+    CHECK_ARG(codes && scales && out, "null pointer");
+    CHECK_ARG(rows > 0 && D > 0, "sizes must be positive");
+    CHECK_ARG(g > 0.f && isfinite(g), "the tensor scale g must be positive and finite");
+    CHECK_ARG(aligned8(codes) && aligned16(out), "codes must be 8-byte and out 16-byte aligned");
+    if (D % 16) return fail(DLLM_ERR_UNSUPPORTED, "D must be a multiple of 16 (got %d)", D);
+    cudaStream_t st = as_stream(stream);
+    Launch t(DLLM_KERNEL_CLUSTER, st);
+    CHECK_CUDA(nvfp4_dequantize(codes, scales, g, out, rows, D, st), "NVFP4 dequantize launch");
+    return DLLM_OK;
+}
+
 DLLM_EXPORT int dllm_cluster_select(const float *C_now, const float *C_prev, const int32_t *assign, int kc,
                                     int32_t *idx, int32_t *count, int B, int N, int D, int K, void *stream) {
     CHECK_ARG(C_now && C_prev && assign && idx && count, "null pointer");

@@ -265,6 +265,40 @@ __global__ void __launch_bounds__(256)
     scales[t] = (uint8_t)(s2 & 0xffu);
 }
 
+// One thread per 16-element block: value = E2M1(code) * E4M3(scale) * g.  The first product
+// is exact in fp32 (2 + 4 significant bits), so each value is rounded once, by * g.
+__global__ void __launch_bounds__(256)
+    k_nvfp4_dequant(const uint8_t *__restrict__ codes, const uint8_t *__restrict__ scales, float g,
+                    float *__restrict__ out, long blocks) {
+    griddep_wait();
+    griddep_launch();
+    const long t = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= blocks) return;
+    unsigned h2;
+    asm("{\n\t.reg .b16 lo;\n\tmov.b16 lo, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+        : "=r"(h2)
+        : "h"((unsigned short)scales[t]));
+    const float s = __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
+    const uint2 q = *reinterpret_cast<const uint2 *>(codes + t * 8);
+    float v[16];
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        const uint32_t word = w == 0 ? q.x : q.y;
+#pragma unroll
+        for (int by = 0; by < 4; ++by) {
+            unsigned pair;   // two codes of one byte -> f16x2 (low nibble -> low half)
+            asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
+                : "=r"(pair)
+                : "r"((word >> (8 * by)) & 0xffu));
+            v[w * 8 + by * 2] = __half2float(__ushort_as_half((unsigned short)(pair & 0xffffu))) * s * g;
+            v[w * 8 + by * 2 + 1] = __half2float(__ushort_as_half((unsigned short)(pair >> 16))) * s * g;
+        }
+    }
+    float4 *dst = reinterpret_cast<float4 *>(out + t * 16);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+}
+
 // One CTA per sequence: cluster drifts, the kc largest, their member rows ascending.
 constexpr int kSelThreads = 256;
 constexpr int kMaxClusters = 256;
@@ -378,6 +412,15 @@ cudaError_t nvfp4_quantize(const float *R, float g, uint8_t *codes, uint8_t *sca
     const long blocks = rows * (D / 16);
     return launch_kernel(k_nvfp4_quant, dim3((unsigned)((blocks + 255) / 256)), dim3(256), 0, st, 1, R, g, codes,
                          scales, blocks);
+}
+
+cudaError_t nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales, float g, float *out, long rows, int D,
+                             cudaStream_t st) {
+    if (rows <= 0) return cudaSuccess;
+    if (D <= 0 || D % 16) return cudaErrorInvalidValue;
+    const long blocks = rows * (D / 16);
+    return launch_kernel(k_nvfp4_dequant, dim3((unsigned)((blocks + 255) / 256)), dim3(256), 0, st, 1, codes, scales,
+                         g, out, blocks);
 }
 
 cudaError_t cluster_select(const float *Cn, const float *Cp, const int32_t *assign, int kc, int32_t *idx,

@@ -105,6 +105,8 @@ cudaError_t cluster_residual(const float *X, const float *C, const int32_t *assi
                              int B, int N, int D, int K, cudaStream_t st);
 cudaError_t nvfp4_quantize(const float *R, float g, uint8_t *codes, uint8_t *scales, long rows, int D,
                            cudaStream_t st);
+cudaError_t nvfp4_dequantize(const uint8_t *codes, const uint8_t *scales, float g, float *out, long rows, int D,
+                             cudaStream_t st);
 cudaError_t cluster_select(const float *Cn, const float *Cp, const int32_t *assign, int kc, int32_t *idx,
                            int32_t *count, int B, int N, int D, int K, cudaStream_t st);
 

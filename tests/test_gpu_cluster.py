@@ -6,7 +6,8 @@ local window and clustering) through the C ABI.
 * residuals: within 1e-5 of max |x| (one fp32 multiply-add per element).
 * NVFP4: codes and block scales bit-exact on the same fp32 inputs (both sides decide in
   fp32, the device conversion's precision), including zero blocks, exact midpoints,
-  negative values that round to zero, saturated scales and subnormal scales.
+  negative values that round to zero, saturated scales and subnormal scales; the
+  dequantised values bit-exact too (code x scale is exact, one rounding by g).
 * selection: the same rows and counts when the k-th cluster drift is not within 1e-5 of
   the next one.
 """
@@ -85,6 +86,10 @@ def test_nvfp4_codes_bit_exact(B):
         c_ref, s_ref = cl.nvfp4_quantize(R, gscale)
         np.testing.assert_array_equal(scales.cpu().numpy(), s_ref)
         np.testing.assert_array_equal(_unpack(codes), c_ref)
+        # the round trip: dequantised values bit-exact (one fp32 rounding, by the tensor scale)
+        deq = B.dllm_nvfp4_dequantize(codes, scales, gscale).cpu().numpy()
+        want = cl.nvfp4_dequantize(c_ref, s_ref, gscale).astype(np.float32)
+        np.testing.assert_array_equal(deq.view(np.uint32), want.view(np.uint32))
 
 
 @pytest.mark.parametrize("kc", [0, 3, 16, 40])
