@@ -107,3 +107,18 @@ def test_ce_step_initialises_new_tokens():
     np.testing.assert_array_equal(st[0, :, 0], [0.4, 0.8])
     assert np.all(st[..., 1] == 0) and np.all(st[..., 2] == prm.R) and np.all(st[..., 4] == prm.p_v0)
     assert not early.any()
+
+
+def test_lower_bound_closed_form():
+    """l = 0.92, v = 0, P00 = 0.01: the 1.645-sigma lower bound one step ahead is
+    0.92 - 0.1645 < 0.9, so no early commit; with a small variance (P00 = 1e-4) it is
+    0.92 - 0.01645 >= 0.9 and the token commits (one committed position to its left)."""
+    prm = ce.CEParams()
+    und = np.array([[False, True]])
+    com = np.array([[True, False]])
+    wide = np.array([[[0.5, 0, 0.01, 0, 0], [0.92, 0.0, 0.01, 0.0, 0.0]]])
+    narrow = np.array([[[0.5, 0, 0.01, 0, 0], [0.92, 0.0, 1e-4, 0.0, 0.0]]])
+    assert not ce.early_commit(wide, und, com, prm)[0, 1]
+    assert ce.early_commit(narrow, und, com, prm)[0, 1]
+    mean, var = ce.forecast(wide[0, 1], 1)
+    assert mean - prm.z * math.sqrt(var) == pytest.approx(0.92 - 1.645 * 0.1)

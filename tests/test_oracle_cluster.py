@@ -40,8 +40,10 @@ def test_kmeans_single_cluster_is_mean_direction_and_scale_free():
 def test_kmeans_ties_and_empty_clusters():
     """Equal cosines go to the lower cluster; a cluster nobody joins keeps its centroid."""
     X = _circle([90, 90])
+    a0, _ = cl.spherical_kmeans(X, _circle([0, 180, 300]), 0)
+    np.testing.assert_array_equal(a0, [0, 0])      # cos 0 to both 0 and 180 degrees: the lower
     a, C = cl.spherical_kmeans(X, _circle([0, 180, 300]), 2)
-    np.testing.assert_array_equal(a, [0, 0])       # cos 0 to both 0 and 180 degrees
+    np.testing.assert_array_equal(a, [0, 0])
     np.testing.assert_allclose(C[1], _circle([180])[0], atol=1e-15)
     np.testing.assert_allclose(C[2], _circle([300])[0], atol=1e-15)
 
