@@ -9,7 +9,9 @@ import numpy as np
 
 from sparse_kv_cache_rank_gb300 import synth
 
-# tolerances ("Parity bar")
+# tolerances: selection and commit decisions exact outside a 1e-5 near-tie band, fp32
+# reductions within 1e-4 relative, bf16 layer outputs within 2e-2 of the largest
+# reference value with cosine >= 0.999
 FP32_REDUCTION_RTOL = 1e-4      # drift, entropy, confidence, fp32 proxies
 BF16_MAX_REL = 2e-2             # bf16 layer outputs: max |err| / max |ref|
 BF16_MIN_COS = 0.999
