@@ -239,12 +239,19 @@ def test_commit_no_valid_rows(B):
                                               (513, 256, 2048, 8), (64, 4096, 4096, 0),
                                               (164, 384, 12288, 0), (256, 1024, 4096, 0),
                                               (200, 2080, 1024, 0), (16, 128, 256, 0),
-                                              (96, 160 * 128 + 96, 256, 0)])
+                                              (96, 160 * 128 + 96, 256, 0),
+                                              (257, 1024, 512, 0), (516, 8192, 512, 0),
+                                              (642, 8192, 512, 0), (705, 8192, 512, 0),
+                                              (775, 8192, 512, 0), (838, 8192, 512, 0),
+                                              (901, 8192, 512, 0)])
 def test_gemm_bf16_parity(B, orc, M, N_out, K, splits):
     """The engine under every projection: X W^T against the oracle's double-precision
     projection (the proxy score computes exactly H . P), ragged M, K splits 1..8, long K
     over few weight tiles (automatic cluster split), a ragged last weight tile (2080 rows),
-    tiny grids, and more weight tiles than SMs."""
+    tiny grids, and more weight tiles than SMs.  The last six have more than 256 tokens and
+    8192 outputs, so that the planner's token-tile width is 160, 176, 192, 208, 224 and 256
+    in turn, each with a ragged last token tile; (257, 1024, 512) gives no width enough
+    tiles and takes the K split."""
     g = synth.rng(3000 + M + K)
     X = synth.round_bf16(g.standard_normal((M, K), dtype=np.float32))
     W = synth.round_bf16((g.standard_normal((N_out, K)) * 0.05).astype(np.float32))
