@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stack", action="store_true",
-                    help="skip the 32-layer LLaDA-8B-shaped stack measurement")
+                    help="skip the 32-layer LLaDA-8B-shaped and 28-layer Dream-7B-shaped stacks")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="approximate budget of the CPU-oracle sample")
     ap.add_argument("--no-configs", action="store_true",
@@ -414,6 +414,8 @@ def native(args):
         torch.cuda.empty_cache()
     if not args.no_stack:
         result["stack"] = stack_measure(dev, args.steps, args.warmup)
+        torch.cuda.empty_cache()
+        result["dream_stack"] = dream_stack_measure(dev, min(args.steps, 20), args.warmup)
     if not args.no_configs:
         result["configs"] = config_points(dev, args.sweep)
     if world > 1:
@@ -487,6 +489,50 @@ def stack_measure(dev, steps, warmup, decode_steps=48):
                         "timing": "wall clock incl. one device->host read and host commit per step"},
         "setup_s": setup_s,
     }
+
+
+def dream_stack_measure(dev, steps, warmup):
+    """28-layer Dream-7B-shaped stack (Qwen2.5-7B layout: d=3584, 28 query / 4 KV heads x
+    128, FFN 18944), batch 8, N=2048 (1024 prompt + 1024 generation, block 32), vocab
+    152064, uniform 16 % update ratio (k = 328 per sequence) plus the block's rows and the
+    8 most recent tokens forced: the partial denoising step (28 layer refreshes, the fused
+    LM head and the commit) timed on the device with CUDA events."""
+    import torch
+    from sparse_kv_cache_rank_gb300 import synth
+    from sparse_kv_cache_rank_gb300.stack import DecodeStack
+    sh = synth.DREAM_STACK
+    t0 = time.perf_counter()
+    st = DecodeStack(sh, 2468, dev, uniform_rho=sh.rho, k_recent=8, proxy_method="lowrank")
+    st.prefill()
+    setup_s = time.perf_counter() - t0
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(98)
+    H0 = []
+    for _ in range(2):
+        h = st.H0.float() + torch.randn(st.H0.shape, generator=gen, device=dev) * 0.002
+        H0.append(h.to(st.H0.dtype).contiguous())
+    for s in range(max(warmup, 3)):
+        st.forward(False, H0=H0[s & 1])
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(steps):
+        out = st.forward(False, H0=H0[s & 1])
+    e1.record()
+    torch.cuda.synchronize(dev)
+    dt = e0.elapsed_time(e1) / 1e3 / steps
+    committed = int((out[0] >= 0).sum().item())
+    rows = st.count_rows(False)
+    res = {"workload": f"dream7b-stack layers={sh.layers} B={sh.B} N={sh.N} d={sh.d} "
+                       f"heads={sh.n_q}q/{sh.n_kv}kv x {sh.hd} F={sh.F} V={sh.V} rho={sh.rho} k_recent=8",
+           "steps_per_s": 1.0 / dt, "ms_per_step": dt * 1e3,
+           "context_tokens_per_s": sh.B * sh.N / dt, "committed_tokens_per_s": committed / dt,
+           "rows_refreshed_per_layer": rows, "budget_per_layer": st.budgets[0],
+           "steps": steps, "timing": "cuda events, device", "setup_s": setup_s}
+    del st, H0, out
+    torch.cuda.empty_cache()
+    return res
 
 
 def layer_point(sh, dev, steps, warmup, seed=77):
