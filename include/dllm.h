@@ -64,7 +64,8 @@ extern "C" {
 const char *dllm_last_error(void);
 
 /* Library ABI version (major * 100 + minor): 1.10 adds the NEXT-row calls (KL drift,
- * drift-aware commit, confidence extrapolation, cluster-granular proxy). */
+ * drift-aware commit, confidence extrapolation, cluster-granular proxy); 1.11 the
+ * host-only GEMM plan query (dllm_gemm_plan). */
 int dllm_version(void);
 
 /* Reads (and with reset != 0 clears) the device status word of the current device.
@@ -405,6 +406,17 @@ int dllm_rows_rmsnorm(const void *H, const int32_t *rows, int R, const void *gam
  * ------------------------------------------------------------------------- */
 int dllm_gemm_bf16(const void *X, const void *W, float *out, int M, int N_out, int K, int splits,
                    void *stream);
+
+/* The launch plan dllm_gemm_bf16 (slices = 0) or the proxy projection's independent K
+ * slices (slices = 1) would use for this shape on a device with `sms` SMs.  Host only:
+ * no device is queried and nothing is launched, so it answers without a GPU (the
+ * library's own launches pass the current device's SM count).  info [8] receives
+ *   { token-tile width BN, K split, pipeline stages, token tiles, weight tiles of 128
+ *     rows, token rows staged per K block, dynamic shared memory bytes, CTAs per SM }.
+ * splits as for dllm_gemm_bf16 (0 = chosen from the shape).  Errors: INVALID_ARG for a
+ * null info, sizes <= 0, sms outside [1, 1024] or splits outside [0, 8]; UNSUPPORTED
+ * when K % 64 or N_out % 32 is not 0. */
+int dllm_gemm_plan(int M, int N_out, int K, int splits, int sms, int slices, int32_t *info);
 
 /* ---------------------------------------------------------------------------
  * Measurement support.  While a timer is armed, every launch of the chosen kernel

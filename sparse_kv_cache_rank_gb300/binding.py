@@ -71,6 +71,7 @@ _SIGS = {
     "dllm_launch_count": (C.c_ulonglong, []),
     "dllm_gemm_bf16": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                  C.c_int, C.c_void_p]),
+    "dllm_gemm_plan": (C.c_int, [C.c_int] * 6 + [C.c_void_p]),
     "dllm_attention_workspace_bytes": (C.c_size_t, [C.c_int] * 6),
     "dllm_attention": (C.c_int, [C.c_void_p] * 6 + [C.c_int] * 7 + [C.c_void_p, C.c_size_t, C.c_void_p]),
     "dllm_embed": (C.c_int, [C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_void_p] + [C.c_int] * 5
@@ -493,6 +494,18 @@ def dllm_gemm_bf16(X, W, out=None, splits: int = 0):
     _check(lib().dllm_gemm_bf16(_ptr(X), _ptr(W), _ptr(out), M, N_out, K, int(splits),
                                 _stream(X.device)), "dllm_gemm_bf16")
     return out
+
+
+PLAN_FIELDS = ("BN", "splits", "stages", "tok_tiles", "w_tiles", "xrows", "smem", "ctas_per_sm")
+
+
+def dllm_gemm_plan(M: int, N_out: int, K: int, splits: int = 0, sms: int = 152, slices: bool = False):
+    """The tensor-core GEMM's launch plan for this shape on `sms` SMs (host only, no GPU
+    needed) -> dict of PLAN_FIELDS."""
+    info = (C.c_int32 * 8)()
+    _check(lib().dllm_gemm_plan(int(M), int(N_out), int(K), int(splits), int(sms), 1 if slices else 0, info),
+           "dllm_gemm_plan")
+    return dict(zip(PLAN_FIELDS, list(info)))
 
 
 # --------------------------------------------------------------------------- vocab

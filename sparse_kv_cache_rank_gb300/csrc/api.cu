@@ -195,7 +195,7 @@ using namespace dllm;
 
 DLLM_EXPORT const char *dllm_last_error(void) { return t_err.c_str(); }
 
-DLLM_EXPORT int dllm_version(void) { return 110; }
+DLLM_EXPORT int dllm_version(void) { return 111; }
 
 DLLM_EXPORT int dllm_check_status(unsigned *status_out, int reset) {
     CHECK_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
@@ -655,6 +655,19 @@ DLLM_EXPORT int dllm_gemm_bf16(const void *X, const void *W, float *out, int M, 
     CHECK_CUDA(gemm_tc(static_cast<const bf16 *>(W), N_out, K, static_cast<const bf16 *>(X), M, epi,
                        splits, false, status_ptr(), st),
                "gemm launch");
+    return DLLM_OK;
+}
+
+DLLM_EXPORT int dllm_gemm_plan(int M, int N_out, int K, int splits, int sms, int slices, int32_t *info) {
+    CHECK_ARG(info, "null pointer");
+    CHECK_ARG(M > 0 && N_out > 0 && K > 0, "sizes must be positive");
+    CHECK_ARG(sms >= 1 && sms <= 1024, "sms must be in [1, 1024] (got %d)", sms);
+    CHECK_ARG(splits >= 0 && splits <= 8, "splits must be in [0, 8]");
+    if (K % 64 || N_out % 32) return fail(DLLM_ERR_UNSUPPORTED, "needs K %% 64 == 0 and N_out %% 32 == 0");
+    int v[8];
+    if (gemm_tc_plan_info(M, N_out, K, splits, sms, slices != 0, v) != 0)
+        return fail(DLLM_ERR_INVALID_ARG, "shape rejected by the planner");
+    for (int i = 0; i < 8; ++i) info[i] = v[i];
     return DLLM_OK;
 }
 

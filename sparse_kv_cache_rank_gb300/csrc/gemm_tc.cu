@@ -443,8 +443,7 @@ int pick_bn_many(int M_tok, int w_tiles, int KB, int sms) {
 //  * few weight tiles: a K split across a cluster sized to fill the SMs.
 // Many tokens: the token-tile width that the tile-time model below finds fastest, two
 // CTAs per SM; a K split only when no width gives half the SMs a tile.
-Plan plan_gemm(int M_tok, int N_out, int K, int splits_req) {
-    const int sms = num_sms();
+Plan plan_gemm(int M_tok, int N_out, int K, int splits_req, int sms) {
     const int w_tiles = (N_out + BM - 1) / BM;
     const int KB = K / BK;
     auto clamp_splits = [&](int s) {
@@ -489,8 +488,7 @@ Plan plan_gemm(int M_tok, int N_out, int K, int splits_req) {
 
 // Independent K slices (no cluster), each writing its own fp32 partial output: token
 // tiles of 64 rows (128 beyond 2048 tokens), slices sized to two CTAs per SM.
-Plan plan_slices(int M_tok, int N_out, int K) {
-    const int sms = num_sms();
+Plan plan_slices(int M_tok, int N_out, int K, int sms) {
     const int KB = K / BK;
     const int BN = M_tok <= 256 ? round16(M_tok) : (M_tok <= 2048 ? 64 : 128);
     const long long tiles = (long long)((N_out + BM - 1) / BM) * ((M_tok + BN - 1) / BN);
@@ -532,20 +530,34 @@ cudaError_t gemm_tc(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, c
                     int splits, bool w_const, unsigned *status, cudaStream_t st) {
     if (M_tok <= 0 || N_out <= 0) return cudaSuccess;
     if (K % BK != 0 || N_out % 32 != 0) return cudaErrorInvalidValue;
-    return launch_plan(plan_gemm(M_tok, N_out, K, splits), false, W, N_out, K, X, M_tok, epi, w_const,
-                       status, st);
+    return launch_plan(plan_gemm(M_tok, N_out, K, splits, num_sms()), false, W, N_out, K, X, M_tok, epi,
+                       w_const, status, st);
 }
 
 int gemm_tc_slices_count(int M_tok, int N_out, int K) {
     if (M_tok <= 0 || N_out <= 0 || K % BK != 0) return 1;
-    return plan_slices(M_tok, N_out, K).splits;
+    return plan_slices(M_tok, N_out, K, num_sms()).splits;
+}
+
+int gemm_tc_plan_info(int M_tok, int N_out, int K, int splits_req, int sms, bool slices, int *info) {
+    if (M_tok <= 0 || N_out <= 0 || K <= 0 || K % BK != 0 || N_out % 32 != 0 || sms <= 0) return -1;
+    const Plan p = slices ? plan_slices(M_tok, N_out, K, sms) : plan_gemm(M_tok, N_out, K, splits_req, sms);
+    info[0] = p.BN;
+    info[1] = p.splits;
+    info[2] = p.stages;
+    info[3] = p.tok_tiles;
+    info[4] = p.w_tiles;
+    info[5] = p.xrows;
+    info[6] = (int)p.smem;
+    info[7] = p.smem <= (size_t)kSmemPair ? 2 : 1;   // CTAs that fit on one SM
+    return 0;
 }
 
 cudaError_t gemm_tc_slices(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, float *parts,
                            bool w_const, unsigned *status, cudaStream_t st) {
     if (M_tok <= 0 || N_out <= 0) return cudaSuccess;
     if (K % BK != 0 || N_out % 32 != 0) return cudaErrorInvalidValue;
-    const Plan p = plan_slices(M_tok, N_out, K);
+    const Plan p = plan_slices(M_tok, N_out, K, num_sms());
     EpiStoreF32 epi{SelRows{}, parts, N_out, N_out};
     return launch_plan(p, true, W, N_out, K, X, M_tok, epi, w_const, status, st);
 }

@@ -57,6 +57,11 @@ cudaError_t gemm_tc(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, c
 // Independent K slices: parts[z * M_tok + m, f] = partial sum of slice z (fp32), for a
 // later fixed-order reduction; gemm_tc_slices_count() tells how many slices it uses.
 int gemm_tc_slices_count(int M_tok, int N_out, int K);
+// The plan the tensor-core GEMM would launch for this shape on `sms` SMs, computed on the
+// host only (no device query): info = {BN, splits, stages, token tiles, weight tiles,
+// staged token rows, shared-memory bytes, CTAs per SM}.  slices: the independent-K-slice
+// plan of gemm_tc_slices instead.  Returns -1 for a shape the GEMM rejects.
+int gemm_tc_plan_info(int M_tok, int N_out, int K, int splits_req, int sms, bool slices, int *info);
 cudaError_t gemm_tc_slices(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, float *parts,
                            bool w_const, unsigned *status, cudaStream_t st);
 
