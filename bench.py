@@ -491,12 +491,18 @@ def stack_measure(dev, steps, warmup, decode_steps=48):
     }
 
 
-def dream_stack_measure(dev, steps, warmup):
+def dream_stack_measure(dev, steps, warmup, decode_steps=8):
     """28-layer Dream-7B-shaped stack (Qwen2.5-7B layout: d=3584, 28 query / 4 KV heads x
     128, FFN 18944), batch 8, N=2048 (1024 prompt + 1024 generation, block 32), vocab
     152064, uniform 16 % update ratio (k = 328 per sequence) plus the block's rows and the
-    8 most recent tokens forced: the partial denoising step (28 layer refreshes, the fused
-    LM head and the commit) timed on the device with CUDA events."""
+    8 most recent tokens forced.
+
+    forced_sparse: the partial denoising step (28 layer refreshes, the fused LM head and
+      the commit) timed on the device with CUDA events.
+    rule_driven: the decode loop with the host-side commit of all 8 sequences (one
+      device->host read per step), wall-clock timed; with random weights the entropy
+      exceeds tau, so every step is a full forward of the 8 x 2048 rows.
+    """
     import torch
     from sparse_kv_cache_rank_gb300 import synth
     from sparse_kv_cache_rank_gb300.stack import DecodeStack
@@ -524,12 +530,27 @@ def dream_stack_measure(dev, steps, warmup):
     dt = e0.elapsed_time(e1) / 1e3 / steps
     committed = int((out[0] >= 0).sum().item())
     rows = st.count_rows(False)
+    st.prefill()
+    for _ in range(2):
+        st.decode_step()
+    torch.cuda.synchronize(dev)
+    n_full, toks = 0, 0
+    t0 = time.perf_counter()
+    for _ in range(decode_steps):
+        n_full += 1 if st.full_next else 0
+        toks += st.decode_step()
+    torch.cuda.synchronize(dev)
+    dec_s = time.perf_counter() - t0
     res = {"workload": f"dream7b-stack layers={sh.layers} B={sh.B} N={sh.N} d={sh.d} "
                        f"heads={sh.n_q}q/{sh.n_kv}kv x {sh.hd} F={sh.F} V={sh.V} rho={sh.rho} k_recent=8",
-           "steps_per_s": 1.0 / dt, "ms_per_step": dt * 1e3,
-           "context_tokens_per_s": sh.B * sh.N / dt, "committed_tokens_per_s": committed / dt,
-           "rows_refreshed_per_layer": rows, "budget_per_layer": st.budgets[0],
-           "steps": steps, "timing": "cuda events, device", "setup_s": setup_s}
+           "forced_sparse": {"steps_per_s": 1.0 / dt, "ms_per_step": dt * 1e3,
+                             "context_tokens_per_s": sh.B * sh.N / dt, "committed_tokens_per_s": committed / dt,
+                             "rows_refreshed_per_layer": rows, "budget_per_layer": st.budgets[0],
+                             "steps": steps, "timing": "cuda events, device"},
+           "rule_driven": {"steps": decode_steps, "warmup": 2, "steps_per_s": decode_steps / dec_s,
+                           "tokens_per_s": toks / dec_s, "full_steps": n_full,
+                           "timing": "wall clock incl. one device->host read and host commit per step"},
+           "setup_s": setup_s}
     del st, H0, out
     torch.cuda.empty_cache()
     return res
