@@ -145,7 +145,10 @@ _ws_cache: dict = {}
 
 
 def _workspace(nbytes: int, device, tag: str) -> torch.Tensor:
-    """Caller-side scratch buffer (the library itself never allocates)."""
+    """Caller-side scratch buffer (the library itself never allocates).  One buffer is kept
+    per (entry point, device) and reused by every call that passes no `ws`, so calls that
+    are ordered on one stream share it safely; calls of the same entry point that may run
+    concurrently (different streams without ordering) must each pass their own `ws`."""
     key = (tag, device.index if device.index is not None else torch.cuda.current_device())
     buf = _ws_cache.get(key)
     if buf is None or buf.numel() < nbytes:
@@ -212,7 +215,7 @@ def dllm_proxy_score(H, Pt, proxy_cache, proxy_cur=None, drift=None, ws=None):
     return proxy_cur, drift
 
 
-def dllm_kl_drift(proxy_cur, proxy_cache, drift=None):
+def dllm_kl_drift(proxy_cur, proxy_cache, drift=None, ws=None):
     """proxy_cur, proxy_cache [B,N,r] f32 -> drift [B,N] f32 = KL of the rows' proxy-attention
     distributions (this step against the cached proxies)."""
     B, N, r = proxy_cur.shape
@@ -222,7 +225,8 @@ def dllm_kl_drift(proxy_cur, proxy_cache, drift=None):
         drift = torch.empty((B, N), dtype=torch.float32, device=proxy_cur.device)
     _cuda(proxy_cur, proxy_cache, drift)
     need = int(lib().dllm_kl_drift_workspace_bytes(B, N))
-    ws = _workspace(need, proxy_cur.device, "kl")
+    if ws is None:
+        ws = _workspace(need, proxy_cur.device, "kl")
     _check(lib().dllm_kl_drift(_ptr(proxy_cur), _ptr(proxy_cache), _ptr(drift), B, N, r, _ptr(ws), ws.numel(),
                                _stream(proxy_cur.device)), "dllm_kl_drift")
     return drift
