@@ -63,9 +63,10 @@ extern "C" {
 /* Message of the last failed call on this thread ("" if none). */
 const char *dllm_last_error(void);
 
-/* Library ABI version (major * 100 + minor): 1.10 adds the NEXT-row calls (KL drift,
- * drift-aware commit, confidence extrapolation, cluster-granular proxy); 1.11 the
- * host-only GEMM plan query (dllm_gemm_plan). */
+/* Library ABI version (major * 100 + minor): 1.00 holds the path's calls and the
+ * allocation-free vocabulary step (dllm_commit_entropy_noalloc); 1.10 adds the NEXT-row
+ * calls (KL drift, drift-aware commit, confidence extrapolation, cluster-granular
+ * proxy); 1.11 the host-only GEMM plan query (dllm_gemm_plan). */
 int dllm_version(void);
 
 /* Reads (and with reset != 0 clears) the device status word of the current device.

@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" entry points of libdllm.so (declared in include/dllm.h):
 // argument checks, workspace carving and the launch sequence of each call.
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -673,7 +674,7 @@ DLLM_EXPORT int dllm_gemm_plan(int M, int N_out, int K, int splits, int sms, int
 
 // ------------------------------------------------------------------ vocabulary
 DLLM_EXPORT size_t dllm_commit_workspace_bytes(int B, int M, int V) {
-    if (B <= 0 || M < 0 || V <= 0) return 0;
+    if (B <= 0 || M < 0 || V <= 0 || (long long)B * M > INT_MAX) return 0;
     return commit_ws_bytes(B, M, V) + 256;
 }
 
@@ -684,6 +685,7 @@ DLLM_EXPORT int dllm_commit_entropy(const float *logits, const uint8_t *valid, i
     CHECK_ARG(max_entropy && full_next, "null pointer");
     CHECK_ARG(B > 0 && M >= 0 && V > 0, "sizes must be positive");
     CHECK_ARG(M <= 1024, "M must be <= 1024 (got %d)", M);
+    CHECK_ARG((long long)B * M <= INT_MAX, "B*M must fit in an int (B=%d M=%d)", B, M);
     if (M > 0) CHECK_ARG(logits && valid && token && conf && entropy, "null pointer");
     const size_t need = commit_ws_bytes(B, M, V) + 256;
     if (!ws || ws_bytes < need)
@@ -793,6 +795,13 @@ DLLM_EXPORT int dllm_commit_entropy_noalloc(const float *logits, const uint8_t *
     CHECK_ARG(B > 0 && M >= 0 && V > 0, "sizes must be positive");
     CHECK_ARG(M <= 1024, "M must be <= 1024 (got %d)", M);
     if (M > 0) CHECK_ARG(logits && valid && token && conf && entropy, "null pointer");
+    // every row needs at least one state, so B*M above the limit is rejected before the
+    // int row count of the launch is formed
+    if ((long long)B * M > commit_noalloc_max_states())
+        return fail(DLLM_ERR_UNSUPPORTED,
+                    "B*M = %lld rows exceed the allocation-free entry point's %d scratch states "
+                    "(use dllm_commit_entropy with a workspace)",
+                    (long long)B * M, commit_noalloc_max_states());
     const size_t states = commit_noalloc_states(B, M, V);
     if (states > (size_t)commit_noalloc_max_states())
         return fail(DLLM_ERR_UNSUPPORTED,

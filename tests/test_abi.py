@@ -74,6 +74,14 @@ def test_invalid_arguments_fail_before_launch(dl):
     # commit: workspace too small, M too large
     assert L.dllm_commit_entropy(p, p, 1, 4, 16, 0.9, 2.0, p, p, p, p, p, p, 0, None) == -3
     assert L.dllm_commit_entropy(p, p, 1, 2000, 16, 0.9, 2.0, p, p, p, p, p, p, 1 << 20, None) == -1
+    # B*M past the int range: rejected before any row count is formed
+    big = 1 << 22
+    assert L.dllm_commit_entropy(p, p, big, 1024, 16, 0.9, 2.0, p, p, p, p, p, p, 1 << 20, None) == -1
+    assert L.dllm_commit_workspace_bytes(big, 1024, 16) == 0
+    # allocation-free commit: more rows than its fixed array holds (also where B*M wraps an int)
+    assert L.dllm_commit_entropy_noalloc(p, p, big, 1024, 16, 0.9, 2.0, p, p, p, p, p, None) == -2
+    assert "allocation-free" in _err(dl)
+    assert L.dllm_commit_entropy_noalloc(p, p, 17, 1024, 16, 0.9, 2.0, p, p, p, p, p, None) == -2
     # pack: unsupported head dim, misaligned destination
     desc = dl.dllm_layer()
     args = [p] * 9
