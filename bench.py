@@ -11,6 +11,11 @@ on resident inputs; consecutive steps alternate between two drifted inputs so th
 every step selects k rows (a refreshed row's cached proxy is the one it was refreshed
 with).  The weights (436 MB) exceed the 129 MB L2, so no L2 flush is needed.
 
+Besides the headline line's keys: the end-to-end leg (host inputs in, refreshed rows
+out), the CPU oracle timed on whole steps, the next-row kernels, the 32-layer
+LLaDA-8B-shaped and 28-layer Dream-7B-shaped stacks, and the other layer
+configurations (tiny fp32, Dream-shaped layer, the 36-point long-context sweep).
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 Under torchrun every rank runs an independent replica (weak scaling, no collective on
 the data path); rank 0 prints one JSON line.
@@ -20,6 +25,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -38,6 +44,15 @@ METRIC = "sparse-refresh denoise steps/s & tokens/s (LLaDA-8B shape); % of roofl
 NCU_TRAFFIC_BYTES = {"gateup": 205.85e6, "qkv": 106.14e6, "down": 110.35e6, "oproj": 36.30e6,
                      "attention": 18.18e6}
 UNIT = "steps/s"
+DATA = "synthetic (seeded random-init weights N(0,0.02), drift model: 10% rows +N(0,0.5), all +N(0,0.05))"
+
+
+def layer_config(sh, k, world):
+    """The `config` object of a layer workload's line (native and reference arms)."""
+    return {"workload": f"{sh.name} B={sh.B} N={sh.N} d={sh.d} heads={sh.n_q}x{sh.hd} F={sh.F} "
+                        f"r={sh.r} rho={sh.rho} k={k}",
+            "l2": "inputs larger than L2 (436 MB of weights per step)" if sh.d >= 1024 else "small layer",
+            "parallelism": f"replicas x{world}"}
 
 
 def parse():
@@ -47,14 +62,16 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-full", action="store_true",
+                    help="also time the single-thread oracle points that take more than a minute per step")
     ap.add_argument("--no-stack", action="store_true",
                     help="skip the 32-layer LLaDA-8B-shaped and 28-layer Dream-7B-shaped stacks")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0,
-                    help="approximate budget of the CPU-oracle sample")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the other layer configurations (tiny fp32, Dream-shaped, long context)")
-    ap.add_argument("--sweep", action="store_true",
-                    help="all 36 long-context points (N x batch x update ratio) instead of 9")
+    ap.add_argument("--quick-sweep", action="store_true",
+                    help="9 long-context points (batch 1, without 50%%) instead of all 36")
+    ap.add_argument("--reference-workload", choices=["llada8b-layer", "tiny-fp32"], default="llada8b-layer",
+                    help="workload of the reference arm (the small one only for quick checks)")
     ap.add_argument("--profile-step", action="store_true",
                     help="profiling mode: set up the layer workload, warm up, then run ONE layer "
                          "step inside a cudaProfilerStart/Stop range (for ncu --profile-from-start off); "
@@ -145,35 +162,49 @@ def layer_kernel_work(sh, M):
 
 
 # --------------------------------------------------------------------------- native arm
+def _layer_weights(sh, seed, dev):
+    """Random-init weights N(0, 0.02) of one layer (nn.Linear layout), packed, and the
+    layer's proxy matrix from the one-time set-up."""
+    import torch
+    from sparse_kv_cache_rank_gb300 import binding as B
+    from sparse_kv_cache_rank_gb300.proxy_setup import build_proxy_matrix
+    bf = torch.float32 if sh.dtype == "f32" else torch.bfloat16
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+
+    def randn(*shape):
+        return (torch.randn(shape, generator=gen, device=dev, dtype=torch.float32) * 0.02).to(bf)
+
+    d, dq, dkv, F = sh.d, sh.d_q, sh.d_kv, sh.F
+    w = {"w_q": randn(dq, d), "w_k": randn(dkv, d), "w_v": randn(dkv, d), "w_o": randn(d, dq),
+         "w_g": randn(F, d), "w_u": randn(F, d), "w_d": randn(d, F),
+         "gamma1": torch.ones(d, device=dev, dtype=bf), "gamma2": torch.ones(d, device=dev, dtype=bf)}
+    layer = B.dllm_pack_layer(w, sh.n_q, sh.n_kv, sh.hd, eps=sh.eps, rope_theta=sh.rope_theta)
+    return w, layer, build_proxy_matrix(w["w_v"], w["gamma1"], sh.r)
+
+
 class LayerWorkload:
     """One layer's resident state for repeated sparse refresh steps: weights (N(0, 0.02)),
     two drifted inputs that alternate step to step, caches from a full refresh of the
     previous input, and the forced rows (the current block's masked rows and the k_recent
-    decoded before them) when the shape has a vocabulary block."""
+    decoded before them) when the shape has a vocabulary block.  `shared` = (w, layer, Pt)
+    of another workload with the same layer shape reuses its weights."""
 
-    def __init__(self, sh, seed, dev):
+    def __init__(self, sh, seed, dev, shared=None):
         import torch
         from sparse_kv_cache_rank_gb300 import binding as B
         self.B_ = B
         self.sh = sh
         self.dev = dev
         bf = torch.float32 if sh.dtype == "f32" else torch.bfloat16
+        self.w, self.layer, self.Pt = shared if shared is not None else _layer_weights(sh, seed, dev)
         gen = torch.Generator(device=dev)
-        gen.manual_seed(seed)
+        gen.manual_seed(seed + 1)
 
         def randn(*shape, std=1.0):
             return torch.randn(shape, generator=gen, device=dev, dtype=torch.float32) * std
 
-        d, dq, dkv, F = sh.d, sh.d_q, sh.d_kv, sh.F
-        w = {"w_q": randn(dq, d, std=0.02).to(bf), "w_k": randn(dkv, d, std=0.02).to(bf),
-             "w_v": randn(dkv, d, std=0.02).to(bf), "w_o": randn(d, dq, std=0.02).to(bf),
-             "w_g": randn(F, d, std=0.02).to(bf), "w_u": randn(F, d, std=0.02).to(bf),
-             "w_d": randn(d, F, std=0.02).to(bf),
-             "gamma1": torch.ones(d, device=dev, dtype=bf), "gamma2": torch.ones(d, device=dev, dtype=bf)}
-        self.w = w
-        self.layer = B.dllm_pack_layer(w, sh.n_q, sh.n_kv, sh.hd, eps=sh.eps, rope_theta=sh.rope_theta)
-        self.Pt = B.build_proxy_matrix(w["w_v"], w["gamma1"], sh.r)
-        Bn, N = sh.B, sh.N
+        Bn, N, d = sh.B, sh.N, sh.d
         H_prev = randn(Bn, N, d)
         n_hot = int(round(0.1 * N))
 
@@ -193,10 +224,13 @@ class LayerWorkload:
         self.O = torch.empty((Bn, N, d), device=dev, dtype=bf)
         idx_all = torch.arange(N, device=dev, dtype=torch.int32).repeat(Bn, 1).contiguous()
         cnt_all = torch.full((Bn,), N, device=dev, dtype=torch.int32)
-        B.dllm_sparse_layer_refresh(self.layer, H_prev, idx_all, cnt_all, N, self.K, self.V, self.O)
+        ws_full = torch.empty(B.dllm_refresh_workspace_bytes(self.layer, Bn, N, N), device=dev, dtype=torch.uint8)
+        B.dllm_sparse_layer_refresh(self.layer, H_prev, idx_all, cnt_all, N, self.K, self.V, self.O, ws=ws_full)
+        del ws_full, idx_all, cnt_all
         self.pc = torch.empty((Bn, N, sh.r), device=dev, dtype=torch.float32)
         ones = torch.ones_like(self.pc)
         B.dllm_proxy_score(H_prev, self.Pt, ones, proxy_cur=self.pc, drift=torch.empty((Bn, N), device=dev))
+        del ones
         self.cur = torch.empty_like(self.pc)
         self.drift = torch.empty((Bn, N), device=dev, dtype=torch.float32)
         self.idx = torch.empty((Bn, N), device=dev, dtype=torch.int32)
@@ -211,9 +245,14 @@ class LayerWorkload:
             self.k_max = min(N, self.k + rows.numel())
         need = B.dllm_refresh_workspace_bytes(self.layer, Bn, N, self.k_max)
         self.ws = torch.empty(need, device=dev, dtype=torch.uint8)
+        pw = int(B.lib().dllm_proxy_workspace_bytes(Bn, N, d, sh.r, B.DLLM_BF16 if sh.dtype == "bf16" else B.DLLM_F32))
+        self.ws_proxy = torch.empty(max(pw, 256), device=dev, dtype=torch.uint8)
         self.H_prev = H_prev
         self.s = 0
         torch.cuda.synchronize(dev)
+
+    def shared(self):
+        return self.w, self.layer, self.Pt
 
     def step(self, H=None, idx=None, cnt=None):
         B = self.B_
@@ -222,10 +261,48 @@ class LayerWorkload:
         idx = self.idx if idx is None else idx
         cnt = self.cnt if cnt is None else cnt
         self.s += 1
-        B.dllm_proxy_score(H, self.Pt, self.pc, proxy_cur=self.cur, drift=self.drift)
+        B.dllm_proxy_score(H, self.Pt, self.pc, proxy_cur=self.cur, drift=self.drift, ws=self.ws_proxy)
         B.dllm_select_topk(self.drift, self.forced, self.k, idx=idx, count=cnt)
         B.dllm_sparse_layer_refresh(self.layer, H, idx, cnt, self.k_max, self.K, self.V, self.O,
                                     self.pc, self.cur, ws=self.ws)
+
+
+def kernel_breakdown(wl, reps=4):
+    """Mean CUDA-event duration of each kernel of the step (ms), each timed over `reps`
+    steps on the launch stream (outside the throughput pass)."""
+    B = wl.B_
+    out = {}
+    for name in layer_kernel_work(wl.sh, 1):
+        B.dllm_timer_start(name, 2 * reps)
+        for _ in range(reps):
+            wl.step()
+        ms, n = B.dllm_timer_stop()
+        out[name] = ms / max(n, 1)
+    return out
+
+
+def roofline_of(sh, M, kernel_ms, name, sustained):
+    """Roofline entry of kernel `name`: algorithmic bytes / FLOPs of one launch over its
+    event-timed duration, against the measured HBM copy or bf16 peak (whichever bounds the
+    kernel's work).  sustained: compare a tensor-bound kernel with the sustained bf16 figure
+    (a kernel timed inside a long step) instead of the burst one."""
+    bw, tc, tc_sus, src = peaks()
+    nbytes, flops = layer_kernel_work(sh, M)[name]
+    s = kernel_ms[name] / 1e3
+    if flops / (tc * 1e12) > nbytes / (bw * 1e9):
+        peak = tc_sus if sustained else tc
+        r = {"bound": "tensor", "achieved": flops / s / 1e12, "peak": peak, "unit": "TFLOP/s"}
+    else:
+        r = {"bound": "hbm", "achieved": nbytes / s / 1e9, "peak": bw, "unit": "GB/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    r["kernel"] = name
+    r["peak_source"] = src + (" (sustained bf16)" if r["bound"] == "tensor" and sustained else "")
+    return r
+
+
+def step_roofline_s(sh, M):
+    bw, tc, _, _ = peaks()
+    return sum(max(b / (bw * 1e9), f / (tc * 1e12)) for b, f in layer_kernel_work(sh, M).values())
 
 
 def native(args):
@@ -256,13 +333,7 @@ def native(args):
 
     # per-kernel breakdown (outside the timed region)
     work = layer_kernel_work(sh, M)
-    per_kernel = {}
-    for name in work:
-        B.dllm_timer_start(name, 8)
-        for _ in range(4):
-            wl.step()
-        ms, n = B.dllm_timer_stop()
-        per_kernel[name] = ms / max(n, 1)
+    per_kernel = kernel_breakdown(wl)
     dominant = max(per_kernel, key=per_kernel.get)
 
     # timed region
@@ -299,18 +370,84 @@ def native(args):
     instrumented_ms = e2.elapsed_time(e3) / args.steps
     B.check_status()
 
-    # end to end through the same calls with host buffers: every step copies its input
-    # from pinned host memory and reads its result (the selection) back, inside the timed
-    # region.  Inputs and selections are double-buffered and every copy runs on a second
-    # stream: after step s, that stream reads back step s's selection and uploads the input
-    # of step s + 2 into the freed buffers, so the compute stream carries only the step's
-    # kernels and one event wait per step.
+    e2e_elapsed, e2e_bytes = e2e_measure(wl, args.steps, barrier)
+
+    t = torch.tensor([elapsed, e2e_elapsed], device=dev, dtype=torch.float64)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    elapsed, e2e_elapsed = float(t[0]), float(t[1])
+
+    roof = roofline_of(sh, M, {dominant: dom_ms / max(dom_n, 1)}, dominant, sustained=False)
+    # DRAM bytes (read + write) per launch from the committed ncu capture; None for a
+    # kernel not captured there or changed since
+    roof["traffic"] = NCU_TRAFFIC_BYTES.get(dominant)
+    roof["timing"] = ("CUDA events around each launch of the kernel on its stream, over a second pass "
+                      f"of the {args.steps} timed steps ({instrumented_ms * 1e3:.1f} us/step with the events)")
+    steps_per_s = world * args.steps / elapsed
+    config = layer_config(sh, wl.k, world)
+    result = {
+        "metric": METRIC, "value": steps_per_s, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": DATA, "config": config,
+        "tokens_per_s": steps_per_s * sh.B * sh.N,
+        "refreshed_rows_per_s": steps_per_s * M,
+        "rows_per_step": M,
+        "roofline": roof,
+        "step_roofline_frac": step_roofline_s(sh, M) / (elapsed / args.steps),
+        "kernel_ms": {k: round(v, 5) for k, v in per_kernel.items()},
+        "kernel_roofline": {k: round(roofline_of(sh, M, per_kernel, k, False)["frac"], 4) for k in per_kernel
+                            if work[k][0] > 0},
+        "e2e": {"value": world * args.steps / e2e_elapsed, "unit": UNIT, **e2e_bytes},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(sh, args.cpu_full)
+    result["next_rows"] = {"kl_drift": kl_drift_measure(wl, args.steps, args.warmup),
+                           "confidence_extrapolation": ce_measure(dev, args.steps, args.warmup),
+                           "drift_aware_commit": polestar_measure(dev, args.steps, args.warmup),
+                           "cluster_proxy": cluster_measure(dev, args.steps, args.warmup)}
+    shared = wl.shared()
+    del wl
+    torch.cuda.empty_cache()
+    if not args.no_stack:
+        result["stack"] = stack_measure(dev, args.steps, args.warmup)
+        torch.cuda.empty_cache()
+        result["dream_stack"] = dream_stack_measure(dev, min(args.steps, 20), args.warmup)
+        torch.cuda.empty_cache()
+    if not args.no_configs:
+        result["configs"] = config_points(dev, shared, args.quick_sweep)
+    del shared
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def e2e_measure(wl, steps, barrier):
+    """The same steps through the same calls with host buffers: every step uploads its
+    input from pinned host memory and brings its result back -- the refreshed rows of the
+    output cache, of the key cache and of the value cache (packed by dllm_gather_rows) and
+    the selection -- inside the timed region.  Inputs, selections and packed rows are
+    double-buffered and every copy (and the packing) runs on a second stream: after step s
+    that stream packs and reads back step s's rows and uploads the input of step s + 2
+    into the freed buffers, so the compute stream carries only the step's kernels and one
+    event wait per step.  -> (seconds for `steps` steps, byte counts per step)."""
+    import torch
+    B = wl.B_
+    dev = wl.dev
+    sh = wl.sh
+    km = wl.k_max
     Hh = [wl.H[0].cpu().pin_memory(), wl.H[1].cpu().pin_memory()]
     Hd = [torch.empty_like(wl.H[0]), torch.empty_like(wl.H[0])]
     idx_d = [torch.empty_like(wl.idx), torch.empty_like(wl.idx)]
     cnt_d = [torch.empty_like(wl.cnt), torch.empty_like(wl.cnt)]
+    rows_d = [[torch.empty((sh.B * km,) + tuple(t.shape[2:]), dtype=t.dtype, device=dev) for t in (wl.O, wl.K, wl.V)]
+              for _ in range(2)]
     idx_h = [torch.empty(wl.idx.shape, dtype=torch.int32).pin_memory() for _ in range(2)]
     cnt_h = [torch.empty(wl.cnt.shape, dtype=torch.int32).pin_memory() for _ in range(2)]
+    rows_h = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in rows_d[0]] for _ in range(2)]
     main = torch.cuda.current_stream(dev)
     cs = torch.cuda.Stream(dev)
     ready = [torch.cuda.Event(), torch.cuda.Event()]   # input of the step in Hd[b] is resident
@@ -320,8 +457,12 @@ def native(args):
     def read_result(s):
         b = s & 1
         cs.wait_event(done[b])
+        for src, dst in zip((wl.O, wl.K, wl.V), rows_d[b]):
+            B.dllm_gather_rows(src, idx_d[b], cnt_d[b], km, dst)
         idx_h[b].copy_(idx_d[b], non_blocking=True)
         cnt_h[b].copy_(cnt_d[b], non_blocking=True)
+        for dsrc, hdst in zip(rows_d[b], rows_h[b]):
+            hdst.copy_(dsrc, non_blocking=True)
 
     def stage(s):   # on the copy stream: step s - 2's result out, step s's input in
         with torch.cuda.stream(cs):
@@ -354,85 +495,142 @@ def native(args):
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
     f0.record()
-    e2e_steps(args.steps, f0)
+    e2e_steps(steps, f0)
     f1.record()
     torch.cuda.synchronize(dev)
-    e2e_elapsed = f0.elapsed_time(f1) / 1e3
     barrier()
-
-    t = torch.tensor([elapsed, e2e_elapsed], device=dev, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    elapsed, e2e_elapsed = float(t[0]), float(t[1])
-
-    bw, tc, tc_sus, src = peaks()
-    dom_bytes, dom_flops = work[dominant]
-    dom_s = dom_ms / 1e3 / max(dom_n, 1)
-    if dom_flops / (tc * 1e12) > dom_bytes / (bw * 1e9):
-        roof = {"bound": "tensor", "achieved": dom_flops / dom_s / 1e12, "peak": tc_sus, "unit": "TFLOP/s"}
-    else:
-        roof = {"bound": "hbm", "achieved": dom_bytes / dom_s / 1e9, "peak": bw, "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    # DRAM bytes (read + write) per launch from the committed full ncu capture
-    # (profiles/gemm_attention_llada8b_full.md); None for a kernel not captured there
-    roof["traffic"] = NCU_TRAFFIC_BYTES.get(dominant)
-    roof["kernel"] = dominant
-    roof["timing"] = ("CUDA events around each launch of the kernel on its stream, over a second pass "
-                      f"of the {args.steps} timed steps ({instrumented_ms * 1e3:.1f} us/step with the events)")
-    roof["peak_source"] = src
-    step_roof_s = sum(max(b / (bw * 1e9), f / (tc * 1e12)) for b, f in work.values())
-    steps_per_s = world * args.steps / elapsed
-    result = {
-        "metric": METRIC, "value": steps_per_s, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic (seeded random-init weights N(0,0.02), drift model: 10% rows +N(0,0.5), all +N(0,0.05))",
-        "config": {"workload": f"llada8b-layer B={sh.B} N={sh.N} d={sh.d} heads={sh.n_q}x{sh.hd} F={sh.F} "
-                               f"r={sh.r} rho={sh.rho} k={wl.k}",
-                   "l2": "inputs larger than L2 (436 MB of weights per step)",
-                   "parallelism": f"replicas x{world}"},
-        "tokens_per_s": steps_per_s * sh.B * sh.N,
-        "refreshed_rows_per_s": steps_per_s * M,
-        "rows_per_step": M,
-        "roofline": roof,
-        "step_roofline_frac": step_roof_s / (elapsed / args.steps),
-        "kernel_ms": {k: round(v, 5) for k, v in per_kernel.items()},
-        "e2e": {"value": world * args.steps / e2e_elapsed, "unit": UNIT,
-                "h2d_bytes_per_step": int(wl.H[0].numel() * 2),
-                "d2h_bytes_per_step": int(wl.idx.numel() * 4 + wl.cnt.numel() * 4)},
-        "gpu_launches": int(launches),
-        "clocks": clk,
-    }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
-    result["next_rows"] = {"kl_drift": kl_drift_measure(wl, args.steps, args.warmup),
-                           "confidence_extrapolation": ce_measure(dev, args.steps, args.warmup),
-                           "drift_aware_commit": polestar_measure(dev, args.steps, args.warmup),
-                           "cluster_proxy": cluster_measure(dev, args.steps, args.warmup)}
-    if not args.no_stack or not args.no_configs:
-        del wl
-        torch.cuda.empty_cache()
-    if not args.no_stack:
-        result["stack"] = stack_measure(dev, args.steps, args.warmup)
-        torch.cuda.empty_cache()
-        result["dream_stack"] = dream_stack_measure(dev, min(args.steps, 20), args.warmup)
-    if not args.no_configs:
-        result["configs"] = config_points(dev, args.sweep)
-    if world > 1:
-        dist.destroy_process_group()
-    if rank == 0:
-        print(json.dumps(result), flush=True)
+    # the rows read back are the refreshed ones: compare the last step's packed output rows
+    # with the device cache (a consistency check of the copies, not of the method)
+    b = (steps - 1) & 1
+    c = int(cnt_h[b][0])
+    got = rows_h[b][0][:c].to(dev)
+    want = wl.O[0, idx_h[b][0, :c].to(dev).long()]
+    if not torch.equal(got, want):
+        raise RuntimeError("e2e read-back does not match the refreshed rows")
+    d2h = idx_h[0].numel() * 4 + cnt_h[0].numel() * 4 + sum(t.numel() * t.element_size() for t in rows_h[0])
+    return f0.elapsed_time(f1) / 1e3, {"h2d_bytes_per_step": int(Hh[0].numel() * Hh[0].element_size()),
+                                       "d2h_bytes_per_step": int(d2h),
+                                       "d2h": "refreshed rows of the output, key and value caches "
+                                              f"({sh.B}x{km} rows each, packed by dllm_gather_rows) + the selection"}
 
 
 # --------------------------------------------------------------------------- full stack
+def stale_proxies(st, seed):
+    """Cached proxies of every layer taken from a drifted copy of the layer's current
+    input -- the drift model of the layer workloads (+N(0, 0.05) on every row, +N(0, 0.5)
+    on 10% of the rows) applied at every depth, the state a layer's cache reaches when its
+    inputs moved since it last refreshed them.  Restoring them before a partial step makes
+    every layer score drift on every row, so each refreshes its full budget rho(l)."""
+    import torch
+    from sparse_kv_cache_rank_gb300 import binding as B
+    dev = st.dev
+    sh = st.sh
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    out = torch.empty_like(st.pc_all)
+    ones = torch.ones_like(st.pc_all[0])
+    drift = torch.empty((sh.B, sh.N), device=dev)
+    n_hot = int(round(0.1 * sh.N))
+    H = st.H0
+    for l, L in enumerate(st.layers):
+        X = H.float() + torch.randn(H.shape, generator=gen, device=dev) * 0.05
+        for b in range(sh.B):
+            rows = torch.randperm(sh.N, generator=gen, device=dev)[:n_hot]
+            X[b, rows] += torch.randn((n_hot, sh.d), generator=gen, device=dev) * 0.5
+        B.dllm_proxy_score(X.to(H.dtype).contiguous(), L.Pt, ones, proxy_cur=out[l], drift=drift)
+        H = L.O
+    torch.cuda.synchronize(dev)
+    return out
+
+
+def _second_block(st, seed):
+    """The state at the start of the second generation block: the first block decoded
+    (random ids), its last k_recent positions the recent history, so the forced rows are
+    the new block's masked positions plus the k_recent recent ones."""
+    import torch
+    from sparse_kv_cache_rank_gb300 import binding as B
+    sh = st.sh
+    g = torch.Generator()
+    g.manual_seed(seed)
+    start = sh.prompt
+    st.tokens_host[:, start:start + sh.block] = torch.randint(0, sh.V - 1, (sh.B, sh.block), generator=g,
+                                                              dtype=torch.int32)
+    for h in st.history:
+        h.clear()
+        h.extend(range(start + sh.block - st.k_recent, start + sh.block))
+    st.tokens.copy_(st.tokens_host.to(st.dev))
+    B.dllm_embed(st.E, st.tokens, st.H0)
+    st.block = 1
+    st._set_block_rows()
+
+
+def _stack_forced_sparse(st, steps, warmup, seed):
+    """The partial denoising step at every layer's budget (see stale_proxies), timed from
+    replays of one captured CUDA graph (restore of the cached proxies + the step) and, for
+    comparison, issued eagerly through the binding."""
+    import torch
+    pc_stale = stale_proxies(st, seed)
+
+    def step():
+        st.pc_all.copy_(pc_stale)
+        return st.forward(False)
+
+    st.pc_all.copy_(pc_stale)
+    rec = []
+    st.forward(False, record=rec)
+    rows = [int(r["cnt"].sum().item()) for r in rec]
+    g = st.graph(step, warmup=max(warmup, 2))
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize(st.dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize(st.dev)
+    dt = e0.elapsed_time(e1) / 1e3 / steps
+    committed = int((st.out[0] >= 0).sum().item())
+    # the same step issued call by call from the host (no graph)
+    t0 = time.perf_counter()
+    e0.record()
+    for _ in range(steps):
+        step()
+    t_issue = (time.perf_counter() - t0) / steps
+    e1.record()
+    torch.cuda.synchronize(st.dev)
+    dt_eager = e0.elapsed_time(e1) / 1e3 / steps
+    del g
+    return dt, dt_eager, t_issue, committed, rows
+
+
+def _decode_loop(st, warmup, decode_steps):
+    """Rule-driven decoding from a fresh prefill, each step replayed from the stack's
+    captured graphs, with the host-side commit (one device->host read per step)."""
+    import torch
+    st.capture()
+    st.prefill()
+    for _ in range(max(warmup, 2)):
+        st.decode_step()
+    torch.cuda.synchronize(st.dev)
+    n_full, toks = 0, 0
+    t0 = time.perf_counter()
+    for _ in range(decode_steps):
+        n_full += 1 if st.full_next else 0
+        toks += st.decode_step()
+    torch.cuda.synchronize(st.dev)
+    return time.perf_counter() - t0, n_full, toks
+
+
 def stack_measure(dev, steps, warmup, decode_steps=48):
     """32-layer LLaDA-8B-shaped stack (N=768: 512 prompt + 256 generation, block 32,
     vocab 126464, rho(l) piecewise Gaussian, 8 recent tokens forced).
 
     forced_sparse: the denoising step with the full/partial decision overridden to
-      partial, device-timed; two drifted layer-0 inputs alternate so that every step
-      sees drift (refreshed rows per layer are reported as measured: a layer can only
-      pick rows whose input changed since it last refreshed them).
+      partial, every layer at its budget rho(l) plus the forced rows (cached proxies from
+      the drift model at every depth, restored inside each timed step), device-timed from
+      CUDA graph replays; the same step issued eagerly is reported beside it.
     rule_driven: the decode loop with the host-side commit (one device->host read per
       step), wall-clock timed; with random weights the maximum entropy always exceeds
       tau, so every step is a full forward.
@@ -442,124 +640,76 @@ def stack_measure(dev, steps, warmup, decode_steps=48):
     from sparse_kv_cache_rank_gb300.stack import DecodeStack
     sh = synth.LLADA_STACK
     t0 = time.perf_counter()
-    st = DecodeStack(sh, 4321, dev, k_recent=8, proxy_method="lowrank")
+    st = DecodeStack(sh, 4321, dev, k_recent=8)
+    _second_block(st, 5)
     st.prefill()
     setup_s = time.perf_counter() - t0
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(99)
-    H0 = []
-    for _ in range(2):
-        h = st.H0.float() + torch.randn(st.H0.shape, generator=gen, device=dev) * 0.002
-        H0.append(h.to(st.H0.dtype).contiguous())
-    for s in range(max(warmup, 3)):
-        st.forward(False, H0=H0[s & 1])
-    torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for s in range(steps):
-        out = st.forward(False, H0=H0[s & 1])
-    e1.record()
-    torch.cuda.synchronize(dev)
-    sparse_s = e0.elapsed_time(e1) / 1e3 / steps
-    committed = int((out[0] >= 0).sum().item())
-    rows = st.count_rows(False)
-    # rule-driven decode loop from a fresh prefill; the first decode steps are warm-up (the
-    # first one pays one-time lazy loading of the kernels the host commit path uses)
-    st.prefill()
-    for _ in range(max(warmup, 3)):
-        st.decode_step()
-    torch.cuda.synchronize(dev)
-    n_full, toks = 0, 0
-    t0 = time.perf_counter()
-    for _ in range(decode_steps):
-        n_full += 1 if st.full_next else 0
-        toks += st.decode_step()
-    torch.cuda.synchronize(dev)
-    dec_s = time.perf_counter() - t0
-    return {
+    dt, dt_eager, t_issue, committed, rows = _stack_forced_sparse(st, steps, warmup, 99)
+    forced = int((st.forced >= 0).sum().item())
+    dec_s, n_full, toks = _decode_loop(st, warmup, decode_steps)
+    res = {
         "workload": f"llada8b-stack layers={sh.layers} B={sh.B} N={sh.N} d={sh.d} V={sh.V} "
                     f"rho(l)=0.05+0.25exp(-(l-16)^2/72) k_recent=8",
-        "forced_sparse": {"steps_per_s": 1.0 / sparse_s, "ms_per_step": sparse_s * 1e3,
-                          "tokens_per_s": committed / sparse_s,
-                          "rows_refreshed_per_layer": rows,
-                          "budget_per_layer": st.budgets, "timing": "cuda events, device"},
-        "rule_driven": {"steps": decode_steps, "warmup": max(warmup, 3), "steps_per_s": decode_steps / dec_s,
+        "forced_sparse": {"steps_per_s": 1.0 / dt, "ms_per_step": dt * 1e3,
+                          "tokens_per_s": committed / dt, "context_tokens_per_s": sh.B * sh.N / dt,
+                          "rows_refreshed_per_layer": rows, "budget_per_layer": st.budgets,
+                          "forced_rows": forced,
+                          "eager": {"ms_per_step": dt_eager * 1e3, "host_issue_ms_per_step": t_issue * 1e3},
+                          "timing": "cuda events around CUDA graph replays of the step (the cached-proxy "
+                                    "restore included)"},
+        "rule_driven": {"steps": decode_steps, "warmup": max(warmup, 2), "steps_per_s": decode_steps / dec_s,
                         "tokens_per_s": toks / dec_s, "full_steps": n_full,
-                        "timing": "wall clock incl. one device->host read and host commit per step"},
+                        "timing": "wall clock, graph-replayed steps incl. one device->host read and the "
+                                  "host commit per step"},
         "setup_s": setup_s,
     }
+    del st
+    torch.cuda.empty_cache()
+    return res
 
 
 def dream_stack_measure(dev, steps, warmup, decode_steps=8):
     """28-layer Dream-7B-shaped stack (Qwen2.5-7B layout: d=3584, 28 query / 4 KV heads x
     128, FFN 18944), batch 8, N=2048 (1024 prompt + 1024 generation, block 32), vocab
     152064, uniform 16 % update ratio (k = 328 per sequence) plus the block's rows and the
-    8 most recent tokens forced.
-
-    forced_sparse: the partial denoising step (28 layer refreshes, the fused LM head and
-      the commit) timed on the device with CUDA events.
-    rule_driven: the decode loop with the host-side commit of all 8 sequences (one
-      device->host read per step), wall-clock timed; with random weights the entropy
-      exceeds tau, so every step is a full forward of the 8 x 2048 rows.
-    """
+    8 most recent tokens forced; the same two modes as the LLaDA stack."""
     import torch
     from sparse_kv_cache_rank_gb300 import synth
     from sparse_kv_cache_rank_gb300.stack import DecodeStack
     sh = synth.DREAM_STACK
     t0 = time.perf_counter()
-    st = DecodeStack(sh, 2468, dev, uniform_rho=sh.rho, k_recent=8, proxy_method="lowrank")
+    st = DecodeStack(sh, 2468, dev, uniform_rho=sh.rho, k_recent=8)
+    _second_block(st, 5)
     st.prefill()
     setup_s = time.perf_counter() - t0
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(98)
-    H0 = []
-    for _ in range(2):
-        h = st.H0.float() + torch.randn(st.H0.shape, generator=gen, device=dev) * 0.002
-        H0.append(h.to(st.H0.dtype).contiguous())
-    for s in range(max(warmup, 3)):
-        st.forward(False, H0=H0[s & 1])
-    torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for s in range(steps):
-        out = st.forward(False, H0=H0[s & 1])
-    e1.record()
-    torch.cuda.synchronize(dev)
-    dt = e0.elapsed_time(e1) / 1e3 / steps
-    committed = int((out[0] >= 0).sum().item())
-    rows = st.count_rows(False)
-    st.prefill()
-    for _ in range(2):
-        st.decode_step()
-    torch.cuda.synchronize(dev)
-    n_full, toks = 0, 0
-    t0 = time.perf_counter()
-    for _ in range(decode_steps):
-        n_full += 1 if st.full_next else 0
-        toks += st.decode_step()
-    torch.cuda.synchronize(dev)
-    dec_s = time.perf_counter() - t0
+    dt, dt_eager, t_issue, committed, rows = _stack_forced_sparse(st, steps, warmup, 98)
+    forced = int((st.forced >= 0).sum().item())
+    dec_s, n_full, toks = _decode_loop(st, 2, decode_steps)
     res = {"workload": f"dream7b-stack layers={sh.layers} B={sh.B} N={sh.N} d={sh.d} "
                        f"heads={sh.n_q}q/{sh.n_kv}kv x {sh.hd} F={sh.F} V={sh.V} rho={sh.rho} k_recent=8",
            "forced_sparse": {"steps_per_s": 1.0 / dt, "ms_per_step": dt * 1e3,
                              "context_tokens_per_s": sh.B * sh.N / dt, "committed_tokens_per_s": committed / dt,
                              "rows_refreshed_per_layer": rows, "budget_per_layer": st.budgets[0],
-                             "steps": steps, "timing": "cuda events, device"},
+                             "forced_rows": forced,
+                             "eager": {"ms_per_step": dt_eager * 1e3, "host_issue_ms_per_step": t_issue * 1e3},
+                             "steps": steps,
+                             "timing": "cuda events around CUDA graph replays of the step (the cached-proxy "
+                                       "restore included)"},
            "rule_driven": {"steps": decode_steps, "warmup": 2, "steps_per_s": decode_steps / dec_s,
                            "tokens_per_s": toks / dec_s, "full_steps": n_full,
-                           "timing": "wall clock incl. one device->host read and host commit per step"},
+                           "timing": "wall clock, graph-replayed steps incl. one device->host read and the "
+                                     "host commit per step"},
            "setup_s": setup_s}
-    del st, H0, out
+    del st
     torch.cuda.empty_cache()
     return res
 
 
-def layer_point(sh, dev, steps, warmup, seed=77):
-    """Layer-steps/s of one configuration (CUDA events over `steps` resident steps)."""
+def layer_point(sh, dev, steps, warmup, seed=77, shared=None):
+    """Layer-steps/s of one configuration (CUDA events over `steps` resident steps), the
+    per-kernel event times and the dominant kernel's roofline fraction."""
     import torch
-    wl = LayerWorkload(sh, seed, dev)
+    wl = LayerWorkload(sh, seed, dev, shared=shared)
     for _ in range(max(warmup, 3)):
         wl.step()
     torch.cuda.synchronize(dev)
@@ -572,9 +722,17 @@ def layer_point(sh, dev, steps, warmup, seed=77):
     torch.cuda.synchronize(dev)
     dt = e0.elapsed_time(e1) / 1e3 / steps
     rows = int(wl.cnt.sum().item())
+    per_kernel = kernel_breakdown(wl, reps=3) if sh.dtype == "bf16" else None
     res = {"B": sh.B, "N": sh.N, "rho": sh.rho, "rows_per_step": rows, "dtype": sh.dtype,
            "steps_per_s": 1.0 / dt, "ms_per_step": dt * 1e3, "tokens_per_s": sh.B * sh.N / dt,
            "refreshed_rows_per_s": rows / dt}
+    if per_kernel is not None:
+        dom = max(per_kernel, key=per_kernel.get)
+        res["kernel_ms"] = {k: round(v, 5) for k, v in per_kernel.items()}
+        res["roofline"] = roofline_of(sh, rows, per_kernel, dom, sustained=True)
+        res["kernel_roofline"] = {k: round(roofline_of(sh, rows, per_kernel, k, True)["frac"], 4)
+                                  for k in per_kernel if layer_kernel_work(sh, rows)[k][0] > 0}
+        res["step_roofline_frac"] = step_roofline_s(sh, rows) / dt
     del wl
     torch.cuda.empty_cache()
     return res
@@ -721,10 +879,12 @@ def cluster_measure(dev, steps, warmup):
             "note": "launch-bound at a 96-row window (13 small launches)", "timing": GRAPH_TIMING}
 
 
-def config_points(dev, full_sweep):
+def config_points(dev, shared, quick):
     """The other layer configurations: the tiny fp32 layer (forced block rows), the
-    Dream-7B-shaped layer (batch 8, GQA) and the long-context LLaDA-8B-shaped points
-    (all 36 with full_sweep, else batch 1 at 5% / 16% / 100%)."""
+    Dream-7B-shaped layer (batch 8, GQA) and the long-context sweep of the LLaDA-8B-shaped
+    layer, N x batch x update ratio (all 36 points; quick: batch 1 without 50 %), every
+    bf16 point with its per-kernel times and the dominant kernel's roofline fraction.  The
+    sweep points share the layer's weights with the headline workload."""
     import dataclasses
     from sparse_kv_cache_rank_gb300 import synth
     out = {"tiny_fp32": layer_point(synth.TINY, dev, 100, 5)}
@@ -732,61 +892,138 @@ def config_points(dev, full_sweep):
     out["dream7b_layer"] = layer_point(dream, dev, 20, 3)
     pts = []
     for sh in synth.sweep_shapes():
-        if not full_sweep and (sh.B != 1 or sh.rho == 0.5):
+        if quick and (sh.B != 1 or sh.rho == 0.5):
             continue
-        pts.append(layer_point(sh, dev, 20, 3))
+        pts.append(layer_point(sh, dev, 10 if sh.B * sh.N * sh.rho > 20000 else 20, 3, shared=shared))
     out["long_context"] = pts
     return out
 
 
 # --------------------------------------------------------------------------- oracle legs
-def _oracle_sample_inputs(wl):
-    """Host copies of one resident step's inputs (identical values to the GPU leg)."""
-    import torch
-    f = lambda t: t.float().cpu().numpy()
-    sh = wl.sh
-    w = {k: f(v) for k, v in wl.w.items()}
-    return dict(w=w, P=np.ascontiguousarray(f(wl.Pt).T), H=f(wl.H[0]), pc=f(wl.pc),
-                K=f(wl.K).reshape(sh.B, sh.N, sh.d_kv), V=f(wl.V).reshape(sh.B, sh.N, sh.d_kv),
-                O=f(wl.O))
+def cpu_model() -> str:
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
 
 
-def _oracle_step_sample(orc, sh, inp, frac):
-    """A fraction `frac` of one layer step on the oracle: proxy + drift of frac*N rows,
-    selection over the whole sequence, refresh of frac*k rows (both linear in rows)."""
-    n_rows = max(1, int(round(frac * sh.N)))
-    cur, drift = orc.proxy_score(inp["H"][:, :n_rows], inp["P"], inp["pc"][:, :n_rows])
-    k = orc.budget(sh.rho, sh.N)
-    d_full = np.zeros((sh.B, sh.N), np.float32)
-    d_full[:, :n_rows] = drift
-    idx, cnt = orc.select_topk(d_full, None, k)
-    n_sel = max(1, int(round(frac * k)))
-    idx_s = np.full_like(idx, -1)
-    idx_s[:, :n_sel] = np.arange(n_sel, dtype=np.int32)[None] * max(1, sh.N // n_sel)
-    cnt_s = np.full(sh.B, n_sel, np.int32)
-    L = orc.Layer(inp["w"], sh.n_q, sh.n_kv, sh.hd, eps=sh.eps, rope_theta=sh.rope_theta)
-    K, V, O = inp["K"].copy(), inp["V"].copy(), inp["O"].copy()
-    orc.layer_refresh(L, inp["H"], idx_s, cnt_s, K, V, O)
+class OracleLayer:
+    """One layer's state on the host for whole oracle steps: fp32 copies of the weights,
+    the proxy matrix, the two alternating inputs, the caches and cached proxies, the
+    forced rows.  Each step is the native step's work: the proxy and drift of all B*N
+    rows, the selection, the refresh of the selected rows (caches updated in place)."""
+
+    def __init__(self, orc, sh, w, P, H, K, V, O, pc, forced):
+        self.orc, self.sh = orc, sh
+        self.L = orc.Layer(w, sh.n_q, sh.n_kv, sh.hd, eps=sh.eps, rope_theta=sh.rope_theta)
+        self.P, self.H, self.forced = P, H, forced
+        self.state0 = (K, V, O, pc)
+        self.reset()
+
+    def reset(self):
+        """Back to the first step's state: caches and cached proxies of the previous input."""
+        self.K, self.V, self.O, self.pc = (a.copy() for a in self.state0)
+        self.s = 0
+
+    def step(self, k):
+        orc, sh = self.orc, self.sh
+        H = self.H[self.s & 1]
+        self.s += 1
+        cur, drift = orc.proxy_score(H, self.P, self.pc)
+        idx, cnt = orc.select_topk(drift, self.forced, k)
+        orc.layer_refresh(self.L, H, idx, cnt, self.K, self.V, self.O, self.pc, cur)
+        return int(cnt.sum())
 
 
-def cpu_baseline(wl, seconds):
+def _time_oracle(ol, k, threads, budget_s, max_reps=8):
+    """Whole oracle steps at `threads` threads: one step, then more while the total stays
+    within budget_s.  -> (seconds per step, steps timed, rows per step)."""
+    ol.orc.set_threads(threads)
+    ol.reset()
+    t0 = time.perf_counter()
+    rows = ol.step(k)
+    t1 = time.perf_counter() - t0
+    reps = 1
+    tot = t1
+    while reps < max_reps and tot + t1 <= budget_s:
+        t0 = time.perf_counter()
+        ol.step(k)
+        tot += time.perf_counter() - t0
+        reps += 1
+    return tot / reps, reps, rows
+
+
+def cpu_baseline(sh, full):
+    """The oracle, as it stands, timed on the host cores: whole layer steps (no sample is
+    scaled up) from the first step's state, each with all host threads and with one
+    thread, for the LLaDA-8B-shaped layer at its 16 % budget and at 100 % (the full
+    recompute) and for the tiny fp32 layer.  The inputs are drawn on the host with the
+    native workload's shapes, distributions and construction (reference_inputs).  Points
+    whose single-thread step would exceed a minute (from the all-thread time x the thread
+    count) are listed as not run unless `full`."""
     import oracle as orc
+    from sparse_kv_cache_rank_gb300 import synth
     orc.build()
     cores = os.cpu_count() or 1
     orc.set_threads(cores)
-    inp = _oracle_sample_inputs(wl)
-    frac = 1.0 / 8
-    t0 = time.perf_counter()
-    _oracle_step_sample(orc, wl.sh, inp, frac)
-    t1 = time.perf_counter() - t0
-    reps = max(1, min(8, int(seconds / max(t1, 1e-3))))
-    t0 = time.perf_counter()
-    for _ in range(reps):
-        _oracle_step_sample(orc, wl.sh, inp, frac)
-    dt = (time.perf_counter() - t0) / reps
-    return {"value": frac / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{reps} x 1/8 of a layer step (proxy of N/8 rows, refresh of k/8 rows), "
-                      f"scaled by 8; {dt:.2f} s per sample"}
+    pts = []
+    ol = reference_inputs(orc, sh, 1234)
+    ot = reference_inputs(orc, synth.TINY, 77)
+    k = orc.budget(sh.rho, sh.N)
+    cases = [("llada8b-layer", ol, k), ("llada8b-layer 100%", ol, sh.N),
+             ("tiny-fp32", ot, orc.budget(synth.TINY.rho, synth.TINY.N)), ("tiny-fp32 100%", ot, synth.TINY.N)]
+    head = None
+    for name, o, k in cases:
+        t_all, reps, rows = _time_oracle(o, k, cores, 20.0)
+        pts.append({"point": name, "threads": cores, "s_per_step": t_all, "steps_per_s": 1.0 / t_all,
+                    "steps_timed": reps, "rows_per_step": rows})
+        if name == "llada8b-layer":
+            head = (t_all, reps)
+        if full or t_all * cores <= 60.0:
+            t1, reps1, _ = _time_oracle(o, k, 1, 60.0)
+            pts.append({"point": name, "threads": 1, "s_per_step": t1, "steps_per_s": 1.0 / t1,
+                        "steps_timed": reps1, "rows_per_step": rows})
+        else:
+            pts.append({"point": name, "threads": 1, "not_run": "cap: one step > 60 s expected "
+                        f"({t_all * cores:.0f} s from the {cores}-thread time); run with --cpu-full"})
+    t_all, reps = head
+    return {"value": 1.0 / t_all, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{reps} whole LLaDA-8B-shaped layer steps (proxy of all {sh.N} rows, selection, refresh "
+                      f"of {k} rows) from the first step's state, on host-drawn inputs of the same workload, "
+                      f"{cores} threads; not extrapolated",
+            "cpu_model": cpu_model(), "points": pts}
+
+
+def reference_inputs(orc, sh, seed):
+    """The native arm's workload drawn on the host (same shapes, distributions and
+    construction: N(0, 0.02) weights, the SVD proxy, two drifted inputs, caches from the
+    oracle's dense forward on the previous input, cached proxies of that input)."""
+    from sparse_kv_cache_rank_gb300 import synth
+    w = synth.layer_weights(sh, seed)
+    P = synth.round_bf16(orc.proxy_matrix(w["w_v"], w["gamma1"], sh.r).astype(np.float32)) \
+        if sh.dtype == "bf16" else orc.proxy_matrix(w["w_v"], w["gamma1"], sh.r).astype(np.float32)
+    H_prev, H0, _ = synth.hidden_pair(sh, seed + 1)
+    H1 = synth.drifted(sh, H0, seed + 2)
+    L = orc.Layer(w, sh.n_q, sh.n_kv, sh.hd, eps=sh.eps, rope_theta=sh.rope_theta)
+    rnd = synth.round_bf16 if sh.dtype == "bf16" else (lambda a: a)
+    K, V, O = (rnd(a) for a in orc.layer_full(L, H_prev))
+    pc, _ = orc.proxy_score(H_prev, P, np.ones((sh.B, sh.N, sh.r), np.float32))
+    forced = None
+    if sh.V and sh.k_recent:
+        rows = np.arange(sh.prompt - sh.k_recent, sh.prompt + sh.block - sh.k_recent, dtype=np.int32)
+        forced = np.repeat(rows[None], sh.B, 0)
+    del L
+    return OracleLayer(orc, sh, w, P, [H0, H1], K, V, O, pc, forced)
 
 
 def reference(args):
@@ -798,36 +1035,26 @@ def reference(args):
     orc.build()
     cores = os.cpu_count() or 1
     orc.set_threads(cores)
-    sh = synth.LLADA_LAYER
-    # same shapes and value distributions as the native arm, drawn on the host
-    g = synth.rng(1234)
-    bf = synth.round_bf16
-    w = synth.layer_weights(sh, 1234)
-    H = bf(g.standard_normal((sh.B, sh.N, sh.d), dtype=np.float32))
-    P = bf((g.standard_normal((sh.d, sh.r)) * 0.02).astype(np.float32))
-    sc = np.float32(0.02 * np.sqrt(sh.d))
-    inp = dict(w=w, P=P, H=H, pc=g.standard_normal((sh.B, sh.N, sh.r), dtype=np.float32),
-               K=bf(g.standard_normal((sh.B, sh.N, sh.d_kv), dtype=np.float32) * sc),
-               V=bf(g.standard_normal((sh.B, sh.N, sh.d_kv), dtype=np.float32) * sc),
-               O=bf(g.standard_normal((sh.B, sh.N, sh.d), dtype=np.float32)))
-    frac = 1.0 / 8
+    sh = synth.TINY if args.reference_workload == "tiny-fp32" else synth.LLADA_LAYER
+    ol = reference_inputs(orc, sh, 1234)
+    k = orc.budget(sh.rho, sh.N)
     for _ in range(args.warmup):
-        _oracle_step_sample(orc, sh, inp, frac)
+        ol.step(k)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _oracle_step_sample(orc, sh, inp, frac)
+        ol.step(k)
     dt = (time.perf_counter() - t0) / max(args.steps, 1)
-    v = frac / dt
+    v = 1.0 / dt
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / v, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded, same shapes and distributions as the native arm)",
-        "config": {"workload": f"llada8b-layer B={sh.B} N={sh.N} d={sh.d} heads={sh.n_q}x{sh.hd} "
-                               f"F={sh.F} r={sh.r} rho={sh.rho} k={orc.budget(sh.rho, sh.N)}"},
+        "data": DATA, "config": layer_config(sh, k, args.gpus),
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": "each step = 1/8 of a layer step (proxy of N/8 rows, refresh of "
-                                   "k/8 rows) on the CPU oracle, scaled by 8"},
+                         "sample": f"{args.steps} whole layer steps of the CPU oracle (proxy of all rows, "
+                                   f"selection, refresh of the selected rows) after {args.warmup} warm-up "
+                                   f"steps, {cores} threads",
+                         "cpu_model": cpu_model()},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 

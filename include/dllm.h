@@ -66,7 +66,9 @@ const char *dllm_last_error(void);
 /* Library ABI version (major * 100 + minor): 1.00 holds the path's calls and the
  * allocation-free vocabulary step (dllm_commit_entropy_noalloc); 1.10 adds the NEXT-row
  * calls (KL drift, drift-aware commit, confidence extrapolation, cluster-granular
- * proxy); 1.11 the host-only GEMM plan query (dllm_gemm_plan). */
+ * proxy); 1.11 the host-only GEMM plan query (dllm_gemm_plan); 1.12 the read-back of
+ * refreshed rows (dllm_gather_rows) and the bounded-wait diagnostic
+ * (dllm_check_wait_timeout). */
 int dllm_version(void);
 
 /* Reads (and with reset != 0 clears) the device status word of the current device.
@@ -74,6 +76,15 @@ int dllm_version(void);
  * DLLM_ERR_CUDA if the shared-memory layout bit is set, DLLM_OK otherwise;
  * *status_out (optional) receives all bits. */
 int dllm_check_status(unsigned *status_out, int reset);
+
+/* Diagnostic of the failure path that replaces traps (no counterpart on the pages): one
+ * CTA of 64 threads waits, with the same bounded mbarrier wait every pipelined kernel of
+ * the library uses, on a barrier that nothing ever completes.  The wait gives up after
+ * its limit (1 s), raises DLLM_STATUS_TIMEOUT and the kernel returns; *gave_up (device,
+ * int32) receives the number of threads whose wait returned false (64 when the path
+ * works).  A following dllm_check_status() reports DLLM_ERR_TIMEOUT, and the context
+ * stays usable.  Errors: INVALID_ARG (null gave_up), CUDA (launch). */
+int dllm_check_wait_timeout(int32_t *gave_up, void *stream);
 
 /* ---------------------------------------------------------------------------
  * [SPA] "1. Update identification via singular proxy"
@@ -395,6 +406,21 @@ int dllm_embed(const void *E, const int32_t *tokens, const int32_t *rows, int R,
 
 int dllm_rows_rmsnorm(const void *H, const int32_t *rows, int R, const void *gamma, float eps,
                       void *out, int B, int N, int d, int dtype, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * [SPA] "3. Sparse execution": the rows a refresh rewrote, packed for the caller (the
+ * refreshed hidden states, keys or values that leave the device after a step):
+ *   dst[b * k_max + s] = src[b, idx[b, s]]   for s < min(count[b], k_max) and
+ *                                            idx[b, s] in [0, N);
+ *   dst[b * k_max + s] = 0 bytes             for the other rows.
+ * src [B, N, row_bytes] bytes (H_out_cache rows: row_bytes = d * element size; K/V cache
+ * rows: n_kv * hd * element size), dst [B * k_max, row_bytes]; idx [B, N] and count [B]
+ * int32 as written by dllm_select_topk.  Requirements: row_bytes % 16 == 0, src and dst
+ * 16-byte aligned, 0 < k_max <= N.  No workspace.  Errors: INVALID_ARG (null pointer,
+ * sizes, alignment), CUDA (launch).
+ * ------------------------------------------------------------------------- */
+int dllm_gather_rows(const void *src, const int32_t *idx, const int32_t *count, int k_max, void *dst,
+                     int B, int N, int row_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
  * Plain product on the tensor cores, the engine under every bf16 projection above

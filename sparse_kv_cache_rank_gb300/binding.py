@@ -78,6 +78,8 @@ _SIGS = {
                    + [C.c_void_p]),
     "dllm_rows_rmsnorm": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_void_p, C.c_float, C.c_void_p]
                           + [C.c_int] * 4 + [C.c_void_p]),
+    "dllm_check_wait_timeout": (C.c_int, [C.c_void_p, C.c_void_p]),
+    "dllm_gather_rows": (C.c_int, [C.c_void_p] * 5 + [C.c_int] * 3 + [C.c_void_p]),
     "dllm_commit_entropy_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                               C.c_float, C.c_float] + [C.c_void_p] * 6),
     "dllm_commit_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
@@ -165,6 +167,18 @@ def check_status(reset: bool = True) -> int:
         raise DllmError(f"device status 0x{st.value:x}: a kernel wait timed out")
     _check(rc, "dllm_check_status")
     return st.value
+
+
+def dllm_check_wait_timeout():
+    """Runs the library's bounded-wait diagnostic (about one second on the device) and
+    returns (threads whose wait gave up, the return code of dllm_check_status after it,
+    the status bits); the status word is cleared."""
+    dev = torch.cuda.current_device()
+    out = torch.zeros(1, dtype=torch.int32, device=dev)
+    _check(lib().dllm_check_wait_timeout(_ptr(out), _stream(dev)), "dllm_check_wait_timeout")
+    st = C.c_uint(0)
+    rc = lib().dllm_check_status(C.byref(st), 1)
+    return int(out.item()), rc, st.value
 
 
 # --------------------------------------------------------------------------- measurement
@@ -336,33 +350,6 @@ def dllm_cluster_select(C_now, C_prev, assign, kc: int, idx=None, count=None):
     return idx, count
 
 
-def build_proxy_matrix(w_v: torch.Tensor, gamma1: torch.Tensor, r: int, method: str = "svd",
-                       generator=None, oversample: int = 16, iters: int = 4) -> torch.Tensor:
-    """One-time set-up (not part of the per-step path): Pt = (U_r S_r)^T of
-    diag(gamma1) W_V^T in double precision on the device, returned in w_v's dtype.
-
-    method="svd": full SVD.  method="lowrank": randomized range finder with `iters`
-    subspace iterations and `oversample` extra columns, then the SVD of the small
-    projected matrix (top-r singular pairs up to the iteration's accuracy; used to set
-    up many large layers quickly when only throughput is measured)."""
-    A = gamma1.double()[:, None] * w_v.double().t()          # [d, d_kv]
-    if method == "svd":
-        U, S, _ = torch.linalg.svd(A, full_matrices=False)
-    elif method == "lowrank":
-        k = min(r + oversample, min(A.shape))
-        G = torch.randn(A.shape[1], k, generator=generator, device=A.device, dtype=torch.float32).double()
-        Y = A @ G
-        for _ in range(iters):
-            Q, _ = torch.linalg.qr(Y)
-            Y = A @ (A.t() @ Q)
-        Q, _ = torch.linalg.qr(Y)
-        Ub, S, _ = torch.linalg.svd(Q.t() @ A, full_matrices=False)
-        U = Q @ Ub
-    else:
-        raise DllmError(f"unknown method {method}")
-    return (U[:, :r] * S[:r]).t().contiguous().to(w_v.dtype)
-
-
 # --------------------------------------------------------------------------- selection
 def dllm_select_topk(drift, forced, k: int, min_drift: float = 1e-6, idx=None, count=None):
     """drift [B,N] f32, forced [B,F] int32 (-1 padded) or None ->
@@ -483,6 +470,21 @@ def dllm_rows_rmsnorm(H, rows, gamma, eps: float = 1e-5, out=None):
     _check(lib().dllm_rows_rmsnorm(_ptr(H), _ptr(rows), R, _ptr(gamma), float(eps), _ptr(out), B, N,
                                    d, _dtype_code(H), _stream(H.device)), "dllm_rows_rmsnorm")
     return out
+
+
+def dllm_gather_rows(src, idx, count, k_max: int, dst=None):
+    """src [B, N, ...] (any row layout, rows of a multiple of 16 bytes) ->
+    dst [B*k_max, ...]: the rows idx[b, :count[b]] packed per sequence, zeros after."""
+    Bn, N = src.shape[0], src.shape[1]
+    row_bytes = src[0, 0].numel() * src.element_size()
+    if dst is None:
+        dst = torch.empty((Bn * k_max,) + tuple(src.shape[2:]), dtype=src.dtype, device=src.device)
+    if dst.numel() * dst.element_size() < Bn * k_max * row_bytes:
+        raise DllmError("dst holds fewer than B*k_max rows")
+    _cuda(src, idx, count, dst)
+    _check(lib().dllm_gather_rows(_ptr(src), _ptr(idx), _ptr(count), int(k_max), _ptr(dst), Bn, N, row_bytes,
+                                  _stream(src.device)), "dllm_gather_rows")
+    return dst
 
 
 # --------------------------------------------------------------------------- plain GEMM

@@ -196,7 +196,7 @@ using namespace dllm;
 
 DLLM_EXPORT const char *dllm_last_error(void) { return t_err.c_str(); }
 
-DLLM_EXPORT int dllm_version(void) { return 111; }
+DLLM_EXPORT int dllm_version(void) { return 112; }
 
 DLLM_EXPORT int dllm_check_status(unsigned *status_out, int reset) {
     CHECK_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
@@ -210,6 +210,12 @@ DLLM_EXPORT int dllm_check_status(unsigned *status_out, int reset) {
     if (v & DLLM_STATUS_TIMEOUT) return fail(DLLM_ERR_TIMEOUT, "a kernel wait timed out (status 0x%x)", v);
     if (v & DLLM_STATUS_SMEM_LAYOUT)
         return fail(DLLM_ERR_CUDA, "a GEMM found its shared memory misaligned and skipped its work (status 0x%x)", v);
+    return DLLM_OK;
+}
+
+DLLM_EXPORT int dllm_check_wait_timeout(int32_t *gave_up, void *stream) {
+    CHECK_ARG(gave_up, "null pointer");
+    CHECK_CUDA(wait_timeout_check(gave_up, status_ptr(), as_stream(stream)), "wait check launch");
     return DLLM_OK;
 }
 
@@ -639,6 +645,20 @@ DLLM_EXPORT int dllm_rows_rmsnorm(const void *H, const int32_t *rows, int R, con
                         : rows_rmsnorm(static_cast<const float *>(H), rows, R, static_cast<const float *>(gamma), eps,
                                        static_cast<float *>(out), B, N, d, st);
     CHECK_CUDA(e, "rows rmsnorm launch");
+    return DLLM_OK;
+}
+
+DLLM_EXPORT int dllm_gather_rows(const void *src, const int32_t *idx, const int32_t *count, int k_max, void *dst,
+                                 int B, int N, int row_bytes, void *stream) {
+    CHECK_ARG(src && idx && count && dst, "null pointer");
+    CHECK_ARG(B > 0 && N > 0 && row_bytes > 0, "sizes must be positive");
+    CHECK_ARG(k_max > 0 && k_max <= N, "k_max must be in [1, N] (got %d, N=%d)", k_max, N);
+    CHECK_ARG((long long)B * k_max <= INT_MAX, "B*k_max must fit in an int");
+    CHECK_ARG(row_bytes % 16 == 0, "row_bytes must be a multiple of 16 (got %d)", row_bytes);
+    CHECK_ARG(aligned16(src) && aligned16(dst), "src and dst must be 16-byte aligned");
+    cudaStream_t st = as_stream(stream);
+    Launch t(DLLM_KERNEL_GATHER, st);
+    CHECK_CUDA(gather_rows(src, SelRows{idx, count, k_max, N}, B, row_bytes, dst, st), "gather rows launch");
     return DLLM_OK;
 }
 

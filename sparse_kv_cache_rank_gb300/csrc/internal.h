@@ -136,9 +136,16 @@ template <class T>
 cudaError_t embed_rows(const T *E, const int32_t *tokens, const int32_t *rows, int R, T *H, int B,
                        int N, int d, int V, cudaStream_t st);
 
+// dst[b * k_max + s] = src row (b, idx[b, s]) of row_bytes bytes (live rows), else 0.
+cudaError_t gather_rows(const void *src, SelRows sel, int B, int row_bytes, void *dst, cudaStream_t st);
+
 template <class T>
 cudaError_t rows_rmsnorm(const T *H, const int32_t *rows, int R, const T *gamma, float eps, T *out,
                          int B, int N, int d, cudaStream_t st);
+
+// One CTA waits on an mbarrier nothing completes (bounded wait); gave_up counts the
+// threads whose wait ran out.
+cudaError_t wait_timeout_check(int32_t *gave_up, unsigned *status, cudaStream_t st);
 
 // ---------------------------------------------------------------- attention
 // A[m, h*hd:(h+1)*hd] = softmax(Q_h K_g^T / sqrt(hd)) V_g over all N rows of the

@@ -210,3 +210,34 @@ cudaError_t select_topk(const float *drift, const int32_t *forced, int F, int k,
 }
 
 }  // namespace dllm
+
+// ---------------------------------------------------------------------------
+// Diagnostic of the bounded wait (dllm_check_wait_timeout): every thread waits on a
+// barrier whose phase never completes; each wait must give up after the limit and
+// return false, and the status word must receive DLLM_STATUS_TIMEOUT.
+namespace dllm {
+namespace {
+
+__global__ void __launch_bounds__(64) k_wait_timeout(int32_t *gave_up, unsigned *status) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const bool ok = mbar_wait(&bar, 0, &abort, status);
+    if (!ok) atomicAdd(gave_up, 1);
+}
+
+}  // namespace
+
+cudaError_t wait_timeout_check(int32_t *gave_up, unsigned *status, cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(gave_up, 0, sizeof(int32_t), st);
+    if (e != cudaSuccess) return e;
+    k_wait_timeout<<<1, 64, 0, st>>>(gave_up, status);
+    return cudaGetLastError();
+}
+
+}  // namespace dllm

@@ -25,7 +25,7 @@ import numpy as np
 __all__ = [
     "LayerShape", "TINY", "LLADA_LAYER", "LLADA_STACK", "DREAM_STACK", "sweep_shapes",
     "rng", "round_bf16", "to_bf16_bits", "from_bf16_bits",
-    "layer_weights", "hidden_pair", "block_layout", "commit_logits",
+    "layer_weights", "hidden_pair", "hidden_ladder", "drifted", "block_layout", "commit_logits",
 ]
 
 
@@ -182,3 +182,35 @@ def commit_logits(B: int, M: int, V: int, seed: int, std: float = 3.0) -> np.nda
     """Logits [B, M, V] ~ N(0, std), fp32."""
     g = rng(seed)
     return (g.standard_normal((B, M, V), dtype=np.float32) * np.float32(std)).astype(np.float32)
+
+
+def hidden_ladder(shape: LayerShape, h_prev: np.ndarray, exclude, seed: int, n_hot: int = 12,
+                  sigma_all: float = 0.0, s0: float = 0.02, ratio: float = 1.8) -> np.ndarray:
+    """Step-t hidden states with graded drift: h_prev + N(0, sigma_all) on every row, and on
+    n_hot rows per sequence (drawn from the rows not in exclude[b], which may hold -1
+    padding) an extra N(0, s0 * ratio^j), j = 0 .. n_hot-1.  The moved rows' drifts then
+    lie on a geometric ladder, each rung well apart from the next."""
+    g = rng(seed)
+    B, N, d = shape.B, shape.N, shape.d
+    h = h_prev.astype(np.float32) + g.standard_normal((B, N, d), dtype=np.float32) * np.float32(sigma_all)
+    for b in range(B):
+        ex = set() if exclude is None else {int(i) for i in np.asarray(exclude[b]) if 0 <= i < N}
+        cand = np.array([i for i in range(N) if i not in ex], np.int64)
+        rows = g.permutation(cand)[:n_hot]
+        for j, i in enumerate(rows):
+            h[b, i] += g.standard_normal(d, dtype=np.float32) * np.float32(s0 * ratio ** j)
+    return _maybe_round(h, shape.dtype)
+
+
+def drifted(shape: LayerShape, h: np.ndarray, seed: int, frac: float = 0.10,
+            sigma_all: float = 0.05, sigma_hot: float = 0.5) -> np.ndarray:
+    """The drift model of hidden_pair applied to given states h [B, N, d]: + N(0, sigma_all)
+    everywhere, + N(0, sigma_hot) on round(frac * N) rows per sequence (seeded)."""
+    g = rng(seed)
+    B, N, d = h.shape
+    out = h.astype(np.float32) + g.standard_normal((B, N, d), dtype=np.float32) * np.float32(sigma_all)
+    n_hot = int(round(frac * N))
+    for b in range(B):
+        rows = np.sort(g.permutation(N)[:n_hot])
+        out[b, rows] += g.standard_normal((n_hot, d), dtype=np.float32) * np.float32(sigma_hot)
+    return _maybe_round(out, shape.dtype)

@@ -61,18 +61,21 @@ def assert_close_layer(x, ref, dtype: str, what: str):
     return rel, cs
 
 
-def assert_update_close(out, ref_out, h_in, dtype: str, what: str):
+def assert_update_close(out, ref_out, h_in, dtype: str, what: str, h_in_ref=None):
     """The layer's update (output minus input).  A bf16 output carries the rounding
     of the whole residual sum, so the update is compared against the reference output
-    rounded the same way, and the max error may include one bf16 ulp of |output|."""
+    rounded the same way, and the max error may include one bf16 ulp of |output|.
+    h_in_ref: the reference side's own input when it differs from the GPU's (a deeper
+    layer of a chained step); default h_in."""
     from sparse_kv_cache_rank_gb300 import synth
     ref = synth.round_bf16(ref_out) if dtype == "bf16" else ref_out
     du = np.asarray(out, np.float64) - h_in
-    dr = np.asarray(ref, np.float64) - h_in
+    dr = np.asarray(ref, np.float64) - (h_in if h_in_ref is None else h_in_ref)
     cs = cosine(du, dr)
     err = np.abs(du - dr).max()
     if dtype == "bf16":
-        ulp = 2.0 ** (np.floor(np.log2(np.abs(ref).max())) - 7)
+        # one ulp for the output's rounding, one more for the inputs' own when they differ
+        ulp = 2.0 ** (np.floor(np.log2(np.abs(ref).max())) - 7) * (1 if h_in_ref is None else 2)
         bound = BF16_MAX_REL * np.abs(dr).max() + ulp
         assert cs >= BF16_MIN_COS and err <= bound, f"{what}: err {err:.3e} > {bound:.3e} or cos {cs:.6f}"
     else:
@@ -112,6 +115,40 @@ def check_selection_band(idx, cnt, drift_ref, forced, k):
                 assert i in sel, f"row {i} drift {drift_ref[b, i]} > kth {kth} not selected"
             if drift_ref[b, i] < kth - TIE_BAND:
                 assert i not in sel, f"row {i} drift {drift_ref[b, i]} < kth {kth} selected"
+
+
+def match_selection(g_idx, g_cnt, drift_ref, o_idx, o_cnt, forced, k):
+    """GPU selection against the oracle's own (each side selects on its own drift): equal
+    counts, the near-tie band rule, and per sequence the rows both sides chose plus the
+    rows only one side chose (which the band rule has already confined to the near-ties
+    of the k-th drift).  -> list of (common, gpu_only, oracle_only) sorted index arrays."""
+    np.testing.assert_array_equal(g_cnt, o_cnt)
+    check_selection_band(g_idx, g_cnt, drift_ref, forced, k)
+    out = []
+    for b in range(len(g_cnt)):
+        gs = set(g_idx[b, :g_cnt[b]].tolist())
+        os_ = set(o_idx[b, :o_cnt[b]].tolist())
+        out.append((np.array(sorted(gs & os_), np.int64), np.array(sorted(gs - os_), np.int64),
+                    np.array(sorted(os_ - gs), np.int64)))
+    return out
+
+
+def softmax_stats_bound(logits_ref, delta):
+    """How far top-1 confidence and entropy may move when every logit of a row moves by at
+    most delta (derived on the path l + t e, |e| <= delta, t in [0, 1]):
+      ln p_k moves by <= 2 delta, so |d p_max| <= p_max (e^{2 delta} - 1);
+      dH/dt = -sum_k p_k (l_k - lbar) e_k, and along the path p_k stays within e^{+-2 delta}
+      of its start and |l_k - lbar| within 2 delta + (e^{2 delta} - 1) m of it, so
+      |d H| <= delta e^{2 delta} (e^{2 delta} m + 2 delta),  m = sum_k p_k |l_k - lbar|.
+    -> (conf bound, entropy bound), arrays over the rows of logits_ref [..., V]."""
+    l = np.asarray(logits_ref, np.float64)
+    z = l - l.max(-1, keepdims=True)
+    p = np.exp(z)
+    p /= p.sum(-1, keepdims=True)
+    lbar = (p * l).sum(-1, keepdims=True)
+    m = (p * np.abs(l - lbar)).sum(-1)
+    e2 = np.exp(2 * delta)
+    return p.max(-1) * (e2 - 1), delta * e2 * (e2 * m + 2 * delta)
 
 
 @dataclasses.dataclass

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(dl):
     missing = [n for n in _declared() if not hasattr(L, n)]
     assert not missing, missing
     assert set(_declared()) <= set(dl.exported_symbols()) | {"dllm_last_error", "dllm_version"}
-    assert dl.lib().dllm_version() == 111
+    assert dl.lib().dllm_version() == 112
 
 
 def test_budget_logic_matches_oracle(dl, orc):

@@ -22,7 +22,8 @@ def _run(args, env_extra=None, timeout=300):
 def test_reference_arm_prints_one_contract_line():
     sys.path.insert(0, ROOT)
     import bench
-    r = _run(["--impl", "reference", "--steps", "1", "--warmup", "3"])
+    # the small workload keeps this CPU check short; the default is the LLaDA-8B-shaped layer
+    r = _run(["--impl", "reference", "--steps", "1", "--warmup", "3", "--reference-workload", "tiny-fp32"])
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.strip()]
     assert len(lines) == 1
@@ -32,16 +33,18 @@ def test_reference_arm_prints_one_contract_line():
     assert d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 3
     assert d["higher_is_better"] is True and d["scaling"] == "weak" and d["vs_baseline"] is None
     assert d["value"] > 0 and d["ms_per_step"] == pytest.approx(1e3 / d["value"], rel=1e-9)
-    assert "workload" in d["config"] and "llada8b-layer" in d["config"]["workload"]
+    assert "workload" in d["config"] and "tiny-fp32" in d["config"]["workload"]
+    assert d["config"]["parallelism"] == "replicas x1"
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["unit"] == d["unit"]
-    assert cb["cores"] >= 1 and cb["sample"]
+    assert cb["cores"] >= 1 and cb["sample"] and cb["cpu_model"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
 
 
 def test_reference_arm_other_ranks_exit_quietly():
-    r = _run(["--impl", "reference", "--steps", "1", "--warmup", "3"], {"RANK": "1", "WORLD_SIZE": "2"})
+    r = _run(["--impl", "reference", "--steps", "1", "--warmup", "3", "--reference-workload", "tiny-fp32"],
+             {"RANK": "1", "WORLD_SIZE": "2"})
     assert r.returncode == 0 and r.stdout.strip() == ""
 
 

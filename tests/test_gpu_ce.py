@@ -57,16 +57,17 @@ def test_ce_steps_parity(B, Bq, M, h_max):
     seen = np.zeros((Bq, M), dtype=bool)
     committed = np.zeros((Bq, M), dtype=bool)
     n_early = 0
+    st_o = np.zeros((Bq, M, 5))         # the oracle's own state, carried from step to step
     for step in range(14):
         c = 1 / (1 + np.exp(-rate * (step - mid))) + 0.03 * g.standard_normal((Bq, M))
         c = np.clip(c, 0, 1).astype(np.float32)
         undecided = ~committed
-        prev = state.cpu().numpy().astype(np.float64)
         early = B.dllm_ce_step(torch.from_numpy(c).cuda(), _u8(seen), _u8(undecided), _u8(committed), state,
                                q_l=prm.q_l, q_v=prm.q_v, R=prm.R, p_v0=prm.p_v0, z=prm.z,
                                h_max=prm.h_max, c_min=prm.c_min)
         torch.cuda.synchronize()
-        st_ref, early_ref = ce.ce_step(prev, seen, c, undecided, committed, prm)
+        st_ref, early_ref = ce.ce_step(st_o, seen, c, undecided, committed, prm)
+        st_o = st_ref
         st_gpu = state.cpu().numpy().astype(np.float64)
         np.testing.assert_allclose(st_gpu, st_ref, rtol=1e-5, atol=1e-6)
         e_gpu = early.cpu().numpy().astype(bool)

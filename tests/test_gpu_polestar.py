@@ -1,8 +1,8 @@
 """GPU-vs-oracle parity of the drift-aware commit (Polestar, "2. B. Polestar-Commit")
-through the C ABI.  Every step feeds both sides the same previous history (the device's,
-read back): histories within 1e-6 relative (one fp32 addition), commits bit-exact except
-where the drift delta lies within 1e-6 of the dynamic threshold (fp32 and fp64 may split
-that tie)."""
+through the C ABI.  Each side carries its own drift history from step to step (fp32 on
+the device, fp64 in the oracle): histories within 2e-6 relative (one fp32 rounding of the
+sum per step, up to 10 steps), commits equal except where the drift delta lies within
+1e-5 of the dynamic threshold (fp32 and fp64 may split that tie)."""
 import numpy as np
 import pytest
 
@@ -12,7 +12,7 @@ from sparse_kv_cache_rank_gb300 import synth
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-BAND = 1e-6
+BAND = 1e-5
 
 
 @pytest.fixture(scope="module")
@@ -37,6 +37,7 @@ def test_polestar_commit_parity(B, Bq, M, alpha):
     hist = torch.zeros((Bq, M, 2), device="cuda")
     committed = np.zeros((Bq, M), dtype=bool)
     n_commit = 0
+    prev = np.zeros((Bq, M, 2))         # the oracle's own history, carried from step to step
     for step in range(10):
         drift = (g.random((Bq, M)) * np.exp(-0.2 * step) + 0.3 * (g.random((Bq, M)) < 0.1)).astype(np.float32)
         conf = g.random((Bq, M)).astype(np.float32)
@@ -44,20 +45,20 @@ def test_polestar_commit_parity(B, Bq, M, alpha):
         suffix[:, block:] = True
         selected = g.random((Bq, M)) < 0.3
         undecided = ~committed
-        prev = hist.cpu().numpy().astype(np.float64)
         c_gpu = B.dllm_polestar_commit(torch.from_numpy(drift).cuda(), torch.from_numpy(conf).cuda(),
                                        _u8(undecided), _u8(suffix), _u8(selected), hist, alpha=alpha,
                                        tau_s=prm.tau_s)
         torch.cuda.synchronize()
         c_ref, hs, hc = ps.commit(drift, conf, undecided, suffix, selected, prev[..., 0], prev[..., 1], prm)
         h_gpu = hist.cpu().numpy().astype(np.float64)
-        np.testing.assert_allclose(h_gpu[..., 0], hs, rtol=1e-6, atol=1e-7)
+        np.testing.assert_allclose(h_gpu[..., 0], hs, rtol=2e-6, atol=1e-7)
         np.testing.assert_array_equal(h_gpu[..., 1], hc)
         delta = ps.drift_delta(drift, prev[..., 0], prev[..., 1])
         tie = undecided & ~suffix & (prev[..., 1] >= 1) & (np.abs(delta - ps.dynamic_threshold(conf, prm)) < BAND)
         cg = c_gpu.cpu().numpy().astype(bool)
         assert np.array_equal(cg & ~tie, c_ref & ~tie)
         n_commit += int(c_ref.sum())
+        prev = np.stack([hs, hc], axis=-1)
         committed |= c_ref
     if M > 8:
         assert n_commit > 0
