@@ -144,21 +144,31 @@ class Clocks:
 # --------------------------------------------------------------------------- work model
 def layer_kernel_work(sh, M):
     """Algorithmic bytes and FLOPs of each kernel of one layer step with M refreshed rows
-    (weights and caches counted once, bf16 = 2 bytes, fp32 = 4)."""
+    (weights and caches counted once, bf16 = 2 bytes, fp32 = 4).  Up to N = 4096 the
+    selection and the gather of the selected rows are one kernel ("select")."""
     B, N, d, r, F = sh.B, sh.N, sh.d, sh.r, sh.F
     dq, dkv = sh.d_q, sh.d_kv
-    return {
+    fold = sh.dtype == "bf16" and M <= 256   # the refresh folds the second RMSNorm up to 256 rows
+    sel = (4 * B * N + 4 * B * N + 4 * B, 0)
+    gat = (2 * M * d * 2 + 8 * M * r, 0)
+    if N <= 4096:
+        sel, gat = (sel[0] + gat[0], 0), None
+    work = {
         "proxy_gemm": (2 * B * N * d + 2 * r * d + 4 * B * N * r, 2 * B * N * d * r),
         "cosine": (8 * B * N * r + 4 * B * N, 0),
-        "select": (4 * B * N + 4 * B * N + 4 * B, 0),
-        "gather": (2 * M * d * 2 + 8 * M * r, 0),
+        "select": sel,
+        "gather": gat,
         "qkv": (2 * (dq + 2 * dkv) * d + 2 * M * d + 2 * M * (dq + 2 * dkv), 2 * M * d * (dq + 2 * dkv)),
         "attention": (2 * M * dq * 2 + 2 * B * N * 2 * dkv, 4 * M * N * dq),
-        "oproj": (2 * d * dq + 2 * M * dq + 2 * M * d + 4 * M * d, 2 * M * dq * d),
-        "rmsnorm2": (4 * M * d + 2 * M * d, 0),
+        # bf16: the second RMSNorm is folded into the O epilogue (which also writes the
+        # bf16 h1 * gamma2 operand and the rows' partial squares) and the gate/up epilogue
+        "oproj": (2 * d * dq + 2 * M * dq + 2 * M * d + 4 * M * d + (2 * M * d + M * d // 8 if fold else 0),
+                  2 * M * dq * d),
+        "rmsnorm2": None if fold else (4 * M * d + 2 * M * d, 0),
         "gateup": (2 * 2 * F * d + 2 * M * d + 2 * M * F, 2 * M * d * 2 * F),
         "down": (2 * d * F + 2 * M * F + 4 * M * d + 2 * M * d, 2 * M * F * d),
     }
+    return {k: v for k, v in work.items() if v is not None}
 
 
 # --------------------------------------------------------------------------- native arm
@@ -247,6 +257,10 @@ class LayerWorkload:
         self.ws = torch.empty(need, device=dev, dtype=torch.uint8)
         pw = int(B.lib().dllm_proxy_workspace_bytes(Bn, N, d, sh.r, B.DLLM_BF16 if sh.dtype == "bf16" else B.DLLM_F32))
         self.ws_proxy = torch.empty(max(pw, 256), device=dev, dtype=torch.uint8)
+        self.ws_step = torch.empty(B.dllm_layer_step_workspace_bytes(self.layer, Bn, N, sh.r,
+                                                                     0 if self.forced is None else self.forced.shape[1],
+                                                                     self.k),
+                                   device=dev, dtype=torch.uint8)
         self.H_prev = H_prev
         self.s = 0
         torch.cuda.synchronize(dev)
@@ -255,15 +269,25 @@ class LayerWorkload:
         return self.w, self.layer, self.Pt
 
     def step(self, H=None, idx=None, cnt=None):
+        """One layer step through dllm_layer_step (one library call)."""
         B = self.B_
         if H is None:
             H = self.H[self.s & 1]
         idx = self.idx if idx is None else idx
         cnt = self.cnt if cnt is None else cnt
         self.s += 1
+        B.dllm_layer_step(self.layer, self.Pt, H, self.pc, self.cur, self.drift, self.forced, self.k, idx, cnt,
+                          self.K, self.V, self.O, ws=self.ws_step)
+
+    def step_calls(self):
+        """The same step as the three calls dllm_proxy_score, dllm_select_topk and
+        dllm_sparse_layer_refresh."""
+        B = self.B_
+        H = self.H[self.s & 1]
+        self.s += 1
         B.dllm_proxy_score(H, self.Pt, self.pc, proxy_cur=self.cur, drift=self.drift, ws=self.ws_proxy)
-        B.dllm_select_topk(self.drift, self.forced, self.k, idx=idx, count=cnt)
-        B.dllm_sparse_layer_refresh(self.layer, H, idx, cnt, self.k_max, self.K, self.V, self.O,
+        B.dllm_select_topk(self.drift, self.forced, self.k, idx=self.idx, count=self.cnt)
+        B.dllm_sparse_layer_refresh(self.layer, H, self.idx, self.cnt, self.k_max, self.K, self.V, self.O,
                                     self.pc, self.cur, ws=self.ws)
 
 
@@ -277,7 +301,8 @@ def kernel_breakdown(wl, reps=4):
         for _ in range(reps):
             wl.step()
         ms, n = B.dllm_timer_stop()
-        out[name] = ms / max(n, 1)
+        if n > 0:
+            out[name] = ms / n
     return out
 
 
@@ -370,6 +395,17 @@ def native(args):
     instrumented_ms = e2.elapsed_time(e3) / args.steps
     B.check_status()
 
+    # the same steps as three library calls each (proxy, selection, refresh)
+    for _ in range(3):
+        wl.step_calls()
+    e4 = torch.cuda.Event(enable_timing=True)
+    e5 = torch.cuda.Event(enable_timing=True)
+    e4.record()
+    for _ in range(args.steps):
+        wl.step_calls()
+    e5.record()
+    torch.cuda.synchronize(dev)
+    three_calls_ms = e4.elapsed_time(e5) / args.steps
     e2e_elapsed, e2e_bytes = e2e_measure(wl, args.steps, barrier)
 
     t = torch.tensor([elapsed, e2e_elapsed], device=dev, dtype=torch.float64)
@@ -395,6 +431,7 @@ def native(args):
         "rows_per_step": M,
         "roofline": roof,
         "step_roofline_frac": step_roofline_s(sh, M) / (elapsed / args.steps),
+        "three_calls_ms_per_step": three_calls_ms,
         "kernel_ms": {k: round(v, 5) for k, v in per_kernel.items()},
         "kernel_roofline": {k: round(roofline_of(sh, M, per_kernel, k, False)["frac"], 4) for k in per_kernel
                             if work[k][0] > 0},

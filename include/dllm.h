@@ -67,8 +67,8 @@ const char *dllm_last_error(void);
  * allocation-free vocabulary step (dllm_commit_entropy_noalloc); 1.10 adds the NEXT-row
  * calls (KL drift, drift-aware commit, confidence extrapolation, cluster-granular
  * proxy); 1.11 the host-only GEMM plan query (dllm_gemm_plan); 1.12 the read-back of
- * refreshed rows (dllm_gather_rows) and the bounded-wait diagnostic
- * (dllm_check_wait_timeout). */
+ * refreshed rows (dllm_gather_rows), the bounded-wait diagnostic
+ * (dllm_check_wait_timeout) and the one-call layer step (dllm_layer_step). */
 int dllm_version(void);
 
 /* Reads (and with reset != 0 clears) the device status word of the current device.
@@ -303,6 +303,29 @@ int dllm_sparse_layer_refresh(const dllm_layer *W, const void *H_in, const int32
                               const int32_t *count, int k_max, void *K_cache, void *V_cache,
                               void *H_out_cache, float *proxy_cache, const float *proxy_cur, int r,
                               int B, int N, void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * One layer's sparse step in one call: [SPA] "1. Update identification via singular
+ * proxy" (dllm_proxy_score on H_in), "2. Adaptive budget allocation" with [EC] "How
+ * EntropyCache works" step 3 (dllm_select_topk with the forced rows and the budget k),
+ * "3. Sparse execution" (dllm_sparse_layer_refresh of the selected rows with
+ * k_max = min(N, k + F)).  The outputs are those of the three calls in sequence:
+ *   proxy_cur, drift                       as dllm_proxy_score (proxy_cache is its cache)
+ *   idx, count                             as dllm_select_topk
+ *   K_cache, V_cache, H_out_cache, proxy_cache   as dllm_sparse_layer_refresh
+ * The selection is fused with the gather of the selected rows for N <= 4096 (one kernel
+ * fewer, no host round trip between the steps); longer sequences run the separate
+ * kernels.  Pt [r, d] in the layer's dtype; forced [B, F] int32 (-1 padded) or NULL.
+ * Requirements: those of the three calls (r % 32 == 0; N <= 16384; H_out_cache not
+ * aliasing H_in; 16-byte aligned arrays).  Workspace:
+ * dllm_layer_step_workspace_bytes(W, B, N, r, F, k) bytes.
+ * ------------------------------------------------------------------------- */
+size_t dllm_layer_step_workspace_bytes(const dllm_layer *W, int B, int N, int r, int F, int k);
+
+int dllm_layer_step(const dllm_layer *W, const void *Pt, const void *H_in, float *proxy_cache,
+                    float *proxy_cur, float *drift, const int32_t *forced, int F, int k, float min_drift,
+                    int32_t *idx, int32_t *count, void *K_cache, void *V_cache, void *H_out_cache,
+                    int B, int N, int r, void *ws, size_t ws_bytes, void *stream);
 
 /* ---------------------------------------------------------------------------
  * Vocabulary step.  [TSPD] "Input features": top-1 confidence and predictive entropy

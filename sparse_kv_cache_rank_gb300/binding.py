@@ -65,6 +65,9 @@ _SIGS = {
                                             C.c_void_p, C.c_int, C.c_void_p, C.c_void_p,
                                             C.c_void_p, C.c_void_p, C.c_void_p, C.c_int, C.c_int,
                                             C.c_int, C.c_void_p, C.c_size_t, C.c_void_p]),
+    "dllm_layer_step_workspace_bytes": (C.c_size_t, [C.POINTER(dllm_layer)] + [C.c_int] * 5),
+    "dllm_layer_step": (C.c_int, [C.POINTER(dllm_layer)] + [C.c_void_p] * 6 + [C.c_int] * 2 + [C.c_float]
+                        + [C.c_void_p] * 5 + [C.c_int] * 3 + [C.c_void_p, C.c_size_t, C.c_void_p]),
     "dllm_set_pdl": (C.c_int, [C.c_int]),
     "dllm_timer_start": (C.c_int, [C.c_int, C.c_int]),
     "dllm_timer_stop": (C.c_int, [C.POINTER(C.c_double), C.POINTER(C.c_int)]),
@@ -427,6 +430,29 @@ def dllm_sparse_layer_refresh(layer: Layer, H_in, idx, count, k_max: int, K_cach
                                            B, N, _ptr(ws), ws.numel(), _stream(H_in.device)),
            "dllm_sparse_layer_refresh")
     return K_cache, V_cache, H_out_cache
+
+
+def dllm_layer_step_workspace_bytes(layer: Layer, B: int, N: int, r: int, F: int, k: int) -> int:
+    return int(lib().dllm_layer_step_workspace_bytes(C.byref(layer.desc), B, N, r, F, k))
+
+
+def dllm_layer_step(layer: Layer, Pt, H_in, proxy_cache, proxy_cur, drift, forced, k: int, idx, count,
+                    K_cache, V_cache, H_out_cache, min_drift: float = 1e-6, ws=None):
+    """One layer's sparse step (proxy + drift, selection with the forced rows, refresh of
+    the selected rows) in one library call; writes proxy_cur, drift, idx, count and the
+    refreshed cache rows in place."""
+    B, N, d = H_in.shape
+    r = proxy_cache.shape[-1]
+    F = 0 if forced is None else forced.shape[1]
+    _cuda(Pt, H_in, proxy_cache, proxy_cur, drift, forced, idx, count, K_cache, V_cache, H_out_cache)
+    need = dllm_layer_step_workspace_bytes(layer, B, N, r, F, k)
+    if ws is None:
+        ws = _workspace(need, H_in.device, "layer_step")
+    _check(lib().dllm_layer_step(C.byref(layer.desc), _ptr(Pt), _ptr(H_in), _ptr(proxy_cache), _ptr(proxy_cur),
+                                 _ptr(drift), _ptr(forced), F, int(k), float(min_drift), _ptr(idx), _ptr(count),
+                                 _ptr(K_cache), _ptr(V_cache), _ptr(H_out_cache), B, N, r, _ptr(ws), ws.numel(),
+                                 _stream(H_in.device)), "dllm_layer_step")
+    return idx, count
 
 
 # --------------------------------------------------------------------------- attention alone

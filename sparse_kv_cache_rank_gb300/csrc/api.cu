@@ -53,6 +53,11 @@ bool aligned8(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Refreshed rows (B * k_max) up to which the bf16 refresh folds the second RMSNorm into
+// the O and gate/up epilogues (measured: a launch saved at the 164-row LLaDA-8B step; at
+// 2624 rows of the Dream-7B-shaped layer the heavier epilogues cost more than the norm).
+constexpr int kFoldNormRows = 256;
+
 size_t el_size(int dtype) { return dtype == DLLM_BF16 ? 2 : 4; }
 
 cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
@@ -131,7 +136,7 @@ PackLayout pack_layout(int d, int n_q, int n_kv, int hd, int F, int dtype) {
 }
 
 struct RefreshWs {
-    size_t xn, q, a, h1, xn2, u, rope, total;
+    size_t xn, q, a, h1, xn2, u, rope, ss, total;
 };
 
 RefreshWs refresh_ws(const dllm_layer *W, int B, int N, int k_max) {
@@ -153,6 +158,8 @@ RefreshWs refresh_ws(const dllm_layer *W, int B, int N, int k_max) {
     off = align256(off + M * W->F * el);
     r.rope = off;
     off = align256(off + M * (size_t)(W->hd / 2) * sizeof(float2));
+    r.ss = off;   // partial squares of h1 per 32 features (the folded second RMSNorm)
+    off = align256(off + M * (size_t)(W->d / 32) * 4);
     (void)N;
     r.total = off + 256;   // room to align the caller's base
     return r;
@@ -483,10 +490,19 @@ DLLM_EXPORT size_t dllm_refresh_workspace_bytes(const dllm_layer *W, int B, int 
 
 namespace {
 
+// The per-layer step's selection arguments, when the selection is fused with the gather.
+struct FusedSelect {
+    const float *drift;
+    const int32_t *forced;
+    int F, k;
+    float min_drift;
+    int32_t *idx, *count;
+};
+
 template <class T>
 int refresh_impl(const dllm_layer *W, const T *H_in, SelRows sel, int B, T *K_cache, T *V_cache,
                  T *H_out, float *proxy_cache, const float *proxy_cur, int r, uint8_t *ws,
-                 cudaStream_t st) {
+                 cudaStream_t st, const FusedSelect *fs = nullptr) {
     const RefreshWs L = refresh_ws(W, B, sel.N, sel.k_max);
     const int M = B * sel.k_max;
     const int d = W->d, dq = W->n_q * W->hd, dkv = W->n_kv * W->hd, F = W->F;
@@ -505,8 +521,14 @@ int refresh_impl(const dllm_layer *W, const T *H_in, SelRows sel, int B, T *K_ca
     const T *g1 = static_cast<const T *>(W->gamma1);
     const T *g2 = static_cast<const T *>(W->gamma2);
 
-    // a3: gather + RMSNorm, proxy cache update
-    {
+    // a2 + a3 fused (the layer step): selection, then gather + RMSNorm, proxy cache update
+    if (fs) {
+        Launch t(DLLM_KERNEL_SELECT, st);
+        CHECK_CUDA(select_gather<T>(fs->drift, fs->forced, fs->F, fs->k, fs->min_drift, fs->idx, fs->count, B, sel.N,
+                                    sel.k_max, H_in, d, g1, W->eps, Xn, proxy_cache, proxy_cur, r, W->rope_inv_freq,
+                                    W->hd / 2, rope_cs, status, st),
+                   "select + gather launch");
+    } else {   // a3: gather + RMSNorm, proxy cache update
         Launch t(DLLM_KERNEL_GATHER, st);
         CHECK_CUDA(gather_rmsnorm<T>(H_in, sel, B, d, g1, W->eps, Xn, proxy_cache, proxy_cur, r,
                                      W->rope_inv_freq, W->hd / 2, rope_cs, status, st),
@@ -528,9 +550,21 @@ int refresh_impl(const dllm_layer *W, const T *H_in, SelRows sel, int B, T *K_ca
                                     W->n_q, W->n_kv, W->hd, status, st),
                        "attention");
         }
-        { Launch t(DLLM_KERNEL_OPROJ, st); CHECK_CUDA(gemm_tc(wo, d, dq, Ac, M, er, 0, true, status, st), "o gemm"); }
-        { Launch t(DLLM_KERNEL_RMSNORM2, st); CHECK_CUDA(rmsnorm_rows<T>(h1, M, d, g2, W->eps, Xn2, st), "rmsnorm2"); }
-        { Launch t(DLLM_KERNEL_GATEUP, st); CHECK_CUDA(gemm_tc(wgu, 2 * F, d, Xn2, M, es, 0, true, status, st), "gate/up gemm"); }
+        if (M <= kFoldNormRows) {
+            // a6 + a7, few rows: the second RMSNorm folded into the O epilogue (bf16 h1 * gamma2
+            // and the rows' partial squares) and into the gate/up epilogue (1 / rms): one
+            // launch fewer where every launch's fixed cost counts
+            float *ss = reinterpret_cast<float *>(ws + L.ss);
+            EpiResidualNorm<T> ern{sel, h1, Xn2, ss, H_in, g2, d, M};
+            EpiSwiGLUNorm<T> esn{SelRows{}, U, ss, F, d, M, W->eps};
+            { Launch t(DLLM_KERNEL_OPROJ, st); CHECK_CUDA(gemm_tc(wo, d, dq, Ac, M, ern, 0, true, status, st), "o gemm"); }
+            { Launch t(DLLM_KERNEL_GATEUP, st); CHECK_CUDA(gemm_tc(wgu, 2 * F, d, Xn2, M, esn, 0, true, status, st), "gate/up gemm"); }
+        } else {
+            // many rows: the heavier epilogues cost more than the norm kernel they replace
+            { Launch t(DLLM_KERNEL_OPROJ, st); CHECK_CUDA(gemm_tc(wo, d, dq, Ac, M, er, 0, true, status, st), "o gemm"); }
+            { Launch t(DLLM_KERNEL_RMSNORM2, st); CHECK_CUDA(rmsnorm_rows<T>(h1, M, d, g2, W->eps, Xn2, st), "rmsnorm2"); }
+            { Launch t(DLLM_KERNEL_GATEUP, st); CHECK_CUDA(gemm_tc(wgu, 2 * F, d, Xn2, M, es, 0, true, status, st), "gate/up gemm"); }
+        }
         { Launch t(DLLM_KERNEL_DOWN, st); CHECK_CUDA(gemm_tc(wdn, d, F, U, M, ed, 0, true, status, st), "down gemm"); }
     } else {
         { Launch t(DLLM_KERNEL_QKV, st); CHECK_CUDA(gemm_simt(wqkv, dq + 2 * dkv, d, Xn, M, eq, st), "qkv gemm"); }
@@ -576,6 +610,69 @@ DLLM_EXPORT int dllm_sparse_layer_refresh(const dllm_layer *W, const void *H_in,
     return refresh_impl<float>(W, static_cast<const float *>(H_in), sel, B, static_cast<float *>(K_cache),
                                static_cast<float *>(V_cache), static_cast<float *>(H_out_cache),
                                proxy_cache, proxy_cur, r, w8, st);
+}
+
+// ------------------------------------------------------------------ one layer step
+DLLM_EXPORT size_t dllm_layer_step_workspace_bytes(const dllm_layer *W, int B, int N, int r, int F, int k) {
+    if (!W || B <= 0 || N <= 0 || r <= 0 || F < 0 || k < 0) return 0;
+    const long long km = (long long)k + F < N ? (long long)k + F : N;
+    const int k_max = km > 0 ? (int)km : 1;
+    return refresh_ws(W, B, N, k_max).total + dllm_proxy_workspace_bytes(B, N, W->d, r, W->dtype) + 256;
+}
+
+DLLM_EXPORT int dllm_layer_step(const dllm_layer *W, const void *Pt, const void *H_in, float *proxy_cache,
+                                float *proxy_cur, float *drift, const int32_t *forced, int F, int k, float min_drift,
+                                int32_t *idx, int32_t *count, void *K_cache, void *V_cache, void *H_out_cache,
+                                int B, int N, int r, void *ws, size_t ws_bytes, void *stream) {
+    int rc = check_layer(W);
+    if (rc != DLLM_OK) return rc;
+    CHECK_ARG(Pt && H_in && proxy_cache && proxy_cur && drift && idx && count && K_cache && V_cache && H_out_cache,
+              "null pointer");
+    CHECK_ARG(B > 0 && N > 0 && r > 0, "sizes must be positive (B=%d N=%d r=%d)", B, N, r);
+    CHECK_ARG(N <= 16384, "N must be <= 16384 (got %d)", N);
+    CHECK_ARG(k >= 0, "k must be >= 0");
+    if (!forced) F = 0;
+    CHECK_ARG(F >= 0, "F must be >= 0");
+    CHECK_ARG((long long)B * N <= INT_MAX, "B*N must fit in an int");
+    CHECK_ARG(H_out_cache != H_in, "H_out_cache must not alias H_in");
+    CHECK_ARG(aligned16(H_in) && aligned16(K_cache) && aligned16(V_cache) && aligned16(H_out_cache) &&
+                  aligned16(Pt) && aligned16(proxy_cache) && aligned16(proxy_cur),
+              "arrays must be 16-byte aligned");
+    CHECK_ARG(W->rope_inv_freq || !W->use_rope, "rope table missing (use dllm_pack_layer)");
+    const int k_max = (int)((long long)k + F < N ? (long long)k + F : N);
+    const size_t need = dllm_layer_step_workspace_bytes(W, B, N, r, F, k);
+    if (!ws || ws_bytes < need)
+        return fail(DLLM_ERR_WORKSPACE, "workspace holds %zu bytes, %zu needed", ws_bytes, need);
+    cudaStream_t st = as_stream(stream);
+    // a1: proxy + drift (its K-slice partials, where it needs them, after the refresh scratch)
+    const size_t rws = k_max > 0 ? refresh_ws(W, B, N, k_max).total : 0;
+    uint8_t *w8 = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255));
+    rc = dllm_proxy_score(H_in, Pt, proxy_cache, proxy_cur, drift, B, N, W->d, r, W->dtype, w8 + rws,
+                          ws_bytes - rws - 256, stream);
+    if (rc != DLLM_OK) return rc;
+    if (k_max == 0) {   // nothing can be selected: empty selection
+        return dllm_select_topk(drift, forced, F, k, min_drift, idx, count, B, N, stream);
+    }
+    SelRows sel{idx, count, k_max, N};
+    if (N > select_gather_max_n()) {   // long sequences: the selection kernel, then the plain refresh
+        rc = dllm_select_topk(drift, forced, F, k, min_drift, idx, count, B, N, stream);
+        if (rc != DLLM_OK) return rc;
+        if (W->dtype == DLLM_BF16)
+            return refresh_impl<bf16>(W, static_cast<const bf16 *>(H_in), sel, B, static_cast<bf16 *>(K_cache),
+                                      static_cast<bf16 *>(V_cache), static_cast<bf16 *>(H_out_cache), proxy_cache,
+                                      proxy_cur, r, w8, st);
+        return refresh_impl<float>(W, static_cast<const float *>(H_in), sel, B, static_cast<float *>(K_cache),
+                                   static_cast<float *>(V_cache), static_cast<float *>(H_out_cache), proxy_cache,
+                                   proxy_cur, r, w8, st);
+    }
+    const FusedSelect fs{drift, forced, F, k, min_drift, idx, count};
+    if (W->dtype == DLLM_BF16)
+        return refresh_impl<bf16>(W, static_cast<const bf16 *>(H_in), sel, B, static_cast<bf16 *>(K_cache),
+                                  static_cast<bf16 *>(V_cache), static_cast<bf16 *>(H_out_cache), proxy_cache,
+                                  proxy_cur, r, w8, st, &fs);
+    return refresh_impl<float>(W, static_cast<const float *>(H_in), sel, B, static_cast<float *>(K_cache),
+                               static_cast<float *>(V_cache), static_cast<float *>(H_out_cache), proxy_cache,
+                               proxy_cur, r, w8, st, &fs);
 }
 
 // ------------------------------------------------------------------ attention alone

@@ -50,6 +50,7 @@ struct FeatRow {
 struct EpiStoreF32 {
     static constexpr bool kSel = false;
     static constexpr bool kTileReduce = false;
+    static constexpr bool kColScale = false;
     using Feat = FeatRow;
     SelRows sel;
     float *out;
@@ -68,6 +69,7 @@ template <class T>
 struct EpiQKV {
     static constexpr bool kSel = true;
     static constexpr bool kTileReduce = false;
+    static constexpr bool kColScale = false;
     SelRows sel;
     T *Q;               // [M, n_q*hd]
     T *Kc, *Vc;         // [B, N, n_kv, hd]
@@ -115,6 +117,7 @@ template <class T>
 struct EpiResidual {
     static constexpr bool kSel = true;
     static constexpr bool kTileReduce = false;
+    static constexpr bool kColScale = false;
     using Feat = FeatRow;
     SelRows sel;
     float *h1;          // [M, d]
@@ -130,11 +133,49 @@ struct EpiResidual {
     }
 };
 
+// The O projection with the second RMSNorm folded in: h1[m, f] = H_in[b, pos, f] + acc
+// (fp32, the down projection's residual), Xh[m, f] = bf16(h1 * gamma2[f]) (the gate/up
+// GEMM's operand: RMSNorm's per-row scale is applied to its accumulators instead), and
+// ss[f / 32][m] = sum of h1^2 over the warp's 32 features (fixed-order partial sums of the
+// row's squares, summed in order by EpiSwiGLUNorm).  0 for rows that are not live.
+template <class T>
+struct EpiResidualNorm {
+    static constexpr bool kSel = true;
+    static constexpr bool kTileReduce = false;
+    static constexpr bool kColScale = false;
+    struct Feat {
+        int f;
+        float g;
+    };
+    SelRows sel;
+    float *h1;          // [M, d]
+    T *Xh;              // [M, d]
+    float *ss;          // [d / 32][M]
+    const T *H_in;      // [B, N, d]
+    const T *gamma2;    // [d]
+    int d, M;
+    __device__ __forceinline__ Feat feat(int f) const { return {f, to_f32<T>(gamma2[f])}; }
+    __device__ __forceinline__ float2 pre(const Feat &F, int, int b, int pos) const {
+        return {pos >= 0 ? to_f32<T>(H_in[((size_t)b * sel.N + pos) * d + F.f]) : 0.f, 0.f};
+    }
+    __device__ __forceinline__ void operator()(const Feat &F, int m, int, int pos, float acc,
+                                               float2 hin) const {
+        const float v = pos >= 0 ? hin.x + acc : 0.f;
+        h1[(size_t)m * d + F.f] = v;
+        Xh[(size_t)m * d + F.f] = from_f32<T>(v * F.g);
+        float sq = v * v;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        if ((F.f & 31) == 0) ss[(size_t)(F.f >> 5) * M + m] = sq;
+    }
+};
+
 // Rows 2j (gate) and 2j+1 (up): U[m, j] = SiLU(gate) * up.
 template <class T>
 struct EpiSwiGLU {
     static constexpr bool kSel = false;
     static constexpr bool kTileReduce = false;
+    static constexpr bool kColScale = false;
     using Feat = FeatRow;
     SelRows sel;
     T *U;               // [M, F]
@@ -147,11 +188,41 @@ struct EpiSwiGLU {
     }
 };
 
+// SwiGLU on the RMSNorm'd rows when the operand is bf16(h1 * gamma2) (EpiResidualNorm):
+// every accumulator of token m is first scaled by 1 / sqrt(mean(h1[m]^2) + eps), from the
+// fixed-order sum of the row's partial squares.  The GEMM evaluates col_scale(m) once per
+// token column and passes it in the column's position slot (this epilogue selects nothing).
+template <class T>
+struct EpiSwiGLUNorm {
+    static constexpr bool kSel = false;
+    static constexpr bool kTileReduce = false;
+    static constexpr bool kColScale = true;
+    using Feat = FeatRow;
+    SelRows sel;
+    T *U;               // [M, F]
+    const float *ss;    // [d / 32][M]
+    int F, d, M;
+    float eps;
+    __device__ __forceinline__ float col_scale(int m) const {
+        float s = 0.f;
+        for (int p = 0; p < d / 32; ++p) s += ss[(size_t)p * M + m];
+        return 1.0f / sqrtf(s / (float)d + eps);
+    }
+    __device__ __forceinline__ Feat feat(int f) const { return {f}; }
+    __device__ __forceinline__ float2 pre(const Feat &, int, int, int) const { return {0.f, 0.f}; }
+    __device__ __forceinline__ void operator()(const Feat &Fr, int m, int, int scale_bits, float acc, float2) const {
+        const float x = acc * __int_as_float(scale_bits);
+        const float partner = __shfl_xor_sync(0xffffffffu, x, 1);
+        if ((Fr.f & 1) == 0) U[(size_t)m * F + (Fr.f >> 1)] = from_f32<T>(silu(x) * partner);
+    }
+};
+
 // H_out_cache[b, pos, f] = h1[m, f] + acc for live rows.
 template <class T>
 struct EpiDownScatter {
     static constexpr bool kSel = true;
     static constexpr bool kTileReduce = false;
+    static constexpr bool kColScale = false;
     using Feat = FeatRow;
     SelRows sel;
     T *H_out;           // [B, N, d]
@@ -200,6 +271,7 @@ __device__ __forceinline__ VocabState vocab_merge(VocabState x, VocabState y) {
 struct EpiVocabStats {
     static constexpr bool kSel = false;
     static constexpr bool kTileReduce = true;
+    static constexpr bool kColScale = false;
     using Feat = FeatRow;
     SelRows sel;
     VocabState *part;   // [M_tok][tiles]

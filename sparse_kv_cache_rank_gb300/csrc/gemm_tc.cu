@@ -33,6 +33,7 @@ constexpr int kEpiWarps = 8;
 constexpr int kWBytes = BM * BK * 2;   // 16 KB
 constexpr int kSmemLimit = 232448;     // 227 KB dynamic shared memory per CTA
 constexpr int kSmemPair = 113 * 1024;  // budget per CTA when two share an SM
+constexpr int kGroupW = 16;            // weight tiles per group of the tile order
 constexpr int kTailBytes = 256;        // barriers, TMEM slot, abort flag
                                        // then per token column (sequence, position): 8 * BN bytes
 
@@ -93,8 +94,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     int *col_pos = col_b + g.BN;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * g.BN;
-    const int n0 = blockIdx.y * BM;
+    // tile order: with several token tiles, consecutive CTAs walk groups of kGroupW
+    // weight tiles one token tile at a time, so that the tiles resident at once share few
+    // weight and token tiles and their re-reads hit L2 (the plain order would stream every
+    // token tile past every weight tile from HBM once the token rows outgrow L2)
+    int tt = blockIdx.x, wt = blockIdx.y;
+    if (gridDim.x > 1) {
+        const int lin = blockIdx.y * gridDim.x + blockIdx.x;
+        const int per_group = kGroupW * gridDim.x;
+        const int first_w = lin / per_group * kGroupW;
+        const int gsize = min((int)gridDim.y - first_w, kGroupW);
+        const int in_group = lin - (first_w / kGroupW) * per_group;
+        wt = first_w + in_group % gsize;
+        tt = in_group / gsize;
+    }
+    const int m0 = tt * g.BN;
+    const int n0 = wt * BM;
     const int split = g.indep ? (int)blockIdx.z : (g.splits > 1 ? (int)cluster_ctarank() : 0);
     const bool cluster_split = g.splits > 1 && !g.indep;
     const int KB = g.K / BK;
@@ -184,6 +199,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         griddep_wait();
         for (int c = threadIdx.x - 64; c < g.BN; c += kThreads - 64) {
             int b = 0, pos = -1;
+            if constexpr (Epi::kColScale) {   // a per-column scale in the position slot
+                col_b[c] = 0;
+                col_pos[c] = __float_as_int(c < ncols ? epi.col_scale(m0 + c) : 0.f);
+                continue;
+            }
             if (Epi::kSel && c < ncols) epi.sel.locate(m0 + c, b, pos);
             col_b[c] = b;
             col_pos[c] = pos;
@@ -230,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 VocabState r = red[c];
 #pragma unroll
                 for (int qq = 1; qq < 4; ++qq) r = vocab_merge(r, red[qq * g.BN + c]);
-                epi.part[(size_t)(m0 + c) * epi.tiles + blockIdx.y] = r;
+                epi.part[(size_t)(m0 + c) * epi.tiles + wt] = r;
             }
         } else if (!cluster_split) {
             // straight from TMEM (independent K slices write rows split * M_tok + m)
@@ -506,8 +526,9 @@ cudaError_t launch_plan(const Plan &p, bool indep, const bf16 *W, int N_out, int
     if (!make_tmap(&tmW, W, (uint64_t)N_out, (uint64_t)K, BM) ||
         !make_tmap(&tmX, X, (uint64_t)M_tok, (uint64_t)K, (uint32_t)p.xrows))
         return cudaErrorInvalidValue;
-    // a weight matrix beyond 1/8 of L2 is streamed, not reused: evict-first lines
-    const int w_stream = (size_t)N_out * (size_t)K * 2 > (size_t)16 << 20 ? 1 : 0;
+    // a weight matrix beyond 1/8 of L2 that one token tile reads once is streamed, not
+    // reused: evict-first lines (with several token tiles its tiles are re-read)
+    const int w_stream = p.tok_tiles == 1 && (size_t)N_out * (size_t)K * 2 > (size_t)16 << 20 ? 1 : 0;
     Shape g{M_tok, N_out, K, p.BN, p.splits, p.stages, w_const ? 1 : 0, indep ? 1 : 0, p.body,
             p.xrows, p.base_aligned, p.col_bytes, w_stream};
     auto kern = k_gemm_tc<Epi>;
@@ -574,6 +595,12 @@ template cudaError_t gemm_tc<EpiResidual<bf16>>(const bf16 *, int, int, const bf
 template cudaError_t gemm_tc<EpiSwiGLU<bf16>>(const bf16 *, int, int, const bf16 *, int,
                                               const EpiSwiGLU<bf16> &, int, bool, unsigned *,
                                               cudaStream_t);
+template cudaError_t gemm_tc<EpiResidualNorm<bf16>>(const bf16 *, int, int, const bf16 *, int,
+                                                    const EpiResidualNorm<bf16> &, int, bool, unsigned *,
+                                                    cudaStream_t);
+template cudaError_t gemm_tc<EpiSwiGLUNorm<bf16>>(const bf16 *, int, int, const bf16 *, int,
+                                                  const EpiSwiGLUNorm<bf16> &, int, bool, unsigned *,
+                                                  cudaStream_t);
 template cudaError_t gemm_tc<EpiDownScatter<bf16>>(const bf16 *, int, int, const bf16 *, int,
                                                    const EpiDownScatter<bf16> &, int, bool, unsigned *,
                                                    cudaStream_t);

@@ -157,12 +157,22 @@ cudaError_t attention_simt(const T *Q, const T *Kc, const T *Vc, T *A, SelRows s
 // Tensor cores (bf16, hd in {64, 128}); the key range is split over a cluster of up to
 // 8 CTAs (attention_tc_splits) merged through distributed shared memory: no workspace.
 int attention_tc_splits(int B, int k_max, int n_q, int N);
+
 cudaError_t attention_tc(const bf16 *Q, const bf16 *Kc, const bf16 *Vc, bf16 *A, SelRows sel, int B,
                          int n_q, int n_kv, int hd, unsigned *status, cudaStream_t st);
 
 // ---------------------------------------------------------------- selection
 cudaError_t select_topk(const float *drift, const int32_t *forced, int F, int k, float min_drift,
                         int32_t *idx, int32_t *count, int B, int N, cudaStream_t st);
+
+// Selection fused with the gather of the selected rows (front.cu): idx / count as
+// select_topk, and for rows m = b * k_max + s the outputs of gather_rmsnorm.  N <= 4096.
+int select_gather_max_n();
+template <class T>
+cudaError_t select_gather(const float *drift, const int32_t *forced, int F, int k, float min_drift, int32_t *idx,
+                          int32_t *count, int B, int N, int k_max, const T *H, int d, const T *gamma, float eps,
+                          T *Xn, float *proxy_cache, const float *proxy_cur, int r, const float *inv_freq,
+                          int half_hd, float2 *rope_cs, unsigned *status, cudaStream_t st);
 
 // ---------------------------------------------------------------- vocabulary
 size_t commit_ws_bytes(int B, int M, int V);

@@ -126,7 +126,9 @@ class DecodeStack:
         self.cnt = torch.empty((Bn,), device=device, dtype=torch.int32)
         self.idx_all = torch.arange(N, device=device, dtype=torch.int32).repeat(Bn, 1).contiguous()
         self.cnt_all = torch.full((Bn,), N, device=device, dtype=torch.int32)
-        self.ws = torch.empty(B.dllm_refresh_workspace_bytes(self.layers[0].layer, Bn, N, N),
+        self.ws = torch.empty(max(B.dllm_refresh_workspace_bytes(self.layers[0].layer, Bn, N, N),
+                                  B.dllm_layer_step_workspace_bytes(self.layers[0].layer, Bn, N, sh.r,
+                                                                    sh.block + k_recent, N)),
                               device=device, dtype=torch.uint8)
         self.ws_proxy = torch.empty(max(256, int(B.lib().dllm_proxy_workspace_bytes(Bn, N, d, sh.r, B.DLLM_BF16))),
                                     device=device, dtype=torch.uint8)
@@ -185,19 +187,19 @@ class DecodeStack:
         is appended: the layer's drift, selection and row count (copies)."""
         sh = self.sh
         H = self.H0 if H0 is None else H0
-        F = self.forced.shape[1]
         for l, L in enumerate(self.layers):
-            B.dllm_proxy_score(H, L.Pt, L.pc, proxy_cur=L.cur, drift=self.drift, ws=self.ws_proxy)
             if full:
-                idx, cnt, k_max = self.idx_all, self.cnt_all, sh.N
+                B.dllm_proxy_score(H, L.Pt, L.pc, proxy_cur=L.cur, drift=self.drift, ws=self.ws_proxy)
+                idx, cnt = self.idx_all, self.cnt_all
+                B.dllm_sparse_layer_refresh(L.layer, H, idx, cnt, sh.N, L.K, L.V, L.O, L.pc, L.cur, ws=self.ws)
             else:
-                k = self.budgets[l]
-                B.dllm_select_topk(self.drift, self.forced, k, idx=self.idx, count=self.cnt)
-                idx, cnt, k_max = self.idx, self.cnt, min(sh.N, k + F)
+                # proxy + drift, the budget's selection with the forced rows, the refresh:
+                # one library call per layer
+                idx, cnt = B.dllm_layer_step(L.layer, L.Pt, H, L.pc, L.cur, self.drift, self.forced,
+                                             self.budgets[l], self.idx, self.cnt, L.K, L.V, L.O, ws=self.ws)
             if record is not None:
                 record.append({"drift": self.drift.clone(), "idx": idx.clone(), "cnt": cnt.clone(),
                                "k": sh.N if full else self.budgets[l]})
-            B.dllm_sparse_layer_refresh(L.layer, H, idx, cnt, k_max, L.K, L.V, L.O, L.pc, L.cur, ws=self.ws)
             H = L.O
         X = B.dllm_rows_rmsnorm(H, self.block_rows, self.gamma_f, sh.eps, out=self.Xf)
         if self.keep_logits:

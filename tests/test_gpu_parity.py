@@ -102,7 +102,7 @@ def test_select_degenerate(B, orc):
 
 
 # --------------------------------------------------------------------------- refresh
-def _step(B, orc, c, k, forced, sample=None, sample_seed=0):
+def _step(B, orc, c, k, forced, sample=None, sample_seed=0, one_call=False):
     """One step on the GPU and on the oracle, each from the same seeded inputs and each
     deciding on its own values: the oracle scores, selects and refreshes by itself.
     sample=n: the oracle computes the layer outputs of n rows drawn from its own
@@ -112,16 +112,24 @@ def _step(B, orc, c, k, forced, sample=None, sample_seed=0):
     Bn, N = sh.B, sh.N
     H = to_dev(c.H_cur, dt)
     pc = to_dev(c.pc0)
-    cur, drift = B.dllm_proxy_score(H, to_dev(c.P.T.copy(), dt), pc)
+    Pt = to_dev(c.P.T.copy(), dt)
     fo = to_dev(forced) if forced is not None else None
-    idx, cnt = B.dllm_select_topk(drift, fo, k)
     k_max = min(N, k + (0 if forced is None else forced.shape[1]))
     layer = B.dllm_pack_layer({n: to_dev(v, dt) for n, v in c.w.items()}, sh.n_q, sh.n_kv, sh.hd,
                               eps=sh.eps, rope_theta=sh.rope_theta)
     K = to_dev(c.K0, dt)
     V = to_dev(c.V0, dt)
     O = to_dev(c.O0, dt)
-    B.dllm_sparse_layer_refresh(layer, H, idx, cnt, k_max, K, V, O, pc, cur)
+    if one_call:   # proxy, selection and refresh through dllm_layer_step
+        cur = torch.empty((Bn, N, sh.r), dtype=torch.float32, device="cuda")
+        drift = torch.empty((Bn, N), dtype=torch.float32, device="cuda")
+        idx = torch.empty((Bn, N), dtype=torch.int32, device="cuda")
+        cnt = torch.empty((Bn,), dtype=torch.int32, device="cuda")
+        B.dllm_layer_step(layer, Pt, H, pc, cur, drift, fo, k, idx, cnt, K, V, O)
+    else:
+        cur, drift = B.dllm_proxy_score(H, Pt, pc)
+        idx, cnt = B.dllm_select_topk(drift, fo, k)
+        B.dllm_sparse_layer_refresh(layer, H, idx, cnt, k_max, K, V, O, pc, cur)
     torch.cuda.synchronize()
     assert B.check_status() == 0
     g = dict(cur=to_np(cur), drift=to_np(drift), idx=to_np(idx), cnt=to_np(cnt), K=to_np(K),
@@ -164,13 +172,51 @@ def _compare_step(c, g, o, forced, k):
                             f"H_out - H_in b={b}")
 
 
+@pytest.mark.parametrize("one_call", [False, True], ids=["three-calls", "layer-step"])
 @pytest.mark.parametrize("shape", [synth.TINY, TINY_BF16, SMALL_BF16, MID_BF16], ids=lambda s: s.name)
-def test_refresh_step_parity(B, orc, shape):
+def test_refresh_step_parity(B, orc, shape, one_call):
     c = layer_case(orc, shape, 20)
     forced = forced_rows(shape, 21) if shape.k_recent else None
     k = orc.budget(shape.rho, shape.N)
-    g, o = _step(B, orc, c, k, forced)
+    g, o = _step(B, orc, c, k, forced, one_call=one_call)
     _compare_step(c, g, o, forced, k)
+
+
+LONG_SMALL = synth.LayerShape("long-small-bf16", B=2, N=5000, d=128, n_q=2, n_kv=1, hd=64, F=128, r=32,
+                              rho=0.02, dtype="bf16", prompt=4900, k_recent=4)
+
+
+@pytest.mark.parametrize("shape", [SMALL_BF16, synth.TINY, LONG_SMALL], ids=lambda s: s.name)
+def test_layer_step_equals_three_calls(B, orc, shape):
+    """dllm_layer_step (selection fused with the gather up to N = 4096, the separate
+    kernels beyond) writes exactly what dllm_proxy_score, dllm_select_topk and
+    dllm_sparse_layer_refresh write in sequence: the same kernels' arithmetic, bit for bit."""
+    c = layer_case(orc, shape, 25, consistent=shape.N <= 1024)
+    forced = forced_rows(shape, 26)
+    k = orc.budget(shape.rho, shape.N)
+    dt = torch_dtype(shape)
+    layer = B.dllm_pack_layer({n: to_dev(v, dt) for n, v in c.w.items()}, shape.n_q, shape.n_kv, shape.hd,
+                              eps=shape.eps, rope_theta=shape.rope_theta)
+    outs = []
+    for one in (False, True):
+        H, Pt, pc = to_dev(c.H_cur, dt), to_dev(c.P.T.copy(), dt), to_dev(c.pc0)
+        K, V, O = to_dev(c.K0, dt), to_dev(c.V0, dt), to_dev(c.O0, dt)
+        fo = to_dev(forced)
+        if one:
+            cur = torch.empty((shape.B, shape.N, shape.r), device="cuda")
+            drift = torch.empty((shape.B, shape.N), device="cuda")
+            idx = torch.empty((shape.B, shape.N), dtype=torch.int32, device="cuda")
+            cnt = torch.empty((shape.B,), dtype=torch.int32, device="cuda")
+            B.dllm_layer_step(layer, Pt, H, pc, cur, drift, fo, k, idx, cnt, K, V, O)
+        else:
+            cur, drift = B.dllm_proxy_score(H, Pt, pc)
+            idx, cnt = B.dllm_select_topk(drift, fo, k)
+            B.dllm_sparse_layer_refresh(layer, H, idx, cnt, min(shape.N, k + forced.shape[1]), K, V, O, pc, cur)
+        torch.cuda.synchronize()
+        outs.append([t.clone() for t in (cur, drift, idx, cnt, K, V, O, pc)])
+    assert B.check_status() == 0
+    for name, a, b in zip(("cur", "drift", "idx", "count", "K", "V", "H_out", "proxy_cache"), *outs):
+        assert torch.equal(a, b), name
 
 
 @pytest.mark.parametrize("shape", [synth.TINY, SMALL_BF16], ids=lambda s: s.name)
@@ -194,7 +240,7 @@ def test_refresh_llada_layer_sampled(B, orc):
     c = layer_case(orc, sh, 40, consistent=False, svd_proxy=False)
     k = orc.budget(sh.rho, sh.N)
     assert k == 164
-    g, o = _step(B, orc, c, k, None, sample=12, sample_seed=41)
+    g, o = _step(B, orc, c, k, None, sample=12, sample_seed=41, one_call=True)
     _compare_step(c, g, o, None, k)
     # every strongly perturbed row is in the selection
     assert set(c.hot[0].tolist()) <= set(g["idx"][0, :g["cnt"][0]].tolist())
@@ -296,13 +342,30 @@ def test_refresh_long_context_point(B, orc):
     _sampled_layer_parity(B, orc, sh, 71, n_sample=6)
 
 
+def test_refresh_long_context_batch4_half(B, orc):
+    """Long-context sweep point with a batch and half the rows refreshed: LLaDA-8B-shaped
+    layer at N = 2048, batch 4, 50 % (1024 rows per sequence, 4096 in all, the
+    tensor-bound side of the sweep, taken by the one-call layer step); K/V of every
+    selected row, outputs of 4 rows per sequence."""
+    sh = dataclasses.replace(synth.LLADA_LAYER, name="llada8b-N2048-B4-rho0.5", N=2048, B=4, rho=0.5,
+                             prompt=1024)
+    c = layer_case(orc, sh, 72, consistent=False, svd_proxy=False)
+    k = orc.budget(sh.rho, sh.N)
+    assert k == 1024
+    g, o = _step(B, orc, c, k, None, sample=4, sample_seed=72, one_call=True)
+    _compare_step(c, g, o, None, k)
+
+
 # --------------------------------------------------------------------------- attention alone
 @pytest.mark.parametrize("Bq,N,k_max,n_q,n_kv,hd,live", [
     (1, 1024, 164, 32, 32, 128, 164), (2, 333, 150, 4, 2, 64, 150), (1, 2048, 328, 28, 4, 128, 300),
-    (3, 200, 37, 8, 8, 128, 37), (1, 129, 129, 2, 1, 64, 100)])
+    (3, 200, 37, 8, 8, 128, 37), (1, 129, 129, 2, 1, 64, 100),
+    # one key slice per CTA (the grid alone fills the GPU), a ragged second query tile
+    (8, 256, 200, 28, 4, 128, 200), (16, 150, 140, 16, 16, 64, 140)])
 def test_attention_parity(B, orc, Bq, N, k_max, n_q, n_kv, hd, live):
     """Selected queries over the whole cache, non-causal, GQA, ragged key tiles and
-    partially live query tiles, against the oracle's attention of every live row."""
+    partially live query tiles, key slices merged in a cluster and single-slice CTAs,
+    against the oracle's attention of every live row."""
     g = synth.rng(400 + N + k_max)
     dq, dkv = n_q * hd, n_kv * hd
     Q = synth.round_bf16(g.standard_normal((Bq * k_max, dq), dtype=np.float32))
