@@ -2,8 +2,8 @@
 
 * Guard bytes: every array an entry point receives sits inside a larger allocation
   whose 4 KB before and after it hold a seeded byte pattern; after the calls of one
-  sparse refresh step (and the vocabulary, LM head, attention, GEMM, KL drift and row
-  read-back calls) at ragged shapes, every guard must be bit-unchanged -- no kernel
+  sparse refresh step, the one-call layer step (and the vocabulary, LM head, attention,
+  GEMM, KL drift and row read-back calls) at ragged shapes, every guard must be bit-unchanged -- no kernel
   wrote past the end (or before the start) of an output, a cache or a workspace.
 * Bounded waits: the library's diagnostic runs the same bounded mbarrier wait the
   pipelined kernels use on a barrier nothing completes; the wait must give up after its
@@ -89,6 +89,11 @@ def test_step_writes_stay_inside_their_arrays(B, orc):
     O = G.new((sh.B, sh.N, sh.d), bf, torch.from_numpy(c.O0).to(bf))
     rws = G.new((B.dllm_refresh_workspace_bytes(layer, sh.B, sh.N, k_max),), torch.uint8)
     B.dllm_sparse_layer_refresh(layer, H, idx, cnt, k_max, K, V, O, pc, cur, ws=rws)
+    # the one-call layer step (proxy, fused selection + gather, stream-K projections)
+    lws = G.new((int(B.dllm_layer_step_workspace_bytes(layer, sh.B, sh.N, sh.r, forced.shape[1], k)),), torch.uint8)
+    idx2 = G.new((sh.B, sh.N), torch.int32)
+    cnt2 = G.new((sh.B,), torch.int32)
+    B.dllm_layer_step(layer, Pt, H, pc, cur, drift, fo, k, idx2, cnt2, K, V, O, ws=lws)
     # attention alone over ragged live rows, and the read-back of the refreshed rows
     Q = G.new((sh.B * k_max, sh.d_q), bf, torch.randn((sh.B * k_max, sh.d_q)).to(bf))
     A = G.new((sh.B * k_max, sh.d_q), bf)
