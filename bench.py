@@ -1025,7 +1025,7 @@ def cpu_baseline(sh, full):
         pts.append({"point": name, "threads": cores, "s_per_step": t_all, "steps_per_s": 1.0 / t_all,
                     "steps_timed": reps, "rows_per_step": rows})
         if name == "llada8b-layer":
-            head = (t_all, reps)
+            head = (t_all, reps, rows)
         if full or t_all * cores <= 60.0:
             t1, reps1, _ = _time_oracle(o, k, 1, 60.0)
             pts.append({"point": name, "threads": 1, "s_per_step": t1, "steps_per_s": 1.0 / t1,
@@ -1033,10 +1033,10 @@ def cpu_baseline(sh, full):
         else:
             pts.append({"point": name, "threads": 1, "not_run": "cap: one step > 60 s expected "
                         f"({t_all * cores:.0f} s from the {cores}-thread time); run with --cpu-full"})
-    t_all, reps = head
+    t_all, reps, rows = head
     return {"value": 1.0 / t_all, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{reps} whole LLaDA-8B-shaped layer steps (proxy of all {sh.N} rows, selection, refresh "
-                      f"of {k} rows) from the first step's state, on host-drawn inputs of the same workload, "
+                      f"of {rows} rows) from the first step's state, on host-drawn inputs of the same workload, "
                       f"{cores} threads; not extrapolated",
             "cpu_model": cpu_model(), "points": pts}
 

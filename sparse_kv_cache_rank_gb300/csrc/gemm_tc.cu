@@ -502,8 +502,13 @@ Plan plan_gemm(int M_tok, int N_out, int K, int splits_req, int sms) {
         while (BN > 64 && (long long)w_tiles * ((M_tok + BN - 1) / BN) * 8 < sms) BN = round16(BN / 2);
     }
     const long long tiles = (long long)w_tiles * ((M_tok + BN - 1) / BN);
-    const int s = tiles >= sms ? 1 : clamp_splits((int)(sms / tiles));
-    return make_plan(M_tok, N_out, K, BN, s, s == 1 ? kSmemPair : kSmemLimit, s > 1);
+    if (tiles >= sms) return make_plan(M_tok, N_out, K, BN, 1, kSmemPair, false);
+    // fewer tiles than SMs (a few hundred tokens against a narrow weight, e.g. the O and
+    // down projections at 257..600 rows): a K split over a cluster so that every SM
+    // streams, two CTAs per SM when the fp32 partial tile fits their share
+    const bool pair = BN * BM * 4 + 1024 + kTailBytes + 8 * BN <= kSmemPair;
+    const int s = clamp_splits((int)((pair ? 2 : 1) * (long long)sms / tiles));
+    return make_plan(M_tok, N_out, K, BN, s, s > 1 && !pair ? kSmemLimit : kSmemPair, s > 1);
 }
 
 // Independent K slices (no cluster), each writing its own fp32 partial output: token

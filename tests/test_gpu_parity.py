@@ -342,6 +342,16 @@ def test_refresh_long_context_point(B, orc):
     _sampled_layer_parity(B, orc, sh, 71, n_sample=6)
 
 
+def test_refresh_long_context_n2048_sixteenth(B, orc):
+    """Long-context sweep point just past the few-token regime: LLaDA-8B-shaped layer at
+    N = 2048 with 16 % (328 rows): the O and down projections (32 weight tiles x 3 token
+    tiles of 128) run with a 3-way cluster K split so that every SM streams."""
+    sh = dataclasses.replace(synth.LLADA_LAYER, name="llada8b-N2048-rho0.16", N=2048, rho=0.16, prompt=1024)
+    p = B.dllm_gemm_plan(orc.budget(sh.rho, sh.N), sh.d, sh.d_q, sms=152)
+    assert p["splits"] == 3 and p["tok_tiles"] == 3
+    _sampled_layer_parity(B, orc, sh, 73, n_sample=6)
+
+
 def test_refresh_long_context_batch4_half(B, orc):
     """Long-context sweep point with a batch and half the rows refreshed: LLaDA-8B-shaped
     layer at N = 2048, batch 4, 50 % (1024 rows per sequence, 4096 in all, the

@@ -50,6 +50,17 @@ def test_layer_step_plans_at_164_rows(B):
             assert p[k] == v, (N_out, K, k, p)
 
 
+def test_few_tiles_get_a_k_split(B):
+    """Past 256 rows, O and down (32 weight tiles of the LLaDA-8B-shaped layer) at a few
+    hundred rows have fewer tiles than SMs: a cluster K split fills the GPU (288 / 256 CTAs
+    at two per SM) instead of leaving 96 / 128 CTAs to stream all K blocks alone."""
+    for M, splits, ctas in ((271, 3, 288), (328, 3, 288), (410, 2, 256)):
+        for N_out, K in ((4096, 4096), (4096, 12288)):
+            p = B.dllm_gemm_plan(M, N_out, K, sms=152)
+            assert p["BN"] == 128 and p["splits"] == splits and p["ctas_per_sm"] == 2, (M, N_out, K, p)
+            assert p["tok_tiles"] * p["w_tiles"] * p["splits"] == ctas
+
+
 def _proj(d, dq, dkv, F):
     return {"qkv": (dq + 2 * dkv, d), "oproj": (d, dq), "gateup": (2 * F, d), "down": (d, F)}
 
