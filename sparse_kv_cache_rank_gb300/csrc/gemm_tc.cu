@@ -424,35 +424,45 @@ Plan make_plan(int M_tok, int N_out, int K, int BN, int splits, int budget, bool
     return p;
 }
 
-// Token-tile width for many tokens (M > 256).  A CTA here is latency-bound: its time per
-// K block barely changes whether it shares the SM or not, and it depends on the width
-// mostly through the pipeline depth that two CTAs per SM leave (three stages up to 160
-// columns, two above).  So a width is charged, per round of two CTAs on every SM, a fixed
-// cost plus K blocks x its time per K block; a last round of at most one CTA per SM
+// Token-tile width (and K split) for many tokens (M > 256).  A CTA here is latency-bound:
+// its time per K block barely changes whether it shares the SM or not, and it depends on
+// the width mostly through the pipeline depth that two CTAs per SM leave (three stages up
+// to 160 columns, two above).  So a width is charged, per round of two CTAs on every SM, a
+// fixed cost plus K blocks x its time per K block; a last round of at most one CTA per SM
 // takes the time of a CTA alone.  The times are least-squares fits to the layer
-// projections of a GB300 over N = 2048..8192 tokens (LLaDA-8B and Dream-7B shapes),
-// where the model picks the fastest width in 19 of 20 cases.  Returns 0 when no width
-// gives at least half the SMs a tile.
-int pick_bn_many(int M_tok, int w_tiles, int KB, int sms) {
+// projections of a GB300 over N = 2048..8192 tokens (LLaDA-8B and Dream-7B shapes), where
+// the model picks the fastest width in 19 of 20 cases.  A K split over a cluster divides a
+// CTA's K blocks and multiplies the CTAs (considered when the fp32 partial tile still fits
+// two CTAs per SM), for a fixed reduction cost; it pays where the tiles alone leave a round
+// far from full.  Returns 0 when no plan gives at least half the SMs a CTA.
+int pick_bn_many(int M_tok, int w_tiles, int KB, int sms, int *splits) {
     static const int bns[] = {128, 160, 176, 192, 208, 224, 256};
     static const float us_pair[] = {0.378f, 0.433f, 0.592f, 0.616f, 0.652f, 0.688f, 0.758f};
     static const float us_alone[] = {0.311f, 0.388f, 0.617f, 0.625f, 0.660f, 0.647f, 0.690f};
-    const float us_fixed = 14.6f;
+    const float us_fixed = 14.6f, us_split = 2.0f;
     const long long slots = 2LL * sms;
-    int best = 0;
+    int best = 0, best_s = 1;
     float best_us = 0.f;
     for (int i = 0; i < 7; ++i) {
         const long long tiles = (long long)w_tiles * ((M_tok + bns[i] - 1) / bns[i]);
-        if (2 * tiles < sms) continue;
-        const long long rounds = (tiles + slots - 1) / slots;
-        const long long last = tiles - slots * (rounds - 1);
-        const float us = (float)(rounds - 1) * (us_fixed + (float)KB * us_pair[i]) + us_fixed +
-                         (float)KB * (last <= sms ? us_alone[i] : us_pair[i]);
-        if (best == 0 || us < best_us) {
-            best = bns[i];
-            best_us = us;
+        const bool pair_split = bns[i] * BM * 4 + 1024 + kTailBytes + 8 * bns[i] <= kSmemPair;
+        for (int s = 1; s <= 8; ++s) {
+            if (s > 1 && (!pair_split || KB / s < 2)) break;
+            const long long ctas = tiles * s;
+            if (2 * ctas < sms) continue;
+            const long long rounds = (ctas + slots - 1) / slots;
+            const long long last = ctas - slots * (rounds - 1);
+            const float kb = (float)KB / (float)s;
+            const float us = (float)(rounds - 1) * (us_fixed + kb * us_pair[i]) + us_fixed +
+                             kb * (last <= sms ? us_alone[i] : us_pair[i]) + (s > 1 ? us_split : 0.f);
+            if (best == 0 || us < best_us) {
+                best = bns[i];
+                best_s = s;
+                best_us = us;
+            }
         }
     }
+    *splits = best_s;
     return best;
 }
 
@@ -496,7 +506,9 @@ Plan plan_gemm(int M_tok, int N_out, int K, int splits_req, int sms) {
         const int s = clamp_splits(sms / (w_tiles * tok_tiles));
         return make_plan(M_tok, N_out, K, BN, s, s == 1 ? kSmemPair : kSmemLimit, s > 1);
     }
-    int BN = pick_bn_many(M_tok, w_tiles, KB, sms);
+    int s_model = 1;
+    int BN = pick_bn_many(M_tok, w_tiles, KB, sms, &s_model);
+    if (BN != 0 && s_model > 1) return make_plan(M_tok, N_out, K, BN, s_model, kSmemPair, true);
     if (BN == 0) {
         BN = 256;
         while (BN > 64 && (long long)w_tiles * ((M_tok + BN - 1) / BN) * 8 < sms) BN = round16(BN / 2);

@@ -3,10 +3,11 @@
 
 * The plans of the LLaDA-8B-shaped layer's projections at 164 gathered rows on a 152-SM
   GB300 are the ones the profiles were measured with (grid, cluster K split, stages).
-* For more than 256 tokens, the widths the tile-time model picks on the 20 measured
+* For more than 256 tokens, the widths the tile-time model picks on the measured
   projections (Dream-7B-shaped layer and the LLaDA-8B-shaped layer at N = 2048 ... 8192)
   are the measured-fastest ones, except N = 8192 at 100 % down (model 160, measured 224,
-  both faster than 256).
+  both faster than 256); where the tiles leave a round far from full (O and down at a
+  few hundred rows) the model adds a K split.
 * Invariants over a grid of shapes, split requests and SM counts: the tile fits the
   tensor-memory and TMA limits, every token row is covered exactly once, K splits leave
   every CTA at least two K blocks, the pipeline has at least two stages and the shared
@@ -52,12 +53,13 @@ def test_layer_step_plans_at_164_rows(B):
 
 def test_few_tiles_get_a_k_split(B):
     """Past 256 rows, O and down (32 weight tiles of the LLaDA-8B-shaped layer) at a few
-    hundred rows have fewer tiles than SMs: a cluster K split fills the GPU (288 / 256 CTAs
-    at two per SM) instead of leaving 96 / 128 CTAs to stream all K blocks alone."""
-    for M, splits, ctas in ((271, 3, 288), (328, 3, 288), (410, 2, 256)):
+    hundred rows have fewer tiles than SMs: the width model's K split over a cluster fills
+    the GPU (256-288 CTAs at two per SM) instead of leaving 96-192 CTAs to stream all K
+    blocks alone (down at 328 rows: 86 -> 45 us on a GB300)."""
+    for M, BN, splits, ctas in ((271, 160, 4, 256), (328, 128, 3, 288), (410, 160, 3, 288), (656, 176, 2, 256)):
         for N_out, K in ((4096, 4096), (4096, 12288)):
             p = B.dllm_gemm_plan(M, N_out, K, sms=152)
-            assert p["BN"] == 128 and p["splits"] == splits and p["ctas_per_sm"] == 2, (M, N_out, K, p)
+            assert p["BN"] == BN and p["splits"] == splits and p["ctas_per_sm"] == 2, (M, N_out, K, p)
             assert p["tok_tiles"] * p["w_tiles"] * p["splits"] == ctas
 
 
@@ -68,12 +70,14 @@ def _proj(d, dq, dkv, F):
 @pytest.mark.parametrize("M,shape,want", [
     (2624, (3584, 3584, 512, 18944), {"qkv": 176, "oproj": 128, "gateup": 256, "down": 128}),
     (2048, (4096, 4096, 4096, 12288), {"qkv": 256, "oproj": 256, "gateup": 256, "down": 256}),
-    (656, (4096, 4096, 4096, 12288), {"qkv": 224, "oproj": 128, "gateup": 224, "down": 128}),
+    (656, (4096, 4096, 4096, 12288), {"qkv": 224, "gateup": 224}),
     (1311, (4096, 4096, 4096, 12288), {"qkv": 224, "oproj": 160, "gateup": 224, "down": 160}),
     (8192, (4096, 4096, 4096, 12288), {"qkv": 256, "oproj": 224, "gateup": 256, "down": 160}),
 ])
 def test_many_token_widths(B, M, shape, want):
     for name, (N_out, K) in _proj(*shape).items():
+        if name not in want:
+            continue
         p = B.dllm_gemm_plan(M, N_out, K, sms=152)
         assert p["BN"] == want[name], (M, name, p)
         assert p["splits"] == 1 and p["ctas_per_sm"] == 2
