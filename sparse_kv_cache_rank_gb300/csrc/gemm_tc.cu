@@ -297,14 +297,24 @@ __global__ void __launch_bounds__(kThreads, 2)
                     float acc[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-                    for (int r = 0; r < g.splits; ++r) {
-                        const uint32_t base = mapa_shared(part_s, (uint32_t)r);
-                        float v[16];
+                    // two CTAs' columns in flight at once, added in rank order
+                    for (int r = 0; r < g.splits; r += 2) {
+                        const bool two = r + 1 < g.splits;
+                        const uint32_t ba = mapa_shared(part_s, (uint32_t)r);
+                        const uint32_t bb = mapa_shared(part_s, (uint32_t)(two ? r + 1 : r));
+                        float va[16], vb[16];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            v[j] = ld_dsmem_f32(base + (uint32_t)(min(c + j, c_end - 1) * BM) * 4u);
+                        for (int j = 0; j < 16; ++j) {
+                            const uint32_t off = (uint32_t)(min(c + j, c_end - 1) * BM) * 4u;
+                            va[j] = ld_dsmem_f32(ba + off);
+                            vb[j] = ld_dsmem_f32(bb + off);
+                        }
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) acc[j] += v[j];
+                        for (int j = 0; j < 16; ++j) acc[j] += va[j];
+                        if (two) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) acc[j] += vb[j];
+                        }
                     }
                     epi_16(epi, F, m0, c, c_end, col_b, col_pos, acc);
                 }
