@@ -759,11 +759,13 @@ def layer_point(sh, dev, steps, warmup, seed=77, shared=None):
     torch.cuda.synchronize(dev)
     dt = e0.elapsed_time(e1) / 1e3 / steps
     rows = int(wl.cnt.sum().item())
-    per_kernel = kernel_breakdown(wl, reps=3) if sh.dtype == "bf16" else None
+    per_kernel = kernel_breakdown(wl, reps=3)
     res = {"B": sh.B, "N": sh.N, "rho": sh.rho, "rows_per_step": rows, "dtype": sh.dtype,
            "steps_per_s": 1.0 / dt, "ms_per_step": dt * 1e3, "tokens_per_s": sh.B * sh.N / dt,
            "refreshed_rows_per_s": rows / dt}
-    if per_kernel is not None:
+    if sh.dtype != "bf16":   # fp32 on the CUDA cores: per-kernel times, no bf16 roofline
+        res["kernel_ms"] = {k: round(v, 5) for k, v in per_kernel.items()}
+    else:
         dom = max(per_kernel, key=per_kernel.get)
         res["kernel_ms"] = {k: round(v, 5) for k, v in per_kernel.items()}
         res["roofline"] = roofline_of(sh, rows, per_kernel, dom, sustained=True)
