@@ -34,6 +34,9 @@ SMALL_BF16 = synth.LayerShape("small-bf16-gqa", B=2, N=200, d=256, n_q=4, n_kv=2
 MID_BF16 = synth.LayerShape("mid-bf16-hd128", B=1, N=333, d=512, n_q=4, n_kv=4, hd=128, F=704,
                             r=128, rho=0.3, dtype="bf16", prompt=200)
 TINY_BF16 = dataclasses.replace(synth.TINY, name="tiny-bf16", dtype="bf16")
+# fp32 on the CUDA cores with 128-dim heads, GQA and a ragged key tail per attention warp
+MID_F32_GQA = synth.LayerShape("mid-f32-hd128-gqa", B=2, N=301, d=512, n_q=4, n_kv=2, hd=128, F=640,
+                               r=32, rho=0.2, dtype="f32", prompt=200)
 
 
 # --------------------------------------------------------------------------- proxy
@@ -173,7 +176,7 @@ def _compare_step(c, g, o, forced, k):
 
 
 @pytest.mark.parametrize("one_call", [False, True], ids=["three-calls", "layer-step"])
-@pytest.mark.parametrize("shape", [synth.TINY, TINY_BF16, SMALL_BF16, MID_BF16], ids=lambda s: s.name)
+@pytest.mark.parametrize("shape", [synth.TINY, TINY_BF16, SMALL_BF16, MID_BF16, MID_F32_GQA], ids=lambda s: s.name)
 def test_refresh_step_parity(B, orc, shape, one_call):
     c = layer_case(orc, shape, 20)
     forced = forced_rows(shape, 21) if shape.k_recent else None
