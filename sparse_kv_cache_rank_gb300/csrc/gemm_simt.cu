@@ -22,8 +22,10 @@ template <class Epi>
 __global__ void __launch_bounds__(kT) k_gemm_simt(const float *__restrict__ W, int N_out, int K,
                                                   const float *__restrict__ X, int M_tok, const Epi epi,
                                                   int splits) {
-    __shared__ float Ws[TK][TF + 1];
-    __shared__ float Xs[TK][TM + 1];
+    // rows padded to 36 words: 16-byte aligned for the float4 reads of Xs, and the
+    // transposed stores below (rows lk + 8i, columns lr) still hit 32 distinct banks
+    __shared__ __align__(16) float Ws[TK][TF + 4];
+    __shared__ __align__(16) float Xs[TK][TM + 4];
     __shared__ float part[TM][TF];   // this CTA's partial tile (K split)
     griddep_wait();
     griddep_launch();
@@ -61,8 +63,11 @@ __global__ void __launch_bounds__(kT) k_gemm_simt(const float *__restrict__ W, i
 #pragma unroll
         for (int k = 0; k < TK; ++k) {
             const float a = Ws[k][lane];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[j] = fmaf(a, Xs[k][warp * 4 + j], acc[j]);
+            const float4 x = *reinterpret_cast<const float4 *>(&Xs[k][warp * 4]);   // broadcast
+            acc[0] = fmaf(a, x.x, acc[0]);
+            acc[1] = fmaf(a, x.y, acc[1]);
+            acc[2] = fmaf(a, x.z, acc[2]);
+            acc[3] = fmaf(a, x.w, acc[3]);
         }
         __syncthreads();
     }
