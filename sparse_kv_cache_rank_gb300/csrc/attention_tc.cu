@@ -310,9 +310,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (row_ok) {
                 const float inv = (r < live && l_tot > 0.f) ? 1.0f / l_tot : 0.f;
                 bf16 *dst = a.A + row * dq + (size_t)h * HD + hf * OH;
+                // 16-byte stores (8 dims): the 32 lanes of a warp write 32 different rows
 #pragma unroll
-                for (int e = 0; e < OH; e += 2)
-                    *reinterpret_cast<__nv_bfloat162 *>(dst + e) = __floats2bfloat162_rn(o[e] * inv, o[e + 1] * inv);
+                for (int e = 0; e < OH; e += 8) {
+                    uint4 u;
+                    const __nv_bfloat162 p0 = __floats2bfloat162_rn(o[e] * inv, o[e + 1] * inv);
+                    const __nv_bfloat162 p1 = __floats2bfloat162_rn(o[e + 2] * inv, o[e + 3] * inv);
+                    const __nv_bfloat162 p2 = __floats2bfloat162_rn(o[e + 4] * inv, o[e + 5] * inv);
+                    const __nv_bfloat162 p3 = __floats2bfloat162_rn(o[e + 6] * inv, o[e + 7] * inv);
+                    u.x = *reinterpret_cast<const uint32_t *>(&p0);
+                    u.y = *reinterpret_cast<const uint32_t *>(&p1);
+                    u.z = *reinterpret_cast<const uint32_t *>(&p2);
+                    u.w = *reinterpret_cast<const uint32_t *>(&p3);
+                    *reinterpret_cast<uint4 *>(dst + e) = u;
+                }
             }
         }
     }
@@ -373,8 +384,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float iv = den > 0.f ? 1.0f / den : 0.f;
                     __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(
                         a.A + (row0 + rr) * dq + (size_t)h * HD + d4 * 4);
-                    dst[0] = __floats2bfloat162_rn(acc.x * iv, acc.y * iv);
-                    dst[1] = __floats2bfloat162_rn(acc.z * iv, acc.w * iv);
+                    const __nv_bfloat162 p0 = __floats2bfloat162_rn(acc.x * iv, acc.y * iv);
+                    const __nv_bfloat162 p1 = __floats2bfloat162_rn(acc.z * iv, acc.w * iv);
+                    uint2 u;   // one 8-byte store
+                    u.x = *reinterpret_cast<const uint32_t *>(&p0);
+                    u.y = *reinterpret_cast<const uint32_t *>(&p1);
+                    *reinterpret_cast<uint2 *>(dst) = u;
                 }
             }
         }
