@@ -10,10 +10,13 @@
 // Weight bytes are read from HBM once (token tiles of one weight tile run side by
 // side and share it through L2).
 //
-// Roles (320 threads):  warp 0 lane 0   TMA producer (multi-stage ring)
-//                       warp 1          TMEM owner; lane 0 issues the MMAs
-//                       warps 2..9      epilogue, two warps per TMEM lane quarter,
-//                                       each taking half of the token columns
+// Roles (64 + 32 EW threads):  warp 0 lane 0   TMA producer (multi-stage ring)
+//                              warp 1          TMEM owner; lane 0 issues the MMAs
+//                              warps 2..EW+1   epilogue, EW / 4 warps per TMEM lane
+//                                              quarter, each taking a share of the token
+//                                              columns (EW = 8 at two CTAs per SM, 16 at
+//                                              one: the epilogue after a K split's main
+//                                              loop is a chain of dependent loads)
 // Without a K split the epilogue reads the accumulator straight from TMEM and the
 // CTA needs no shared memory beyond the ring, so two CTAs fit on an SM and one
 // CTA's epilogue overlaps the other's main loop.
@@ -28,8 +31,6 @@ namespace {
 
 constexpr int BM = 128;                // weight rows per tile (MMA M)
 constexpr int BK = 64;                 // K per stage: one 128-byte swizzled row of bf16
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
 constexpr int kWBytes = BM * BK * 2;   // 16 KB
 constexpr int kSmemLimit = 232448;     // 227 KB dynamic shared memory per CTA
 constexpr int kSmemPair = 113 * 1024;  // budget per CTA when two share an SM
@@ -73,10 +74,11 @@ __device__ __forceinline__ void epi_16(const Epi &epi, const typename Epi::Feat 
         if (c0 + j < ncols) epi(F, m0 + c0 + j, col_b[c0 + j], col_pos[c0 + j], v[j], pr[j]);
 }
 
-template <class Epi>
-__global__ void __launch_bounds__(kThreads, 2)
+template <class Epi, int EW>
+__global__ void __launch_bounds__(64 + 32 * EW, EW == 8 ? 2 : 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
               const Shape g, const Epi epi, unsigned *status) {
+    constexpr int NP = EW / 4;   // epilogue warps per TMEM lane quarter
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;   // 1024-byte aligned: required by the 128-byte swizzle
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // ---------------- epilogue warps (2..9): resolve every token column's (sequence,
         // position) while the main loop runs
         griddep_wait();
-        for (int c = threadIdx.x - 64; c < g.BN; c += kThreads - 64) {
+        for (int c = threadIdx.x - 64; c < g.BN; c += 32 * EW) {
             int b = 0, pos = -1;
             if constexpr (Epi::kColScale) {   // a per-column scale in the position slot
                 col_b[c] = 0;
@@ -209,15 +211,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             col_pos[c] = pos;
         }
         __syncwarp();
-        named_bar_sync(1, kEpiWarps * 32);
+        named_bar_sync(1, EW * 32);
         mbar_wait(done, 0, abort_flag, status);
         tc_fence_after();
         const int q = warp & 3;                  // TMEM lane quarter this warp may access
-        const int half = (warp - 2) >> 2;        // which half of the columns
+        const int part = (warp - 2) >> 2;        // which share of the columns
         const int f = q * 32 + lane;
         const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16);
         const int nchunk = (g.BN + 15) / 16;
-        const int ch0 = half == 0 ? 0 : (nchunk + 1) / 2, ch1 = half == 0 ? (nchunk + 1) / 2 : nchunk;
+        const int ch0 = part * nchunk / NP, ch1 = (part + 1) * nchunk / NP;
         if constexpr (Epi::kTileReduce) {
             // one softmax state per token column over this tile's 128 weight rows: a
             // butterfly over the 32 rows of each warp, then the 4 lane quarters in order
@@ -245,8 +247,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
             __syncwarp();
-            named_bar_sync(1, kEpiWarps * 32);
-            for (int c = threadIdx.x - 64; c < ncols; c += kEpiWarps * 32) {
+            named_bar_sync(1, EW * 32);
+            for (int c = threadIdx.x - 64; c < ncols; c += EW * 32) {
                 VocabState r = red[c];
 #pragma unroll
                 for (int qq = 1; qq < 4; ++qq) r = vocab_merge(r, red[qq * g.BN + c]);
@@ -282,14 +284,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         cluster_sync_all();
         if (warp >= 2) {   // ---------------- reduce the cluster's partials, epilogue on my share
             const int q = warp & 3;
-            const int half = (warp - 2) >> 2;
+            const int part = (warp - 2) >> 2;
             const int f = q * 32 + lane;
             const int per = (((g.BN + g.splits - 1) / g.splits) + 15) / 16 * 16;
             const int cb = split * per;
             const int ce = min(min(g.BN, cb + per), ncols);
-            const int hper = (((ce - cb) + 1) / 2 + 15) / 16 * 16;
-            const int c_begin = cb + half * hper;
-            const int c_end = half == 0 ? min(ce, cb + hper) : ce;
+            const int pper = (((ce - cb) + NP - 1) / NP + 15) / 16 * 16;   // 16-column aligned shares
+            const int c_begin = min(ce, cb + part * pper);
+            const int c_end = part == NP - 1 ? ce : min(ce, cb + (part + 1) * pper);
             const uint32_t part_s = smem_u32(smem) + (uint32_t)f * 4u;
             if (n0 + q * 32 < g.N_out) {
                 const typename Epi::Feat F = epi.feat(n0 + f);
@@ -558,16 +560,20 @@ cudaError_t launch_plan(const Plan &p, bool indep, const bf16 *W, int N_out, int
     const int w_stream = p.tok_tiles == 1 && (size_t)N_out * (size_t)K * 2 > (size_t)16 << 20 ? 1 : 0;
     Shape g{M_tok, N_out, K, p.BN, p.splits, p.stages, w_const ? 1 : 0, indep ? 1 : 0, p.body,
             p.xrows, p.base_aligned, p.col_bytes, w_stream};
-    auto kern = k_gemm_tc<Epi>;
-    static bool configured[64] = {};   // per device: raise the shared-memory limit once
+    // one CTA per SM (the shared memory of two exceeds an SM): 16 epilogue warps
+    const bool wide = !Epi::kTileReduce && p.smem > (size_t)kSmemPair;
+    auto kern = wide ? k_gemm_tc<Epi, 16> : k_gemm_tc<Epi, 8>;
+    static bool configured[64] = {};   // per device: raise the shared-memory limit once (both kernels)
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || !configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<Epi, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_gemm_tc<Epi, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
-    return launch_kernel(kern, dim3(p.tok_tiles, p.w_tiles, p.splits), dim3(kThreads), p.smem, st,
+    return launch_kernel(kern, dim3(p.tok_tiles, p.w_tiles, p.splits), dim3(64 + 32 * (wide ? 16 : 8)), p.smem, st,
                          indep ? 1 : p.splits, tmW, tmX, g, epi, status);
 }
 
