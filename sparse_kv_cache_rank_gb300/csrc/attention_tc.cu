@@ -15,8 +15,11 @@
 // thread-block cluster: each keeps its (O, m, l) in shared memory and the CTAs merge
 // disjoint row ranges through distributed shared memory (no workspace, no second launch).
 //
-// Roles (320 threads): warp 0 TMA, warp 1 TMEM owner + MMA issuer, warps 2..9 softmax:
-// two warps per TMEM lane quarter, thread = (query row, half of the key / head columns).
+// Roles (64 + 128 SG threads): warp 0 TMA, warp 1 TMEM owner + MMA issuer, the other warps
+// softmax: SG warps per TMEM lane quarter, thread = (query row, 1/SG of the key and head
+// columns).  The kernel takes the whole SM (one CTA).  With few key tiles per CTA (the
+// batch-1 steps) a tile's dependent chain sets the time and SG = 4 shortens it; with many
+// (long contexts, batches) SG = 2 exchanges less per tile and keeps the pipe busier.
 #include <cudaTypedefs.h>
 
 #include "internal.h"
@@ -29,8 +32,7 @@ namespace {
 
 constexpr int AQ = 128;          // query rows per CTA
 constexpr int AKV = 128;         // keys per tile
-constexpr int kThreads = 320;
-constexpr int kSoftThreads = 256;
+
 constexpr int kChunk = 128 * 128;   // one 64-column (128-byte) box of 128 rows: 16 KB
 
 struct AttnArgs {
@@ -53,15 +55,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <int HD>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int HD, int SG>
+__global__ void __launch_bounds__(64 + 128 * SG, 1)
     k_attention_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const AttnArgs a, unsigned *status) {
     constexpr int NCH = HD / 64;               // 64-column boxes per row of Q / K / V
     constexpr int QB = NCH * kChunk;           // bytes of the Q tile
     constexpr int KB = NCH * kChunk;           // bytes of one K (or V) tile
     constexpr int PB = 2 * kChunk;             // P tile: 128 rows x 128 keys bf16
-    constexpr int OH = HD / 2;                 // head-dim columns per thread
+    constexpr int kSoftThreads = 128 * SG;
+    constexpr int OH = HD / SG;                // head-dim columns per thread
+    constexpr int KC = AKV / SG;               // key columns per thread and tile
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;
@@ -69,9 +73,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sK = sQ + QB;                     // [2][KB]
     uint8_t *sV = sK + 2 * KB;                 // [2][KB]
     uint8_t *sP = sV + 2 * KB;                 // [PB]
-    float *xmax = reinterpret_cast<float *>(sP + PB);   // [2][128] partner exchange
-    float *xsum = xmax + 256;                            // [2][128]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(xsum + 256);
+    float *xmax = reinterpret_cast<float *>(sP + PB);   // [SG][128] exchange between a row's threads
+    float *xsum = xmax + 128 * SG;                       // [SG][128]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(xsum + 128 * SG);
     uint64_t *q_full = bars + 0;
     uint64_t *k_full = bars + 1;               // [2]
     uint64_t *v_full = bars + 3;               // [2]
@@ -102,9 +106,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t row0 = (size_t)b * a.k_max + q0;   // flattened row of query 0
     if (live <= 0) {   // no live query (the same in every slice of the cluster): zero outputs
         if (split == 0 && warp >= 2) {
-            const int r = (warp & 3) * 32 + lane, hf = (warp - 2) >> 2;
+            const int r = (warp & 3) * 32 + lane, qt = (warp - 2) >> 2;
             if (q0 + r < a.k_max) {
-                bf16 *dst = a.A + (row0 + r) * dq + (size_t)h * HD + hf * OH;
+                bf16 *dst = a.A + (row0 + r) * dq + (size_t)h * HD + qt * OH;
                 for (int e = 0; e < OH; ++e) dst[e] = __float2bfloat16_rn(0.f);
             }
         }
@@ -219,16 +223,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&v_empty[s]);
             }
         }
-    } else {   // ---------------- softmax warps: thread = (query row, half)
+    } else {   // ---------------- softmax warps: thread = (query row, quarter)
         const int q = warp & 3;
-        const int hf = (warp - 2) >> 2;              // key columns hf*64.., head dims hf*OH..
+        const int qt = (warp - 2) >> 2;              // key columns qt*KC.., head dims qt*OH..
         const int r = q * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
 #pragma unroll
         for (int e = 0; e < OH; ++e) o[e] = 0.f;
         float m_run = -INFINITY, l_run = 0.f;
         float corr_prev = 1.f;   // rescale factor of the PV product still in flight
-        uint8_t *prow = sP + hf * kChunk + (r >> 3) * 1024 + (r & 7) * 128;
+        // P row r, keys qt*KC..: 64-key chunk qt*KC / 64, first 16-byte unit (qt*KC % 64) / 8
+        uint8_t *prow = sP + (qt * KC / 64) * kChunk + (r >> 3) * 1024 + (r & 7) * 128;
+        const int u0 = (qt * KC % 64) / 8;
         // O <- O * corr + PV of the previous tile (its MMA overlapped this tile's softmax)
         auto fold_pv = [&](int tile) -> bool {
             if (!mbar_wait(pv_full, (uint32_t)tile & 1u, abort_flag, status)) return false;
@@ -236,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c0 = 0; c0 < OH; c0 += 16) {
                 float t[16];
-                tmem_ld_x16(tPV + lane_addr + (uint32_t)(hf * OH + c0), t);
+                tmem_ld_x16(tPV + lane_addr + (uint32_t)(qt * OH + c0), t);
                 tmem_ld_wait(t);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) o[c0 + j] = fmaf(o[c0 + j], corr_prev, t[j]);
@@ -249,33 +255,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ph = (uint32_t)(it >> 1) & 1u;
             if (!mbar_wait(&s_full[s], ph, abort_flag, status)) { ok = false; break; }
             tc_fence_after();
-            const int nvalid = a.N - (t0 + it) * AKV - hf * 64;   // keys of my half inside [0, N)
-            float v[64];
+            const int nvalid = a.N - (t0 + it) * AKV - qt * KC;   // keys of my quarter inside [0, N)
+            float v[KC];
 #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 16)
-                tmem_ld_x16(tS[s] + lane_addr + (uint32_t)(hf * 64 + c0), slice16(v + c0));
+            for (int c0 = 0; c0 < KC; c0 += 16)
+                tmem_ld_x16(tS[s] + lane_addr + (uint32_t)(qt * KC + c0), slice16(v + c0));
 #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld_wait(slice16(v + c0));
+            for (int c0 = 0; c0 < KC; c0 += 16) tmem_ld_wait(slice16(v + c0));
             tc_fence_before();
             mbar_arrive(&s_free[s]);                    // S buffer may be overwritten now
-            if (nvalid < 64) {   // keys past N (last tile only): out of the max and the sum
+            if (nvalid < KC) {   // keys past N (last tile only): out of the max and the sum
 #pragma unroll
-                for (int j = 0; j < 64; ++j)
+                for (int j = 0; j < KC; ++j)
                     if (j >= nvalid) v[j] = -INFINITY;
             }
             float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int j = 0; j < 64; ++j) mq[j & 3] = fmaxf(mq[j & 3], v[j]);
+            for (int j = 0; j < KC; ++j) mq[j & 3] = fmaxf(mq[j & 3], v[j]);
             float mt = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-            xmax[hf * 128 + r] = mt;
-            named_bar_sync(2 + q, 64);                 // the two warps of this lane quarter
-            mt = fmaxf(mt, xmax[(hf ^ 1) * 128 + r]);
+            xmax[qt * 128 + r] = mt;
+            named_bar_sync(2 + q, 32 * SG);            // the SG warps of this lane quarter
+#pragma unroll
+            for (int p = 0; p < SG; ++p) mt = fmaxf(mt, xmax[p * 128 + r]);
             const float m_new = fmaxf(m_run, mt * a.scale_log2);
             const float corr = ex2_approx(m_run - m_new);
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t pk[32];                           // P of this tile, bf16 pairs
+            uint32_t pk[KC / 2];                       // P of this tile, bf16 pairs
 #pragma unroll
-            for (int j = 0; j < 64; j += 2) {          // 2^(-inf) = 0 for the masked keys
+            for (int j = 0; j < KC; j += 2) {          // 2^(-inf) = 0 for the masked keys
                 const float p0 = ex2_approx(fmaf(v[j], a.scale_log2, -m_new));
                 const float p1 = ex2_approx(fmaf(v[j + 1], a.scale_log2, -m_new));
                 const __nv_bfloat162 pp = __floats2bfloat162_rn(p0, p1);
@@ -286,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the P buffer is free once the previous tile's PV product has completed
             if (it > 0 && !(ok = fold_pv(it - 1))) break;
 #pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 8) {
-                const int u = (c0 >> 3) ^ (r & 7);       // 16-byte unit in the swizzled row
+            for (int c0 = 0; c0 < KC; c0 += 8) {
+                const int u = (u0 + (c0 >> 3)) ^ (r & 7);   // 16-byte unit in the swizzled row
                 *reinterpret_cast<uint4 *>(prow + u * 16) =
                     make_uint4(pk[c0 / 2], pk[c0 / 2 + 1], pk[c0 / 2 + 2], pk[c0 / 2 + 3]);
             }
@@ -298,10 +305,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             corr_prev = corr;
         }
         if (ok && nt > 0) fold_pv(nt - 1);
-        // combine the two halves' row sums
-        xsum[hf * 128 + r] = l_run;
-        named_bar_sync(2 + q, 64);
-        const float l_tot = l_run + xsum[(hf ^ 1) * 128 + r];
+        // combine the row's quarter sums (the same order in every thread of the row)
+        xsum[qt * 128 + r] = l_run;
+        named_bar_sync(2 + q, 32 * SG);
+        float l_tot = 0.f;
+#pragma unroll
+        for (int p = 0; p < SG; ++p) l_tot += xsum[p * 128 + r];
         const bool row_ok = q0 + r < a.k_max;
         const size_t row = row0 + r;
         m_fin = (r < live && nt > 0) ? m_run : -INFINITY;
@@ -309,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (a.splits == 1) {
             if (row_ok) {
                 const float inv = (r < live && l_tot > 0.f) ? 1.0f / l_tot : 0.f;
-                bf16 *dst = a.A + row * dq + (size_t)h * HD + hf * OH;
+                bf16 *dst = a.A + row * dq + (size_t)h * HD + qt * OH;
                 // 16-byte stores (8 dims): the 32 lanes of a warp write 32 different rows
 #pragma unroll
                 for (int e = 0; e < OH; e += 8) {
@@ -341,13 +350,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *rML = rO + (size_t)S * per * HD;         // [S senders][per rows][m, l]
         cluster_sync_all();
         if (warp >= 2) {
-            const int q = warp & 3, hf = (warp - 2) >> 2, r = q * 32 + lane;
+            const int q = warp & 3, qt = (warp - 2) >> 2, r = q * 32 + lane;
             const int owner = r / per, lr = r - owner * per;
-            const uint32_t dO = mapa_shared(smem_u32(rO + ((size_t)(my * per + lr) * HD + hf * OH)), (uint32_t)owner);
+            const uint32_t dO = mapa_shared(smem_u32(rO + ((size_t)(my * per + lr) * HD + qt * OH)), (uint32_t)owner);
 #pragma unroll
             for (int e = 0; e < OH; e += 4)
                 st_dsmem_f32x4(dO + (uint32_t)(e * 4), make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]));
-            if (hf == 0) {
+            if (qt == 0) {
                 const uint32_t dM = mapa_shared(smem_u32(rML + (size_t)(my * per + lr) * 2), (uint32_t)owner);
                 st_dsmem_f32(dM, m_fin);
                 st_dsmem_f32(dM + 4, l_fin);
@@ -402,9 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int HD>
+template <int HD, int SG>
 size_t attn_smem() {
-    return 1024 + (size_t)(HD / 64) * kChunk * 5 + 2 * kChunk + 512 * 4 + 16 * 8 + 64;
+    return 1024 + (size_t)(HD / 64) * kChunk * 5 + 2 * kChunk + 2 * 128 * SG * 4 + 16 * 8 + 64;
 }
 
 }  // namespace
@@ -445,21 +454,32 @@ cudaError_t attention_tc(const bf16 *Q, const bf16 *Kc, const bf16 *Vc, bf16 *A,
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)hd);
     a.A = A;
     dim3 grid(a.q_tiles, n_q, B * a.splits);
-    static bool configured[2][64] = {};   // per head size and device: raise the smem limit once
+    // threads per query row: 4 when each CTA runs few key tiles (latency), else 2
+    const int tiles_per_cta = (a.kv_tiles + a.splits - 1) / a.splits;
+    const bool sg4 = tiles_per_cta <= 8;
+    static bool configured[64] = {};   // per device: raise the shared-memory limit once
     int dev = 0;
     cudaGetDevice(&dev);
-    const int hv = hd == 128 ? 1 : 0;
-    if (dev < 0 || dev >= 64 || !configured[hv][dev]) {
-        cudaError_t e = hv ? cudaFuncSetAttribute(k_attention_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem<128>())
-                           : cudaFuncSetAttribute(k_attention_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem<64>());
+    if (dev < 0 || dev >= 64 || !configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(k_attention_tc<128, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem<128, 2>());
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_attention_tc<128, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem<128, 4>());
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_attention_tc<64, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem<64, 2>());
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_attention_tc<64, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem<64, 4>());
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) configured[hv][dev] = true;
+        if (dev >= 0 && dev < 64) configured[dev] = true;
     }
-    if (hv)
-        return launch_kernel(k_attention_tc<128>, grid, dim3(kThreads), attn_smem<128>(), st, a.splits, tq, tk,
-                             tv, a, status);
-    return launch_kernel(k_attention_tc<64>, grid, dim3(kThreads), attn_smem<64>(), st, a.splits, tq, tk, tv,
-                         a, status);
+    if (hd == 128)
+        return sg4 ? launch_kernel(k_attention_tc<128, 4>, grid, dim3(64 + 128 * 4), attn_smem<128, 4>(), st, a.splits, tq,
+                                   tk, tv, a, status)
+                   : launch_kernel(k_attention_tc<128, 2>, grid, dim3(64 + 128 * 2), attn_smem<128, 2>(), st, a.splits, tq,
+                                   tk, tv, a, status);
+    return sg4 ? launch_kernel(k_attention_tc<64, 4>, grid, dim3(64 + 128 * 4), attn_smem<64, 4>(), st, a.splits, tq, tk,
+                               tv, a, status)
+               : launch_kernel(k_attention_tc<64, 2>, grid, dim3(64 + 128 * 2), attn_smem<64, 2>(), st, a.splits, tq, tk,
+                               tv, a, status);
 }
 
 }  // namespace dllm

@@ -372,6 +372,8 @@ def test_refresh_long_context_batch4_half(B, orc):
 # --------------------------------------------------------------------------- attention alone
 @pytest.mark.parametrize("Bq,N,k_max,n_q,n_kv,hd,live", [
     (1, 1024, 164, 32, 32, 128, 164), (2, 333, 150, 4, 2, 64, 150), (1, 2048, 328, 28, 4, 128, 300),
+    # 64-dim heads over 16 key tiles per CTA (two softmax threads per row)
+    (4, 2048, 256, 16, 8, 64, 250),
     (3, 200, 37, 8, 8, 128, 37), (1, 129, 129, 2, 1, 64, 100),
     # one key slice per CTA (the grid alone fills the GPU), a ragged second query tile
     (8, 256, 200, 28, 4, 128, 200), (16, 150, 140, 16, 16, 64, 140)])
