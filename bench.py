@@ -42,7 +42,7 @@ METRIC = "sparse-refresh denoise steps/s & tokens/s (LLaDA-8B shape); % of roofl
 # dram__bytes_read.sum + dram__bytes_write.sum per launch, LLaDA-8B layer at k = 164
 # (profiles/layer_step_llada8b_full.md); to be re-taken whenever these kernels change
 NCU_TRAFFIC_BYTES = {"gateup": 206.12e6, "qkv": 106.21e6, "down": 110.58e6, "oproj": 36.32e6,
-                     "attention": 18.17e6, "proxy_gemm": 9.47e6, "cosine": 4.74e6, "select": 1.49e6}
+                     "attention": 18.17e6}
 UNIT = "steps/s"
 DATA = "synthetic (seeded random-init weights N(0,0.02), drift model: 10% rows +N(0,0.5), all +N(0,0.05))"
 
@@ -142,10 +142,19 @@ class Clocks:
 
 
 # --------------------------------------------------------------------------- work model
+def _proxy_slices(rows, r, d):
+    """K slices of the proxy projection's plan on this device (host-only plan query)."""
+    import torch
+    from sparse_kv_cache_rank_gb300 import binding as B
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 152
+    return B.dllm_gemm_plan(rows, r, d, sms=sms, slices=1)["splits"]
+
+
 def layer_kernel_work(sh, M):
     """Algorithmic bytes and FLOPs of each kernel of one layer step with M refreshed rows
     (weights and caches counted once, bf16 = 2 bytes, fp32 = 4).  Up to N = 4096 the
-    selection and the gather of the selected rows are one kernel ("select")."""
+    selection and the gather of the selected rows are one kernel ("select"); with bf16,
+    r <= 128 and no K split the proxy projection computes the drift itself ("proxy_gemm")."""
     B, N, d, r, F = sh.B, sh.N, sh.d, sh.r, sh.F
     dq, dkv = sh.d_q, sh.d_kv
     fold = sh.dtype == "bf16" and M <= 256   # the refresh folds the second RMSNorm up to 256 rows
@@ -153,9 +162,15 @@ def layer_kernel_work(sh, M):
     gat = (2 * M * d * 2 + 8 * M * r, 0)
     if N <= 4096:
         sel, gat = (sel[0] + gat[0], 0), None
+    # bf16 with r <= 128 and no K split (the token tiles fill the GPU): the projection's
+    # epilogue computes the drift (reads the cached proxies, writes the new ones and the
+    # drift); no separate cosine kernel
+    fused = sh.dtype == "bf16" and r <= 128 and r % 32 == 0 and d % 64 == 0 and \
+        _proxy_slices(B * N, r, d) == 1
     work = {
-        "proxy_gemm": (2 * B * N * d + 2 * r * d + 4 * B * N * r, 2 * B * N * d * r),
-        "cosine": (8 * B * N * r + 4 * B * N, 0),
+        "proxy_gemm": (2 * B * N * d + 2 * r * d + 4 * B * N * r + ((4 * B * N * r + 4 * B * N) if fused else 0),
+                       2 * B * N * d * r),
+        "cosine": None if fused else (8 * B * N * r + 4 * B * N, 0),
         "select": sel,
         "gather": gat,
         "qkv": (2 * (dq + 2 * dkv) * d + 2 * M * d + 2 * M * (dq + 2 * dkv), 2 * M * d * (dq + 2 * dkv)),

@@ -100,9 +100,11 @@ int dllm_check_wait_timeout(int32_t *gave_up, void *stream);
  *   proxy_cur   [B, N, r]  fp32 out
  *   drift       [B, N]     fp32 out
  * Requirements: r % 32 == 0, r <= 1024; d % 64 == 0 for DLLM_BF16.
- * Workspace: dllm_proxy_workspace_bytes() (fp32 partial proxies of independent K slices,
- * summed in a fixed order, so identical inputs always give identical proxies); 0 bytes
- * when the shape needs no K split.
+ * Workspace: dllm_proxy_workspace_bytes() bytes (fp32 partial proxies of independent K
+ * slices, summed in a fixed order by a second kernel that computes the drift), 0 when
+ * the shape needs no K split.  Without a split (bf16, r <= 128, the token tiles alone fill
+ * the GPU) one launch computes the proxies and, in its epilogue, their drift.  Either way
+ * identical inputs always give identical results.
  * ------------------------------------------------------------------------- */
 size_t dllm_proxy_workspace_bytes(int B, int N, int d, int r, int dtype);
 
@@ -457,15 +459,17 @@ int dllm_gather_rows(const void *src, const int32_t *idx, const int32_t *count, 
 int dllm_gemm_bf16(const void *X, const void *W, float *out, int M, int N_out, int K, int splits,
                    void *stream);
 
-/* The launch plan dllm_gemm_bf16 (slices = 0) or the proxy projection's independent K
- * slices (slices = 1) would use for this shape on a device with `sms` SMs.  Host only:
+/* The launch plan dllm_gemm_bf16 (slices = 0), the proxy projection's independent K
+ * slices (slices = 1) or the proxy projection with its drift in the epilogue (slices = 2,
+ * N_out = r <= 128; dllm_proxy_score takes it when the slice plan has no K split) would
+ * use for this shape on a device with `sms` SMs.  Host only:
  * no device is queried and nothing is launched, so it answers without a GPU (the
  * library's own launches pass the current device's SM count).  info [8] receives
  *   { token-tile width BN, K split, pipeline stages, token tiles, weight tiles of 128
  *     rows, token rows staged per K block, dynamic shared memory bytes, CTAs per SM }.
  * splits as for dllm_gemm_bf16 (0 = chosen from the shape).  Errors: INVALID_ARG for a
- * null info, sizes <= 0, sms outside [1, 1024] or splits outside [0, 8]; UNSUPPORTED
- * when K % 64 or N_out % 32 is not 0. */
+ * null info, sizes <= 0, sms outside [1, 1024], splits outside [0, 8], slices outside
+ * [0, 2] or slices = 2 with N_out > 128; UNSUPPORTED when K % 64 or N_out % 32 is not 0. */
 int dllm_gemm_plan(int M, int N_out, int K, int splits, int sms, int slices, int32_t *info);
 
 /* ---------------------------------------------------------------------------

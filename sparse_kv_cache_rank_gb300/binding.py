@@ -531,11 +531,12 @@ def dllm_gemm_bf16(X, W, out=None, splits: int = 0):
 PLAN_FIELDS = ("BN", "splits", "stages", "tok_tiles", "w_tiles", "xrows", "smem", "ctas_per_sm")
 
 
-def dllm_gemm_plan(M: int, N_out: int, K: int, splits: int = 0, sms: int = 152, slices: bool = False):
+def dllm_gemm_plan(M: int, N_out: int, K: int, splits: int = 0, sms: int = 152, slices: int = 0):
     """The tensor-core GEMM's launch plan for this shape on `sms` SMs (host only, no GPU
-    needed) -> dict of PLAN_FIELDS."""
+    needed) -> dict of PLAN_FIELDS.  slices: 0 the plain GEMM, 1 the proxy projection's
+    independent K slices, 2 the proxy projection with its drift in the epilogue."""
     info = (C.c_int32 * 8)()
-    _check(lib().dllm_gemm_plan(int(M), int(N_out), int(K), int(splits), int(sms), 1 if slices else 0, info),
+    _check(lib().dllm_gemm_plan(int(M), int(N_out), int(K), int(splits), int(sms), int(slices), info),
            "dllm_gemm_plan")
     return dict(zip(PLAN_FIELDS, list(info)))
 

@@ -228,6 +228,13 @@ DLLM_EXPORT int dllm_check_wait_timeout(int32_t *gave_up, void *stream) {
 
 // ------------------------------------------------------------------ proxy score
 namespace {
+// bf16 with r <= 128 and no K split (the token tiles fill the GPU): the projection
+// computes the drift in its epilogue.  Otherwise independent K slices write fp32 partials
+// (or one slice its proxies) that the cosine kernel sums in order.
+bool proxy_fused(int B, int N, int d, int r, int dtype) {
+    return dtype == DLLM_BF16 && gemm_tc_cosine_ok(B * N, r, d);
+}
+
 int proxy_slices(int B, int N, int d, int r, int dtype) {
     if (dtype != DLLM_BF16 || B <= 0 || N <= 0 || d % 64 || r % 32) return 1;
     return gemm_tc_slices_count(B * N, r, d);
@@ -261,8 +268,15 @@ DLLM_EXPORT int dllm_proxy_score(const void *H, const void *Pt, const float *pro
             return fail(DLLM_ERR_WORKSPACE, "workspace holds %zu bytes, %zu needed", ws_bytes, need);
         parts = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255));
     }
+    if (dtype == DLLM_BF16 && d % 64) return fail(DLLM_ERR_UNSUPPORTED, "bf16 path needs d % 64 == 0 (got %d)", d);
+    if (proxy_fused(B, N, d, r, dtype)) {
+        Launch t(DLLM_KERNEL_PROXY_GEMM, st);
+        CHECK_CUDA(gemm_tc_cosine(static_cast<const bf16 *>(Pt), r, d, static_cast<const bf16 *>(H), rows,
+                                  proxy_cur, proxy_cache, drift, true, status_ptr(), st),
+                   "proxy projection launch");
+        return DLLM_OK;
+    }
     if (dtype == DLLM_BF16) {
-        if (d % 64) return fail(DLLM_ERR_UNSUPPORTED, "bf16 path needs d % 64 == 0 (got %d)", d);
         Launch t(DLLM_KERNEL_PROXY_GEMM, st);
         e = gemm_tc_slices(static_cast<const bf16 *>(Pt), r, d, static_cast<const bf16 *>(H), rows, parts,
                            true, status_ptr(), st);
@@ -783,7 +797,8 @@ DLLM_EXPORT int dllm_gemm_plan(int M, int N_out, int K, int splits, int sms, int
     CHECK_ARG(splits >= 0 && splits <= 8, "splits must be in [0, 8]");
     if (K % 64 || N_out % 32) return fail(DLLM_ERR_UNSUPPORTED, "needs K %% 64 == 0 and N_out %% 32 == 0");
     int v[8];
-    if (gemm_tc_plan_info(M, N_out, K, splits, sms, slices != 0, v) != 0)
+    CHECK_ARG(slices >= 0 && slices <= 2, "slices must be 0, 1 or 2 (got %d)", slices);
+    if (gemm_tc_plan_info(M, N_out, K, splits, sms, slices, v) != 0)
         return fail(DLLM_ERR_INVALID_ARG, "shape rejected by the planner");
     for (int i = 0; i < 8; ++i) info[i] = v[i];
     return DLLM_OK;

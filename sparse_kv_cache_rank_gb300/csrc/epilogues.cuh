@@ -62,6 +62,29 @@ struct EpiStoreF32 {
     }
 };
 
+// Singular proxy with its cosine drift (SPA-Cache, "1. Update identification via singular
+// proxy"): cur[m, :] = acc over the proxy's r <= 128 features (one weight tile) and
+// drift[m] = 1 - cos(cur[m], cached[m]), computed as 0.5 |cur/|cur| - cached/|cached||^2
+// (exactly 0 for identical proxies), 0 when both are zero, 1 when exactly one is, clamped
+// to [0, 2].  The drift needs every feature of a token: the GEMM hands this epilogue whole
+// 16-column chunks (kCosine) and reduces over the 128 TMEM lanes itself, so the operator
+// below is never called.
+struct EpiCosine {
+    static constexpr bool kSel = false;
+    static constexpr bool kTileReduce = false;
+    static constexpr bool kColScale = false;
+    static constexpr bool kCosine = true;
+    using Feat = FeatRow;
+    SelRows sel;
+    float *cur;            // [rows, r]
+    const float *cached;   // [rows, r]
+    float *drift;          // [rows]
+    int r;
+    __device__ __forceinline__ Feat feat(int f) const { return {f}; }
+    __device__ __forceinline__ float2 pre(const Feat &, int, int, int) const { return {0.f, 0.f}; }
+    __device__ __forceinline__ void operator()(const Feat &, int, int, int, float, float2) const {}
+};
+
 // [Q | K | V] rows -> rotary embedding at the token's position; Q to the compact
 // query buffer, K and V scattered into the cache rows.  rope_cs [M, hd/2] holds
 // (cos, sin) of pos * theta^(-2i/hd) for every selected row (written by the gather).

@@ -23,6 +23,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "internal.h"
 
@@ -74,11 +75,121 @@ __device__ __forceinline__ void epi_16(const Epi &epi, const typename Epi::Feat 
         if (c0 + j < ncols) epi(F, m0 + c0 + j, col_b[c0 + j], col_pos[c0 + j], v[j], pr[j]);
 }
 
+// Epilogues that reduce over the tile's features (EpiCosine) declare kCosine = true.
+template <class E, class = void>
+struct epi_cosine : std::false_type {};
+template <class E>
+struct epi_cosine<E, std::void_t<decltype(E::kCosine)>> : std::integral_constant<bool, E::kCosine> {};
+
+// Scratch of the feature reduction per share of columns: [4 quarters][32] squared norms,
+// then [4 quarters][16] squared differences.
+constexpr int kCosRed = 4 * 32 + 4 * 16;
+
+// Warp reduce-scatter of 2W values: afterwards v[0] of lane l holds the warp's sum of
+// value (l & (2W - 1)) (rounds over lane bits log2(W) .. 0; lanes that differ only above
+// them hold the same sums when every lane starts with the same set).
+template <int W>
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[2 * W], int lane) {
+#pragma unroll
+    for (int w = W; w >= 1; w >>= 1) {
+        const bool up = (lane & w) != 0;
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+            const float send = up ? v[i] : v[i + w];
+            const float keep = up ? v[i + w] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+    }
+}
+
+// Barrier of the four warps of column share `part` (ids 2..5, immediates so that the
+// kernel reserves only the barriers it names).
+__device__ __forceinline__ void share_bar(int part) {
+    __syncwarp();
+    switch (part) {
+        case 0: asm volatile("bar.sync 2, 128;" ::: "memory"); break;
+        case 1: asm volatile("bar.sync 3, 128;" ::: "memory"); break;
+        case 2: asm volatile("bar.sync 4, 128;" ::: "memory"); break;
+        default: asm volatile("bar.sync 5, 128;" ::: "memory"); break;
+    }
+}
+
+// Cosine drift of token columns c0 .. c0+15 (live below cend) of a tile whose thread holds
+// feature f = 32 q + lane of each column in acc[].  The four warps of one share of the
+// columns (one per TMEM lane quarter) call this together.
+template <class Epi>
+__device__ __forceinline__ void cosine_16(const Epi &epi, int f, int q, int lane, int m0, int c0, int cend,
+                                          const float (&acc)[16], float *red, int part) {
+    const bool fv = f < epi.r;
+    float a[16], cv[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const bool live = fv && c0 + j < cend;
+        const size_t o = (size_t)(m0 + c0 + j) * (size_t)epi.r + (size_t)f;
+        a[j] = live ? acc[j] : 0.f;
+        cv[j] = live ? __ldcg(epi.cached + o) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        if (fv && c0 + j < cend) epi.cur[(size_t)(m0 + c0 + j) * (size_t)epi.r + (size_t)f] = a[j];
+    // squared norms: lane l of quarter q ends with column (l & 15)'s sum over the
+    // quarter's 32 features, of the current proxy (l < 16) or the cached one
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        v[j] = a[j] * a[j];
+        v[16 + j] = cv[j] * cv[j];
+    }
+    warp_reduce_scatter<16>(v, lane);
+    red[q * 32 + lane] = v[0];
+    share_bar(part);
+    float na[16], nc[16], t[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        na[j] = ((red[j] + red[32 + j]) + red[64 + j]) + red[96 + j];
+        nc[j] = ((red[16 + j] + red[48 + j]) + red[80 + j]) + red[112 + j];
+        float d = 0.f;
+        if (na[j] != 0.f && nc[j] != 0.f) {
+            const float ia = 1.0f / sqrtf(na[j]), ic = 1.0f / sqrtf(nc[j]);
+            // separately rounded products (no FMA contraction): equal inputs give d == 0
+            d = __fsub_rn(__fmul_rn(a[j], ia), __fmul_rn(cv[j], ic));
+        }
+        t[j] = d * d;
+    }
+    // the squared differences: both lane halves hold the same 16 sums after the
+    // exchange across lane bit 4, then lane l holds column (l & 15)'s quarter sum
+#pragma unroll
+    for (int j = 0; j < 16; ++j) t[j] += __shfl_xor_sync(0xffffffffu, t[j], 16);
+    warp_reduce_scatter<8>(t, lane);
+    if (lane < 16) red[128 + q * 16 + lane] = t[0];
+    share_bar(part);
+    if (q == 0 && lane < 16 && c0 + lane < cend) {
+        float n_a = 0.f, n_c = 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (j == lane) {
+                n_a = na[j];
+                n_c = nc[j];
+            }
+        float out;
+        if (n_a == 0.f && n_c == 0.f) {
+            out = 0.f;
+        } else if (n_a == 0.f || n_c == 0.f) {
+            out = 1.f;
+        } else {
+            const float sd = ((red[128 + lane] + red[144 + lane]) + red[160 + lane]) + red[176 + lane];
+            out = fminf(fmaxf(0.5f * sd, 0.f), 2.f);
+        }
+        epi.drift[m0 + c0 + lane] = out;
+    }
+}
+
 template <class Epi, int EW>
 __global__ void __launch_bounds__(64 + 32 * EW, EW == 8 ? 2 : 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
               const Shape g, const Epi epi, unsigned *status) {
     constexpr int NP = EW / 4;   // epilogue warps per TMEM lane quarter
+    constexpr bool kCos = epi_cosine<Epi>::value;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
     uint8_t *smem = smem_raw + pad;   // 1024-byte aligned: required by the 128-byte swizzle
@@ -199,7 +310,7 @@ __global__ void __launch_bounds__(64 + 32 * EW, EW == 8 ? 2 : 1)
         // ---------------- epilogue warps (2..9): resolve every token column's (sequence,
         // position) while the main loop runs
         griddep_wait();
-        for (int c = threadIdx.x - 64; c < g.BN; c += 32 * EW) {
+        for (int c = threadIdx.x - 64; c < (kCos ? 0 : g.BN); c += 32 * EW) {
             int b = 0, pos = -1;
             if constexpr (Epi::kColScale) {   // a per-column scale in the position slot
                 col_b[c] = 0;
@@ -253,6 +364,17 @@ __global__ void __launch_bounds__(64 + 32 * EW, EW == 8 ? 2 : 1)
 #pragma unroll
                 for (int qq = 1; qq < 4; ++qq) r = vocab_merge(r, red[qq * g.BN + c]);
                 epi.part[(size_t)(m0 + c) * epi.tiles + wt] = r;
+            }
+        } else if (kCos) {
+            // the drift of each token column straight from TMEM (no K split: the planner
+            // gives EpiCosine one CTA per token tile; the scratch follows the ring, in the
+            // per-column area this epilogue does not use)
+            float *red = reinterpret_cast<float *>(smem + g.body_bytes) + part * kCosRed;
+            for (int ch = ch0; ch < ch1 && ch * 16 < ncols; ++ch) {
+                float v[16];
+                tmem_ld_x16(taddr + (uint32_t)(ch * 16), v);
+                tmem_ld_wait(v);
+                if constexpr (kCos) cosine_16(epi, f, q, lane, m0, ch * 16, ncols, v, red, part);
             }
         } else if (!cluster_split) {
             // straight from TMEM (independent K slices write rows split * M_tok + m)
@@ -402,7 +524,8 @@ struct Plan {
 
 int round16(int x) { return (x + 15) / 16 * 16; }
 
-Plan make_plan(int M_tok, int N_out, int K, int BN, int splits, int budget, bool smem_partial) {
+Plan make_plan(int M_tok, int N_out, int K, int BN, int splits, int budget, bool smem_partial,
+               int min_col_bytes = 0) {
     Plan p{};
     p.BN = BN;
     p.splits = splits;
@@ -414,6 +537,7 @@ Plan make_plan(int M_tok, int N_out, int K, int BN, int splits, int budget, bool
     const int sb = stage_bytes(p.xrows);
     const int over = (BN - p.xrows) * BK * 2;   // read by the MMA past the last stage
     p.col_bytes = 8 * BN > over ? 8 * BN : over;
+    if (p.col_bytes < min_col_bytes) p.col_bytes = min_col_bytes;
     const int tail = p.col_bytes + kTailBytes;
     const int part = smem_partial ? BN * BM * 4 : 0;
     const int KB = K / BK;
@@ -425,9 +549,10 @@ Plan make_plan(int M_tok, int N_out, int K, int BN, int splits, int budget, bool
     };
     p.stages = fit(1024);
     p.base_aligned = 0;
-    // one stage more when only the 1 KB alignment slack stands in the way (not in a
-    // cluster: a CTA that finds its base misaligned returns alone)
-    if (!smem_partial && splits == 1 && fit(0) > p.stages) {
+    // one stage more when only the 1 KB alignment slack stands in the way.  The offset of
+    // dynamic shared memory is the same in every CTA of a launch, so a misaligned base
+    // sends every CTA of a cluster back before its first cluster barrier, together.
+    if (fit(0) > p.stages) {
         p.stages = fit(0);
         p.base_aligned = 1;
     }
@@ -536,7 +661,9 @@ Plan plan_gemm(int M_tok, int N_out, int K, int splits_req, int sms) {
 }
 
 // Independent K slices (no cluster), each writing its own fp32 partial output: token
-// tiles of 64 rows (128 beyond 2048 tokens), slices sized to two CTAs per SM.
+// tiles of 64 rows (128 beyond 2048 tokens), slices sized to two CTAs per SM.  (At 1024
+// tokens the 128 CTAs fit one per SM; giving each the whole SM's shared memory, so that
+// all 8 K blocks of a slice are in flight, measured 1 us slower: 10.8 against 9.9 us.)
 Plan plan_slices(int M_tok, int N_out, int K, int sms) {
     const int KB = K / BK;
     const int BN = M_tok <= 256 ? round16(M_tok) : (M_tok <= 2048 ? 64 : 128);
@@ -545,6 +672,18 @@ Plan plan_slices(int M_tok, int N_out, int K, int sms) {
     s = s < 1 ? 1 : (s > 8 ? 8 : s);
     while (s > 1 && KB / s < 2) --s;
     return make_plan(M_tok, N_out, K, BN, s, kSmemPair, false);
+}
+
+// The proxy projection with its cosine drift in the epilogue (r <= 128: one weight tile
+// holds every feature of a token), for the shapes whose slice plan needs no K split (the
+// token tiles alone give every SM two CTAs, or K is too short to split): the tiles of
+// plan_slices, one CTA each.  The per-column area after the ring holds the epilogue's
+// feature-reduction scratch.  (Split shapes keep the slices and the cosine kernel: a K
+// split reduced inside 8-CTA clusters measured 24.5 us against 9.9 + 4.3 us at 1024
+// tokens, because no more than 15 such clusters fit on the GPU at once.)
+Plan plan_cosine(int M_tok, int N_out, int K, int sms) {
+    const Plan ps = plan_slices(M_tok, N_out, K, sms);
+    return make_plan(M_tok, N_out, K, ps.BN, 1, kSmemPair, false, 4 * kCosRed * 4);
 }
 
 template <class Epi>
@@ -593,9 +732,12 @@ int gemm_tc_slices_count(int M_tok, int N_out, int K) {
     return plan_slices(M_tok, N_out, K, num_sms()).splits;
 }
 
-int gemm_tc_plan_info(int M_tok, int N_out, int K, int splits_req, int sms, bool slices, int *info) {
+int gemm_tc_plan_info(int M_tok, int N_out, int K, int splits_req, int sms, int kind, int *info) {
     if (M_tok <= 0 || N_out <= 0 || K <= 0 || K % BK != 0 || N_out % 32 != 0 || sms <= 0) return -1;
-    const Plan p = slices ? plan_slices(M_tok, N_out, K, sms) : plan_gemm(M_tok, N_out, K, splits_req, sms);
+    if (kind == 2 && N_out > BM) return -1;
+    const Plan p = kind == 1   ? plan_slices(M_tok, N_out, K, sms)
+                   : kind == 2 ? plan_cosine(M_tok, N_out, K, sms)
+                               : plan_gemm(M_tok, N_out, K, splits_req, sms);
     info[0] = p.BN;
     info[1] = p.splits;
     info[2] = p.stages;
@@ -614,6 +756,20 @@ cudaError_t gemm_tc_slices(const bf16 *W, int N_out, int K, const bf16 *X, int M
     const Plan p = plan_slices(M_tok, N_out, K, num_sms());
     EpiStoreF32 epi{SelRows{}, parts, N_out, N_out};
     return launch_plan(p, true, W, N_out, K, X, M_tok, epi, w_const, status, st);
+}
+
+bool gemm_tc_cosine_ok(int M_tok, int N_out, int K) {
+    return M_tok > 0 && N_out > 0 && N_out <= BM && N_out % 32 == 0 && K % BK == 0 &&
+           plan_slices(M_tok, N_out, K, num_sms()).splits == 1;
+}
+
+cudaError_t gemm_tc_cosine(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, float *cur,
+                           const float *cached, float *drift, bool w_const, unsigned *status, cudaStream_t st) {
+    if (M_tok <= 0) return cudaSuccess;
+    if (!gemm_tc_cosine_ok(M_tok, N_out, K)) return cudaErrorInvalidValue;
+    const Plan p = plan_cosine(M_tok, N_out, K, num_sms());
+    EpiCosine epi{SelRows{}, cur, cached, drift, N_out};
+    return launch_plan(p, false, W, N_out, K, X, M_tok, epi, w_const, status, st);
 }
 
 template cudaError_t gemm_tc<EpiStoreF32>(const bf16 *, int, int, const bf16 *, int,

@@ -59,11 +59,18 @@ cudaError_t gemm_tc(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, c
 int gemm_tc_slices_count(int M_tok, int N_out, int K);
 // The plan the tensor-core GEMM would launch for this shape on `sms` SMs, computed on the
 // host only (no device query): info = {BN, splits, stages, token tiles, weight tiles,
-// staged token rows, shared-memory bytes, CTAs per SM}.  slices: the independent-K-slice
-// plan of gemm_tc_slices instead.  Returns -1 for a shape the GEMM rejects.
-int gemm_tc_plan_info(int M_tok, int N_out, int K, int splits_req, int sms, bool slices, int *info);
+// staged token rows, shared-memory bytes, CTAs per SM}.  kind 0: gemm_tc; 1: the
+// independent-K-slice plan of gemm_tc_slices; 2: the plan of gemm_tc_cosine.  Returns -1
+// for a shape the GEMM rejects.
+int gemm_tc_plan_info(int M_tok, int N_out, int K, int splits_req, int sms, int kind, int *info);
 cudaError_t gemm_tc_slices(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, float *parts,
                            bool w_const, unsigned *status, cudaStream_t st);
+// The singular proxy with its cosine drift in one launch (EpiCosine): cur [M_tok, N_out] =
+// X W^T and drift [M_tok] against cached [M_tok, N_out]; needs N_out <= 128, N_out % 32 == 0,
+// K % 64 == 0 and a shape whose slice plan has no K split (gemm_tc_cosine_ok).  No workspace.
+bool gemm_tc_cosine_ok(int M_tok, int N_out, int K);
+cudaError_t gemm_tc_cosine(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, float *cur,
+                           const float *cached, float *drift, bool w_const, unsigned *status, cudaStream_t st);
 
 // CUDA cores (fp32 FMA): any K.
 template <class Epi>

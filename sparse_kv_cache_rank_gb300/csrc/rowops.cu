@@ -73,30 +73,36 @@ __global__ void __launch_bounds__(256) k_cosine_drift(const float *__restrict__ 
     if (row >= rows) return;
     float *a = cur + row * r;
     const float *c = cached + row * r;
-    // float4 chunks (r % 32 == 0); for each chunk every partial load is issued before
-    // the first add, and the adds run in slice order
+    // float4 chunks (r % 32 == 0, r <= 1024: at most 8 per lane), held in registers for
+    // both passes; for each chunk every partial load is issued before the first add, and
+    // the adds run in slice order
     const int nch = r >> 2;
     const size_t stride4 = (size_t)rows * nch;
     const float4 *p4 = reinterpret_cast<const float4 *>(parts) + (size_t)row * nch;
     float4 *a4 = reinterpret_cast<float4 *>(a);
     const float4 *c4 = reinterpret_cast<const float4 *>(c);
+    constexpr int kMaxCh = 8;
+    float4 xs[kMaxCh], cs[kMaxCh];
     float na = 0.f, nc = 0.f;
-    for (int ch = lane; ch < nch; ch += 32) {
+#pragma unroll
+    for (int u = 0; u < kMaxCh; ++u) {
+        const int ch = lane + 32 * u;
+        if (ch >= nch) break;
         float4 x;
         const float4 cc = c4[ch];
         if (nparts > 1) {
             float4 t[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (u < nparts) t[u] = __ldcg(p4 + (size_t)u * stride4 + ch);
+            for (int z = 0; z < 8; ++z)
+                if (z < nparts) t[z] = __ldcg(p4 + (size_t)z * stride4 + ch);
             x = t[0];
 #pragma unroll
-            for (int u = 1; u < 8; ++u)
-                if (u < nparts) {
-                    x.x += t[u].x;
-                    x.y += t[u].y;
-                    x.z += t[u].z;
-                    x.w += t[u].w;
+            for (int z = 1; z < 8; ++z)
+                if (z < nparts) {
+                    x.x += t[z].x;
+                    x.y += t[z].y;
+                    x.z += t[z].z;
+                    x.w += t[z].w;
                 }
             for (int z = 8; z < nparts; ++z) {
                 const float4 y = __ldcg(p4 + (size_t)z * stride4 + ch);
@@ -109,6 +115,8 @@ __global__ void __launch_bounds__(256) k_cosine_drift(const float *__restrict__ 
         } else {
             x = a4[ch];
         }
+        xs[u] = x;
+        cs[u] = cc;
         na = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, na))));
         nc = fmaf(cc.x, cc.x, fmaf(cc.y, cc.y, fmaf(cc.z, cc.z, fmaf(cc.w, cc.w, nc))));
     }
@@ -125,8 +133,10 @@ __global__ void __launch_bounds__(256) k_cosine_drift(const float *__restrict__ 
     } else {
         const float ia = 1.0f / sqrtf(na), ic = 1.0f / sqrtf(nc);
         float s = 0.f;
-        for (int ch = lane; ch < nch; ch += 32) {   // the chunks this lane summed above
-            const float4 x = a4[ch], cc = c4[ch];
+#pragma unroll
+        for (int u = 0; u < kMaxCh; ++u) {   // the chunks this lane summed above
+            if (lane + 32 * u >= nch) break;
+            const float4 x = xs[u], cc = cs[u];
             // separately rounded products (no FMA contraction): equal inputs give t == 0
             const float t0 = __fsub_rn(__fmul_rn(x.x, ia), __fmul_rn(cc.x, ic));
             const float t1 = __fsub_rn(__fmul_rn(x.y, ia), __fmul_rn(cc.y, ic));

@@ -3,10 +3,12 @@
 // allocation"; EntropyCache, "How EntropyCache works", step 3), as a block-level device
 // function shared by the selection kernel and the fused selection + gather kernel.
 //
-// The k-th largest drift is found exactly by a 4-pass radix select on order-preserving
-// 32-bit keys (256-bin shared histograms); rows above it are taken, rows equal to it are
-// taken in index order until the budget is met (lower row index wins ties), and the
-// union with the forced rows is compacted in ascending order by a block-wide scan.
+// The k-th largest drift is found exactly by a radix select on order-preserving 32-bit
+// keys (up to 4 passes of 256-bin shared histograms); rows above it are taken, rows equal
+// to it are taken in index order until the budget is met (lower row index wins ties), and
+// the union with the forced rows is compacted in ascending order by a block-wide scan.
+// The passes stop early once the digit holding the k-th key is taken whole: every key
+// from that digit's lower bound up is then selected and no tie needs ranking.
 #pragma once
 
 #include "internal.h"
@@ -53,7 +55,7 @@ __device__ uint32_t select_sequence(const float *__restrict__ dr, const int32_t 
                                     int k, float min_drift, int N, uint32_t *key, uint8_t *flag, int32_t *out) {
     __shared__ uint32_t hist[256];
     __shared__ uint32_t wsum[33];
-    __shared__ uint32_t sh_prefix, sh_rem;
+    __shared__ uint32_t sh_prefix, sh_rem, sh_whole;
     const int tid = threadIdx.x;
     for (int i = tid; i < N; i += kT) flag[i] = 0;
     __syncthreads();
@@ -98,8 +100,9 @@ __device__ uint32_t select_sequence(const float *__restrict__ dr, const int32_t 
         rem = 0;
     } else {
         uint32_t prefix = 0, mask = 0;
+        bool whole = false;
         rem = take;
-        for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int shift = 24; shift >= 0 && !whole; shift -= 8) {
             for (int i = tid; i < 256; i += kT) hist[i] = 0;
             __syncthreads();
             // warp-aggregated counts: most keys share their leading digits, so one
@@ -137,6 +140,7 @@ __device__ uint32_t select_sequence(const float *__restrict__ dr, const int32_t 
                         if (cum + h[j] >= rem) {
                             sh_prefix = prefix | ((uint32_t)(255 - 8 * tid - j) << shift);
                             sh_rem = rem - cum;
+                            sh_whole = cum + h[j] == rem;   // the digit's keys are all taken
                             break;
                         }
                         cum += h[j];
@@ -146,18 +150,26 @@ __device__ uint32_t select_sequence(const float *__restrict__ dr, const int32_t 
             __syncthreads();
             prefix = sh_prefix;
             rem = sh_rem;
+            whole = sh_whole != 0;
             mask |= 255u << shift;
             __syncthreads();
         }
-        T = prefix;
+        if (whole) {   // take every key >= the digit's lower bound (prefix, low bits 0)
+            T = prefix ? prefix - 1u : 0u;
+            rem = 0;
+        } else {
+            T = prefix;
+        }
     }
 
-    // rank of each key == T among equals, in index order
-    uint32_t neq = 0;
-    if (rem > 0)
+    // rank of each key == T among equals, in index order (rem is the same in every thread:
+    // no ranking, and no scan, when no tie straddles the budget)
+    uint32_t eq_before = 0;
+    if (rem > 0) {
+        uint32_t neq = 0, tot_eq;
         for (int i = i0; i < i1; ++i) neq += (key[i] == T);
-    uint32_t tot_eq;
-    uint32_t eq_before = block_scan<kT>(neq, wsum, &tot_eq);
+        eq_before = block_scan<kT>(neq, wsum, &tot_eq);
+    }
     uint32_t nsel = 0;
     for (int i = i0; i < i1; ++i) {
         const uint32_t kk = key[i];

@@ -76,6 +76,48 @@ def test_proxy_llada_width(B, orc, N):
     assert_drift_close(to_np(drift), drift_o)
 
 
+@pytest.mark.parametrize("Bq,N,d,r", [
+    (1, 1024, 4096, 128),   # 8 independent K slices summed by the cosine kernel
+    (10, 4096, 128, 128),   # 320 token tiles of 128 rows fill the GPU: drift in the epilogue
+    (10, 3950, 256, 96),    # the same with a ragged last tile and a proxy narrower than the
+                            # tile (the fourth TMEM lane quarter holds no feature)
+    (2, 9, 128, 64),        # d = 128 too short to split: one ragged tile, drift in the epilogue
+    (3, 17, 256, 32),       # one ragged tile in 2 K slices, cosine kernel
+    (1, 300, 512, 256),     # r > 128: K slices and the cosine kernel
+], ids=["slices8", "epilogue-40960rows", "epilogue-r96-ragged", "epilogue-short-k", "slices2-r32",
+        "slices-r256"])
+def test_proxy_plans_parity(B, orc, Bq, N, d, r):
+    """Every launch plan of the singular proxy and its drift (SPA-Cache, "1. Update
+    identification via singular proxy") against the oracle on every row, with the
+    degenerate rows of the drift's definition: a zero current proxy (drift 1), a zero
+    cached proxy (drift 1) and both zero (drift 0); a second call against the first
+    call's own proxies gives exactly zero drift on every row."""
+    g = synth.rng(14 + N + r)
+    H0 = synth.round_bf16(g.standard_normal((Bq, N, d), dtype=np.float32))
+    H1 = synth.round_bf16(H0 + g.standard_normal((Bq, N, d), dtype=np.float32) * np.float32(0.05))
+    P = synth.round_bf16((g.standard_normal((d, r)) * 0.02).astype(np.float32))
+    pc, _ = orc.proxy_score(H0, P, np.ones((Bq, N, r), np.float32))
+    last = Bq - 1
+    H1[0, 1] = 0.0                  # current proxy zero, cached not: drift 1
+    pc[last, N - 1] = 0.0           # cached proxy zero, current not: drift 1
+    if N > 3:
+        H1[0, 3] = 0.0              # both zero: drift 0
+        pc[0, 3] = 0.0
+    Hd = to_dev(H1, torch.bfloat16)
+    Pt = to_dev(P.T.copy(), torch.bfloat16)
+    cur, drift = B.dllm_proxy_score(Hd, Pt, to_dev(pc))
+    torch.cuda.synchronize()
+    cur_o, drift_o = orc.proxy_score(H1, P, pc)
+    assert normwise_rel(to_np(cur), cur_o) < FP32_REDUCTION_RTOL
+    dg = to_np(drift)
+    assert_drift_close(dg, drift_o)
+    assert dg[0, 1] == 1.0 and dg[last, N - 1] == 1.0
+    if N > 3:
+        assert dg[0, 3] == 0.0
+    _, again = B.dllm_proxy_score(Hd, Pt, cur.clone())
+    assert (again == 0).all().item()
+
+
 # --------------------------------------------------------------------------- selection
 @pytest.mark.parametrize("Bq,N,k,F,ties", [(1, 1, 1, 0, False), (3, 37, 5, 3, True),
                                             (2, 1024, 164, 0, False), (1, 1024, 164, 40, True),

@@ -34,12 +34,12 @@ def B():
 
 
 def test_layer_step_plans_at_164_rows(B):
-    """QKV: 96 weight tiles x K split 3 (288 CTAs, two per SM); O and down: 32 x 4 in
-    clusters of 4 with the whole shared memory (one CTA per SM); gate/up: 192 weight
-    tiles, no split, three stages at two CTAs per SM.  The 164 rows are staged as 168
-    (the 8-row swizzle atom) in a 176-column MMA."""
+    """QKV: 96 weight tiles x K split 3 (288 CTAs, two per SM, three stages once the 1 KB
+    alignment slack is dropped); O and down: 32 x 4 in clusters of 4 with the whole shared
+    memory (one CTA per SM); gate/up: 192 weight tiles, no split, three stages at two CTAs
+    per SM.  The 164 rows are staged as 168 (the 8-row swizzle atom) in a 176-column MMA."""
     want = {
-        (12288, 4096): dict(splits=3, w_tiles=96, ctas_per_sm=2),
+        (12288, 4096): dict(splits=3, w_tiles=96, ctas_per_sm=2, stages=3),
         (4096, 4096): dict(splits=4, w_tiles=32, ctas_per_sm=1),
         (24576, 4096): dict(splits=1, w_tiles=192, ctas_per_sm=2, stages=3),
         (4096, 12288): dict(splits=4, w_tiles=32, ctas_per_sm=1),
@@ -94,7 +94,9 @@ def test_plan_invariants(B, sms, splits):
     for M in MS:
         for N_out in NS:
             for K in KS:
-                for slices in ((False, True) if splits == 0 else (False,)):
+                for slices in ((0, 1, 2) if splits == 0 else (0,)):
+                    if slices == 2 and N_out > 128:
+                        continue
                     p = B.dllm_gemm_plan(M, N_out, K, splits=splits, sms=sms, slices=slices)
                     case = (M, N_out, K, splits, sms, slices, p)
                     BN, s, KB = p["BN"], p["splits"], K // 64
@@ -113,6 +115,24 @@ def test_plan_invariants(B, sms, splits):
                     assert p["stages"] >= 2, case
                     assert p["smem"] <= SMEM_LIMIT, case
                     assert p["ctas_per_sm"] * (p["smem"] + 1024) <= SMEM_PER_SM, case
+
+
+def test_proxy_drift_plan(B):
+    """The proxy projection at r = 128, d = 4096.  At 1024 tokens (the LLaDA-8B-shaped
+    layer) its slice plan splits K 8 ways over 16 token tiles of 64 rows (128 CTAs, four
+    stages each at two CTAs per SM): partials summed by the cosine kernel.  At 16 x 8192 tokens the 1024 token
+    tiles of 128 rows fill the GPU without a split, and the drift plan (the same tiles,
+    one CTA each, two per SM) computes the drift in the epilogue."""
+    p = B.dllm_gemm_plan(1024, 128, 4096, sms=152, slices=1)
+    assert (p["BN"], p["splits"], p["tok_tiles"], p["stages"], p["ctas_per_sm"]) == (64, 8, 16, 4, 2)
+    p = B.dllm_gemm_plan(16 * 8192, 128, 4096, sms=152, slices=1)
+    assert (p["BN"], p["splits"], p["tok_tiles"]) == (128, 1, 1024)
+    p = B.dllm_gemm_plan(16 * 8192, 128, 4096, sms=152, slices=2)
+    assert (p["BN"], p["splits"], p["tok_tiles"], p["w_tiles"], p["ctas_per_sm"]) == (128, 1, 1024, 1, 2)
+    with pytest.raises(B.DllmError):
+        B.dllm_gemm_plan(1024, 256, 4096, slices=2)    # the drift needs every feature in one tile
+    with pytest.raises(B.DllmError):
+        B.dllm_gemm_plan(1024, 128, 4096, slices=3)
 
 
 def test_plan_rejects_bad_shapes(B):
