@@ -154,7 +154,8 @@ def layer_kernel_work(sh, M):
     """Algorithmic bytes and FLOPs of each kernel of one layer step with M refreshed rows
     (weights and caches counted once, bf16 = 2 bytes, fp32 = 4).  Up to N = 4096 the
     selection and the gather of the selected rows are one kernel ("select"); with bf16,
-    r <= 128 and no K split the proxy projection computes the drift itself ("proxy_gemm")."""
+    r <= 128 and no K split the proxy projection computes the drift itself ("proxy_gemm"),
+    with a K split the selection kernel does ("select")."""
     B, N, d, r, F = sh.B, sh.N, sh.d, sh.r, sh.F
     dq, dkv = sh.d_q, sh.d_kv
     fold = sh.dtype == "bf16" and M <= 256   # the refresh folds the second RMSNorm up to 256 rows
@@ -165,12 +166,17 @@ def layer_kernel_work(sh, M):
     # bf16 with r <= 128 and no K split (the token tiles fill the GPU): the projection's
     # epilogue computes the drift (reads the cached proxies, writes the new ones and the
     # drift); no separate cosine kernel
-    fused = sh.dtype == "bf16" and r <= 128 and r % 32 == 0 and d % 64 == 0 and \
-        _proxy_slices(B * N, r, d) == 1
+    slices = _proxy_slices(B * N, r, d) if sh.dtype == "bf16" and d % 64 == 0 and r % 32 == 0 else 1
+    fused = sh.dtype == "bf16" and r <= 128 and r % 32 == 0 and d % 64 == 0 and slices == 1
+    # the one-call layer step with bf16 K-slice partials (r <= 128, N <= 4096): the
+    # selection kernel sums the partials and computes the drift, no cosine kernel
+    in_select = sh.dtype == "bf16" and r <= 128 and slices > 1 and N <= 4096
+    if in_select:
+        sel = (sel[0] + 8 * B * N * r + 4 * B * N, 0)
     work = {
         "proxy_gemm": (2 * B * N * d + 2 * r * d + 4 * B * N * r + ((4 * B * N * r + 4 * B * N) if fused else 0),
                        2 * B * N * d * r),
-        "cosine": None if fused else (8 * B * N * r + 4 * B * N, 0),
+        "cosine": None if (fused or in_select) else (8 * B * N * r + 4 * B * N, 0),
         "select": sel,
         "gather": gat,
         "qkv": (2 * (dq + 2 * dkv) * d + 2 * M * d + 2 * M * (dq + 2 * dkv), 2 * M * d * (dq + 2 * dkv)),

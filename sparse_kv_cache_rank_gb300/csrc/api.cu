@@ -504,18 +504,20 @@ DLLM_EXPORT size_t dllm_refresh_workspace_bytes(const dllm_layer *W, int B, int 
 
 namespace {
 
-// The per-layer step's selection arguments, when the selection is fused with the gather.
+// The per-layer step's selection arguments, when the selection is fused with the gather
+// (and, with dp.parts set, preceded by the drift computed from the projection's partials).
 struct FusedSelect {
-    const float *drift;
+    float *drift;
     const int32_t *forced;
     int F, k;
     float min_drift;
     int32_t *idx, *count;
+    DriftParts dp;
 };
 
 template <class T>
 int refresh_impl(const dllm_layer *W, const T *H_in, SelRows sel, int B, T *K_cache, T *V_cache,
-                 T *H_out, float *proxy_cache, const float *proxy_cur, int r, uint8_t *ws,
+                 T *H_out, float *proxy_cache, float *proxy_cur, int r, uint8_t *ws,
                  cudaStream_t st, const FusedSelect *fs = nullptr) {
     const RefreshWs L = refresh_ws(W, B, sel.N, sel.k_max);
     const int M = B * sel.k_max;
@@ -540,7 +542,7 @@ int refresh_impl(const dllm_layer *W, const T *H_in, SelRows sel, int B, T *K_ca
         Launch t(DLLM_KERNEL_SELECT, st);
         CHECK_CUDA(select_gather<T>(fs->drift, fs->forced, fs->F, fs->k, fs->min_drift, fs->idx, fs->count, B, sel.N,
                                     sel.k_max, H_in, d, g1, W->eps, Xn, proxy_cache, proxy_cur, r, W->rope_inv_freq,
-                                    W->hd / 2, rope_cs, status, st),
+                                    W->hd / 2, rope_cs, fs->dp, status, st),
                    "select + gather launch");
     } else {   // a3: gather + RMSNorm, proxy cache update
         Launch t(DLLM_KERNEL_GATHER, st);
@@ -617,13 +619,15 @@ DLLM_EXPORT int dllm_sparse_layer_refresh(const dllm_layer *W, const void *H_in,
     uint8_t *w8 = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255));
     SelRows sel{idx, count, k_max, N};
     cudaStream_t st = as_stream(stream);
+    // (without a fused selection the refresh only reads proxy_cur)
+    float *cur = const_cast<float *>(proxy_cur);
     if (W->dtype == DLLM_BF16)
         return refresh_impl<bf16>(W, static_cast<const bf16 *>(H_in), sel, B, static_cast<bf16 *>(K_cache),
                                   static_cast<bf16 *>(V_cache), static_cast<bf16 *>(H_out_cache),
-                                  proxy_cache, proxy_cur, r, w8, st);
+                                  proxy_cache, cur, r, w8, st);
     return refresh_impl<float>(W, static_cast<const float *>(H_in), sel, B, static_cast<float *>(K_cache),
                                static_cast<float *>(V_cache), static_cast<float *>(H_out_cache),
-                               proxy_cache, proxy_cur, r, w8, st);
+                               proxy_cache, cur, r, w8, st);
 }
 
 // ------------------------------------------------------------------ one layer step
@@ -631,7 +635,9 @@ DLLM_EXPORT size_t dllm_layer_step_workspace_bytes(const dllm_layer *W, int B, i
     if (!W || B <= 0 || N <= 0 || r <= 0 || F < 0 || k < 0) return 0;
     const long long km = (long long)k + F < N ? (long long)k + F : N;
     const int k_max = km > 0 ? (int)km : 1;
-    return refresh_ws(W, B, N, k_max).total + dllm_proxy_workspace_bytes(B, N, W->d, r, W->dtype) + 256;
+    // refresh scratch, the proxy projection's partials, the selection's arrival counters
+    return refresh_ws(W, B, N, k_max).total + dllm_proxy_workspace_bytes(B, N, W->d, r, W->dtype) +
+           (size_t)B * sizeof(unsigned) + 256 + 256;
 }
 
 DLLM_EXPORT int dllm_layer_step(const dllm_layer *W, const void *Pt, const void *H_in, float *proxy_cache,
@@ -661,9 +667,28 @@ DLLM_EXPORT int dllm_layer_step(const dllm_layer *W, const void *Pt, const void 
     // a1: proxy + drift (its K-slice partials, where it needs them, after the refresh scratch)
     const size_t rws = k_max > 0 ? refresh_ws(W, B, N, k_max).total : 0;
     uint8_t *w8 = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255));
-    rc = dllm_proxy_score(H_in, Pt, proxy_cache, proxy_cur, drift, B, N, W->d, r, W->dtype, w8 + rws,
-                          ws_bytes - rws - 256, stream);
-    if (rc != DLLM_OK) return rc;
+    const int nparts = proxy_slices(B, N, W->d, r, W->dtype);
+    // bf16 K-slice partials and a selection fused with the gather: the selection kernel sums
+    // the partials and computes the drift itself (no cosine kernel); the projection clears
+    // the selection's per-sequence arrival counters, placed after the partials
+    const DriftParts no_parts{nullptr, 0, nullptr};
+    DriftParts dp = no_parts;
+    if (W->dtype == DLLM_BF16 && nparts > 1 && r <= 128 && k_max > 0 && N <= select_gather_max_n() &&
+        select_gather_fused_ok(B, N, k_max, W->dtype)) {
+        const size_t pbytes = dllm_proxy_workspace_bytes(B, N, W->d, r, W->dtype);
+        float *parts = reinterpret_cast<float *>(
+            (reinterpret_cast<uintptr_t>(w8 + rws) + 255) & ~uintptr_t(255));
+        unsigned *arrive = reinterpret_cast<unsigned *>(w8 + rws + pbytes);
+        dp = DriftParts{parts, nparts, arrive};
+        Launch t(DLLM_KERNEL_PROXY_GEMM, st);
+        CHECK_CUDA(gemm_tc_slices(static_cast<const bf16 *>(Pt), r, W->d, static_cast<const bf16 *>(H_in), B * N,
+                                  parts, true, status_ptr(), st, arrive, B),
+                   "proxy projection launch");
+    } else {
+        rc = dllm_proxy_score(H_in, Pt, proxy_cache, proxy_cur, drift, B, N, W->d, r, W->dtype, w8 + rws,
+                              ws_bytes - rws - 256, stream);
+        if (rc != DLLM_OK) return rc;
+    }
     if (k_max == 0) {   // nothing can be selected: empty selection
         return dllm_select_topk(drift, forced, F, k, min_drift, idx, count, B, N, stream);
     }
@@ -679,7 +704,7 @@ DLLM_EXPORT int dllm_layer_step(const dllm_layer *W, const void *Pt, const void 
                                    static_cast<float *>(V_cache), static_cast<float *>(H_out_cache), proxy_cache,
                                    proxy_cur, r, w8, st);
     }
-    const FusedSelect fs{drift, forced, F, k, min_drift, idx, count};
+    const FusedSelect fs{drift, forced, F, k, min_drift, idx, count, dp};
     if (W->dtype == DLLM_BF16)
         return refresh_impl<bf16>(W, static_cast<const bf16 *>(H_in), sel, B, static_cast<bf16 *>(K_cache),
                                   static_cast<bf16 *>(V_cache), static_cast<bf16 *>(H_out_cache), proxy_cache,

@@ -54,6 +54,8 @@ struct Shape {
                       // >= the bytes the MMA reads past the last stage; barriers follow
     int w_stream;     // the weights are larger than a fraction of L2 and read once per call:
                       // their lines are loaded with an evict-first policy
+    unsigned *zero;   // nzero words the first CTA clears once the previous kernel is done
+    int nzero;        // (counters of the kernel that follows; nullptr / 0: none)
 };
 
 __host__ __device__ inline int stage_bytes(int xrows) { return kWBytes + xrows * BK * 2; }
@@ -310,6 +312,8 @@ __global__ void __launch_bounds__(64 + 32 * EW, EW == 8 ? 2 : 1)
         // ---------------- epilogue warps (2..9): resolve every token column's (sequence,
         // position) while the main loop runs
         griddep_wait();
+        if (g.zero && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+            for (int i = threadIdx.x - 64; i < g.nzero; i += 32 * EW) g.zero[i] = 0u;
         for (int c = threadIdx.x - 64; c < (kCos ? 0 : g.BN); c += 32 * EW) {
             int b = 0, pos = -1;
             if constexpr (Epi::kColScale) {   // a per-column scale in the position slot
@@ -688,7 +692,8 @@ Plan plan_cosine(int M_tok, int N_out, int K, int sms) {
 
 template <class Epi>
 cudaError_t launch_plan(const Plan &p, bool indep, const bf16 *W, int N_out, int K, const bf16 *X,
-                        int M_tok, const Epi &epi, bool w_const, unsigned *status, cudaStream_t st) {
+                        int M_tok, const Epi &epi, bool w_const, unsigned *status, cudaStream_t st,
+                        unsigned *zero = nullptr, int nzero = 0) {
     if (p.stages < 2) return cudaErrorInvalidValue;
     CUtensorMap tmW, tmX;
     if (!make_tmap(&tmW, W, (uint64_t)N_out, (uint64_t)K, BM) ||
@@ -698,7 +703,7 @@ cudaError_t launch_plan(const Plan &p, bool indep, const bf16 *W, int N_out, int
     // reused: evict-first lines (with several token tiles its tiles are re-read)
     const int w_stream = p.tok_tiles == 1 && (size_t)N_out * (size_t)K * 2 > (size_t)16 << 20 ? 1 : 0;
     Shape g{M_tok, N_out, K, p.BN, p.splits, p.stages, w_const ? 1 : 0, indep ? 1 : 0, p.body,
-            p.xrows, p.base_aligned, p.col_bytes, w_stream};
+            p.xrows, p.base_aligned, p.col_bytes, w_stream, zero, zero ? nzero : 0};
     // one CTA per SM (the shared memory of two exceeds an SM): 16 epilogue warps
     const bool wide = !Epi::kTileReduce && p.smem > (size_t)kSmemPair;
     auto kern = wide ? k_gemm_tc<Epi, 16> : k_gemm_tc<Epi, 8>;
@@ -750,12 +755,12 @@ int gemm_tc_plan_info(int M_tok, int N_out, int K, int splits_req, int sms, int 
 }
 
 cudaError_t gemm_tc_slices(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, float *parts,
-                           bool w_const, unsigned *status, cudaStream_t st) {
+                           bool w_const, unsigned *status, cudaStream_t st, unsigned *zero, int nzero) {
     if (M_tok <= 0 || N_out <= 0) return cudaSuccess;
     if (K % BK != 0 || N_out % 32 != 0) return cudaErrorInvalidValue;
     const Plan p = plan_slices(M_tok, N_out, K, num_sms());
     EpiStoreF32 epi{SelRows{}, parts, N_out, N_out};
-    return launch_plan(p, true, W, N_out, K, X, M_tok, epi, w_const, status, st);
+    return launch_plan(p, true, W, N_out, K, X, M_tok, epi, w_const, status, st, zero, nzero);
 }
 
 bool gemm_tc_cosine_ok(int M_tok, int N_out, int K) {

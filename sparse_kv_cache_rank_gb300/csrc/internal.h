@@ -63,8 +63,11 @@ int gemm_tc_slices_count(int M_tok, int N_out, int K);
 // independent-K-slice plan of gemm_tc_slices; 2: the plan of gemm_tc_cosine.  Returns -1
 // for a shape the GEMM rejects.
 int gemm_tc_plan_info(int M_tok, int N_out, int K, int splits_req, int sms, int kind, int *info);
+// zero [nzero] (optional): words the first CTA clears after the previous kernel has
+// completed, for the counters of the kernel that follows.
 cudaError_t gemm_tc_slices(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, float *parts,
-                           bool w_const, unsigned *status, cudaStream_t st);
+                           bool w_const, unsigned *status, cudaStream_t st, unsigned *zero = nullptr,
+                           int nzero = 0);
 // The singular proxy with its cosine drift in one launch (EpiCosine): cur [M_tok, N_out] =
 // X W^T and drift [M_tok] against cached [M_tok, N_out]; needs N_out <= 128, N_out % 32 == 0,
 // K % 64 == 0 and a shape whose slice plan has no K split (gemm_tc_cosine_ok).  No workspace.
@@ -174,12 +177,22 @@ cudaError_t select_topk(const float *drift, const int32_t *forced, int F, int k,
 
 // Selection fused with the gather of the selected rows (front.cu): idx / count as
 // select_topk, and for rows m = b * k_max + s the outputs of gather_rmsnorm.  N <= 4096.
+// With dp.parts set, the kernel first computes drift [B, N] (and proxy_cur) from the
+// proxy projection's K-slice partials, as cosine_drift would (r <= 128), its CTAs meeting
+// at a per-sequence barrier on dp.arrive [B] (zero at launch); the grid must then fit on
+// the GPU at once (select_gather_fused_ok).
+struct DriftParts {
+    const float *parts;   // [nparts, B*N, r] fp32, or nullptr: drift is an input
+    int nparts;
+    unsigned *arrive;     // [B] arrival counters, zeroed before the launch
+};
 int select_gather_max_n();
+bool select_gather_fused_ok(int B, int N, int k_max, int dtype);
 template <class T>
-cudaError_t select_gather(const float *drift, const int32_t *forced, int F, int k, float min_drift, int32_t *idx,
+cudaError_t select_gather(float *drift, const int32_t *forced, int F, int k, float min_drift, int32_t *idx,
                           int32_t *count, int B, int N, int k_max, const T *H, int d, const T *gamma, float eps,
-                          T *Xn, float *proxy_cache, const float *proxy_cur, int r, const float *inv_freq,
-                          int half_hd, float2 *rope_cs, unsigned *status, cudaStream_t st);
+                          T *Xn, float *proxy_cache, float *proxy_cur, int r, const float *inv_freq,
+                          int half_hd, float2 *rope_cs, DriftParts dp, unsigned *status, cudaStream_t st);
 
 // ---------------------------------------------------------------- vocabulary
 size_t commit_ws_bytes(int B, int M, int V);

@@ -3,6 +3,7 @@
 // rows, RMSNorm of the attention residual, the cosine drift score, and the one-time
 // weight packing.  All of them are memory-bound row sweeps: one CTA (or warp) per
 // row, coalesced loads, shuffle reductions.
+#include "cosine.cuh"
 #include "rownorm.cuh"
 
 namespace dllm {
@@ -56,12 +57,9 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float *__restrict__ 
     norm_row<float, T>(h1 + (size_t)blockIdx.x * d, d, gamma, eps, Xn2 + (size_t)blockIdx.x * d, red);
 }
 
-// drift = 1 - cos(cur, cached), evaluated as |cur/|cur| - cached/|cached||^2 / 2, which
-// equals 1 - cos for unit vectors and keeps the small drifts of nearly unchanged rows
-// free of the cancellation in 1 - dot/norm.  Identical inputs give exactly 0; both
-// norms zero -> 0, one zero -> 1; clamped to [0, 2].  One warp per row.  With
-// nparts > 1 the proxy is first summed from the K-slice partials in slice order (the
-// same order every call, so identical inputs still give identical proxies).
+// The cosine drift of every row (cosine.cuh), one warp per row: r <= 128 keeps one float4
+// chunk per lane, wider proxies (r <= 1024) up to eight.
+template <int MAXCH>
 __global__ void __launch_bounds__(256) k_cosine_drift(const float *__restrict__ parts, int nparts,
                                                       const float *__restrict__ cached,
                                                       float *__restrict__ cur,
@@ -71,83 +69,7 @@ __global__ void __launch_bounds__(256) k_cosine_drift(const float *__restrict__ 
     const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
-    float *a = cur + row * r;
-    const float *c = cached + row * r;
-    // float4 chunks (r % 32 == 0, r <= 1024: at most 8 per lane), held in registers for
-    // both passes; for each chunk every partial load is issued before the first add, and
-    // the adds run in slice order
-    const int nch = r >> 2;
-    const size_t stride4 = (size_t)rows * nch;
-    const float4 *p4 = reinterpret_cast<const float4 *>(parts) + (size_t)row * nch;
-    float4 *a4 = reinterpret_cast<float4 *>(a);
-    const float4 *c4 = reinterpret_cast<const float4 *>(c);
-    constexpr int kMaxCh = 8;
-    float4 xs[kMaxCh], cs[kMaxCh];
-    float na = 0.f, nc = 0.f;
-#pragma unroll
-    for (int u = 0; u < kMaxCh; ++u) {
-        const int ch = lane + 32 * u;
-        if (ch >= nch) break;
-        float4 x;
-        const float4 cc = c4[ch];
-        if (nparts > 1) {
-            float4 t[8];
-#pragma unroll
-            for (int z = 0; z < 8; ++z)
-                if (z < nparts) t[z] = __ldcg(p4 + (size_t)z * stride4 + ch);
-            x = t[0];
-#pragma unroll
-            for (int z = 1; z < 8; ++z)
-                if (z < nparts) {
-                    x.x += t[z].x;
-                    x.y += t[z].y;
-                    x.z += t[z].z;
-                    x.w += t[z].w;
-                }
-            for (int z = 8; z < nparts; ++z) {
-                const float4 y = __ldcg(p4 + (size_t)z * stride4 + ch);
-                x.x += y.x;
-                x.y += y.y;
-                x.z += y.z;
-                x.w += y.w;
-            }
-            a4[ch] = x;
-        } else {
-            x = a4[ch];
-        }
-        xs[u] = x;
-        cs[u] = cc;
-        na = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, na))));
-        nc = fmaf(cc.x, cc.x, fmaf(cc.y, cc.y, fmaf(cc.z, cc.z, fmaf(cc.w, cc.w, nc))));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        na += __shfl_xor_sync(0xffffffffu, na, o);
-        nc += __shfl_xor_sync(0xffffffffu, nc, o);
-    }
-    float out;
-    if (na == 0.f && nc == 0.f) {
-        out = 0.f;
-    } else if (na == 0.f || nc == 0.f) {
-        out = 1.f;
-    } else {
-        const float ia = 1.0f / sqrtf(na), ic = 1.0f / sqrtf(nc);
-        float s = 0.f;
-#pragma unroll
-        for (int u = 0; u < kMaxCh; ++u) {   // the chunks this lane summed above
-            if (lane + 32 * u >= nch) break;
-            const float4 x = xs[u], cc = cs[u];
-            // separately rounded products (no FMA contraction): equal inputs give t == 0
-            const float t0 = __fsub_rn(__fmul_rn(x.x, ia), __fmul_rn(cc.x, ic));
-            const float t1 = __fsub_rn(__fmul_rn(x.y, ia), __fmul_rn(cc.y, ic));
-            const float t2 = __fsub_rn(__fmul_rn(x.z, ia), __fmul_rn(cc.z, ic));
-            const float t3 = __fsub_rn(__fmul_rn(x.w, ia), __fmul_rn(cc.w, ic));
-            s = fmaf(t0, t0, fmaf(t1, t1, fmaf(t2, t2, fmaf(t3, t3, s))));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        out = fminf(fmaxf(0.5f * s, 0.f), 2.f);
-    }
+    const float out = cosine_row<MAXCH>(parts, nparts, cached, cur, row, rows, r, lane);
     if (lane == 0) drift[row] = out;
 }
 
@@ -198,7 +120,10 @@ cudaError_t rmsnorm_rows(const float *h1, int M, int d, const T *gamma, float ep
 cudaError_t cosine_drift(const float *parts, int nparts, const float *cached, float *cur,
                          float *drift, long rows, int r, cudaStream_t st) {
     if (rows <= 0) return cudaSuccess;
-    return launch_kernel(k_cosine_drift, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, st, 1, parts,
+    if (r <= 128)
+        return launch_kernel(k_cosine_drift<1>, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, st, 1, parts,
+                             nparts, cached, cur, drift, rows, r);
+    return launch_kernel(k_cosine_drift<8>, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, st, 1, parts,
                          nparts, cached, cur, drift, rows, r);
 }
 

@@ -72,7 +72,7 @@ __device__ uint32_t select_sequence(const float *__restrict__ dr, const int32_t 
     uint32_t nf = 0, ne = 0;
     for (int i = i0; i < i1; ++i) {
         uint32_t kk = 0;
-        const float x = dr[i];
+        const float x = __ldcg(dr + i);   // L2: the drifts may have been written by other CTAs
         if (flag[i]) {
             ++nf;
         } else if (x > min_drift) {   // false for NaN

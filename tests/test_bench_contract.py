@@ -55,3 +55,27 @@ def test_native_arm_fails_loudly_without_a_gpu():
     r = _run(["--steps", "1", "--warmup", "3", "--no-stack", "--no-configs", "--no-cpu-baseline"])
     assert r.returncode != 0
     assert not any(l.strip().startswith("{") for l in r.stdout.splitlines())
+
+
+def test_kernel_work_model_follows_the_launches():
+    """The bench's per-kernel work model (the roofline's algorithmic bytes) names the
+    kernels each configuration launches: at the LLaDA-8B-shaped layer the selection
+    kernel computes the drift from the proxy projection's K-slice partials (no cosine
+    kernel); at 16 x 8192 tokens the projection's epilogue does (no split, no cosine
+    kernel, a separate gather beyond N = 4096); the fp32 layer keeps the cosine kernel."""
+    sys.path.insert(0, ROOT)
+    import dataclasses
+    import bench
+    from sparse_kv_cache_rank_gb300 import binding, synth
+    if not os.path.exists(binding.LIB_PATH):
+        pytest.skip("libdllm.so not built")
+    llada = bench.layer_kernel_work(synth.LLADA_LAYER, 164)
+    assert "cosine" not in llada and "gather" not in llada
+    B, N, r = 1, 1024, 128
+    assert llada["select"][0] == 8 * B * N + 4 * B + 2 * 164 * 4096 * 2 + 8 * 164 * r + 8 * B * N * r + 4 * B * N
+    wide = bench.layer_kernel_work(dataclasses.replace(synth.LLADA_LAYER, B=16, N=8192), 164)
+    assert "cosine" not in wide and "gather" in wide
+    tiny = bench.layer_kernel_work(synth.TINY, 96)
+    assert "cosine" in tiny and "rmsnorm2" in tiny
+    for w in (llada, wide, tiny):
+        assert all(v[0] > 0 for v in w.values())
