@@ -88,33 +88,20 @@ __global__ void __launch_bounds__(64 + 128 * SG, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 15);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
-    griddep_wait();
-    griddep_launch();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q0 = blockIdx.x * AQ;
     const int h = blockIdx.y;
     const int b = blockIdx.z / a.splits;
     const int split = blockIdx.z - b * a.splits;
     const int g = h / (a.n_q / a.n_kv);
-    int live = a.count[b];
-    live = live < a.k_max ? live : a.k_max;
-    live -= q0;                                 // live query rows of this tile
     const int t0 = (int)((long long)split * a.kv_tiles / a.splits);
     const int t1 = (int)((long long)(split + 1) * a.kv_tiles / a.splits);
     const int nt = t1 - t0;
     const int dq = a.n_q * HD;
     const size_t row0 = (size_t)b * a.k_max + q0;   // flattened row of query 0
-    if (live <= 0) {   // no live query (the same in every slice of the cluster): zero outputs
-        if (split == 0 && warp >= 2) {
-            const int r = (warp & 3) * 32 + lane, qt = (warp - 2) >> 2;
-            if (q0 + r < a.k_max) {
-                bf16 *dst = a.A + (row0 + r) * dq + (size_t)h * HD + qt * OH;
-                for (int e = 0; e < OH; ++e) dst[e] = __float2bfloat16_rn(0.f);
-            }
-        }
-        return;
-    }
 
+    // barriers, descriptors and tensor memory first: none of it reads what the previous
+    // kernel writes, so it overlaps that kernel's tail
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         for (int i = 0; i < 2; ++i) {
@@ -144,6 +131,28 @@ __global__ void __launch_bounds__(64 + 128 * SG, 1)
     const uint32_t tmem = *tmem_slot;
     const uint32_t tS[2] = {tmem, tmem + 128};
     const uint32_t tPV = tmem + 256;
+
+    griddep_wait();
+    griddep_launch();
+    int live = a.count[b];
+    live = live < a.k_max ? live : a.k_max;
+    live -= q0;                                 // live query rows of this tile
+    if (live <= 0) {   // no live query (the same in every slice of the cluster): zero outputs
+        if (split == 0 && warp >= 2) {
+            const int r = (warp & 3) * 32 + lane, qt = (warp - 2) >> 2;
+            if (q0 + r < a.k_max) {
+                bf16 *dst = a.A + (row0 + r) * dq + (size_t)h * HD + qt * OH;
+                for (int e = 0; e < OH; ++e) dst[e] = __float2bfloat16_rn(0.f);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 1) {
+            tc_fence_after();
+            tmem_dealloc(tmem, 512);
+        }
+        return;
+    }
 
     // softmax threads' results for the key-split merge: (O row half, m, l) of the row
     float o[OH];
