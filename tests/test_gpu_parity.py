@@ -412,21 +412,26 @@ def test_refresh_long_context_batch4_half(B, orc):
 
 
 # --------------------------------------------------------------------------- attention alone
-@pytest.mark.parametrize("Bq,N,k_max,n_q,n_kv,hd,live", [
-    (1, 1024, 164, 32, 32, 128, 164), (2, 333, 150, 4, 2, 64, 150), (1, 2048, 328, 28, 4, 128, 300),
-    # 64-dim heads over 16 key tiles per CTA (two softmax threads per row)
-    (4, 2048, 256, 16, 8, 64, 250),
-    (3, 200, 37, 8, 8, 128, 37), (1, 129, 129, 2, 1, 64, 100),
+@pytest.mark.parametrize("Bq,N,k_max,n_q,n_kv,hd,live,growth", [
+    (1, 1024, 164, 32, 32, 128, 164, 0), (2, 333, 150, 4, 2, 64, 150, 0), (1, 2048, 328, 28, 4, 128, 300, 0),
+    # 64-dim heads over 16 key tiles per CTA (two softmax threads per row, pipelined)
+    (4, 2048, 256, 16, 8, 64, 250, 0),
+    # scores growing from key tile to key tile: every tile raises the rows' running
+    # maximum (the streaming softmax rescales O at every tile), 128- and 64-dim heads
+    (1, 2048, 328, 28, 4, 128, 300, 3), (4, 2048, 256, 16, 8, 64, 250, 3),
+    (3, 200, 37, 8, 8, 128, 37, 0), (1, 129, 129, 2, 1, 64, 100, 0),
     # one key slice per CTA (the grid alone fills the GPU), a ragged second query tile
-    (8, 256, 200, 28, 4, 128, 200), (16, 150, 140, 16, 16, 64, 140)])
-def test_attention_parity(B, orc, Bq, N, k_max, n_q, n_kv, hd, live):
+    (8, 256, 200, 28, 4, 128, 200, 0), (16, 150, 140, 16, 16, 64, 140, 0)])
+def test_attention_parity(B, orc, Bq, N, k_max, n_q, n_kv, hd, live, growth):
     """Selected queries over the whole cache, non-causal, GQA, ragged key tiles and
     partially live query tiles, key slices merged in a cluster and single-slice CTAs,
-    against the oracle's attention of every live row."""
-    g = synth.rng(400 + N + k_max)
+    against the oracle's attention of every live row.  growth > 0 scales the keys of
+    tile t by 1 + growth * t, so the row maxima climb tile after tile."""
+    g = synth.rng(400 + N + k_max + growth)
     dq, dkv = n_q * hd, n_kv * hd
     Q = synth.round_bf16(g.standard_normal((Bq * k_max, dq), dtype=np.float32))
-    K = synth.round_bf16(g.standard_normal((Bq, N, dkv), dtype=np.float32))
+    kscale = (1.0 + growth * (np.arange(N) // 128)).astype(np.float32)[None, :, None]
+    K = synth.round_bf16(g.standard_normal((Bq, N, dkv), dtype=np.float32) * kscale)
     V = synth.round_bf16(g.standard_normal((Bq, N, dkv), dtype=np.float32))
     idx = np.full((Bq, N), -1, np.int32)
     cnt = np.zeros(Bq, np.int32)
