@@ -317,7 +317,13 @@ int dllm_sparse_layer_refresh(const dllm_layer *W, const void *H_in, const int32
  *   K_cache, V_cache, H_out_cache, proxy_cache   as dllm_sparse_layer_refresh
  * The selection is fused with the gather of the selected rows for N <= 4096 (one kernel
  * fewer, no host round trip between the steps); longer sequences run the separate
- * kernels.  Pt [r, d] in the layer's dtype; forced [B, F] int32 (-1 padded) or NULL.
+ * kernels.  For bf16 with r <= 128 and a proxy projection that splits K, that kernel also
+ * sums the projection's partials and computes the drift (no cosine kernel): its CTAs of a
+ * sequence wait for one another at an arrival counter in the workspace (bounded: after
+ * 1 s the wait gives up and raises DLLM_STATUS_TIMEOUT), which the launch takes only when
+ * the whole grid fits the GPU at once, and otherwise keeps the cosine kernel.  Results
+ * are the same either way.  Pt [r, d] in the layer's dtype; forced [B, F] int32 (-1
+ * padded) or NULL.
  * Requirements: those of the three calls (r % 32 == 0; N <= 16384; H_out_cache not
  * aliasing H_in; 16-byte aligned arrays).  Workspace:
  * dllm_layer_step_workspace_bytes(W, B, N, r, F, k) bytes.

@@ -231,11 +231,19 @@ LONG_SMALL = synth.LayerShape("long-small-bf16", B=2, N=5000, d=128, n_q=2, n_kv
                               rho=0.02, dtype="bf16", prompt=4900, k_recent=4)
 
 
-@pytest.mark.parametrize("shape", [SMALL_BF16, synth.TINY, LONG_SMALL], ids=lambda s: s.name)
+# 320 short sequences: the fused drift + selection grid (one CTA per sequence) would not
+# fit the GPU at once, so the layer step falls back to the cosine kernel
+MANY_SEQ = synth.LayerShape("many-seq-bf16", B=320, N=40, d=256, n_q=2, n_kv=1, hd=64, F=128, r=32,
+                            rho=0.05, dtype="bf16", prompt=8, k_recent=2)
+
+
+@pytest.mark.parametrize("shape", [SMALL_BF16, synth.TINY, LONG_SMALL, MANY_SEQ], ids=lambda s: s.name)
 def test_layer_step_equals_three_calls(B, orc, shape):
-    """dllm_layer_step (selection fused with the gather up to N = 4096, the separate
-    kernels beyond) writes exactly what dllm_proxy_score, dllm_select_topk and
-    dllm_sparse_layer_refresh write in sequence: the same kernels' arithmetic, bit for bit."""
+    """dllm_layer_step (selection fused with the gather up to N = 4096 and, with K-slice
+    partials, the drift computed by that kernel; the separate kernels beyond N = 4096 or
+    when the fused grid would not fit the GPU at once) writes exactly what
+    dllm_proxy_score, dllm_select_topk and dllm_sparse_layer_refresh write in sequence:
+    the same arithmetic, bit for bit."""
     c = layer_case(orc, shape, 25, consistent=shape.N <= 1024)
     forced = forced_rows(shape, 26)
     k = orc.budget(shape.rho, shape.N)
