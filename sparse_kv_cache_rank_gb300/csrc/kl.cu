@@ -17,7 +17,8 @@
 // fp32 on the CUDA cores: the drift is made of score differences that bf16 tensor-core
 // scores would swamp.  One CTA (8 warps) = 64 query rows x one slice of the 128-row key
 // tiles; thread (ty, tx) owns rows 8 ty .. 8 ty + 7 and key columns 4 tx .. 4 tx + 3 of both
-// score tiles (64 FMA per 6 shared-memory loads), so one warp holds eight whole rows of a
+// score tiles (64 FMA per 6 shared-memory loads, issued as 32 packed two-lane FMAs on
+// row pairs), so one warp holds eight whole rows of a
 // tile.  The query tile (both steps, all
 // r dimensions) stays in shared memory, transposed; the key tiles stream through a two-chunk
 // ring of 32 dimensions each, the next chunk's global loads held in registers while the
@@ -142,17 +143,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         zy[a] = 0.f;
         w[a] = 0.f;
     }
-    float x[kRows][4], y[kRows][4];
+    // score accumulators of row pairs (2h, 2h+1) x column e: one packed fp32 FMA updates
+    // both rows (each lane of the pair rounds exactly as a scalar fmaf would)
+    float2 xx[kRows / 2][4], yy[kRows / 2][4];
     for (int it = 0; it < nit; ++it) {
         const int kt = kt0 + it / nch, ch = it % nch;
         const int k0 = kt * kK;
         if (ch == 0) {
 #pragma unroll
-            for (int a = 0; a < kRows; ++a)
+            for (int h = 0; h < kRows / 2; ++h)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    x[a][e] = 0.f;
-                    y[a][e] = 0.f;
+                    xx[h][e] = make_float2(0.f, 0.f);
+                    yy[h][e] = make_float2(0.f, 0.f);
                 }
         }
         if (it + 1 < nit) {   // next chunk's loads in flight during this chunk's products
@@ -172,16 +175,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float4 ap1 = *reinterpret_cast<const float4 *>(qpb + c * kPq + ty * kRows + 4);
             const float4 bc = *reinterpret_cast<const float4 *>(kcb + c * kPk + tx * 4);
             const float4 bp = *reinterpret_cast<const float4 *>(kpb + c * kPk + tx * 4);
-            const float av[kRows] = {ac0.x, ac0.y, ac0.z, ac0.w, ac1.x, ac1.y, ac1.z, ac1.w};
-            const float pv[kRows] = {ap0.x, ap0.y, ap0.z, ap0.w, ap1.x, ap1.y, ap1.z, ap1.w};
+            const float2 av[kRows / 2] = {make_float2(ac0.x, ac0.y), make_float2(ac0.z, ac0.w),
+                                          make_float2(ac1.x, ac1.y), make_float2(ac1.z, ac1.w)};
+            const float2 pv[kRows / 2] = {make_float2(ap0.x, ap0.y), make_float2(ap0.z, ap0.w),
+                                          make_float2(ap1.x, ap1.y), make_float2(ap1.z, ap1.w)};
             const float bv[4] = {bc.x, bc.y, bc.z, bc.w}, qv[4] = {bp.x, bp.y, bp.z, bp.w};
 #pragma unroll
-            for (int a = 0; a < kRows; ++a)
+            for (int e = 0; e < 4; ++e) {
+                const float2 be = make_float2(bv[e], bv[e]), qe = make_float2(qv[e], qv[e]);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    x[a][e] = fmaf(av[a], bv[e], x[a][e]);
-                    y[a][e] = fmaf(pv[a], qv[e], y[a][e]);
+                for (int h = 0; h < kRows / 2; ++h) {
+                    xx[h][e] = __ffma2_rn(av[h], be, xx[h][e]);
+                    yy[h][e] = __ffma2_rn(pv[h], qe, yy[h][e]);
                 }
+            }
         }
         if (it + 1 < nit) {   // the other buffer was last read in iteration it - 1
             float *nb = ring + (size_t)((it + 1) & 1) * 2 * kR * kPk;
@@ -190,6 +197,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
         if (ch != nch - 1) continue;
+        float x[kRows][4], y[kRows][4];
+#pragma unroll
+        for (int h = 0; h < kRows / 2; ++h)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                x[2 * h][e] = xx[h][e].x;
+                x[2 * h + 1][e] = xx[h][e].y;
+                y[2 * h][e] = yy[h][e].x;
+                y[2 * h + 1][e] = yy[h][e].y;
+            }
         // online update of the thread's rows over this tile's live key columns (j < N, j != i)
 #pragma unroll
         for (int a = 0; a < kRows; ++a) {
