@@ -289,16 +289,22 @@ class LayerWorkload:
     def shared(self):
         return self.w, self.layer, self.Pt
 
-    def step(self, H=None, idx=None, cnt=None):
-        """One layer step through dllm_layer_step (one library call)."""
+    def caches(self):
+        """The state a step reads and writes: (K, V, O, proxy cache, proxy, drift)."""
+        return self.K, self.V, self.O, self.pc, self.cur, self.drift
+
+    def step(self, H=None, idx=None, cnt=None, caches=None):
+        """One layer step through dllm_layer_step (one library call), on this workload's
+        caches or on another set of the same shapes."""
         B = self.B_
         if H is None:
             H = self.H[self.s & 1]
         idx = self.idx if idx is None else idx
         cnt = self.cnt if cnt is None else cnt
+        K, V, O, pc, cur, drift = self.caches() if caches is None else caches
         self.s += 1
-        B.dllm_layer_step(self.layer, self.Pt, H, self.pc, self.cur, self.drift, self.forced, self.k, idx, cnt,
-                          self.K, self.V, self.O, ws=self.ws_step)
+        B.dllm_layer_step(self.layer, self.Pt, H, pc, cur, drift, self.forced, self.k, idx, cnt, K, V, O,
+                          ws=self.ws_step)
 
     def step_calls(self):
         """The same step as the three calls dllm_proxy_score, dllm_select_topk and
@@ -487,11 +493,14 @@ def e2e_measure(wl, steps, barrier):
     """The same steps through the same calls with host buffers: every step uploads its
     input from pinned host memory and brings its result back -- the refreshed rows of the
     output cache, of the key cache and of the value cache (packed by dllm_gather_rows) and
-    the selection -- inside the timed region.  Inputs, selections and packed rows are
-    double-buffered and every copy (and the packing) runs on a second stream: after step s
-    that stream packs and reads back step s's rows and uploads the input of step s + 2
-    into the freed buffers, so the compute stream carries only the step's kernels and one
-    event wait per step.  -> (seconds for `steps` steps, byte counts per step)."""
+    the selection -- inside the timed region.  Inputs, selections, packed rows and the
+    caches themselves are double-buffered (steps of even and odd index work on two cache
+    sets of the same shapes) and every copy (and the packing) runs on a second stream:
+    after step s that stream packs and reads back step s's rows and uploads the input of
+    step s + 2 into the freed buffers.  The compute stream carries only the step's kernels
+    and one event wait per step, and step s + 2, the next to write step s's caches, waits
+    until they have been read, so the rows read back are exactly step s's.
+    -> (seconds for `steps` steps, byte counts per step)."""
     import torch
     B = wl.B_
     dev = wl.dev
@@ -506,6 +515,7 @@ def e2e_measure(wl, steps, barrier):
     idx_h = [torch.empty(wl.idx.shape, dtype=torch.int32).pin_memory() for _ in range(2)]
     cnt_h = [torch.empty(wl.cnt.shape, dtype=torch.int32).pin_memory() for _ in range(2)]
     rows_h = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in rows_d[0]] for _ in range(2)]
+    sets = [wl.caches(), tuple(t.clone() for t in wl.caches())]
     main = torch.cuda.current_stream(dev)
     cs = torch.cuda.Stream(dev)
     ready = [torch.cuda.Event(), torch.cuda.Event()]   # input of the step in Hd[b] is resident
@@ -515,7 +525,8 @@ def e2e_measure(wl, steps, barrier):
     def read_result(s):
         b = s & 1
         cs.wait_event(done[b])
-        for src, dst in zip((wl.O, wl.K, wl.V), rows_d[b]):
+        K, V, O = sets[b][:3]
+        for src, dst in zip((O, K, V), rows_d[b]):
             B.dllm_gather_rows(src, idx_d[b], cnt_d[b], km, dst)
         idx_h[b].copy_(idx_d[b], non_blocking=True)
         cnt_h[b].copy_(cnt_d[b], non_blocking=True)
@@ -537,7 +548,7 @@ def e2e_measure(wl, steps, barrier):
         for s in range(n):
             b = s & 1
             main.wait_event(ready[b])
-            wl.step(Hd[b], idx=idx_d[b], cnt=cnt_d[b])
+            wl.step(Hd[b], idx=idx_d[b], cnt=cnt_d[b], caches=sets[b])
             done[b].record(main)
             if s + 2 < n:
                 stage(s + 2)
@@ -562,9 +573,10 @@ def e2e_measure(wl, steps, barrier):
     b = (steps - 1) & 1
     c = int(cnt_h[b][0])
     got = rows_h[b][0][:c].to(dev)
-    want = wl.O[0, idx_h[b][0, :c].to(dev).long()]
+    want = sets[b][2][0, idx_h[b][0, :c].to(dev).long()]
     if not torch.equal(got, want):
         raise RuntimeError("e2e read-back does not match the refreshed rows")
+    del sets
     d2h = idx_h[0].numel() * 4 + cnt_h[0].numel() * 4 + sum(t.numel() * t.element_size() for t in rows_h[0])
     return f0.elapsed_time(f1) / 1e3, {"h2d_bytes_per_step": int(Hh[0].numel() * Hh[0].element_size()),
                                        "d2h_bytes_per_step": int(d2h),
