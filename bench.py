@@ -489,76 +489,92 @@ def native(args):
         print(json.dumps(result), flush=True)
 
 
-def e2e_measure(wl, steps, barrier):
+def e2e_batches(n, cap):
+    """Batch sizes for n end-to-end steps: 1, 1, 2, 4 ... up to cap at the start and back
+    down to 1 at the end, so that the first step waits for one upload only and the last
+    read-back is one step's."""
+    head = [b for b in (1, 1, 2, 4, 8, 16) if b < cap] + [cap]
+    tail = head[::-1]
+    if n <= sum(head) + sum(tail):
+        return [1] * n
+    mid = n - sum(head) - sum(tail)
+    return head + [cap] * (mid // cap) + ([mid % cap] if mid % cap else []) + tail
+
+
+def e2e_measure(wl, steps, barrier, slots=8, batch=4):
     """The same steps through the same calls with host buffers: every step uploads its
     input from pinned host memory and brings its result back -- the refreshed rows of the
-    output cache, of the key cache and of the value cache (packed by dllm_gather_rows) and
-    the selection -- inside the timed region.  Inputs, selections, packed rows and the
-    caches themselves are double-buffered (steps of even and odd index work on two cache
-    sets of the same shapes) and every copy (and the packing) runs on a second stream:
-    after step s that stream packs and reads back step s's rows and uploads the input of
-    step s + 2 into the freed buffers.  The compute stream carries only the step's kernels
-    and one event wait per step, and step s + 2, the next to write step s's caches, waits
-    until they have been read, so the rows read back are exactly step s's.
-    -> (seconds for `steps` steps, byte counts per step)."""
+    output cache, of the key cache and of the value cache and the selection -- inside the
+    timed region.  The steps share one set of caches, as in the device-resident loop.
+    Right after each step the compute stream packs that step's refreshed rows (one
+    dllm_gather_rows_n launch, before the next step can rewrite them) into the step's
+    slot; inputs, selections and packed rows live in `slots` slots used in turn.  A second
+    stream does every copy: it uploads each step's input as soon as its slot is free and
+    reads back a batch of steps' results once the batch has finished.  The compute stream
+    waits on one event (the upload of the batch's last input) and records one per batch
+    of up to `batch` steps (each such wait ends the programmatic-launch overlap between two
+    steps' kernels); the batches grow from 1 to `batch` steps at the start and shrink back
+    at the end (e2e_batches).  -> (seconds for `steps` steps, byte counts per step)."""
     import torch
     B = wl.B_
     dev = wl.dev
     sh = wl.sh
     km = wl.k_max
-    Hh = [wl.H[0].cpu().pin_memory(), wl.H[1].cpu().pin_memory()]
-    Hd = [torch.empty_like(wl.H[0]), torch.empty_like(wl.H[0])]
-    idx_d = [torch.empty_like(wl.idx), torch.empty_like(wl.idx)]
-    cnt_d = [torch.empty_like(wl.cnt), torch.empty_like(wl.cnt)]
+    Hh = [wl.H[i & 1].cpu().pin_memory() for i in range(slots)]   # step parity = slot parity
+    Hd = [torch.empty_like(wl.H[0]) for _ in range(slots)]
+    idx_d = [torch.empty_like(wl.idx) for _ in range(slots)]
+    cnt_d = [torch.empty_like(wl.cnt) for _ in range(slots)]
     rows_d = [[torch.empty((sh.B * km,) + tuple(t.shape[2:]), dtype=t.dtype, device=dev) for t in (wl.O, wl.K, wl.V)]
-              for _ in range(2)]
-    idx_h = [torch.empty(wl.idx.shape, dtype=torch.int32).pin_memory() for _ in range(2)]
-    cnt_h = [torch.empty(wl.cnt.shape, dtype=torch.int32).pin_memory() for _ in range(2)]
-    rows_h = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in rows_d[0]] for _ in range(2)]
-    sets = [wl.caches(), tuple(t.clone() for t in wl.caches())]
+              for _ in range(slots)]
+    idx_h = [torch.empty(wl.idx.shape, dtype=torch.int32).pin_memory() for _ in range(slots)]
+    cnt_h = [torch.empty(wl.cnt.shape, dtype=torch.int32).pin_memory() for _ in range(slots)]
+    rows_h = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in rows_d[0]] for _ in range(slots)]
     main = torch.cuda.current_stream(dev)
     cs = torch.cuda.Stream(dev)
-    ready = [torch.cuda.Event(), torch.cuda.Event()]   # input of the step in Hd[b] is resident
-    done = [torch.cuda.Event(), torch.cuda.Event()]    # the step using buffers b has finished
+    ready = [torch.cuda.Event() for _ in range(slots)]   # the input of the step in a slot is resident
     read_back = torch.cuda.Event()
 
-    def read_result(s):
-        b = s & 1
-        cs.wait_event(done[b])
-        K, V, O = sets[b][:3]
-        for src, dst in zip((O, K, V), rows_d[b]):
-            B.dllm_gather_rows(src, idx_d[b], cnt_d[b], km, dst)
-        idx_h[b].copy_(idx_d[b], non_blocking=True)
-        cnt_h[b].copy_(cnt_d[b], non_blocking=True)
-        for dsrc, hdst in zip(rows_d[b], rows_h[b]):
+    def upload(s):   # on the copy stream
+        sl = s % slots
+        Hd[sl].copy_(Hh[sl], non_blocking=True)
+        ready[sl].record(cs)
+
+    def read_result(s):   # on the copy stream
+        sl = s % slots
+        idx_h[sl].copy_(idx_d[sl], non_blocking=True)
+        cnt_h[sl].copy_(cnt_d[sl], non_blocking=True)
+        for dsrc, hdst in zip(rows_d[sl], rows_h[sl]):
             hdst.copy_(dsrc, non_blocking=True)
 
-    def stage(s):   # on the copy stream: step s - 2's result out, step s's input in
-        with torch.cuda.stream(cs):
-            if s >= 2:
-                read_result(s - 2)
-            Hd[s & 1].copy_(Hh[s & 1], non_blocking=True)
-            ready[s & 1].record(cs)
-
     def e2e_steps(n, start_event=None):
-        if start_event is not None:
-            cs.wait_event(start_event)
-        stage(0)
-        stage(1)
-        for s in range(n):
-            b = s & 1
-            main.wait_event(ready[b])
-            wl.step(Hd[b], idx=idx_d[b], cnt=cnt_d[b], caches=sets[b])
-            done[b].record(main)
-            if s + 2 < n:
-                stage(s + 2)
+        sizes = e2e_batches(n, batch)
         with torch.cuda.stream(cs):
-            for s in range(max(n - 2, 0), n):
-                read_result(s)
-            read_back.record(cs)
+            if start_event is not None:
+                cs.wait_event(start_event)
+            for s in range(min(slots, n)):
+                upload(s)
+        first = 0
+        for bs in sizes:
+            last = first + bs - 1
+            main.wait_event(ready[last % slots])   # uploads complete in order
+            for s in range(first, last + 1):
+                sl = s % slots
+                wl.step(Hd[sl], idx=idx_d[sl], cnt=cnt_d[sl])
+                B.dllm_gather_rows_n((wl.O, wl.K, wl.V), idx_d[sl], cnt_d[sl], km, rows_d[sl])
+            done = torch.cuda.Event()
+            done.record(main)
+            with torch.cuda.stream(cs):   # this batch's results out, then the inputs of its slots' next steps
+                cs.wait_event(done)
+                for s in range(first, last + 1):
+                    read_result(s)
+                for s in range(first + slots, min(last + slots + 1, n)):
+                    upload(s)
+            first = last + 1
+        read_back.record(cs)
         main.wait_event(read_back)
+        return n
 
-    e2e_steps(2)
+    e2e_steps(2 * slots)
     torch.cuda.synchronize(dev)
     barrier()
     f0 = torch.cuda.Event(enable_timing=True)
@@ -570,18 +586,20 @@ def e2e_measure(wl, steps, barrier):
     barrier()
     # the rows read back are the refreshed ones: compare the last step's packed output rows
     # with the device cache (a consistency check of the copies, not of the method)
-    b = (steps - 1) & 1
-    c = int(cnt_h[b][0])
-    got = rows_h[b][0][:c].to(dev)
-    want = sets[b][2][0, idx_h[b][0, :c].to(dev).long()]
+    sl = (steps - 1) % slots
+    c = int(cnt_h[sl][0])
+    got = rows_h[sl][0][:c].to(dev)
+    want = wl.O[0, idx_h[sl][0, :c].to(dev).long()]
     if not torch.equal(got, want):
         raise RuntimeError("e2e read-back does not match the refreshed rows")
-    del sets
     d2h = idx_h[0].numel() * 4 + cnt_h[0].numel() * 4 + sum(t.numel() * t.element_size() for t in rows_h[0])
     return f0.elapsed_time(f1) / 1e3, {"h2d_bytes_per_step": int(Hh[0].numel() * Hh[0].element_size()),
                                        "d2h_bytes_per_step": int(d2h),
                                        "d2h": "refreshed rows of the output, key and value caches "
-                                              f"({sh.B}x{km} rows each, packed by dllm_gather_rows) + the selection"}
+                                              f"({sh.B}x{km} rows each, packed by dllm_gather_rows_n right "
+                                              "after the step) + the selection",
+                                       "copies": f"{slots} input/result slots; one event wait per batch of "
+                                                 f"steps: {e2e_batches(steps, batch)}"}
 
 
 # --------------------------------------------------------------------------- full stack

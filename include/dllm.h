@@ -68,7 +68,8 @@ const char *dllm_last_error(void);
  * calls (KL drift, drift-aware commit, confidence extrapolation, cluster-granular
  * proxy); 1.11 the host-only GEMM plan query (dllm_gemm_plan); 1.12 the read-back of
  * refreshed rows (dllm_gather_rows), the bounded-wait diagnostic
- * (dllm_check_wait_timeout) and the one-call layer step (dllm_layer_step). */
+ * (dllm_check_wait_timeout) and the one-call layer step (dllm_layer_step); 1.13 the
+ * read-back of several caches' refreshed rows in one launch (dllm_gather_rows_n). */
 int dllm_version(void);
 
 /* Reads (and with reset != 0 clears) the device status word of the current device.
@@ -452,6 +453,15 @@ int dllm_rows_rmsnorm(const void *H, const int32_t *rows, int R, const void *gam
  * ------------------------------------------------------------------------- */
 int dllm_gather_rows(const void *src, const int32_t *idx, const int32_t *count, int k_max, void *dst,
                      int B, int N, int row_bytes, void *stream);
+
+/* The same packing for n <= 4 caches that share one selection, in one launch (a step's
+ * refreshed H_out, K and V rows): for t < n, dsts[t] [B * k_max, row_bytes[t]] receives the
+ * rows of srcs[t] [B, N, row_bytes[t]] as dllm_gather_rows would.  srcs, dsts and
+ * row_bytes are host arrays of n entries (read during the call); the pointers they hold
+ * are device pointers.  Requirements and errors as dllm_gather_rows, per cache; n outside
+ * [1, 4] is INVALID_ARG. */
+int dllm_gather_rows_n(int n, const void *const *srcs, void *const *dsts, const int *row_bytes,
+                       const int32_t *idx, const int32_t *count, int k_max, int B, int N, void *stream);
 
 /* ---------------------------------------------------------------------------
  * Plain product on the tensor cores, the engine under every bf16 projection above

@@ -83,6 +83,7 @@ _SIGS = {
                           + [C.c_int] * 4 + [C.c_void_p]),
     "dllm_check_wait_timeout": (C.c_int, [C.c_void_p, C.c_void_p]),
     "dllm_gather_rows": (C.c_int, [C.c_void_p] * 5 + [C.c_int] * 3 + [C.c_void_p]),
+    "dllm_gather_rows_n": (C.c_int, [C.c_int] + [C.c_void_p] * 5 + [C.c_int] * 3 + [C.c_void_p]),
     "dllm_commit_entropy_noalloc": (C.c_int, [C.c_void_p, C.c_void_p, C.c_int, C.c_int, C.c_int,
                                               C.c_float, C.c_float] + [C.c_void_p] * 6),
     "dllm_commit_workspace_bytes": (C.c_size_t, [C.c_int, C.c_int, C.c_int]),
@@ -511,6 +512,32 @@ def dllm_gather_rows(src, idx, count, k_max: int, dst=None):
     _check(lib().dllm_gather_rows(_ptr(src), _ptr(idx), _ptr(count), int(k_max), _ptr(dst), Bn, N, row_bytes,
                                   _stream(src.device)), "dllm_gather_rows")
     return dst
+
+
+def dllm_gather_rows_n(srcs, idx, count, k_max: int, dsts=None):
+    """The rows idx[b, :count[b]] of several caches [B, N, ...] sharing one selection,
+    packed per sequence in one launch -> list of dst [B*k_max, ...] (zeros after)."""
+    srcs = list(srcs)
+    if not 1 <= len(srcs) <= 4:
+        raise DllmError("between 1 and 4 caches")
+    Bn, N = srcs[0].shape[0], srcs[0].shape[1]
+    if dsts is None:
+        dsts = [torch.empty((Bn * k_max,) + tuple(s.shape[2:]), dtype=s.dtype, device=s.device) for s in srcs]
+    rb = []
+    for s_, d_ in zip(srcs, dsts):
+        if s_.shape[:2] != (Bn, N):
+            raise DllmError("the caches must share [B, N]")
+        rb.append(s_[0, 0].numel() * s_.element_size())
+        if d_.numel() * d_.element_size() < Bn * k_max * rb[-1]:
+            raise DllmError("dst holds fewer than B*k_max rows")
+    _cuda(*srcs, *dsts, idx, count)
+    n = len(srcs)
+    src_arr = (C.c_void_p * n)(*[_ptr(t) for t in srcs])
+    dst_arr = (C.c_void_p * n)(*[_ptr(t) for t in dsts])
+    rb_arr = (C.c_int * n)(*rb)
+    _check(lib().dllm_gather_rows_n(n, src_arr, dst_arr, rb_arr, _ptr(idx), _ptr(count), int(k_max), Bn, N,
+                                    _stream(srcs[0].device)), "dllm_gather_rows_n")
+    return dsts
 
 
 # --------------------------------------------------------------------------- plain GEMM

@@ -203,7 +203,7 @@ using namespace dllm;
 
 DLLM_EXPORT const char *dllm_last_error(void) { return t_err.c_str(); }
 
-DLLM_EXPORT int dllm_version(void) { return 112; }
+DLLM_EXPORT int dllm_version(void) { return 113; }
 
 DLLM_EXPORT int dllm_check_status(unsigned *status_out, int reset) {
     CHECK_CUDA(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
@@ -793,8 +793,36 @@ DLLM_EXPORT int dllm_gather_rows(const void *src, const int32_t *idx, const int3
     CHECK_ARG(row_bytes % 16 == 0, "row_bytes must be a multiple of 16 (got %d)", row_bytes);
     CHECK_ARG(aligned16(src) && aligned16(dst), "src and dst must be 16-byte aligned");
     cudaStream_t st = as_stream(stream);
+    GatherSet gs{};
+    gs.src[0] = src;
+    gs.dst[0] = dst;
+    gs.vecs[0] = row_bytes / 16;
     Launch t(DLLM_KERNEL_GATHER, st);
-    CHECK_CUDA(gather_rows(src, SelRows{idx, count, k_max, N}, B, row_bytes, dst, st), "gather rows launch");
+    CHECK_CUDA(gather_rows(gs, 1, SelRows{idx, count, k_max, N}, B, st), "gather rows launch");
+    return DLLM_OK;
+}
+
+DLLM_EXPORT int dllm_gather_rows_n(int n, const void *const *srcs, void *const *dsts, const int *row_bytes,
+                                   const int32_t *idx, const int32_t *count, int k_max, int B, int N,
+                                   void *stream) {
+    CHECK_ARG(srcs && dsts && row_bytes && idx && count, "null pointer");
+    CHECK_ARG(n >= 1 && n <= kGatherMax, "n must be in [1, %d] (got %d)", kGatherMax, n);
+    CHECK_ARG(B > 0 && N > 0, "sizes must be positive");
+    CHECK_ARG(k_max > 0 && k_max <= N, "k_max must be in [1, N] (got %d, N=%d)", k_max, N);
+    CHECK_ARG((long long)B * k_max <= INT_MAX, "B*k_max must fit in an int");
+    GatherSet gs{};
+    for (int t = 0; t < n; ++t) {
+        CHECK_ARG(srcs[t] && dsts[t], "null pointer (cache %d)", t);
+        CHECK_ARG(row_bytes[t] > 0 && row_bytes[t] % 16 == 0,
+                  "row_bytes[%d] must be a positive multiple of 16 (got %d)", t, row_bytes[t]);
+        CHECK_ARG(aligned16(srcs[t]) && aligned16(dsts[t]), "cache %d: src and dst must be 16-byte aligned", t);
+        gs.src[t] = srcs[t];
+        gs.dst[t] = dsts[t];
+        gs.vecs[t] = row_bytes[t] / 16;
+    }
+    cudaStream_t st = as_stream(stream);
+    Launch t(DLLM_KERNEL_GATHER, st);
+    CHECK_CUDA(gather_rows(gs, n, SelRows{idx, count, k_max, N}, B, st), "gather rows launch");
     return DLLM_OK;
 }
 

@@ -146,8 +146,16 @@ template <class T>
 cudaError_t embed_rows(const T *E, const int32_t *tokens, const int32_t *rows, int R, T *H, int B,
                        int N, int d, int V, cudaStream_t st);
 
-// dst[b * k_max + s] = src row (b, idx[b, s]) of row_bytes bytes (live rows), else 0.
-cudaError_t gather_rows(const void *src, SelRows sel, int B, int row_bytes, void *dst, cudaStream_t st);
+// dst[t][b * k_max + s] = src[t] row (b, idx[b, s]) of vecs[t] 16-byte units for the live
+// rows, else 0; up to kGatherMax caches sharing one selection in one launch
+// (dllm_gather_rows packs one, dllm_gather_rows_n several).
+constexpr int kGatherMax = 4;
+struct GatherSet {
+    const void *src[kGatherMax];
+    void *dst[kGatherMax];
+    int vecs[kGatherMax];
+};
+cudaError_t gather_rows(const GatherSet &gs, int n, SelRows sel, int B, cudaStream_t st);
 
 template <class T>
 cudaError_t rows_rmsnorm(const T *H, const int32_t *rows, int R, const T *gamma, float eps, T *out,

@@ -218,29 +218,31 @@ __global__ void __launch_bounds__(256) k_rows_rmsnorm(const T *__restrict__ H, c
 }
 
 // One CTA per packed row: 16-byte copies of the selected cache row, or zeros.
-__global__ void __launch_bounds__(128) k_gather_rows(const uint4 *__restrict__ src, SelRows sel, int vecs,
-                                                     uint4 *__restrict__ dst) {
+// dst_t[m] = src_t[b, pos] for each of the caches t = blockIdx.y that share one selection
+// (zeros for rows that are not live).
+__global__ void __launch_bounds__(128) k_gather_rows(GatherSet gs, SelRows sel) {
     griddep_wait();
     griddep_launch();
-    const int m = blockIdx.x;
+    const int m = blockIdx.x, t = blockIdx.y;
+    const int vecs = gs.vecs[t];
     int b, pos;
     sel.locate(m, b, pos);
-    uint4 *o = dst + (size_t)m * vecs;
+    uint4 *o = static_cast<uint4 *>(gs.dst[t]) + (size_t)m * vecs;
     if (pos < 0) {
         for (int v = threadIdx.x; v < vecs; v += 128) o[v] = make_uint4(0u, 0u, 0u, 0u);
         return;
     }
-    const uint4 *row = src + ((size_t)b * sel.N + pos) * vecs;
+    const uint4 *row = static_cast<const uint4 *>(gs.src[t]) + ((size_t)b * sel.N + pos) * vecs;
     for (int v = threadIdx.x; v < vecs; v += 128) o[v] = row[v];
 }
 
 }  // namespace
 
-cudaError_t gather_rows(const void *src, SelRows sel, int B, int row_bytes, void *dst, cudaStream_t st) {
+cudaError_t gather_rows(const GatherSet &gs, int n, SelRows sel, int B, cudaStream_t st) {
     const long M = (long)B * sel.k_max;
-    if (M <= 0) return cudaSuccess;
-    return launch_kernel(k_gather_rows, dim3((unsigned)M), dim3(128), 0, st, 1,
-                         static_cast<const uint4 *>(src), sel, row_bytes / 16, static_cast<uint4 *>(dst));
+    if (M <= 0 || n <= 0) return cudaSuccess;
+    if (n > kGatherMax) return cudaErrorInvalidValue;
+    return launch_kernel(k_gather_rows, dim3((unsigned)M, (unsigned)n), dim3(128), 0, st, 1, gs, sel);
 }
 
 template <class T>

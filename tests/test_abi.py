@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(dl):
     missing = [n for n in _declared() if not hasattr(L, n)]
     assert not missing, missing
     assert set(_declared()) <= set(dl.exported_symbols()) | {"dllm_last_error", "dllm_version"}
-    assert dl.lib().dllm_version() == 112
+    assert dl.lib().dllm_version() == 113
 
 
 def test_budget_logic_matches_oracle(dl, orc):
@@ -103,6 +103,18 @@ def test_invalid_arguments_fail_before_launch(dl):
     bad = dl.dllm_layer(p.value, p.value, p.value, p.value, p.value, p.value, p.value,
                         128, 1, 1, 96, 128, 1e-5, 1e4, 1, 1)
     assert rf(C.byref(bad), p, p, p, 4, p, p, C.c_void_p(512), None, None, 0, 1, 16, p, ws_need, None) == -2
+    # read-back of several caches: n outside [1, 4], a null cache, a misaligned one, row sizes
+    srcs = (C.c_void_p * 3)(256, 512, 768)
+    dsts = (C.c_void_p * 3)(1024, 1280, 1536)
+    rb = (C.c_int * 3)(8192, 8192, 8192)
+    gn = L.dllm_gather_rows_n
+    assert gn(0, srcs, dsts, rb, p, p, 4, 1, 16, None) == -1
+    assert gn(5, srcs, dsts, rb, p, p, 4, 1, 16, None) == -1
+    assert gn(3, srcs, dsts, rb, p, p, 17, 1, 16, None) == -1            # k_max > N
+    assert gn(3, (C.c_void_p * 3)(256, None, 768), dsts, rb, p, p, 4, 1, 16, None) == -1
+    assert "cache 1" in _err(dl)
+    assert gn(3, (C.c_void_p * 3)(256, 520, 768), dsts, rb, p, p, 4, 1, 16, None) == -1   # alignment
+    assert gn(3, srcs, dsts, (C.c_int * 3)(8192, 8200, 8192), p, p, 4, 1, 16, None) == -1
 
 
 def test_binding_fails_loudly_without_cuda_tensors(dl):

@@ -488,3 +488,26 @@ def test_gather_rows_bit_exact(B, Bq, N, k_max, row_bytes):
             if 0 <= p < N:
                 want[b * k_max + s] = src[b, p]
     np.testing.assert_array_equal(got, want)
+
+
+def test_gather_rows_n_bit_exact(B):
+    """dllm_gather_rows_n packs three caches of different row sizes (a step's H_out, K and
+    V rows) sharing one selection in one launch, each exactly as dllm_gather_rows packs it."""
+    g = synth.rng(5100)
+    Bq, N, k_max = 3, 300, 40
+    srcs = [g.integers(0, 256, size=(Bq, N, rb), dtype=np.uint8) for rb in (512, 256, 4096)]
+    idx = np.full((Bq, N), -1, np.int32)
+    cnt = np.zeros(Bq, np.int32)
+    for b in range(Bq):
+        n = k_max - 7 * b
+        idx[b, :n] = np.sort(g.permutation(N)[:n])
+        cnt[b] = n
+    d_idx, d_cnt = to_dev(idx), to_dev(cnt)
+    outs = B.dllm_gather_rows_n([to_dev(x) for x in srcs], d_idx, d_cnt, k_max)
+    for x, o in zip(srcs, outs):
+        one = B.dllm_gather_rows(to_dev(x), d_idx, d_cnt, k_max)
+        assert torch.equal(o, one)
+        want = np.zeros((Bq * k_max, x.shape[2]), np.uint8)
+        for b in range(Bq):
+            want[b * k_max:b * k_max + cnt[b]] = x[b, idx[b, :cnt[b]]]
+        np.testing.assert_array_equal(to_np(o).reshape(want.shape), want)
