@@ -76,6 +76,9 @@ def parse():
                     help="profiling mode: set up the layer workload, warm up, then run ONE layer "
                          "step inside a cudaProfilerStart/Stop range (for ncu --profile-from-start off); "
                          "prints a short JSON line, no measurement")
+    ap.add_argument("--profile-proxy", action="store_true",
+                    help="one proxy score with the drift in the projection's epilogue (B=4, N=8192) "
+                         "inside a profiler range, for ncu")
     ap.add_argument("--profile-kl", action="store_true",
                     help="profiling mode: ONE KL drift call on the layer workload's proxies inside a "
                          "cudaProfilerStart/Stop range; prints a short JSON line, no measurement")
@@ -1204,10 +1207,38 @@ def profile_kl(args):
     print(json.dumps({"profile_kl": "llada8b-layer proxies", "N": int(wl.cur.shape[1])}), flush=True)
 
 
+def profile_proxy(args):
+    """One warmed-up proxy score of the long-context batch (B = 4, N = 8192, d = 4096,
+    r = 128: the projection needs no K split and computes the drift in its epilogue)
+    inside a profiler range."""
+    import torch
+    from sparse_kv_cache_rank_gb300 import binding as B
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(11)
+    Bn, N, d, r = 4, 8192, 4096, 128
+    H = torch.randn((Bn, N, d), generator=gen, device=dev).to(torch.bfloat16)
+    Pt = (torch.randn((r, d), generator=gen, device=dev) * 0.02).to(torch.bfloat16)
+    pc = torch.randn((Bn, N, r), generator=gen, device=dev)
+    cur = torch.empty_like(pc)
+    drift = torch.empty((Bn, N), device=dev)
+    for _ in range(3):
+        B.dllm_proxy_score(H, Pt, pc, proxy_cur=cur, drift=drift)
+    torch.cuda.synchronize(dev)
+    torch.cuda.profiler.start()
+    B.dllm_proxy_score(H, Pt, pc, proxy_cur=cur, drift=drift)
+    torch.cuda.synchronize(dev)
+    torch.cuda.profiler.stop()
+    B.check_status()
+    print(json.dumps({"profile_proxy": f"B={Bn} N={N} d={d} r={r}"}), flush=True)
+
+
 def main():
     args = parse()
     if args.profile_step:
         profile_step(args)
+    elif args.profile_proxy:
+        profile_proxy(args)
     elif args.profile_kl:
         profile_kl(args)
     elif args.impl == "reference":
