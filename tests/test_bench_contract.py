@@ -79,3 +79,17 @@ def test_kernel_work_model_follows_the_launches():
     assert "cosine" in tiny and "rmsnorm2" in tiny
     for w in (llada, wide, tiny):
         assert all(v[0] > 0 for v in w.values())
+
+
+@pytest.mark.parametrize("n", [1, 5, 16, 17, 20, 37, 100, 1000])
+def test_e2e_batches_cover_every_step(n):
+    """The end-to-end leg's batches cover the steps exactly once, never exceed the cap,
+    and start and end with single steps once there are enough of them (the first step
+    waits for one upload, the last read-back is one step's)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    b = bench.e2e_batches(n, 4)
+    assert sum(b) == n and all(1 <= x <= 4 for x in b)
+    assert b[0] == 1 and b[-1] == 1
+    if n > 16:
+        assert max(b) == 4 and len(b) < n
