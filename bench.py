@@ -41,7 +41,7 @@ if ROOT not in sys.path:
 METRIC = "sparse-refresh denoise steps/s & tokens/s (LLaDA-8B shape); % of roofline"
 # dram__bytes_read.sum + dram__bytes_write.sum per launch, LLaDA-8B layer at k = 164
 # (profiles/layer_step_llada8b_full.md); to be re-taken whenever these kernels change
-NCU_TRAFFIC_BYTES = {"gateup": 206.12e6, "qkv": 106.07e6, "down": 110.58e6, "oproj": 36.32e6,
+NCU_TRAFFIC_BYTES = {"gateup": 205.64e6, "qkv": 106.07e6, "down": 110.29e6, "oproj": 36.32e6,
                      "attention": 18.17e6, "proxy_gemm": 9.47e6, "select": 6.13e6}
 UNIT = "steps/s"
 DATA = "synthetic (seeded random-init weights N(0,0.02), drift model: 10% rows +N(0,0.5), all +N(0,0.05))"
