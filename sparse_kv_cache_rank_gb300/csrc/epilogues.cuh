@@ -66,8 +66,9 @@ struct EpiStoreF32 {
 // proxy"): cur[m, :] = acc over the proxy's r <= 128 features (one weight tile) and
 // drift[m] = 1 - cos(cur[m], cached[m]), computed as 0.5 |cur/|cur| - cached/|cached||^2
 // (exactly 0 for identical proxies), 0 when both are zero, 1 when exactly one is, clamped
-// to [0, 2].  The drift needs every feature of a token: the GEMM hands this epilogue whole
-// 16-column chunks (kCosine) and reduces over the 128 TMEM lanes itself, so the operator
+// to [0, 2].  The drift needs every feature of a token, so the GEMM runs it only without a
+// K split (each CTA's accumulators hold a token's whole proxy): it hands the epilogue whole
+// 16-column chunks (kCosine) and reduces over the 128 TMEM lanes itself, and the operator
 // below is never called.
 struct EpiCosine {
     static constexpr bool kSel = false;
