@@ -372,7 +372,7 @@ def native(args):
     import torch
     import torch.distributed as dist
     from sparse_kv_cache_rank_gb300 import binding as B
-    from sparse_kv_cache_rank_gb300 import synth
+    from sparse_kv_cache_rank_gb300 import replicas, synth
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -386,8 +386,12 @@ def native(args):
         if world > 1:
             dist.barrier()
 
+    # replicas: the job is world * B independent sequences; this rank owns a contiguous
+    # shard of them (B = 1 each here) and seeds its inputs by the shard's first sequence
     sh = synth.LLADA_LAYER
-    wl = LayerWorkload(sh, 1234 + rank, dev)
+    first, stop = replicas.shard_sequences(world * sh.B, world, rank)
+    assert stop - first == sh.B
+    wl = LayerWorkload(sh, 1234 + first, dev)
     for _ in range(max(args.warmup, 3)):
         wl.step()
     torch.cuda.synchronize(dev)
@@ -450,10 +454,8 @@ def native(args):
     three_calls_ms = e4.elapsed_time(e5) / args.steps
     e2e_elapsed, e2e_bytes = e2e_measure(wl, args.steps, barrier)
 
-    t = torch.tensor([elapsed, e2e_elapsed], device=dev, dtype=torch.float64)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    elapsed, e2e_elapsed = float(t[0]), float(t[1])
+    # the job's time is the slowest replica's
+    elapsed, e2e_elapsed = replicas.max_over_ranks([elapsed, e2e_elapsed], device=dev)
 
     roof = roofline_of(sh, M, {dominant: dom_ms / max(dom_n, 1)}, dominant, sustained=False)
     # DRAM bytes (read + write) per launch from the committed ncu capture; None for a
