@@ -1,5 +1,6 @@
 // api.cu -- the extern "C" entry points of libdllm.so (declared in include/dllm.h):
 // argument checks, workspace carving and the launch sequence of each call.
+#include <nvtx3/nvToolsExt.h>
 #include <atomic>
 #include <climits>
 #include <cmath>
@@ -89,13 +90,27 @@ struct KernelTimer {
     std::vector<cudaEvent_t> ev;
 } g_timer;
 
-// Counts the launches of one library call site and, when the timer is armed for
-// this kernel, brackets them with a pair of events on the launch stream.
+// NVTX range names of the kernels (DLLM_KERNEL_* ids): a profiler shows each library
+// launch inside "dllm:<kernel>" (nvtx3 is header-only; without a tool attached the calls
+// return at once).
+const char *kernel_range_name(int id) {
+    static const char *names[] = {"dllm:other",     "dllm:proxy_gemm", "dllm:cosine",  "dllm:select",
+                                  "dllm:gather",    "dllm:qkv",        "dllm:attention", "dllm:oproj",
+                                  "dllm:rmsnorm2",  "dllm:gateup",     "dllm:down",    "dllm:vocab",
+                                  "dllm:gemm",      "dllm:kl_drift",   "dllm:ce",      "dllm:polestar",
+                                  "dllm:cluster"};
+    return id > 0 && id < (int)(sizeof(names) / sizeof(names[0])) ? names[id] : names[0];
+}
+
+// Counts the launches of one library call site, opens an NVTX range named after the
+// kernel around them and, when the timer is armed for this kernel, brackets them with a
+// pair of events on the launch stream.
 struct Launch {
     cudaEvent_t stop = nullptr;
     cudaStream_t st;
     Launch(int kernel_id, cudaStream_t s, int nlaunch = 1) : st(s) {
         g_launches.fetch_add((unsigned long long)nlaunch, std::memory_order_relaxed);
+        nvtxRangePushA(kernel_range_name(kernel_id));
         if (g_timer.armed != kernel_id) return;
         std::lock_guard<std::mutex> lock(g_timer.mu);
         if (g_timer.armed != kernel_id || g_timer.n >= g_timer.cap) return;
@@ -106,6 +121,7 @@ struct Launch {
     }
     ~Launch() {
         if (stop) cudaEventRecord(stop, st);
+        nvtxRangePop();
     }
 };
 
