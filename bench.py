@@ -171,9 +171,9 @@ def layer_kernel_work(sh, M):
     # drift); no separate cosine kernel
     slices = _proxy_slices(B * N, r, d) if sh.dtype == "bf16" and d % 64 == 0 and r % 32 == 0 else 1
     fused = sh.dtype == "bf16" and r <= 128 and r % 32 == 0 and d % 64 == 0 and slices == 1
-    # the one-call layer step with bf16 K-slice partials (r <= 128, N <= 4096): the
-    # selection kernel sums the partials and computes the drift, no cosine kernel
-    in_select = sh.dtype == "bf16" and r <= 128 and slices > 1 and N <= 4096
+    # the one-call layer step with bf16 K-slice partials or fp32 proxies (r <= 128,
+    # N <= 4096): the selection kernel computes the drift, no cosine kernel
+    in_select = (sh.dtype == "f32" or slices > 1) and r <= 128 and N <= 4096
     if in_select:
         sel = (sel[0] + 8 * B * N * r + 4 * B * N, 0)
     work = {

@@ -684,22 +684,32 @@ DLLM_EXPORT int dllm_layer_step(const dllm_layer *W, const void *Pt, const void 
     const size_t rws = k_max > 0 ? refresh_ws(W, B, N, k_max).total : 0;
     uint8_t *w8 = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(ws) + 255) & ~uintptr_t(255));
     const int nparts = proxy_slices(B, N, W->d, r, W->dtype);
-    // bf16 K-slice partials and a selection fused with the gather: the selection kernel sums
-    // the partials and computes the drift itself (no cosine kernel); the projection clears
-    // the selection's per-sequence arrival counters, placed after the partials
+    // a selection fused with the gather that also computes the drift (no cosine kernel):
+    // from the bf16 projection's K-slice partials, or from the fp32 projection's proxies;
+    // the projection clears the selection's per-sequence arrival counters, placed after
+    // the partials
     const DriftParts no_parts{nullptr, 0, nullptr};
     DriftParts dp = no_parts;
-    if (W->dtype == DLLM_BF16 && nparts > 1 && r <= 128 && k_max > 0 && N <= select_gather_max_n() &&
-        select_gather_fused_ok(B, N, k_max, W->dtype)) {
+    const bool front_fused = (W->dtype == DLLM_F32 || nparts > 1) && r <= 128 && k_max > 0 &&
+                             N <= select_gather_max_n() && select_gather_fused_ok(B, N, k_max, W->dtype);
+    if (front_fused) {
         const size_t pbytes = dllm_proxy_workspace_bytes(B, N, W->d, r, W->dtype);
-        float *parts = reinterpret_cast<float *>(
-            (reinterpret_cast<uintptr_t>(w8 + rws) + 255) & ~uintptr_t(255));
         unsigned *arrive = reinterpret_cast<unsigned *>(w8 + rws + pbytes);
-        dp = DriftParts{parts, nparts, arrive};
         Launch t(DLLM_KERNEL_PROXY_GEMM, st);
-        CHECK_CUDA(gemm_tc_slices(static_cast<const bf16 *>(Pt), r, W->d, static_cast<const bf16 *>(H_in), B * N,
-                                  parts, true, status_ptr(), st, arrive, B),
-                   "proxy projection launch");
+        if (W->dtype == DLLM_BF16) {
+            float *parts = reinterpret_cast<float *>(
+                (reinterpret_cast<uintptr_t>(w8 + rws) + 255) & ~uintptr_t(255));
+            dp = DriftParts{parts, nparts, arrive};
+            CHECK_CUDA(gemm_tc_slices(static_cast<const bf16 *>(Pt), r, W->d, static_cast<const bf16 *>(H_in),
+                                      B * N, parts, true, status_ptr(), st, arrive, B),
+                       "proxy projection launch");
+        } else {   // one fp32 product straight into proxy_cur
+            dp = DriftParts{proxy_cur, 1, arrive};
+            EpiStoreF32 epi{SelRows{}, proxy_cur, r, r};
+            CHECK_CUDA(gemm_simt(static_cast<const float *>(Pt), r, W->d, static_cast<const float *>(H_in), B * N,
+                                 epi, st, arrive, B),
+                       "proxy projection launch");
+        }
     } else {
         rc = dllm_proxy_score(H_in, Pt, proxy_cache, proxy_cur, drift, B, N, W->d, r, W->dtype, w8 + rws,
                               ws_bytes - rws - 256, stream);

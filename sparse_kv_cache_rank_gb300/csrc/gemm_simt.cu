@@ -21,7 +21,7 @@ constexpr int kT = 256;
 template <class Epi>
 __global__ void __launch_bounds__(kT) k_gemm_simt(const float *__restrict__ W, int N_out, int K,
                                                   const float *__restrict__ X, int M_tok, const Epi epi,
-                                                  int splits) {
+                                                  int splits, unsigned *zero, int nzero) {
     // rows padded to 36 words: 16-byte aligned for the float4 reads of Xs, and the
     // transposed stores below (rows lk + 8i, columns lr) still hit 32 distinct banks
     __shared__ __align__(16) float Ws[TK][TF + 4];
@@ -29,6 +29,9 @@ __global__ void __launch_bounds__(kT) k_gemm_simt(const float *__restrict__ W, i
     __shared__ float part[TM][TF];   // this CTA's partial tile (K split)
     griddep_wait();
     griddep_launch();
+    // counters of the kernel that follows, cleared once the previous kernel is done
+    if (zero && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+        for (int i = threadIdx.x; i < nzero; i += kT) zero[i] = 0u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * TM, f0 = blockIdx.y * TF;
     const int split = splits > 1 ? (int)cluster_ctarank() : 0;
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(kT) k_gemm_simt(const float *__restrict__ W, i
 
 template <class Epi>
 cudaError_t gemm_simt(const float *W, int N_out, int K, const float *X, int M_tok, const Epi &epi,
-                      cudaStream_t st) {
+                      cudaStream_t st, unsigned *zero, int nzero) {
     if (M_tok <= 0 || N_out <= 0) return cudaSuccess;
     if (N_out % 32 != 0 || K <= 0) return cudaErrorInvalidValue;
     const dim3 tiles((M_tok + TM - 1) / TM, N_out / TF);
@@ -122,18 +125,18 @@ cudaError_t gemm_simt(const float *W, int N_out, int K, const float *X, int M_to
     s = s < 1 ? 1 : (s > 8 ? 8 : s);
     while (s > 1 && nkt / s < 2) --s;
     return launch_kernel(k_gemm_simt<Epi>, dim3(tiles.x, tiles.y, s), dim3(kT), 0, st, s, W, N_out, K, X, M_tok,
-                         epi, s);
+                         epi, s, zero, zero ? nzero : 0);
 }
 
 template cudaError_t gemm_simt<EpiStoreF32>(const float *, int, int, const float *, int,
-                                            const EpiStoreF32 &, cudaStream_t);
+                                            const EpiStoreF32 &, cudaStream_t, unsigned *, int);
 template cudaError_t gemm_simt<EpiQKV<float>>(const float *, int, int, const float *, int,
-                                              const EpiQKV<float> &, cudaStream_t);
+                                              const EpiQKV<float> &, cudaStream_t, unsigned *, int);
 template cudaError_t gemm_simt<EpiResidual<float>>(const float *, int, int, const float *, int,
-                                                   const EpiResidual<float> &, cudaStream_t);
+                                                   const EpiResidual<float> &, cudaStream_t, unsigned *, int);
 template cudaError_t gemm_simt<EpiSwiGLU<float>>(const float *, int, int, const float *, int,
-                                                 const EpiSwiGLU<float> &, cudaStream_t);
+                                                 const EpiSwiGLU<float> &, cudaStream_t, unsigned *, int);
 template cudaError_t gemm_simt<EpiDownScatter<float>>(const float *, int, int, const float *, int,
-                                                      const EpiDownScatter<float> &, cudaStream_t);
+                                                      const EpiDownScatter<float> &, cudaStream_t, unsigned *, int);
 
 }  // namespace dllm

@@ -75,10 +75,10 @@ bool gemm_tc_cosine_ok(int M_tok, int N_out, int K);
 cudaError_t gemm_tc_cosine(const bf16 *W, int N_out, int K, const bf16 *X, int M_tok, float *cur,
                            const float *cached, float *drift, bool w_const, unsigned *status, cudaStream_t st);
 
-// CUDA cores (fp32 FMA): any K.
+// CUDA cores (fp32 FMA): any K.  zero [nzero] (optional) as for gemm_tc_slices.
 template <class Epi>
 cudaError_t gemm_simt(const float *W, int N_out, int K, const float *X, int M_tok, const Epi &epi,
-                      cudaStream_t st);
+                      cudaStream_t st, unsigned *zero = nullptr, int nzero = 0);
 
 // ---------------------------------------------------------------- row kernels
 template <class T>
@@ -190,7 +190,8 @@ cudaError_t select_topk(const float *drift, const int32_t *forced, int F, int k,
 // at a per-sequence barrier on dp.arrive [B] (zero at launch); the grid must then fit on
 // the GPU at once (select_gather_fused_ok).
 struct DriftParts {
-    const float *parts;   // [nparts, B*N, r] fp32, or nullptr: drift is an input
+    const float *parts;   // [nparts, B*N, r] fp32 (nparts = 1: the proxies themselves, in
+                          // proxy_cur), or nullptr: drift is an input
     int nparts;
     unsigned *arrive;     // [B] arrival counters, zeroed before the launch
 };

@@ -62,7 +62,8 @@ def test_kernel_work_model_follows_the_launches():
     kernels each configuration launches: at the LLaDA-8B-shaped layer the selection
     kernel computes the drift from the proxy projection's K-slice partials (no cosine
     kernel); at 16 x 8192 tokens the projection's epilogue does (no split, no cosine
-    kernel, a separate gather beyond N = 4096); the fp32 layer keeps the cosine kernel."""
+    kernel, a separate gather beyond N = 4096); the fp32 layer's selection kernel takes the
+    drift from the fp32 proxies."""
     sys.path.insert(0, ROOT)
     import dataclasses
     import bench
@@ -76,7 +77,7 @@ def test_kernel_work_model_follows_the_launches():
     wide = bench.layer_kernel_work(dataclasses.replace(synth.LLADA_LAYER, B=16, N=8192), 164)
     assert "cosine" not in wide and "gather" in wide
     tiny = bench.layer_kernel_work(synth.TINY, 96)
-    assert "cosine" in tiny and "rmsnorm2" in tiny
+    assert "cosine" not in tiny and "rmsnorm2" in tiny
     for w in (llada, wide, tiny):
         assert all(v[0] > 0 for v in w.values())
 
