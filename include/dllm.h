@@ -100,7 +100,7 @@ int dllm_check_wait_timeout(int32_t *gave_up, void *stream);
  *   proxy_cache [B, N, r]  fp32       proxies stored when each row was last refreshed
  *   proxy_cur   [B, N, r]  fp32 out
  *   drift       [B, N]     fp32 out
- * Requirements: r % 32 == 0, r <= 1024; d % 64 == 0 for DLLM_BF16.
+ * Requirements: r % 32 == 0, r <= 1024; d % 64 == 0 for DLLM_BF16; B * N <= INT_MAX.
  * Workspace: dllm_proxy_workspace_bytes() bytes (fp32 partial proxies of independent K
  * slices, summed in a fixed order by a second kernel that computes the drift), 0 when
  * the shape needs no K split.  Without a split (bf16, r <= 128, the token tiles alone fill

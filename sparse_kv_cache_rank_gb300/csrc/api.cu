@@ -268,6 +268,7 @@ DLLM_EXPORT int dllm_proxy_score(const void *H, const void *Pt, const float *pro
                                  int dtype, void *ws, size_t ws_bytes, void *stream) {
     CHECK_ARG(H && Pt && proxy_cache && proxy_cur && drift, "null pointer");
     CHECK_ARG(B > 0 && N > 0 && d > 0 && r > 0, "sizes must be positive (B=%d N=%d d=%d r=%d)", B, N, d, r);
+    CHECK_ARG((long long)B * N <= INT_MAX, "B*N must fit in an int");
     CHECK_ARG(r <= 1024, "r must be <= 1024");
     CHECK_ARG(aligned16(H) && aligned16(Pt) && aligned16(proxy_cache) && aligned16(proxy_cur),
               "arrays must be 16-byte aligned");

@@ -68,6 +68,7 @@ def test_invalid_arguments_fail_before_launch(dl):
     assert L.dllm_proxy_score(p, p, p, p, p, 1, 8, 100, 32, 1, None, 0, None) == -2      # d % 64 (bf16)
     assert L.dllm_proxy_score(p, p, p, p, p, 0, 8, 64, 32, 1, None, 0, None) == -1
     assert L.dllm_proxy_score(C.c_void_p(258), p, p, p, p, 1, 8, 64, 32, 1, None, 0, None) == -1   # alignment
+    assert L.dllm_proxy_score(p, p, p, p, p, 1 << 16, 1 << 16, 64, 32, 1, None, 0, None) == -1   # B*N > int
     assert L.dllm_select_topk(p, None, 0, -1, 0.0, p, p, 1, 8, None) == -1      # k < 0
     assert L.dllm_select_topk(p, None, 0, 4, 0.0, p, p, 1, 20000, None) == -1   # N too large
     assert L.dllm_select_topk(None, None, 0, 4, 0.0, p, p, 1, 8, None) == -1
