@@ -258,7 +258,7 @@ int proxy_slices(int B, int N, int d, int r, int dtype) {
 }  // namespace
 
 DLLM_EXPORT size_t dllm_proxy_workspace_bytes(int B, int N, int d, int r, int dtype) {
-    if (B <= 0 || N <= 0 || d <= 0 || r <= 0) return 0;
+    if (B <= 0 || N <= 0 || d <= 0 || r <= 0 || (long long)B * N > INT_MAX) return 0;
     const int s = proxy_slices(B, N, d, r, dtype);
     return s > 1 ? (size_t)s * B * N * r * sizeof(float) + 256 : 0;
 }
