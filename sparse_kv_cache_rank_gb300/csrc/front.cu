@@ -11,9 +11,10 @@
 // every CTA costs a few microseconds of one block's work in parallel; it saves the launch
 // of a separate gather kernel that would wait for the selection to finish.
 //
-// With the proxy projection's K-slice partials as input, the kernel first computes the
-// drift itself: CTA g of sequence b sums the partials and takes the cosine drift of rows
-// g*N/G .. (g+1)*N/G-1 (one warp per row, the arithmetic of the cosine kernel), then the G
+// With the proxy projection's K-slice partials (bf16) or its proxies (fp32, one slice) as
+// input, the kernel first computes the drift itself: CTA g of sequence b sums the partials
+// and takes the cosine drift of rows g*N/G .. (g+1)*N/G-1 (one warp per row, the
+// arithmetic of the cosine kernel), then the G
 // CTAs of the sequence meet at a barrier (an arrival counter per sequence that the proxy
 // projection zeroed; bounded wait) before they select.  The next kernel is released only
 // after the barrier, so it cannot take the SM slots that the sequence's CTAs still need.
